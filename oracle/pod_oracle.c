@@ -1,0 +1,236 @@
+/*
+ * POD paged-attention ORACLE: plain, slow, fp64, single file of C.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product library links, loads or
+ * calls this file; only the tests, the package smoke check and the CPU
+ * baseline leg of the benchmark do. It shares no code, header, table or helper
+ * with the CUDA path.
+ *
+ * What it computes is the plain definition of softmax attention over a paged
+ * KV cache, written out one (query token, qo head) at a time:
+ *
+ *  - Paged KV cache, NHD layout [num_pages, 2, page_size, num_kv_heads, head_dim],
+ *    addressed through kv_indptr / kv_indices / last_page_len
+ *    (POD walkthrough, the two wrapper docstring examples and "plan 内部做了什么":
+ *    kv_len = (pages - 1) * page_size + last_page_len).
+ *  - GQA: qo head h reads kv head h / (num_qo_heads / num_kv_heads)
+ *    (POD walkthrough, "plan/run 生命周期": num_qo_heads must be a multiple
+ *    of num_kv_heads; unequal counts mean grouped-query attention).
+ *  - Bottom-right causal diagonal: query row i of a request with q_len rows
+ *    and kv_len keys sits at key position p = kv_len - q_len + i and may see
+ *    keys 0..p (flashinfer.cudnn page, "Decode 能力矩阵与参数", q_len_per_req row).
+ *  - window_left counts the keys strictly before the diagonal; the diagonal is
+ *    attended too, so key t is allowed iff t >= p - window_left; -1 disables it
+ *    (flashinfer.cudnn page, "Decode 能力矩阵与参数", window paragraph).
+ *  - Sinks: one extra logit per qo head in the softmax denominator with a zero
+ *    value row (flashinfer.cudnn page, "Decode 能力矩阵与参数", sinks row).
+ *    Reading taken here: the sink is already a logit (not multiplied by
+ *    sm_scale) and it does not enter the LSE.
+ *  - LSE in base 2: lse = log2(sum over allowed keys of exp(sm_scale * q.k))
+ *    (flashinfer.cudnn page, "LSE 契约").
+ *  - Merge of split partials (o_i, lse_i): weights 2^(lse_i - max), the
+ *    property that lets base-2 LSE feed a cascade merge (same section).
+ *
+ * Inputs are the same rounded fp16/bf16 values the GPU reads, widened to
+ * double by decoders written from the IEEE-754 binary16 and bfloat16 bit
+ * layouts. Nothing is blocked, fused or reordered: keys are visited in order
+ * 0..kv_len-1.
+ *
+ * Parity pins (tests under tests/, run on the CPU): brute-force dense attention
+ * on tiny inputs, page-permutation and page-size invariance, split/merge
+ * identity, the hand-worked two-token example, closed forms (q = 0,
+ * window_left = 0, kv_len = 1, equal keys), GQA head duplication, exhaustive
+ * checks of the two 16-bit decoders.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARG 1
+#define ORACLE_EMPTY_ROW 2
+
+/* IEEE-754 binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+double oracle_f16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -24);               /* subnormal: f * 2^-14 * 2^-10 */
+    } else if (e == 31) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(1024 + f), e - 25);    /* (1 + f/1024) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* bfloat16: the upper 16 bits of an IEEE-754 binary32. */
+double oracle_bf16_to_f64(uint16_t b)
+{
+    uint32_t u = ((uint32_t)b) << 16;
+    float x;
+    memcpy(&x, &u, sizeof(x));
+    return (double)x;
+}
+
+static double widen(uint16_t v, int dtype)
+{
+    return dtype == 0 ? oracle_f16_to_f64(v) : oracle_bf16_to_f64(v);
+}
+
+/* kv_len of request r from its page table (POD walkthrough, plan step 1). */
+int64_t oracle_kv_len(const int32_t* kv_indptr, const int32_t* last_page_len,
+                      int r, int page_size)
+{
+    int64_t pages = (int64_t)kv_indptr[r + 1] - kv_indptr[r];
+    if (pages <= 0) return 0;
+    return (pages - 1) * (int64_t)page_size + last_page_len[r];
+}
+
+void oracle_seq_lens(const int32_t* kv_indptr, const int32_t* last_page_len,
+                     int batch, int page_size, int32_t* kv_len_out)
+{
+    for (int r = 0; r < batch; ++r)
+        kv_len_out[r] = (int32_t)oracle_kv_len(kv_indptr, last_page_len, r, page_size);
+}
+
+static int find_request(const int32_t* q_indptr, int batch, int64_t token)
+{
+    for (int r = 0; r < batch; ++r)
+        if (token >= q_indptr[r] && token < q_indptr[r + 1]) return r;
+    return -1;
+}
+
+/*
+ * Attention for a list of selected (token, qo head) pairs of one half.
+ *   q   : [rows, H, d] 16-bit codes       kv : [num_pages, 2, ps, Hk, d] codes
+ *   sel_token[n], sel_head[n]             : which outputs to compute
+ *   key_lo/key_hi (may be NULL)           : extra restriction key in [lo, hi)
+ *                                           per selection (split-KV partials)
+ *   sinks (may be NULL)                   : fp32 [H] extra logit per qo head
+ *   out [n, d], lse [n]                   : fp64 results
+ * Returns the first error code met (rows are still filled where possible).
+ */
+int oracle_attention_rows(const uint16_t* q, const uint16_t* kv, int dtype,
+                          const int32_t* q_indptr, const int32_t* kv_indptr,
+                          const int32_t* kv_indices, const int32_t* last_page_len,
+                          int batch, int num_pages,
+                          int H, int Hk, int d, int page_size,
+                          int causal, int window_left, double sm_scale,
+                          const float* sinks,
+                          int64_t n_sel, const int64_t* sel_token, const int32_t* sel_head,
+                          const int64_t* key_lo, const int64_t* key_hi,
+                          double* out, double* lse, int nthreads)
+{
+    if (H <= 0 || Hk <= 0 || H % Hk != 0 || d <= 0 || page_size <= 0) return ORACLE_BAD_ARG;
+    int group = H / Hk;
+    int status = ORACLE_OK;
+    (void)nthreads;
+
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads > 0 ? nthreads : 1)
+    for (int64_t s = 0; s < n_sel; ++s) {
+        int64_t token = sel_token[s];
+        int h = sel_head[s];
+        double* o = out + s * (int64_t)d;
+        for (int e = 0; e < d; ++e) o[e] = 0.0;
+        lse[s] = -INFINITY;
+        int r = find_request(q_indptr, batch, token);
+        if (r < 0 || h < 0 || h >= H) {
+#pragma omp atomic write
+            status = ORACLE_BAD_ARG;
+            continue;
+        }
+        int64_t q_len = (int64_t)q_indptr[r + 1] - q_indptr[r];
+        int64_t i = token - q_indptr[r];
+        int64_t kv_len = oracle_kv_len(kv_indptr, last_page_len, r, page_size);
+        int64_t p = kv_len - q_len + i;          /* bottom-right diagonal */
+        int hk = h / group;                       /* GQA mapping */
+
+        double* qv = (double*)malloc(sizeof(double) * (size_t)d);
+        double* logit = (double*)malloc(sizeof(double) * (size_t)(kv_len > 0 ? kv_len : 1));
+        char* allowed = (char*)malloc((size_t)(kv_len > 0 ? kv_len : 1));
+        for (int e = 0; e < d; ++e)
+            qv[e] = widen(q[(token * H + h) * (int64_t)d + e], dtype);
+
+        /* logits of the allowed keys */
+        double m = -INFINITY;
+        int64_t n_allowed = 0;
+        for (int64_t t = 0; t < kv_len; ++t) {
+            int ok = 1;
+            if (causal && t > p) ok = 0;
+            if (window_left >= 0 && t < p - window_left) ok = 0;
+            if (key_lo && t < key_lo[s]) ok = 0;
+            if (key_hi && t >= key_hi[s]) ok = 0;
+            allowed[t] = (char)ok;
+            if (!ok) continue;
+            int64_t page = kv_indices[kv_indptr[r] + t / page_size];
+            int64_t slot = t % page_size;
+            if (page < 0 || page >= num_pages) {
+                allowed[t] = 0;
+#pragma omp atomic write
+                status = ORACLE_BAD_ARG;
+                continue;
+            }
+            const uint16_t* k = kv + (((page * 2 + 0) * page_size + slot) * Hk + hk) * (int64_t)d;
+            double dot = 0.0;
+            for (int e = 0; e < d; ++e) dot += qv[e] * widen(k[e], dtype);
+            logit[t] = sm_scale * dot;
+            if (logit[t] > m) m = logit[t];
+            ++n_allowed;
+        }
+        if (n_allowed == 0) {
+#pragma omp atomic write
+            status = ORACLE_EMPTY_ROW;
+            free(qv); free(logit); free(allowed);
+            continue;
+        }
+        /* explicit softmax with an optional sink logit in the denominator */
+        double z = 0.0;
+        for (int64_t t = 0; t < kv_len; ++t)
+            if (allowed[t]) z += exp(logit[t] - m);
+        double denom = z;
+        if (sinks) denom += exp((double)sinks[h] - m);
+        for (int64_t t = 0; t < kv_len; ++t) {
+            if (!allowed[t]) continue;
+            int64_t page = kv_indices[kv_indptr[r] + t / page_size];
+            int64_t slot = t % page_size;
+            const uint16_t* v = kv + (((page * 2 + 1) * page_size + slot) * Hk + hk) * (int64_t)d;
+            double w = exp(logit[t] - m) / denom;
+            for (int e = 0; e < d; ++e) o[e] += w * widen(v[e], dtype);
+        }
+        lse[s] = (m + log(z)) / log(2.0);
+        free(qv); free(logit); free(allowed);
+    }
+    return status;
+}
+
+/*
+ * Merge n partial results of the same (row, head) computed over disjoint key
+ * sets. Partial i is a normalised output o_i with Z_i = 2^lse_i the sum of
+ * exponentials of its keys (no sink). The merged output is
+ *   o = sum_i Z_i o_i / (sum_i Z_i + [sink] exp(sink)),  lse = log2 sum_i Z_i,
+ * evaluated with every Z_i divided by 2^M, M = max_i lse_i.
+ *   o_parts [n, d], lse_parts [n]  ->  o [d], *lse
+ */
+void oracle_merge(int n, int d, const double* o_parts, const double* lse_parts,
+                  int has_sink, double sink, double* o, double* lse)
+{
+    double M = -INFINITY;
+    for (int i = 0; i < n; ++i) if (lse_parts[i] > M) M = lse_parts[i];
+    double wsum = 0.0;
+    for (int e = 0; e < d; ++e) o[e] = 0.0;
+    for (int i = 0; i < n; ++i) {
+        double w = pow(2.0, lse_parts[i] - M);
+        wsum += w;
+        for (int e = 0; e < d; ++e) o[e] += w * o_parts[(int64_t)i * d + e];
+    }
+    double lse_all = M + log2(wsum);       /* log2 sum_t exp(s_t) over all parts */
+    double denom = wsum;                     /* = sum_t exp(s_t) / 2^M */
+    if (has_sink) denom += exp(sink - M * log(2.0));
+    for (int e = 0; e < d; ++e) o[e] /= denom;
+    *lse = lse_all;
+}

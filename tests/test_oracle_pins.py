@@ -1,0 +1,434 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle.
+
+Each check here is either a closed form, a hand-worked example, an invariant
+that the definition implies (page permutation, page size, split/merge), an
+exhaustive check of a decoder against a library routine, or brute-force dense
+attention written independently with numpy/scipy (sink as an explicit extra
+key column with a zero value row).
+
+``test_planted_mistakes`` compiles mutated copies of the oracle's C source
+(each with one plausible mistake) and checks that at least one pin fails for
+every mutant, so the pins are shown to be sensitive.
+"""
+import json
+import math
+import os
+import re
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import logsumexp, softmax
+
+import oracle
+from pod_workloads import HalfInputs, make_custom, page_table_from_lens
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+GOLDEN = os.path.join(HERE, "golden")
+
+
+# --------------------------------------------------------------------------
+# helpers (independent of the oracle)
+# --------------------------------------------------------------------------
+
+def dense_kv(h: HalfInputs, r: int, ps: int):
+    """Dense K, V [kv_len, Hk, d] of request r, gathered with numpy indexing."""
+    kv = h.kv.float().numpy().astype(np.float64)
+    lo, hi = int(h.kv_indptr[r]), int(h.kv_indptr[r + 1])
+    pages = h.kv_indices[lo:hi]
+    kvl = int(h.kv_lens[r])
+    t = np.arange(kvl)
+    pg = pages[t // ps]
+    sl = t % ps
+    return kv[pg, 0, sl], kv[pg, 1, sl]
+
+
+def brute_force(inp, half="d"):
+    """Textbook masked softmax(QK^T)V per request/head, all rows."""
+    h = inp.p if half == "p" else inp.d
+    H, Hk, d = inp.num_qo_heads, inp.num_kv_heads, inp.head_dim
+    G = H // Hk
+    q = h.q.float().numpy().astype(np.float64)
+    rows = h.rows
+    out = np.zeros((rows, H, d))
+    lse = np.zeros((rows, H))
+    for r in range(h.batch):
+        q0, q1 = int(h.q_indptr[r]), int(h.q_indptr[r + 1])
+        ql = q1 - q0
+        if ql == 0:
+            continue
+        K, V = dense_kv(h, r, inp.page_size)
+        kvl = K.shape[0]
+        i = np.arange(ql)[:, None]
+        t = np.arange(kvl)[None, :]
+        p = kvl - ql + i
+        mask = np.ones((ql, kvl), dtype=bool)
+        if inp.causal:
+            mask &= t <= p
+        if inp.window_left >= 0:
+            mask &= t >= p - inp.window_left
+        for hh in range(H):
+            S = inp.sm_scale * (q[q0:q1, hh, :] @ K[:, hh // G, :].T)
+            S = np.where(mask, S, -np.inf)
+            lse[q0:q1, hh] = logsumexp(S, axis=1) / math.log(2.0)
+            if inp.sinks is not None:
+                sink_col = np.full((ql, 1), float(inp.sinks[hh]))
+                Vz = np.concatenate([V[:, hh // G, :], np.zeros((1, d))], axis=0)
+                P = softmax(np.concatenate([S, sink_col], axis=1), axis=1)
+                out[q0:q1, hh] = P @ Vz
+            else:
+                out[q0:q1, hh] = softmax(S, axis=1) @ V[:, hh // G, :]
+    return out, lse
+
+
+def run_oracle(inp, half="d", fn=None, **kw):
+    fn = fn or oracle.attention_rows
+    h = inp.p if half == "p" else inp.d
+    out, lse, st = fn(h.q, h.kv, h.q_indptr, h.kv_indptr, h.kv_indices, h.last_page_len,
+                      inp.num_qo_heads, inp.num_kv_heads, inp.head_dim, inp.page_size,
+                      inp.causal, inp.window_left, inp.sm_scale, sinks=inp.sinks, nthreads=2, **kw)
+    assert st == 0
+    return out.reshape(h.rows, inp.num_qo_heads, inp.head_dim), lse.reshape(h.rows, inp.num_qo_heads)
+
+
+def tiny_case(seed, G=None, ps=None, causal=None, window=None, sinks=None, d=None, dtype=torch.float16):
+    rng = np.random.default_rng(seed)
+    G = G or int(rng.choice([1, 2, 3]))
+    Hk = int(rng.choice([1, 2]))
+    d = d or int(rng.choice([4, 8, 16]))
+    ps = ps or int(rng.choice([1, 3, 4, 16]))
+    causal = bool(rng.integers(0, 2)) if causal is None else causal
+    window = int(rng.choice([-1, 0, 2, 5])) if window is None else window
+    sinks = bool(rng.integers(0, 2)) if sinks is None else sinks
+    B = int(rng.integers(1, 4))
+    kv = rng.integers(1, 41, size=B)
+    ql = np.array([int(rng.integers(1, k + 1)) for k in kv])
+    return make_custom("tiny", dtype, G * Hk, Hk, d, ps, causal, window,
+                       [], [], ql, kv, seed=seed, sinks=sinks, extra_pages=3)
+
+
+# --------------------------------------------------------------------------
+# pins, written as functions of an attention callable so mutants can be run
+# --------------------------------------------------------------------------
+
+def pin_two_token(fn):
+    g = json.load(open(os.path.join(GOLDEN, "two_token.json")))
+    for case in g["cases"]:
+        ql = case["q_len"]
+        e = math.e
+        # closed forms recomputed here; the fixture decimals must agree with them
+        if case["name"] == "no_sink":
+            cf = [[(e + 3) / (e + 1), (2 * e + 4) / (e + 1), math.log2(e + 1)]]
+        elif case["name"] == "sink_zero":
+            cf = [[(e + 3) / (e + 2), (2 * e + 4) / (e + 2), math.log2(e + 1)]]
+        else:
+            cf = [[1.0, 2.0, 1.0 / math.log(2.0)],
+                  [(e + 3) / (e + 1), (2 * e + 4) / (e + 1), math.log2(e + 1)]]
+        for row, c in zip(case["rows"], cf):
+            assert np.allclose(row["out"] + [row["lse"]], c, rtol=0, atol=1e-15)
+        # page_size 1, pages 0 and 1 hold keys 0 and 1
+        kv = torch.zeros(2, 2, 1, 1, 2, dtype=torch.float16)
+        kv[0, 0, 0, 0] = torch.tensor([1.0, 0.0])
+        kv[1, 0, 0, 0] = torch.tensor([0.0, 1.0])
+        kv[0, 1, 0, 0] = torch.tensor([1.0, 2.0])
+        kv[1, 1, 0, 0] = torch.tensor([3.0, 4.0])
+        q = torch.tensor([[[1.0, 0.0]]] * ql, dtype=torch.float16)
+        sinks = None if case["sink"] is None else torch.tensor([case["sink"]], dtype=torch.float32)
+        out, lse, st = fn(q, kv, np.array([0, ql]), np.array([0, 2]), np.array([0, 1]), np.array([1]),
+                          1, 1, 2, 1, case["causal"], -1, 1.0, sinks=sinks, nthreads=1)
+        assert st == 0
+        for i, row in enumerate(case["rows"]):
+            assert np.allclose(out[i], row["out"], rtol=0, atol=1e-12), (case["name"], out[i])
+            assert abs(lse[i] - row["lse"]) < 1e-12, (case["name"], lse[i])
+
+
+def pin_brute_force(fn, seeds=range(12)):
+    for s in seeds:
+        inp = tiny_case(s)
+        ref_o, ref_l = brute_force(inp, "d")
+        o, l = run_oracle(inp, "d", fn)
+        assert np.max(np.abs(o - ref_o)) < 1e-12, f"seed {s}: out differs"
+        assert np.max(np.abs(l - ref_l)) < 1e-12, f"seed {s}: lse differs"
+
+
+def pin_closed_forms(fn):
+    # q = 0: uniform weights over the allowed keys, lse = log2(n_allowed)
+    inp = make_custom("q0", torch.bfloat16, 4, 2, 8, 4, True, 3, [], [], [2, 1], [9, 6], seed=5,
+                      extra_pages=2)
+    inp.d.q.zero_()
+    o, l = run_oracle(inp, "d", fn)
+    for r in range(2):
+        K, V = dense_kv(inp.d, r, inp.page_size)
+        q0, ql, kvl = inp.d.q_indptr[r], inp.d.q_lens[r], inp.d.kv_lens[r]
+        for i in range(ql):
+            p = kvl - ql + i
+            allowed = [t for t in range(kvl) if t <= p and t >= p - 3]
+            for hh in range(4):
+                assert np.allclose(o[q0 + i, hh], V[allowed, hh // 2].mean(axis=0), atol=1e-13)
+                assert abs(l[q0 + i, hh] - math.log2(len(allowed))) < 1e-13
+    # window_left = 0: only the diagonal key; out = v_p, lse = s_p / ln 2
+    inp = make_custom("w0", torch.float16, 2, 1, 8, 3, True, 0, [], [], [3], [7], seed=6)
+    o, l = run_oracle(inp, "d", fn)
+    K, V = dense_kv(inp.d, 0, 3)
+    q = inp.d.q.double().numpy()
+    for i in range(3):
+        p = 7 - 3 + i
+        for hh in range(2):
+            assert np.allclose(o[i, hh], V[p, 0], atol=0)
+            assert abs(l[i, hh] - inp.sm_scale * float(q[i, hh] @ K[p, 0]) / math.log(2)) < 1e-13
+    # kv_len = 1: out = v_0
+    inp = make_custom("kv1", torch.bfloat16, 3, 3, 16, 16, False, -1, [], [], [1], [1], seed=7)
+    o, l = run_oracle(inp, "d", fn)
+    K, V = dense_kv(inp.d, 0, 16)
+    for hh in range(3):
+        assert np.allclose(o[0, hh], V[0, hh], atol=0)
+    # equal keys: uniform weights, lse = s + log2(n)
+    inp = make_custom("eqk", torch.float16, 2, 1, 8, 4, False, -1, [], [], [1], [10], seed=8)
+    inp.d.kv[:, 0] = inp.d.kv[0, 0, 0]
+    o, l = run_oracle(inp, "d", fn)
+    K, V = dense_kv(inp.d, 0, 4)
+    q = inp.d.q.double().numpy()
+    for hh in range(2):
+        assert np.allclose(o[0, hh], V[:, 0].mean(axis=0), atol=1e-13)
+        s = inp.sm_scale * float(q[0, hh] @ K[0, 0])
+        assert abs(l[0, hh] - (s / math.log(2) + math.log2(10))) < 1e-12
+    # sink with q = 0: out = sum v / (n + e^sink)
+    inp = make_custom("sq0", torch.float16, 2, 1, 4, 2, False, -1, [], [], [1], [5], seed=9, sinks=True)
+    inp.d.q.zero_()
+    o, l = run_oracle(inp, "d", fn)
+    K, V = dense_kv(inp.d, 0, 2)
+    for hh in range(2):
+        ref = V[:, 0].sum(axis=0) / (5 + math.exp(float(inp.sinks[hh])))
+        assert np.allclose(o[0, hh], ref, atol=1e-13)
+        assert abs(l[0, hh] - math.log2(5)) < 1e-13
+
+
+def pin_gqa(fn):
+    inp = make_custom("gqa", torch.bfloat16, 8, 2, 16, 4, True, -1, [], [], [3, 2], [11, 17], seed=10)
+    q = inp.d.q
+    for g in range(2):
+        q[:, g * 4 + 1: g * 4 + 4] = q[:, g * 4: g * 4 + 1]
+    o, l = run_oracle(inp, "d", fn)
+    for g in range(2):
+        for j in range(1, 4):
+            assert np.array_equal(o[:, g * 4 + j], o[:, g * 4])
+            assert np.array_equal(l[:, g * 4 + j], l[:, g * 4])
+    # different groups read different kv heads: outputs must differ
+    assert not np.allclose(o[:, 0], o[:, 4])
+
+
+def pin_page_invariance(fn):
+    inp = make_custom("perm", torch.float16, 4, 2, 8, 4, True, 6, [], [], [3, 1, 5], [13, 22, 9],
+                      seed=11, sinks=True, extra_pages=5)
+    o0, l0 = run_oracle(inp, "d", fn)
+    h = inp.d
+    rng = np.random.default_rng(1)
+    perm = rng.permutation(h.num_pages)
+    kv2 = torch.empty_like(h.kv)
+    kv2[torch.from_numpy(perm)] = h.kv
+    h2 = HalfInputs(h.q_indptr, h.kv_indptr, perm[h.kv_indices].astype(np.int32), h.last_page_len,
+                    h.num_pages, h.q, kv2, h.q_lens, h.kv_lens)
+    inp.d = h2
+    o1, l1 = run_oracle(inp, "d", fn)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+    # re-page the same token sequence with other page sizes
+    inp.d = h
+    for ps2 in (1, 3, 16):
+        ks, vs = [], []
+        for r in range(h.batch):
+            K, V = dense_kv(h, r, 4)
+            ks.append(K)
+            vs.append(V)
+        indptr, last = page_table_from_lens(h.kv_lens, ps2)
+        npg = int(indptr[-1])
+        kvn = torch.zeros(npg, 2, ps2, 2, 8, dtype=torch.float16)
+        for r in range(h.batch):
+            for t in range(int(h.kv_lens[r])):
+                pg, sl = indptr[r] + t // ps2, t % ps2
+                kvn[pg, 0, sl] = torch.from_numpy(ks[r][t]).half()
+                kvn[pg, 1, sl] = torch.from_numpy(vs[r][t]).half()
+        inp.d = HalfInputs(h.q_indptr, indptr, np.arange(npg, dtype=np.int32), last, npg,
+                           h.q, kvn, h.q_lens, h.kv_lens)
+        inp.page_size = ps2
+        o2, l2 = run_oracle(inp, "d", fn)
+        assert np.array_equal(o0, o2) and np.array_equal(l0, l2), ps2
+    inp.page_size = 4
+    inp.d = h
+
+
+def pin_split_merge(fn, merge=None):
+    merge = merge or oracle.merge
+    for seed, sinks in ((12, False), (13, True)):
+        inp = make_custom("sm", torch.bfloat16, 2, 1, 8, 4, True, -1, [], [], [2], [37],
+                          seed=seed, sinks=sinks)
+        o, l = run_oracle(inp, "d", fn)
+        h = inp.d
+        cuts = [0, 5, 16, 17, 30, 37]
+        for tok in range(2):
+            for hh in range(2):
+                parts_o, parts_l = [], []
+                for a, b in zip(cuts[:-1], cuts[1:]):
+                    po, pl, st = fn(h.q, h.kv, h.q_indptr, h.kv_indptr, h.kv_indices, h.last_page_len,
+                                    2, 1, 8, 4, True, -1, inp.sm_scale, sinks=None,
+                                    sel_token=[tok], sel_head=[hh], key_lo=[a], key_hi=[b], nthreads=1)
+                    if st == 2:      # every key of this chunk is masked for this row
+                        continue
+                    assert st == 0
+                    parts_o.append(po[0])
+                    parts_l.append(pl[0])
+                sink = float(inp.sinks[hh]) if sinks else None
+                mo, ml = merge(np.array(parts_o), np.array(parts_l), sink)
+                assert np.max(np.abs(mo - o[tok, hh])) < 1e-12
+                assert abs(ml - l[tok, hh]) < 1e-12
+
+
+ALL_PINS = (pin_two_token, pin_brute_force, pin_closed_forms, pin_gqa, pin_page_invariance,
+            pin_split_merge)
+
+
+# --------------------------------------------------------------------------
+# tests
+# --------------------------------------------------------------------------
+
+def test_f16_decoder_exhaustive():
+    codes = np.arange(65536, dtype=np.uint16)
+    ref = codes.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_to_f64(int(c)) for c in codes])
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all()
+
+
+def test_bf16_decoder_exhaustive():
+    codes = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+    ref = codes.double().numpy()
+    got = np.array([oracle.bf16_to_f64(c) for c in range(65536)])
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all()
+
+
+def test_seq_lens_docstring_page_table():
+    g = json.load(open(os.path.join(GOLDEN, "docstring_page_table.json")))
+    got = oracle.seq_lens(g["kv_page_indptr"], g["kv_last_page_len"], g["page_size"])
+    assert got.tolist() == g["kv_len"]
+
+
+def test_two_token_example():
+    pin_two_token(oracle.attention_rows)
+
+
+def test_brute_force_dense():
+    pin_brute_force(oracle.attention_rows, seeds=range(40))
+
+
+@pytest.mark.parametrize("ps", [1, 5, 16])
+@pytest.mark.parametrize("window", [-1, 0, 7])
+def test_brute_force_grid(ps, window):
+    for s in range(3):
+        inp = tiny_case(100 + s, ps=ps, window=window, causal=True, sinks=(s == 1), d=16,
+                        dtype=torch.bfloat16)
+        ref_o, ref_l = brute_force(inp, "d")
+        o, l = run_oracle(inp, "d")
+        assert np.max(np.abs(o - ref_o)) < 1e-12
+        assert np.max(np.abs(l - ref_l)) < 1e-12
+
+
+def test_closed_forms():
+    pin_closed_forms(oracle.attention_rows)
+
+
+def test_gqa_duplication():
+    pin_gqa(oracle.attention_rows)
+
+
+def test_page_permutation_and_size_invariance():
+    pin_page_invariance(oracle.attention_rows)
+
+
+def test_split_merge_identity():
+    pin_split_merge(oracle.attention_rows)
+
+
+def test_prefill_half_matches_brute_force():
+    inp = make_custom("pf", torch.float16, 6, 2, 16, 4, True, 9, [7, 12, 1], [7, 20, 3], [], [],
+                      seed=21, sinks=True)
+    ref_o, ref_l = brute_force(inp, "p")
+    o, l = run_oracle(inp, "p")
+    assert np.max(np.abs(o - ref_o)) < 1e-12 and np.max(np.abs(l - ref_l)) < 1e-12
+
+
+# --------------------------------------------------------------------------
+# planted mistakes: every mutant of the oracle must fail at least one pin
+# --------------------------------------------------------------------------
+
+MUTANTS = {
+    "causal_off_by_one": ("if (causal && t > p) ok = 0;", "if (causal && t >= p) ok = 0;"),
+    "window_excludes_diagonal_bound": ("t < p - window_left) ok = 0;", "t <= p - window_left) ok = 0;"),
+    "gqa_modulo": ("int hk = h / group;", "int hk = h % Hk;"),
+    "top_left_causal": ("int64_t p = kv_len - q_len + i;", "int64_t p = i;"),
+    "natural_log_lse": ("lse[s] = (m + log(z)) / log(2.0);", "lse[s] = (m + log(z));"),
+    "sink_in_lse": ("lse[s] = (m + log(z)) / log(2.0);", "lse[s] = (m + log(denom)) / log(2.0);"),
+    "sink_dropped": ("if (sinks) denom += exp((double)sinks[h] - m);", ""),
+    "sink_scaled": ("denom += exp((double)sinks[h] - m);", "denom += exp(sm_scale * (double)sinks[h] - m);"),
+    "k_for_v": ("(((page * 2 + 1) * page_size + slot) * Hk + hk)", "(((page * 2 + 0) * page_size + slot) * Hk + hk)"),
+    "last_page_off": ("return (pages - 1) * (int64_t)page_size + last_page_len[r];",
+                      "return pages * (int64_t)page_size;"),
+    "scale_dropped": ("logit[t] = sm_scale * dot;", "logit[t] = dot;"),
+    "merge_natural_weights": ("double w = pow(2.0, lse_parts[i] - M);", "double w = exp(lse_parts[i] - M);"),
+    "f16_bias": ("e - 25", "e - 24"),
+}
+
+
+def _mutant_fns(tmpdir, name, old, new):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "pod_oracle.c")).read()
+    assert old in src, name
+    so = os.path.join(tmpdir, f"m_{name}.so")
+    cpath = os.path.join(tmpdir, f"m_{name}.c")
+    open(cpath, "w").write(src.replace(old, new))
+    subprocess.check_call(["gcc", "-O1", "-fopenmp", "-shared", "-fPIC", "-o", so, cpath, "-lm"])
+    import ctypes
+    L = ctypes.CDLL(so)
+    # reuse the wrapper by swapping the library object temporarily
+    def fn(*a, **k):
+        saved = oracle._lib
+        oracle._lib = L
+        L.oracle_attention_rows.restype = ctypes.c_int
+        L.oracle_attention_rows.argtypes = saved.oracle_attention_rows.argtypes
+        L.oracle_merge.argtypes = saved.oracle_merge.argtypes
+        L.oracle_merge.restype = None
+        try:
+            return oracle.attention_rows(*a, **k)
+        finally:
+            oracle._lib = saved
+
+    def mg(*a, **k):
+        saved = oracle._lib
+        oracle._lib = L
+        L.oracle_merge.argtypes = saved.oracle_merge.argtypes
+        L.oracle_merge.restype = None
+        try:
+            return oracle.merge(*a, **k)
+        finally:
+            oracle._lib = saved
+    return fn, mg
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistakes(name):
+    oracle.lib()
+    old, new = MUTANTS[name]
+    with tempfile.TemporaryDirectory() as td:
+        fn, mg = _mutant_fns(td, name, old, new)
+        failures = 0
+        for pin in ALL_PINS:
+            try:
+                if pin is pin_split_merge:
+                    pin(fn, mg)
+                elif pin is pin_brute_force:
+                    pin(fn, seeds=range(12))
+                else:
+                    pin(fn)
+            except AssertionError:
+                failures += 1
+        assert failures > 0, f"mutant {name} passed every pin"
