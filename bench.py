@@ -1,0 +1,537 @@
+"""Benchmark of the fused POD launch on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5] [--impl ours|reference]
+
+A step is one fused POD launch (prefill tiles + decode items of one batch,
+plus the split merge when the plan has one) over a batch of synthetic inputs
+already resident in HBM. The default workload is c5 ("ragged stress", the
+largest single-GPU configuration): bf16, 64/8 heads, head_dim 128, page_size 16,
+4 causal prefill requests q = kv = {1000, 3000, 700, 4096}, 512 decode requests
+with 4 query tokens each and lognormal KV lengths, window_left 4096, sinks.
+
+Printed JSON (one line, rank 0): the metric is the fused-launch time in
+microseconds (lower is better); `roofline` reports the fused kernel against the
+measured HBM or tensor peak; extra keys give prefill TFLOP/s and decode GB/s
+from single-half runs of the same kernel, the CPU oracle baseline, end-to-end
+time through the public API with host buffers, and SM clocks sampled during
+the measurement.
+
+Under torchrun each rank runs its own independent batch of the same workload
+(no collective on the data path); the job time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused POD launch µs; prefill TFLOP/s & decode KV GB/s vs GB300 roofline"
+WORKLOAD_DESC = {
+    "c1": "c1 tiny POD fp16 4/1/64/16: prefill 64/64, decode kv {17,29,5,48}",
+    "c2": "c2 single-request POD fp16 64/8/128/16: prefill 1024/1024, 7 decode (docstring page table)",
+    "c3": "c3 batch POD bf16 64/8/128/1: prefill 2x2048, decode 128x2048, contiguous pages",
+    "c4": "c4 chunked-prefill overlap bf16 32/8/128/16: prefill 512 vs kv 8192, 256 decode kv~U[512,16384]",
+    "c5": "c5 ragged stress bf16 64/8/128/16: prefill {1000,3000,700,4096}, 512 decode x 4 tokens, "
+          "kv lognormal(median 2048), window 4096, sinks",
+}
+
+
+# ----------------------------------------------------------------- algorithmic work
+def allowed_keys(kv_len, q_len, causal, window_left):
+    """Number of (query row, key) pairs allowed per qo head, per request."""
+    tot = 0
+    for i in range(q_len):
+        p = kv_len - q_len + i
+        hi = min(kv_len, p + 1) if causal else kv_len
+        lo = max(0, p - window_left) if window_left >= 0 else 0
+        tot += max(0, hi - lo)
+    return tot
+
+
+def touched_keys(kv_len, q_len, causal, window_left):
+    """Keys read at least once by a request (union over its query rows)."""
+    if q_len == 0:
+        return 0
+    p0, p1 = kv_len - q_len, kv_len - 1
+    hi = min(kv_len, p1 + 1) if causal else kv_len
+    lo = max(0, p0 - window_left) if window_left >= 0 else 0
+    return max(0, hi - lo)
+
+
+def work(inp):
+    """Algorithmic FLOPs and bytes of one launch (per half)."""
+    H, Hk, d = inp.num_qo_heads, inp.num_kv_heads, inp.head_dim
+    el = 2
+    out = {}
+    for name, h in (("p", inp.p), ("d", inp.d)):
+        pairs = keys = 0
+        for r in range(h.batch):
+            ql, kl = int(h.q_lens[r]), int(h.kv_lens[r])
+            pairs += allowed_keys(kl, ql, inp.causal, inp.window_left)
+            keys += touched_keys(kl, ql, inp.causal, inp.window_left)
+        flops = 4.0 * d * H * pairs
+        kv_bytes = keys * Hk * d * el * 2.0
+        qo_bytes = h.rows * H * (d * el * 2 + 4)
+        out[name] = dict(pairs=pairs, keys=keys, flops=flops, kv_bytes=kv_bytes,
+                         bytes=kv_bytes + qo_bytes, rows=h.rows)
+    return out
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "utilization.gpu")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 10:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        load = [r for r in rows if (num(r[9]) or 0) >= 50] or rows
+        sm = [num(r[1]) for r in load if num(r[1]) is not None]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in load:
+            for i, nm in enumerate(names):
+                if r[5 + i].lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": num(rows[0][2]), "reasons": sorted(reasons),
+                "samples": len(rows), "samples_under_load": len(load),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+# ----------------------------------------------------------------- helpers
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), tc=float(d["bf16_tflops"]),
+                    tc_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm=6800.0, tc=1900.0, tc_sustained=1700.0, source="fallback")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "prefill_decode_paged_pod_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h", ".hpp", ".cpp")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None
+    e = d.get(workload)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int, device=None) -> float:
+    if ws <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def sample_pairs(inp, half, n, seed):
+    """Deterministic sample of (token, head) pairs of one half."""
+    h = inp.p if half == "p" else inp.d
+    if h.rows == 0 or n <= 0:
+        return np.zeros(0, np.int64), np.zeros(0, np.int32)
+    rng = np.random.default_rng(seed)
+    tok = rng.integers(0, h.rows, size=n).astype(np.int64)
+    hd = rng.integers(0, inp.num_qo_heads, size=n).astype(np.int32)
+    return tok, hd
+
+
+def pairs_work(inp, half, tok, hd):
+    """Allowed keys summed over the sampled pairs (oracle cost units)."""
+    h = inp.p if half == "p" else inp.d
+    req = np.searchsorted(h.q_indptr, tok, side="right") - 1
+    tot = 0
+    for t, r in zip(tok, req):
+        ql, kl = int(h.q_lens[r]), int(h.kv_lens[r])
+        i = int(t - h.q_indptr[r])
+        p = kl - ql + i
+        hi = min(kl, p + 1) if inp.causal else kl
+        lo = max(0, p - inp.window_left) if inp.window_left >= 0 else 0
+        tot += max(0, hi - lo)
+    return tot
+
+
+def oracle_launch_estimate(inp, w, target_s=10.0, seed=0, nthreads=None):
+    """Time the fp64 oracle on a bounded sample of (token, head) pairs of both
+    halves and scale to one whole launch. Returns (us_per_launch, info)."""
+    import oracle
+    nthreads = nthreads or os.cpu_count() or 1
+    total_work = (w["p"]["pairs"] + w["d"]["pairs"]) * inp.num_qo_heads
+    # calibrate on a small sample, then size the main sample for ~target_s
+    n = 64
+    spent, done_work, n_pairs = 0.0, 0, 0
+    while True:
+        t0 = time.perf_counter()
+        for half, frac in (("p", 0.5), ("d", 0.5)):
+            tok, hd = sample_pairs(inp, half, max(1, int(n * frac)), seed + n)
+            if len(tok) == 0:
+                continue
+            oracle.attention_half(inp, half, sel_token=tok, sel_head=hd, nthreads=nthreads)
+            done_work += pairs_work(inp, half, tok, hd)
+            n_pairs += len(tok)
+        spent += time.perf_counter() - t0
+        if spent >= target_s or n >= 1 << 20:
+            break
+        rate = done_work / max(spent, 1e-6)
+        want = (target_s - spent) * rate
+        per_pair = done_work / max(n_pairs, 1)
+        n = int(min(max(64, want / max(per_pair, 1)), 1 << 20))
+    us = spent / max(done_work, 1) * total_work * 1e6
+    info = dict(pairs=n_pairs, key_work=done_work, seconds=spent)
+    return us, info
+
+
+# ----------------------------------------------------------------- arms
+def run_reference(args, ws, rank):
+    """The fp64 CPU oracle as the reference arm, on the host cores."""
+    from pod_workloads import make_config
+    if rank != 0:
+        return 0
+    inp = make_config(args.workload)
+    w = work(inp)
+    nthreads = os.cpu_count() or 1
+    per_step = max(1.0, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
+    vals = []
+    info = None
+    for s in range(args.warmup + args.steps):
+        us, info = oracle_launch_estimate(inp, w, target_s=per_step, seed=1000 * s, nthreads=nthreads)
+        if s >= args.warmup:
+            vals.append(us)
+    v = float(np.mean(vals))
+    sample = (f"per step ~{per_step:.0f} s of fp64 oracle on random (token, head) pairs of both "
+              f"halves (last step: {info['pairs']} pairs), scaled by allowed (row, key) pairs to one launch")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "us", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1000.0,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD_DESC[args.workload]},
+            "cpu_baseline": {"value": v, "unit": "us", "cores": nthreads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def time_loop(fn, steps, stream, per_launch=True):
+    """Run fn() `steps` times; returns (total_ms, list of per-call ms)."""
+    import torch
+    if per_launch:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        if per_launch:
+            evs[i][0].record(stream)
+        fn()
+        if per_launch:
+            evs[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    per = [a.elapsed_time(b) for a, b in evs] if per_launch else []
+    return start.elapsed_time(end), per
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+    import prefill_decode_paged_pod_gb300 as pod
+    from prefill_decode_paged_pod_gb300 import _build
+    from pod_workloads import make_config
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    _build.build()
+    pod.load_library()
+    idx = ["c1", "c2", "c3", "c4", "c5"].index(args.workload) + 1
+    inp = make_config(args.workload, seed=idx + 1000 * rank)
+    w = work(inp)
+    stream = torch.cuda.current_stream(device)
+    dev = dict(q_p=inp.p.q.to(device) if inp.p.rows else None,
+               kv_p=inp.p.kv.to(device) if inp.p.rows else None,
+               q_d=inp.d.q.to(device) if inp.d.rows else None,
+               kv_d=inp.d.kv.to(device) if inp.d.rows else None,
+               sinks=inp.sinks.to(device) if inp.sinks is not None else None)
+    h = pod.plan_inputs(inp)
+    summ = pod.plan_summary(h)
+    wsb = torch.empty(pod.pod_workspace_size(h), dtype=torch.uint8, device=device)
+    pod.pod_bind_workspace(h, wsb)
+    H, d = inp.num_qo_heads, inp.head_dim
+    out_p = torch.empty((inp.p.rows, H, d), dtype=inp.dtype, device=device)
+    lse_p = torch.empty((inp.p.rows, H), dtype=torch.float32, device=device)
+    out_d = torch.empty((inp.d.rows, H, d), dtype=inp.dtype, device=device)
+    lse_d = torch.empty((inp.d.rows, H), dtype=torch.float32, device=device)
+
+    def step():
+        pod.pod_run(h, dev["q_p"], dev["kv_p"], dev["q_d"], dev["kv_d"], wsb, sinks=dev["sinks"],
+                    out_p=out_p, lse_p=lse_p, out_d=out_d, lse_d=lse_d)
+
+    kv_total = (inp.p.kv.numel() + inp.d.kv.numel()) * inp.p.kv.element_size()
+    l2_bytes = 129 * 1024 * 1024
+    flush = None
+    if kv_total < 2 * l2_bytes:
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+
+    def step_flush():
+        if flush is not None:
+            flush.zero_()
+        step()
+
+    for _ in range(max(args.warmup, 3)):
+        step_flush()
+    torch.cuda.synchronize()
+    assert pod.pod_read_device_status(h, wsb) == 0
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    # --- main timed region: K steps (flush between steps only when inputs fit in L2)
+    barrier(ws)
+    torch.cuda.synchronize()
+    if flush is None:
+        total_ms, per = time_loop(step, args.steps, stream)
+    else:
+        # per-launch events exclude the flush; the total includes it
+        total_ms, per = time_loop(step_flush, args.steps, stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    kernel_ms = float(np.mean(per))
+    step_ms = total_ms / args.steps if flush is None else kernel_ms
+    step_ms = max_over_ranks(step_ms, ws, device)
+    launches = 1 + (1 if summ["n_mrows"] > 0 else 0)
+
+    # --- single-half runs of the same kernel: prefill TFLOP/s and decode GB/s
+    halves = {}
+    for half in ("p", "d"):
+        hh = inp.p if half == "p" else inp.d
+        if hh.rows == 0:
+            continue
+        import copy
+        sub = copy.copy(inp)
+        empty = copy.copy(inp.d if half == "p" else inp.p)
+        empty.q_indptr = np.zeros(1, np.int32)
+        empty.kv_indptr = np.zeros(1, np.int32)
+        empty.kv_indices = np.zeros(0, np.int32)
+        empty.last_page_len = np.zeros(0, np.int32)
+        if half == "p":
+            sub.d = empty
+        else:
+            sub.p = empty
+        hs = pod.plan_inputs(sub)
+        wss = torch.empty(pod.pod_workspace_size(hs), dtype=torch.uint8, device=device)
+        pod.pod_bind_workspace(hs, wss)
+
+        def step_half(hs=hs, wss=wss, half=half):
+            if half == "p":
+                pod.pod_run(hs, dev["q_p"], dev["kv_p"], None, None, wss, sinks=dev["sinks"],
+                            out_p=out_p, lse_p=lse_p)
+            else:
+                pod.pod_run(hs, None, None, dev["q_d"], dev["kv_d"], wss, sinks=dev["sinks"],
+                            out_d=out_d, lse_d=lse_d)
+
+        for _ in range(3):
+            step_half()
+        torch.cuda.synchronize()
+        n = max(10, args.steps // 2)
+        _, per_h = time_loop(step_half, n, stream)
+        halves[half] = float(np.median(per_h))
+
+    # --- end to end through the public API with host buffers
+    pin = lambda t: t.pin_memory() if t is not None else None
+    hq_p, hq_d = pin(inp.p.q) if inp.p.rows else None, pin(inp.d.q) if inp.d.rows else None
+    ho = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (out_p, lse_p, out_d, lse_d)]
+    h2d = (inp.p.q.numel() + inp.d.q.numel()) * inp.p.q.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in (out_p, lse_p, out_d, lse_d))
+
+    def step_e2e():
+        if hq_p is not None:
+            dev["q_p"].copy_(hq_p, non_blocking=True)
+        if hq_d is not None:
+            dev["q_d"].copy_(hq_d, non_blocking=True)
+        step()
+        for dst, src in zip(ho, (out_p, lse_p, out_d, lse_d)):
+            if src.numel():
+                dst.copy_(src, non_blocking=True)
+
+    for _ in range(3):
+        step_e2e()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms, _ = time_loop(step_e2e, args.steps, stream, per_launch=False)
+    barrier(ws)
+    e2e_step_ms = max_over_ranks(e2e_ms / args.steps, ws, device)
+    clk = clocks.stop()
+    assert pod.pod_read_device_status(h, wsb) == 0
+
+    # --- roofline of the fused kernel
+    peaks = measured_peaks()
+    B = w["p"]["bytes"] + w["d"]["bytes"]
+    F = w["p"]["flops"]
+    t_s = kernel_ms / 1e3
+    t_hbm = B / (peaks["hbm"] * 1e9)
+    t_tc = F / (peaks["tc"] * 1e12)
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": B / t_s / 1e9, "peak": peaks["hbm"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": F / t_s / 1e12, "peak": peaks["tc"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = ncu_traffic(args.workload)
+    roof["peak_source"] = peaks["source"]
+    roof["fused_frac"] = max(t_hbm, t_tc) / t_s
+    roof["algorithmic_bytes_per_launch"] = B
+    roof["algorithmic_prefill_flops_per_launch"] = F
+    extra = {}
+    if "p" in halves:
+        tf = w["p"]["flops"] / (halves["p"] / 1e3) / 1e12
+        extra["prefill_only_us"] = halves["p"] * 1e3
+        extra["prefill_tflops"] = tf
+        extra["prefill_frac_of_measured_bf16"] = tf / peaks["tc"]
+    if "d" in halves:
+        gbs = w["d"]["bytes"] / (halves["d"] / 1e3) / 1e9
+        extra["decode_only_us"] = halves["d"] * 1e3
+        extra["decode_gbs"] = gbs
+        extra["decode_frac_of_measured_hbm"] = gbs / peaks["hbm"]
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        nthreads = os.cpu_count() or 1
+        us, info = oracle_launch_estimate(inp, w, target_s=args.cpu_seconds, nthreads=nthreads)
+        cpu = {"value": us, "unit": "us", "cores": nthreads, "kind": "oracle",
+               "sample": f"{info['pairs']} random (token, head) pairs of both halves "
+                         f"({info['seconds']:.1f} s, fp64), scaled by allowed (row, key) pairs to one launch"}
+
+    value_us = step_ms * 1e3
+    line = {
+        "metric": METRIC, "value": value_us, "unit": "us", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if inp.dtype.__repr__().endswith("bfloat16") else "f16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC[args.workload], "num_qo_heads": H,
+                   "num_kv_heads": inp.num_kv_heads, "head_dim": d, "page_size": inp.page_size,
+                   "prefill_rows": inp.p.rows, "decode_rows": inp.d.rows,
+                   "l2": ("inputs larger than L2" if flush is None else
+                          "L2 flushed (256 MB write) between timed launches"),
+                   "kv_cache_bytes": kv_total, "parallelism": f"replicas x{ws} (independent batches)"},
+        "roofline": roof, "cpu_baseline": cpu,
+        "e2e": {"value": e2e_step_ms * 1e3, "unit": "us", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches * args.steps, "clocks": clk,
+        "plan": {k: summ[k] for k in ("grid", "n_p_ctas", "n_d_ctas", "n_tiles", "n_items",
+                                       "n_groups", "decode_chunk")},
+        "launch_us_median": float(np.median(per)) * 1e3,
+    }
+    line.update(extra)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="c5", choices=["c1", "c2", "c3", "c4", "c5"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+    return run_ours(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,171 @@
+/*
+ * pod.h — C ABI of the GB300 (sm_103a) POD paged-attention library.
+ *
+ * POD ("prefill-on-decode") runs causal prefill attention for one or more
+ * requests and batched decode attention for many in-flight requests in ONE
+ * kernel launch, both reading a paged KV cache with GQA, and returns outputs
+ * plus base-2 LSE for both halves (POD walkthrough, "POD 是什么" and "批量
+ * POD：BatchPODWithPagedKVCacheWrapper 完整示例"; run returns
+ * ((out_p, lse_p), (out_d, lse_d)) per "BatchPOD 的 run 差异").
+ *
+ * Life cycle (POD walkthrough, "plan/run 生命周期"): plan once on the host,
+ * run many times (for example once per transformer layer) with the same page
+ * tables. Every policy (causal, window_left, sm_scale, sinks on/off, dtype) is
+ * fixed at plan time, as the walkthrough's "plan 覆盖" rule does for the decode
+ * side ("Decode 侧参数与'plan 覆盖'行为"); run takes tensors only.
+ *
+ * Conventions shared by every entry point
+ *  - Errors are returned as pod_status codes; nothing aborts or throws.
+ *    pod_last_error() returns a thread-local message for the last failure.
+ *  - Index arrays passed to pod_plan are HOST int32 arrays (read during the
+ *    call only; the caller keeps ownership). Tensor arguments of pod_run are
+ *    DEVICE pointers owned by the caller; the library never frees them.
+ *  - The handle (host memory) is owned by the library until pod_destroy.
+ *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy stream.
+ *
+ * Tensor layouts (all row-major, contiguous)
+ *  - q_p : [p_q_indptr[p_batch], H, d]    q_d : [d_q_indptr[d_batch], H, d]
+ *  - kv_p: [p_num_pages, 2, page_size, Hk, d]   kv_d: [d_num_pages, 2, page_size, Hk, d]
+ *    (NHD paged cache, index 0 = K, 1 = V; POD walkthrough single-request
+ *    docstring example)
+ *  - out_p / out_d: same shape and dtype as q_p / q_d
+ *  - lse_p / lse_d: fp32 [rows, H], base 2 (flashinfer.cudnn page, "LSE 契约")
+ *  - sinks: fp32 [H] or NULL (flashinfer.cudnn page, "Decode 能力矩阵与参数")
+ *  with H = num_qo_heads, Hk = num_kv_heads, d = head_dim.
+ */
+#ifndef POD_GB300_H
+#define POD_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct pod_plan_s* pod_handle;
+
+typedef enum {
+    POD_OK = 0,
+    POD_ERR_INVALID_ARG = 1,    /* inconsistent page tables, heads, lengths */
+    POD_ERR_UNSUPPORTED = 2,    /* head_dim / dtype / group size not built */
+    POD_ERR_WORKSPACE = 3,      /* workspace missing or too small */
+    POD_ERR_CUDA = 4,           /* a CUDA runtime call failed */
+    POD_ERR_DEVICE_STATUS = 5   /* a kernel recorded an error (bounded wait ran out) */
+} pod_status;
+
+typedef enum { POD_F16 = 0, POD_BF16 = 1 } pod_dtype;
+
+/*
+ * pod_plan — host planner (POD walkthrough, "plan 内部做了什么" and "Batch 版本
+ * plan 的 colocated-CTA 调度细节").
+ *
+ * Validates the two page tables, computes kv_len per request
+ * (kv_len = (pages - 1) * page_size + last_page_len), cuts prefill queries
+ * into 128-row tiles (GQA heads of one KV head packed into rows), splits
+ * decode KV ranges into chunks, assigns the work of both halves to the CTAs
+ * of one persistent launch and lays out the workspace.
+ *
+ * Arguments
+ *  p_q_indptr[p_batch+1], p_kv_indptr[p_batch+1], p_kv_indices[p_kv_indptr[p_batch]],
+ *  p_last_page_len[p_batch]: prefill page tables (host int32). Same for d_*.
+ *  p_batch / d_batch may be 0 (that half is empty; its pointers may be NULL).
+ *  p_num_pages / d_num_pages: page-pool sizes; every index must be below them.
+ *  causal: bottom-right diagonal mask on both halves; window_left: -1 = off,
+ *  else keys strictly before the diagonal that stay visible; sm_scale <= 0
+ *  means 1/sqrt(head_dim). dtype: element type of q/kv/out. has_sinks: pod_run
+ *  will receive a sinks array. num_sms: SM count the schedule is built for
+ *  (0 = the current device's); the plan is a pure function of its inputs and
+ *  num_sms.
+ *  workspace / workspace_bytes: device buffer the plan metadata is copied into
+ *  (one cudaMemcpyAsync on `stream`, the only host-to-device copy of the
+ *  library). workspace == NULL plans on the host only: the returned handle can
+ *  be inspected (pod_workspace_size, pod_plan_table) and bound later with
+ *  pod_bind_workspace. Not capturable in a CUDA graph (POD walkthrough,
+ *  "plan/run 生命周期": plan cannot run inside CUDA Graph capture).
+ *  required_workspace_bytes (may be NULL): receives the size the plan needs,
+ *  also when POD_ERR_WORKSPACE is returned.
+ *
+ * Errors: POD_ERR_INVALID_ARG when num_qo_heads % num_kv_heads != 0, an indptr
+ * is not monotone from 0, last_page_len is outside [1, page_size] for a
+ * request with queries, an index is outside the pool, kv_len < q_len under
+ * causal, or kv_len == 0 for a request with queries. POD_ERR_UNSUPPORTED for
+ * head_dim other than 64/128, more than 128 qo heads per KV head, or more
+ * than 32 qo heads per KV head on the decode half. POD_ERR_WORKSPACE when the
+ * workspace is too small. On error *out_handle is NULL.
+ */
+pod_status pod_plan(const int32_t* p_q_indptr, const int32_t* p_kv_indptr,
+                    const int32_t* p_kv_indices, const int32_t* p_last_page_len,
+                    int32_t p_batch, int32_t p_num_pages,
+                    const int32_t* d_q_indptr, const int32_t* d_kv_indptr,
+                    const int32_t* d_kv_indices, const int32_t* d_last_page_len,
+                    int32_t d_batch, int32_t d_num_pages,
+                    int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t page_size, int32_t causal, int32_t window_left,
+                    float sm_scale, pod_dtype dtype, int32_t has_sinks, int32_t num_sms,
+                    void* workspace, size_t workspace_bytes, void* stream,
+                    pod_handle* out_handle, size_t* required_workspace_bytes);
+
+/* Bytes of device workspace the plan needs (0 for a NULL handle). */
+size_t pod_workspace_size(pod_handle h);
+
+/*
+ * pod_bind_workspace — copy a host-only plan's metadata into `workspace`
+ * (device, >= pod_workspace_size bytes) on `stream`. After it, pod_run may be
+ * called with this workspace. Errors: POD_ERR_WORKSPACE, POD_ERR_CUDA.
+ */
+pod_status pod_bind_workspace(pod_handle h, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pod_run — the fused launch (POD walkthrough, "run 的两次'设置'与一次 launch"
+ * and "PDL：让两个任务真正并发").
+ *
+ * Launches the persistent POD kernel (prefill tiles on tcgen05 tensor cores
+ * and split-KV decode on the same grid), then, when the plan split any KV
+ * range, the partial-output/LSE merge kernel chained with programmatic
+ * dependent launch. No host synchronisation; capturable in a CUDA graph.
+ * q_p/kv_p may be NULL when the prefill half is empty (same for the decode
+ * half). lse_p / lse_d may be NULL (LSE not written). sinks must be non-NULL
+ * exactly when the plan has has_sinks. `workspace` must be the buffer the
+ * plan was bound to; it is read and written (plan metadata, split partials,
+ * device status word); calls that share a workspace must not overlap.
+ * Errors: POD_ERR_INVALID_ARG (NULL tensor for a non-empty half, sinks
+ * mismatch, unbound handle), POD_ERR_CUDA (launch failure).
+ */
+pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p,
+                   const void* q_d, const void* kv_d, const float* sinks,
+                   void* workspace, void* out_p, float* lse_p,
+                   void* out_d, float* lse_d, void* stream);
+
+/* Release the handle (host memory only). NULL is accepted. */
+pod_status pod_destroy(pod_handle h);
+
+/* Thread-local message of the last error ("" if none). Valid until the next call. */
+const char* pod_last_error(void);
+
+/*
+ * pod_read_device_status — synchronise `stream`, read and clear the device
+ * status word in `workspace`. *device_status receives 0 when every kernel
+ * finished its work; otherwise a bit mask (1 = a bounded wait of the prefill
+ * pipeline ran out, 2 = shared-memory alignment check failed). Returns
+ * POD_ERR_DEVICE_STATUS when the word was non-zero.
+ */
+pod_status pod_read_device_status(pod_handle h, void* workspace, void* stream,
+                                  int32_t* device_status);
+
+/*
+ * pod_plan_table — host copy of one plan table, for inspection and tests.
+ * which: 0 = summary ints, 1 = prefill tiles, 2 = decode items, 3 = CTA work
+ * offsets, 4 = CTA work list, 5 = merge groups, 6 = p kv_len, 7 = d kv_len.
+ * Copies min(count, capacity) int32 values into `out` (may be NULL to query
+ * *count). Each table's record format is documented beside the planner
+ * (csrc/pod_plan.h in the library sources).
+ */
+pod_status pod_plan_table(pod_handle h, int32_t which, int32_t* out, int64_t capacity,
+                          int64_t* count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* POD_GB300_H */

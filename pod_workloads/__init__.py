@@ -99,7 +99,7 @@ def _randn(gen: torch.Generator, shape, dtype: torch.dtype, chunk: int = 1 << 26
 
 def make_half(gen: torch.Generator, q_lens, kv_lens, H, Hk, d, ps, dtype,
               pages: str = "perm", extra_pages: int = 0,
-              kv_indptr=None, last_page_len=None) -> HalfInputs:
+              kv_indptr=None, last_page_len=None, with_data: bool = True) -> HalfInputs:
     """Build one half. ``pages`` is "perm" (random permutation of the pool),
     "contig" (0..n-1 in order). ``kv_indptr``/``last_page_len`` may be given
     directly (the single-request docstring example prints them)."""
@@ -120,8 +120,12 @@ def make_half(gen: torch.Generator, q_lens, kv_lens, H, Hk, d, ps, dtype,
     q_indptr = np.zeros(len(q_lens) + 1, dtype=np.int64)
     q_indptr[1:] = np.cumsum(q_lens)
     rows = int(q_indptr[-1])
-    q = _randn(gen, (rows, H, d), dtype)
-    kv = _randn(gen, (max(num_pages, 1), 2, ps, Hk, d), dtype)
+    if with_data:
+        q = _randn(gen, (rows, H, d), dtype)
+        kv = _randn(gen, (max(num_pages, 1), 2, ps, Hk, d), dtype)
+    else:   # page tables only (planner tests); tensors are empty placeholders
+        q = torch.empty((0, H, d), dtype=dtype)
+        kv = torch.empty((0, 2, ps, Hk, d), dtype=dtype)
     npg = kv_indptr[1:] - kv_indptr[:-1]
     kv_lens_arr = np.where(npg > 0, (npg - 1) * ps + last_page_len, 0).astype(np.int32)
     return HalfInputs(q_indptr=q_indptr.astype(np.int32), kv_indptr=kv_indptr,
@@ -147,39 +151,43 @@ def make_custom(name, dtype, H, Hk, d, ps, causal, window_left,
                      p=p, d=dd, sinks=s)
 
 
-def make_config(name: str, seed: Optional[int] = None) -> PODInputs:
-    """The five benchmark workloads. Seed defaults to the config index (1..5)."""
+def make_config(name: str, seed: Optional[int] = None, with_data: bool = True) -> PODInputs:
+    """The five benchmark workloads. Seed defaults to the config index (1..5).
+    ``with_data=False`` builds the page tables only (same page ids as with data
+    only for the "contig" workloads, since tensor draws share the generator)."""
     idx = CONFIG_NAMES.index(name) + 1
     gen = torch.Generator().manual_seed(idx if seed is None else int(seed))
+    import functools
+    make_half_l = functools.partial(make_half, with_data=with_data)
     if name == "c1":
         H, Hk, d, ps, dt = 4, 1, 64, 16, torch.float16
-        p = make_half(gen, [64], [64], H, Hk, d, ps, dt, "perm")
-        dd = make_half(gen, [1] * 4, [17, 29, 5, 48], H, Hk, d, ps, dt, "perm")
+        p = make_half_l(gen, [64], [64], H, Hk, d, ps, dt, "perm")
+        dd = make_half_l(gen, [1] * 4, [17, 29, 5, 48], H, Hk, d, ps, dt, "perm")
         return PODInputs(name, dt, H, Hk, d, ps, True, -1, 1.0 / math.sqrt(d), p, dd, None)
     if name == "c2":
         H, Hk, d, ps, dt = 64, 8, 128, 16, torch.float16
-        p = make_half(gen, [1024], [1024], H, Hk, d, ps, dt, "contig")
-        dd = make_half(gen, [1] * 7, None, H, Hk, d, ps, dt, "contig",
+        p = make_half_l(gen, [1024], [1024], H, Hk, d, ps, dt, "contig")
+        dd = make_half_l(gen, [1] * 7, None, H, Hk, d, ps, dt, "contig",
                        kv_indptr=[0, 17, 29, 44, 48, 66, 100, 128],
                        last_page_len=[1, 7, 14, 4, 3, 1, 16])
         return PODInputs(name, dt, H, Hk, d, ps, True, -1, 1.0 / math.sqrt(d), p, dd, None)
     if name == "c3":
         H, Hk, d, ps, dt = 64, 8, 128, 1, torch.bfloat16
-        p = make_half(gen, [2048] * 2, [2048] * 2, H, Hk, d, ps, dt, "contig")
-        dd = make_half(gen, [1] * 128, [2048] * 128, H, Hk, d, ps, dt, "contig")
+        p = make_half_l(gen, [2048] * 2, [2048] * 2, H, Hk, d, ps, dt, "contig")
+        dd = make_half_l(gen, [1] * 128, [2048] * 128, H, Hk, d, ps, dt, "contig")
         return PODInputs(name, dt, H, Hk, d, ps, True, -1, 1.0 / math.sqrt(d), p, dd, None)
     if name == "c4":
         H, Hk, d, ps, dt = 32, 8, 128, 16, torch.bfloat16
         kv_d = torch.randint(512, 16384 + 1, (256,), generator=gen).numpy()
-        p = make_half(gen, [512], [8192], H, Hk, d, ps, dt, "perm")
-        dd = make_half(gen, [1] * 256, kv_d, H, Hk, d, ps, dt, "perm")
+        p = make_half_l(gen, [512], [8192], H, Hk, d, ps, dt, "perm")
+        dd = make_half_l(gen, [1] * 256, kv_d, H, Hk, d, ps, dt, "perm")
         return PODInputs(name, dt, H, Hk, d, ps, True, -1, 1.0 / math.sqrt(d), p, dd, None)
     if name == "c5":
         H, Hk, d, ps, dt = 64, 8, 128, 16, torch.bfloat16
         z = torch.randn(512, generator=gen, dtype=torch.float64).numpy()
         kv_d = np.clip(np.rint(np.exp(math.log(2048.0) + z)), 8, 32768).astype(np.int64)
-        p = make_half(gen, [1000, 3000, 700, 4096], [1000, 3000, 700, 4096], H, Hk, d, ps, dt, "perm")
-        dd = make_half(gen, [4] * 512, kv_d, H, Hk, d, ps, dt, "perm")
+        p = make_half_l(gen, [1000, 3000, 700, 4096], [1000, 3000, 700, 4096], H, Hk, d, ps, dt, "perm")
+        dd = make_half_l(gen, [4] * 512, kv_d, H, Hk, d, ps, dt, "perm")
         sinks = torch.randn(H, generator=gen, dtype=torch.float32)
         return PODInputs(name, dt, H, Hk, d, ps, True, 4096, 1.0 / math.sqrt(d), p, dd, sinks)
     raise ValueError(f"unknown workload {name!r}")

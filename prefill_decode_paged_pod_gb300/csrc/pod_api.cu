@@ -1,0 +1,234 @@
+// pod_api.cu — the extern "C" boundary declared in include/pod.h.
+//
+// Host-side only: argument checks, the planner call, the one metadata upload
+// and the kernel launches. Every step of the attention itself runs in the
+// kernels of pod_kernels.cu.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include <new>
+#include <string>
+
+#include "../../include/pod.h"
+#include "pod_launch.h"
+#include "pod_planner.hpp"
+
+struct pod_plan_s {
+  PodPlanHost plan;
+  void* workspace = nullptr;      // bound device workspace (nullptr = host-only plan)
+  size_t workspace_bytes = 0;
+};
+
+namespace {
+
+thread_local std::string g_err;
+
+pod_status set_err(pod_status code, const std::string& msg) {
+  g_err = msg;
+  return code;
+}
+
+pod_status cuda_err(cudaError_t e, const char* what) {
+  return set_err(POD_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+int log_level() {
+  static int lvl = -1;
+  if (lvl < 0) {
+    const char* s = getenv("POD_LOGLEVEL");
+    lvl = s ? atoi(s) : 0;
+  }
+  return lvl;
+}
+
+pod_status upload(pod_plan_s* h, void* ws, size_t bytes, void* stream) {
+  const PodPlanHost& P = h->plan;
+  if (ws == nullptr || bytes < P.total_bytes)
+    return set_err(POD_ERR_WORKSPACE, "workspace of " + std::to_string(bytes) +
+                                          " bytes is smaller than the plan's " +
+                                          std::to_string(P.total_bytes));
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return set_err(POD_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  cudaError_t e = cudaMemcpyAsync(ws, P.int_image.data(), P.int_image.size(),
+                                  cudaMemcpyHostToDevice, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_err(e, "cudaMemcpyAsync(plan metadata)");
+  // the copy reads pageable host memory owned by the handle: finish it before returning
+  e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_err(e, "cudaStreamSynchronize(plan metadata)");
+  h->workspace = ws;
+  h->workspace_bytes = bytes;
+  return POD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pod_status pod_plan(const int32_t* p_q_indptr, const int32_t* p_kv_indptr,
+                    const int32_t* p_kv_indices, const int32_t* p_last_page_len, int32_t p_batch,
+                    int32_t p_num_pages, const int32_t* d_q_indptr, const int32_t* d_kv_indptr,
+                    const int32_t* d_kv_indices, const int32_t* d_last_page_len, int32_t d_batch,
+                    int32_t d_num_pages, int32_t num_qo_heads, int32_t num_kv_heads,
+                    int32_t head_dim, int32_t page_size, int32_t causal, int32_t window_left,
+                    float sm_scale, pod_dtype dtype, int32_t has_sinks, int32_t num_sms,
+                    void* workspace, size_t workspace_bytes, void* stream,
+                    pod_handle* out_handle, size_t* required_workspace_bytes) {
+  g_err.clear();
+  if (!out_handle) return set_err(POD_ERR_INVALID_ARG, "out_handle is NULL");
+  *out_handle = nullptr;
+  if (required_workspace_bytes) *required_workspace_bytes = 0;
+  if (num_sms <= 0) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_err(e, "cudaGetDevice");
+    e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_err(e, "cudaDeviceGetAttribute(SM count)");
+  }
+  PodPlanArgs a;
+  a.p_q_indptr = p_q_indptr; a.p_kv_indptr = p_kv_indptr; a.p_kv_indices = p_kv_indices;
+  a.p_last_page_len = p_last_page_len; a.p_batch = p_batch; a.p_num_pages = p_num_pages;
+  a.d_q_indptr = d_q_indptr; a.d_kv_indptr = d_kv_indptr; a.d_kv_indices = d_kv_indices;
+  a.d_last_page_len = d_last_page_len; a.d_batch = d_batch; a.d_num_pages = d_num_pages;
+  a.H = num_qo_heads; a.Hk = num_kv_heads; a.d = head_dim; a.ps = page_size;
+  a.causal = causal; a.window_left = window_left; a.sm_scale = sm_scale;
+  a.dtype = (int)dtype; a.has_sinks = has_sinks; a.num_sms = num_sms;
+
+  pod_plan_s* h = new (std::nothrow) pod_plan_s();
+  if (!h) return set_err(POD_ERR_INVALID_ARG, "out of host memory");
+  std::string err;
+  int rc = pod_build_plan(a, h->plan, &err);
+  if (rc != 0) {
+    delete h;
+    return set_err((pod_status)rc, err);
+  }
+  if (required_workspace_bytes) *required_workspace_bytes = h->plan.total_bytes;
+  if (workspace != nullptr) {
+    pod_status st = upload(h, workspace, workspace_bytes, stream);
+    if (st != POD_OK) {
+      delete h;
+      return st;
+    }
+  }
+  if (log_level() >= 1) {
+    const PodPlanHost& P = h->plan;
+    fprintf(stderr,
+            "[pod] plan: H=%d Hk=%d d=%d ps=%d causal=%d window=%d | prefill rows=%d tiles=%zu "
+            "ctas=%d | decode rows=%d items=%zu ctas=%d chunk=%d | merge rows=%d | workspace=%zu B\n",
+            P.H, P.Hk, P.d, P.ps, P.causal, P.window_left, P.p.rows, P.ptiles.size() / POD_REC,
+            P.n_p_ctas, P.dd.rows, P.ditems.size() / POD_REC, P.n_d_ctas, P.decode_chunk,
+            P.n_mrows, P.total_bytes);
+  }
+  *out_handle = h;
+  return POD_OK;
+}
+
+size_t pod_workspace_size(pod_handle h) { return h ? h->plan.total_bytes : 0; }
+
+pod_status pod_bind_workspace(pod_handle h, void* workspace, size_t workspace_bytes, void* stream) {
+  g_err.clear();
+  if (!h) return set_err(POD_ERR_INVALID_ARG, "handle is NULL");
+  return upload(h, workspace, workspace_bytes, stream);
+}
+
+pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* q_d,
+                   const void* kv_d, const float* sinks, void* workspace, void* out_p,
+                   float* lse_p, void* out_d, float* lse_d, void* stream) {
+  g_err.clear();
+  if (!h) return set_err(POD_ERR_INVALID_ARG, "handle is NULL");
+  const PodPlanHost& P = h->plan;
+  if (!h->workspace) return set_err(POD_ERR_WORKSPACE, "the plan has no bound workspace");
+  if (workspace != h->workspace)
+    return set_err(POD_ERR_WORKSPACE, "workspace differs from the one the plan was bound to");
+  if (P.p.rows > 0 && (!q_p || !kv_p || !out_p))
+    return set_err(POD_ERR_INVALID_ARG, "prefill half is non-empty but q_p/kv_p/out_p is NULL");
+  if (P.dd.rows > 0 && (!q_d || !kv_d || !out_d))
+    return set_err(POD_ERR_INVALID_ARG, "decode half is non-empty but q_d/kv_d/out_d is NULL");
+  if (P.has_sinks && !sinks) return set_err(POD_ERR_INVALID_ARG, "plan has sinks but sinks is NULL");
+  if (!P.has_sinks && sinks)
+    return set_err(POD_ERR_INVALID_ARG, "sinks given but the plan was made without sinks");
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  PodParams K;
+  K.H = P.H; K.Hk = P.Hk; K.G = P.G; K.d = P.d; K.ps = P.ps;
+  K.ps_shift = -1;
+  for (int s = 0; s < 31; ++s)
+    if ((1 << s) == P.ps) K.ps_shift = s;
+  K.causal = P.causal; K.window_left = P.window_left; K.has_sinks = P.has_sinks;
+  K.scale_log2 = P.scale_log2;
+  K.n_p_ctas = P.n_p_ctas; K.grid = P.grid;
+  K.n_groups = (int)(P.mgroups.size() / POD_REC); K.n_mrows = P.n_mrows;
+  K.p_batch = P.p.batch; K.d_batch = P.dd.batch;
+  auto I = [&](size_t off) { return reinterpret_cast<const int32_t*>(ws + off); };
+  K.p_q_indptr = I(P.off_p_q_indptr); K.p_kv_indptr = I(P.off_p_kv_indptr);
+  K.p_kv_indices = I(P.off_p_kv_indices); K.p_kv_len = I(P.off_p_kv_len);
+  K.d_q_indptr = I(P.off_d_q_indptr); K.d_kv_indptr = I(P.off_d_kv_indptr);
+  K.d_kv_indices = I(P.off_d_kv_indices); K.d_kv_len = I(P.off_d_kv_len);
+  K.ptiles = I(P.off_ptiles); K.ditems = I(P.off_ditems);
+  K.cta_ptr = I(P.off_cta_ptr); K.cta_list = I(P.off_cta_list);
+  K.mgroups = I(P.off_mgroups); K.mrow_ptr = I(P.off_mrow_ptr);
+  K.part_o = reinterpret_cast<float*>(ws + P.off_part_o);
+  K.part_lse = reinterpret_cast<float*>(ws + P.off_part_lse);
+  K.status = reinterpret_cast<int32_t*>(ws + P.off_status);
+  K.q_p = q_p; K.kv_p = kv_p; K.q_d = q_d; K.kv_d = kv_d; K.sinks = sinks;
+  K.out_p = out_p; K.out_d = out_d; K.lse_p = lse_p; K.lse_d = lse_d;
+
+  cudaError_t e = pod_launch(K, P.dtype, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_err(e, "kernel launch");
+  return POD_OK;
+}
+
+pod_status pod_destroy(pod_handle h) {
+  delete h;
+  return POD_OK;
+}
+
+const char* pod_last_error(void) { return g_err.c_str(); }
+
+pod_status pod_read_device_status(pod_handle h, void* workspace, void* stream,
+                                  int32_t* device_status) {
+  g_err.clear();
+  if (!h || !workspace) return set_err(POD_ERR_INVALID_ARG, "handle or workspace is NULL");
+  int32_t v = 0;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = cudaMemcpyAsync(&v, ws + h->plan.off_status, sizeof(v), cudaMemcpyDeviceToHost,
+                                  (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_err(e, "cudaMemcpyAsync(status)");
+  e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_err(e, "cudaStreamSynchronize(status)");
+  if (device_status) *device_status = v;
+  if (v != 0) {
+    e = cudaMemsetAsync(ws + h->plan.off_status, 0, sizeof(v), (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_err(e, "cudaMemsetAsync(status)");
+    return set_err(POD_ERR_DEVICE_STATUS, "a kernel recorded device status " + std::to_string(v));
+  }
+  return POD_OK;
+}
+
+pod_status pod_plan_table(pod_handle h, int32_t which, int32_t* out, int64_t capacity,
+                          int64_t* count) {
+  g_err.clear();
+  if (!h) return set_err(POD_ERR_INVALID_ARG, "handle is NULL");
+  const PodPlanHost& P = h->plan;
+  const std::vector<int32_t>* v = nullptr;
+  switch (which) {
+    case 0: v = &P.summary; break;
+    case 1: v = &P.ptiles; break;
+    case 2: v = &P.ditems; break;
+    case 3: v = &P.cta_ptr; break;
+    case 4: v = &P.cta_list; break;
+    case 5: v = &P.mgroups; break;
+    case 6: v = &P.p.kv_len; break;
+    case 7: v = &P.dd.kv_len; break;
+    default: return set_err(POD_ERR_INVALID_ARG, "unknown plan table");
+  }
+  if (count) *count = (int64_t)v->size();
+  if (out) {
+    int64_t n = (int64_t)v->size() < capacity ? (int64_t)v->size() : capacity;
+    for (int64_t i = 0; i < n; ++i) out[i] = (*v)[i];
+  }
+  return POD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,57 @@
+// pod_plan.h — plan records shared by the host planner and the CUDA kernels.
+//
+// The plan is the "auxiliary data structure built once and reused by every
+// run" of the POD walkthrough ("plan/run 生命周期"). Every table is int32 and
+// lives, on the device, in the integer part of the caller's workspace.
+//
+// Record formats (POD_REC = 8 int32 per record)
+//   prefill tile  : req, kv_head, tok0, ntok, kv_lo, kv_hi, prow, 0
+//                   rows of the tile = ntok tokens x G qo heads (token-major),
+//                   keys [kv_lo, kv_hi) of request `req`; prow = first partial
+//                   row when the tile writes a split partial, -1 when it writes
+//                   the final output.
+//   decode item   : req, kv_head, tok0, ntok, k0, k1, prow, 0
+//                   keys [k0, k1) of one (request, kv head, token group).
+//   merge group   : half (0 prefill, 1 decode), req, kv_head, tok0, ntok,
+//                   prow0, nsplit, R   with R = ntok * G; split j, row r of the
+//                   group is partial row prow0 + j * R + r.
+//   cta_ptr[grid+1], cta_list[]: CTA c runs the records cta_list[cta_ptr[c] ..
+//                   cta_ptr[c+1]) — prefill tiles when c < n_prefill_ctas,
+//                   decode items otherwise.
+//   mrow_ptr[n_groups+1]: prefix sums of R over merge groups.
+//   summary (pod_plan_table which = 0): see PodSummary below.
+#pragma once
+#include <stdint.h>
+
+#define POD_REC 8
+#define POD_TILE_ROWS 128      // prefill tile rows (tcgen05 M)
+#define POD_KBLOCK 64          // keys per prefill KV block
+#define POD_DECODE_ROWS 32     // max rows of a decode item (2 mma.sync m16 tiles)
+#define POD_DECODE_STAGE 64    // keys per decode pipeline stage
+#define POD_CTAS_PER_SM 2
+
+enum PodSummary {
+  S_H = 0, S_HK, S_D, S_PS, S_CAUSAL, S_WINDOW, S_DTYPE, S_SINKS, S_NUM_SMS, S_GRID,
+  S_NP_CTAS, S_ND_CTAS, S_NTILES, S_NITEMS, S_NGROUPS, S_NMROWS, S_NPROWS,
+  S_P_ROWS, S_D_ROWS, S_P_BATCH, S_D_BATCH, S_DECODE_CHUNK, S_WS_LO, S_WS_HI,
+  S_COUNT
+};
+
+// Everything a kernel needs, passed by value at launch.
+struct PodParams {
+  int H, Hk, G, d, ps, ps_shift, causal, window_left, has_sinks;
+  float scale_log2;          // sm_scale * log2(e)
+  int n_p_ctas, grid;
+  int n_groups, n_mrows;
+  int p_batch, d_batch;
+  const int32_t *p_q_indptr, *p_kv_indptr, *p_kv_indices, *p_kv_len;
+  const int32_t *d_q_indptr, *d_kv_indptr, *d_kv_indices, *d_kv_len;
+  const int32_t *ptiles, *ditems, *cta_ptr, *cta_list, *mgroups, *mrow_ptr;
+  float* part_o;             // [n_prows, d]
+  float* part_lse;           // [n_prows]
+  int32_t* status;           // device status word
+  const void *q_p, *kv_p, *q_d, *kv_d;
+  const float* sinks;
+  void *out_p, *out_d;
+  float *lse_p, *lse_d;
+};

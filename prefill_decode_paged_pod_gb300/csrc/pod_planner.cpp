@@ -1,0 +1,445 @@
+// pod_planner.cpp — host-side POD planner.
+//
+// What the POD walkthrough's plan does ("plan 内部做了什么"): read the page
+// tables on the host, derive each request's kv_len (get_seq_lens), and build
+// the auxiliary structures every later run reuses. The batch wrapper plans the
+// decode side first and decides from it how CTAs are shared with prefill
+// ("Batch 版本 plan 的 colocated-CTA 调度细节", with the 1536-prefill-row cutoff).
+//
+// This planner does the same job for one persistent sm_103a launch:
+//  1. validate both halves and compute kv_len / q_len;
+//  2. cut prefill queries into 128-row tiles (ntok tokens x G qo heads of one
+//     KV head) and trim each tile's key range by the causal diagonal and the
+//     window;
+//  3. cut decode queries into units of at most 32 rows and split each unit's
+//     key range into chunks whose size is searched to balance the decode CTAs;
+//  4. choose how many CTAs run prefill tiles and how many run decode items so
+//     that both halves are predicted to finish together, and assign the work
+//     with longest-processing-time-first list scheduling;
+//  5. lay out the workspace: metadata (uploaded once) then split partials.
+// Everything is a deterministic function of the inputs and num_sms.
+#include "pod_planner.hpp"
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <functional>
+#include <queue>
+#include <utility>
+
+namespace {
+
+constexpr int kInvalid = 1, kUnsupported = 2;
+
+// ---- cost model (nanoseconds); constants calibrated on GB300 -------------
+struct CostModel {
+  double p_block_ns;     // one 64-key block of one 128-row prefill tile, one CTA
+  double p_tile_ns;      // per-tile setup + epilogue
+  double p_flops_per_s;  // whole-GPU prefill rate floor
+  double d_key_ns;       // one key (K+V rows) of one decode item, one CTA
+  double d_item_ns;      // per-item setup, pipeline drain and partial write
+  double d_bytes_per_s;  // whole-GPU HBM rate floor
+};
+
+CostModel cost_model(int d) {
+  CostModel c;
+  c.p_block_ns = 420.0 + 730.0 * d / 128.0;
+  c.p_tile_ns = 1500.0;
+  c.p_flops_per_s = 1.10e15;
+  c.d_key_ns = (4.0 * d) / 40.0;      // 2 rows x d x 2 B at ~40 GB/s per CTA
+  c.d_item_ns = 2500.0;
+  c.d_bytes_per_s = 5.6e12;
+  return c;
+}
+
+int fail(std::string* err, int code, const std::string& msg) {
+  if (err) *err = msg;
+  return code;
+}
+
+int load_half(const char* name, const int32_t* q_indptr, const int32_t* kv_indptr,
+              const int32_t* kv_indices, const int32_t* last, int batch, int num_pages, int ps,
+              int causal, PodHalfHost& h, std::string* err) {
+  std::string n(name);
+  if (batch < 0) return fail(err, kInvalid, n + "_batch < 0");
+  h.batch = batch;
+  h.num_pages = num_pages;
+  h.q_indptr.assign(1, 0);
+  h.kv_indptr.assign(1, 0);
+  h.kv_indices.clear();
+  h.last_page_len.clear();
+  h.kv_len.clear();
+  h.q_len.clear();
+  h.rows = 0;
+  if (batch == 0) return 0;
+  if (!q_indptr || !kv_indptr || !last)
+    return fail(err, kInvalid, n + ": NULL page-table pointer for a non-empty half");
+  if (q_indptr[0] != 0 || kv_indptr[0] != 0)
+    return fail(err, kInvalid, n + ": q_indptr[0] and kv_indptr[0] must be 0");
+  h.q_indptr.assign(q_indptr, q_indptr + batch + 1);
+  h.kv_indptr.assign(kv_indptr, kv_indptr + batch + 1);
+  h.last_page_len.assign(last, last + batch);
+  for (int r = 0; r < batch; ++r) {
+    if (q_indptr[r + 1] < q_indptr[r]) return fail(err, kInvalid, n + "_q_indptr is not monotone");
+    if (kv_indptr[r + 1] < kv_indptr[r]) return fail(err, kInvalid, n + "_kv_indptr is not monotone");
+  }
+  int64_t npages_total = kv_indptr[batch];
+  if (npages_total > 0) {
+    if (!kv_indices) return fail(err, kInvalid, n + "_kv_indices is NULL");
+    h.kv_indices.assign(kv_indices, kv_indices + npages_total);
+    for (int64_t i = 0; i < npages_total; ++i)
+      if (kv_indices[i] < 0 || kv_indices[i] >= num_pages)
+        return fail(err, kInvalid, n + "_kv_indices[" + std::to_string(i) + "] = " +
+                                       std::to_string(kv_indices[i]) + " is outside the page pool of " +
+                                       std::to_string(num_pages));
+  }
+  h.kv_len.resize(batch);
+  h.q_len.resize(batch);
+  for (int r = 0; r < batch; ++r) {
+    int64_t ql = (int64_t)q_indptr[r + 1] - q_indptr[r];
+    int64_t np = (int64_t)kv_indptr[r + 1] - kv_indptr[r];
+    int64_t kl = 0;
+    if (np > 0) {
+      if (last[r] < 1 || last[r] > ps)
+        return fail(err, kInvalid, n + "_last_page_len[" + std::to_string(r) + "] = " +
+                                       std::to_string(last[r]) + " is outside [1, page_size]");
+      kl = (np - 1) * (int64_t)ps + last[r];
+    }
+    if (kl > INT32_MAX) return fail(err, kInvalid, n + ": kv_len overflows int32");
+    if (ql > 0 && kl == 0)
+      return fail(err, kInvalid, n + ": request " + std::to_string(r) + " has queries but no keys");
+    if (ql > 0 && causal && kl < ql)
+      return fail(err, kInvalid, n + ": request " + std::to_string(r) +
+                                     " has kv_len < q_len under the causal mask");
+    h.kv_len[r] = (int32_t)kl;
+    h.q_len[r] = (int32_t)ql;
+  }
+  h.rows = q_indptr[batch];
+  return 0;
+}
+
+// Key range [lo, hi) needed by the query tokens [t0, t0 + ntok) of a request:
+// bottom-right diagonal p = kv_len - q_len + i, window keeps t >= p - window_left.
+void key_range(int kv_len, int q_len, int t0, int ntok, int causal, int window_left, int* lo,
+               int* hi) {
+  int64_t p_first = (int64_t)kv_len - q_len + t0;
+  int64_t p_last = p_first + ntok - 1;
+  int64_t h = kv_len;
+  if (causal) h = std::min<int64_t>(kv_len, p_last + 1);
+  int64_t l = 0;
+  if (window_left >= 0) l = std::max<int64_t>(0, p_first - window_left);
+  if (l > h) l = h;
+  *lo = (int)l;
+  *hi = (int)h;
+}
+
+int64_t nblocks(int lo, int hi) {
+  int64_t b0 = (int64_t)(lo / POD_KBLOCK) * POD_KBLOCK;
+  return (hi - b0 + POD_KBLOCK - 1) / POD_KBLOCK;
+}
+
+// Longest-processing-time-first list scheduling. Returns the makespan and, if
+// `assign` is given, the CTA of each job. Ties: larger cost first, then lower
+// job index; the least-loaded CTA with the lowest index wins.
+double lpt(const std::vector<double>& cost, int n_cta, std::vector<int>* order,
+           std::vector<int>* assign) {
+  if (n_cta <= 0 || cost.empty()) return 0.0;
+  std::vector<int> idx(cost.size());
+  for (size_t i = 0; i < idx.size(); ++i) idx[i] = (int)i;
+  std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return cost[a] > cost[b]; });
+  typedef std::pair<double, int> Slot;
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int c = 0; c < n_cta; ++c) heap.push(Slot(0.0, c));
+  if (assign) assign->assign(cost.size(), -1);
+  double makespan = 0.0;
+  for (int j : idx) {
+    Slot s = heap.top();
+    heap.pop();
+    s.first += cost[j];
+    makespan = std::max(makespan, s.first);
+    if (assign) (*assign)[j] = s.second;
+    heap.push(s);
+  }
+  if (order) *order = idx;
+  return makespan;
+}
+
+struct DecodeUnit {
+  int req, kv_head, tok0, ntok, lo, hi;
+};
+
+// Split [lo, hi) into ceil(len / chunk) nearly equal chunks with inner
+// boundaries on multiples of 64 keys.
+void split_range(int lo, int hi, int chunk, std::vector<std::pair<int, int>>& out) {
+  out.clear();
+  int64_t len = hi - lo;
+  if (chunk <= 0 || len <= chunk) {
+    out.push_back({lo, hi});
+    return;
+  }
+  int64_t n = (len + chunk - 1) / chunk;
+  int prev = lo;
+  for (int64_t j = 1; j < n; ++j) {
+    int64_t b = lo + (j * len) / n;
+    b = (b / POD_DECODE_STAGE) * POD_DECODE_STAGE;
+    if (b <= prev || b >= hi) continue;
+    out.push_back({prev, (int)b});
+    prev = (int)b;
+  }
+  out.push_back({prev, hi});
+}
+
+struct DecodeChoice {
+  double time = 0.0;
+  int chunk = 0;
+};
+
+double decode_time(const std::vector<DecodeUnit>& units, int n_cta, int chunk, int G, int d,
+                   const CostModel& cm, double total_bytes) {
+  std::vector<double> cost;
+  std::vector<std::pair<int, int>> parts;
+  double split_bytes = 0.0;
+  for (const DecodeUnit& u : units) {
+    split_range(u.lo, u.hi, chunk, parts);
+    for (auto& pr : parts) cost.push_back(cm.d_item_ns + cm.d_key_ns * (pr.second - pr.first));
+    if (parts.size() > 1) split_bytes += (double)parts.size() * u.ntok * G * (d + 1) * 4.0 * 2.0;
+  }
+  double t = lpt(cost, n_cta, nullptr, nullptr);
+  t = std::max(t, 1e9 * total_bytes / cm.d_bytes_per_s);
+  if (split_bytes > 0) t += 3000.0 + 1e9 * split_bytes / cm.d_bytes_per_s;
+  return t;
+}
+
+DecodeChoice best_decode(const std::vector<DecodeUnit>& units, int n_cta, int G, int d,
+                         const CostModel& cm, double total_bytes) {
+  DecodeChoice best;
+  best.time = -1.0;
+  // 0 = no split; then 16 Ki .. 256 keys
+  const int cands[] = {0, 16384, 8192, 4096, 2048, 1024, 512, 256};
+  for (int c : cands) {
+    double t = decode_time(units, n_cta, c, G, d, cm, total_bytes);
+    if (best.time < 0 || t < best.time * (1.0 - 1e-9)) {
+      best.time = t;
+      best.chunk = c;
+    }
+  }
+  return best;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
+  if (a.H <= 0 || a.Hk <= 0) return fail(err, kInvalid, "num_qo_heads and num_kv_heads must be positive");
+  if (a.H % a.Hk != 0)
+    return fail(err, kInvalid, "num_qo_heads must be a multiple of num_kv_heads");
+  if (a.ps <= 0) return fail(err, kInvalid, "page_size must be positive");
+  if (a.d != 64 && a.d != 128) return fail(err, kUnsupported, "head_dim must be 64 or 128");
+  if (a.dtype != 0 && a.dtype != 1) return fail(err, kUnsupported, "dtype must be fp16 or bf16");
+  if (a.window_left < -1) return fail(err, kInvalid, "window_left must be -1 or >= 0");
+  if (a.num_sms <= 0) return fail(err, kInvalid, "num_sms must be positive");
+  const int G = a.H / a.Hk;
+  if (G > POD_TILE_ROWS) return fail(err, kUnsupported, "more than 128 qo heads per kv head");
+
+  P.H = a.H; P.Hk = a.Hk; P.G = G; P.d = a.d; P.ps = a.ps;
+  P.causal = a.causal ? 1 : 0; P.window_left = a.window_left;
+  P.dtype = a.dtype; P.has_sinks = a.has_sinks ? 1 : 0; P.num_sms = a.num_sms;
+  P.sm_scale = a.sm_scale > 0.f ? a.sm_scale : (float)(1.0 / std::sqrt((double)a.d));
+  P.scale_log2 = (float)((double)P.sm_scale * 1.4426950408889634);
+
+  int rc = load_half("p", a.p_q_indptr, a.p_kv_indptr, a.p_kv_indices, a.p_last_page_len,
+                     a.p_batch, a.p_num_pages, a.ps, P.causal, P.p, err);
+  if (rc) return rc;
+  rc = load_half("d", a.d_q_indptr, a.d_kv_indptr, a.d_kv_indices, a.d_last_page_len, a.d_batch,
+                 a.d_num_pages, a.ps, P.causal, P.dd, err);
+  if (rc) return rc;
+  if (P.dd.rows > 0 && G > POD_DECODE_ROWS)
+    return fail(err, kUnsupported, "more than 32 qo heads per kv head on the decode half");
+
+  const CostModel cm = cost_model(a.d);
+
+  // ---- prefill tiles --------------------------------------------------------
+  const int Tq = std::max(1, POD_TILE_ROWS / G);
+  P.ptiles.clear();
+  std::vector<double> tile_cost;
+  double p_flops = 0.0;
+  for (int r = 0; r < P.p.batch; ++r) {
+    int ql = P.p.q_len[r], kl = P.p.kv_len[r];
+    for (int t0 = 0; t0 < ql; t0 += Tq) {
+      int nt = std::min(Tq, ql - t0);
+      int lo, hi;
+      key_range(kl, ql, t0, nt, P.causal, P.window_left, &lo, &hi);
+      for (int g = 0; g < P.Hk; ++g) {
+        int32_t rec[POD_REC] = {r, g, t0, nt, lo, hi, -1, 0};
+        P.ptiles.insert(P.ptiles.end(), rec, rec + POD_REC);
+        tile_cost.push_back(cm.p_tile_ns + cm.p_block_ns * (double)nblocks(lo, hi));
+        p_flops += 4.0 * a.d * (double)nt * G * (double)(hi - lo);
+      }
+    }
+  }
+  const int n_tiles = (int)tile_cost.size();
+
+  // ---- decode units ---------------------------------------------------------
+  const int Tu = std::max(1, POD_DECODE_ROWS / G);
+  std::vector<DecodeUnit> units;
+  double d_bytes = 0.0;
+  for (int r = 0; r < P.dd.batch; ++r) {
+    int ql = P.dd.q_len[r], kl = P.dd.kv_len[r];
+    for (int t0 = 0; t0 < ql; t0 += Tu) {
+      int nt = std::min(Tu, ql - t0);
+      int lo, hi;
+      key_range(kl, ql, t0, nt, P.causal, P.window_left, &lo, &hi);
+      for (int g = 0; g < P.Hk; ++g) {
+        units.push_back({r, g, t0, nt, lo, hi});
+        d_bytes += 4.0 * a.d * (double)(hi - lo);
+      }
+    }
+  }
+
+  // ---- CTA split between the halves ----------------------------------------
+  const int grid_max = a.num_sms * POD_CTAS_PER_SM;
+  int n_p = 0;
+  if (n_tiles > 0 && units.empty()) {
+    n_p = std::min(grid_max, n_tiles);
+  } else if (n_tiles > 0) {
+    auto t_p = [&](int n) {
+      return std::max(lpt(tile_cost, n, nullptr, nullptr), 1e9 * p_flops / cm.p_flops_per_s);
+    };
+    auto t_d = [&](int n) { return best_decode(units, n, G, a.d, cm, d_bytes).time; };
+    int lo = 1, hi = std::max(1, std::min(grid_max - 1, n_tiles));
+    // smallest n_p whose prefill time fits under the decode time of the rest
+    while (lo < hi) {
+      int mid = (lo + hi) / 2;
+      if (t_p(mid) <= t_d(grid_max - mid)) hi = mid; else lo = mid + 1;
+    }
+    n_p = lo;
+    if (n_p > 1) {
+      double a1 = std::max(t_p(n_p), t_d(grid_max - n_p));
+      double a0 = std::max(t_p(n_p - 1), t_d(grid_max - n_p + 1));
+      if (a0 < a1) n_p = n_p - 1;
+    }
+  }
+  int n_d_max = grid_max - n_p;
+  int chunk = 0;
+  if (!units.empty()) {
+    if (n_d_max <= 0) { n_p = grid_max - 1; n_d_max = 1; }
+    chunk = best_decode(units, n_d_max, G, a.d, cm, d_bytes).chunk;
+  }
+
+  // ---- decode items, partial rows, merge groups -------------------------------
+  P.ditems.clear();
+  P.mgroups.clear();
+  P.mrow_ptr.assign(1, 0);
+  std::vector<double> item_cost;
+  int n_prows = 0;
+  std::vector<std::pair<int, int>> parts;
+  for (const DecodeUnit& u : units) {
+    split_range(u.lo, u.hi, chunk, parts);
+    const int R = u.ntok * G;
+    int prow0 = -1;
+    if (parts.size() > 1) {
+      prow0 = n_prows;
+      n_prows += (int)parts.size() * R;
+      int32_t g[POD_REC] = {1, u.req, u.kv_head, u.tok0, u.ntok, prow0, (int)parts.size(), R};
+      P.mgroups.insert(P.mgroups.end(), g, g + POD_REC);
+      P.mrow_ptr.push_back(P.mrow_ptr.back() + R);
+    }
+    for (size_t j = 0; j < parts.size(); ++j) {
+      int prow = prow0 < 0 ? -1 : prow0 + (int)j * R;
+      int32_t rec[POD_REC] = {u.req, u.kv_head, u.tok0, u.ntok, parts[j].first, parts[j].second,
+                              prow, 0};
+      P.ditems.insert(P.ditems.end(), rec, rec + POD_REC);
+      item_cost.push_back(cm.d_item_ns + cm.d_key_ns * (parts[j].second - parts[j].first));
+    }
+  }
+  const int n_items = (int)item_cost.size();
+  int n_d = std::min(n_d_max, n_items);
+  if (n_items == 0) n_d = 0;
+  P.n_p_ctas = n_p;
+  P.n_d_ctas = n_d;
+  P.grid = n_p + n_d;
+  P.decode_chunk = chunk;
+  P.n_prows = n_prows;
+  P.n_mrows = P.mrow_ptr.back();
+
+  // ---- per-CTA work lists -----------------------------------------------------
+  P.cta_ptr.assign(P.grid + 1, 0);
+  P.cta_list.clear();
+  {
+    std::vector<int> order, assign;
+    std::vector<std::vector<int>> lists(P.grid);
+    if (n_p > 0) {
+      lpt(tile_cost, n_p, &order, &assign);
+      for (int j : order) lists[assign[j]].push_back(j);
+    }
+    if (n_d > 0) {
+      lpt(item_cost, n_d, &order, &assign);
+      for (int j : order) lists[n_p + assign[j]].push_back(j);
+    }
+    for (int c = 0; c < P.grid; ++c) {
+      P.cta_ptr[c] = (int32_t)P.cta_list.size();
+      P.cta_list.insert(P.cta_list.end(), lists[c].begin(), lists[c].end());
+    }
+    P.cta_ptr[P.grid] = (int32_t)P.cta_list.size();
+  }
+
+  // ---- workspace layout -----------------------------------------------------------
+  size_t off = 0;
+  auto place = [&](size_t n_int32) {
+    size_t o = off;
+    off = align_up(off + std::max<size_t>(n_int32, 1) * 4, 16);
+    return o;
+  };
+  P.off_status = place(64);
+  P.off_p_q_indptr = place(P.p.q_indptr.size());
+  P.off_p_kv_indptr = place(P.p.kv_indptr.size());
+  P.off_p_kv_indices = place(P.p.kv_indices.size());
+  P.off_p_kv_len = place(P.p.kv_len.size());
+  P.off_d_q_indptr = place(P.dd.q_indptr.size());
+  P.off_d_kv_indptr = place(P.dd.kv_indptr.size());
+  P.off_d_kv_indices = place(P.dd.kv_indices.size());
+  P.off_d_kv_len = place(P.dd.kv_len.size());
+  P.off_ptiles = place(P.ptiles.size());
+  P.off_ditems = place(P.ditems.size());
+  P.off_cta_ptr = place(P.cta_ptr.size());
+  P.off_cta_list = place(P.cta_list.size());
+  P.off_mgroups = place(P.mgroups.size());
+  P.off_mrow_ptr = place(P.mrow_ptr.size());
+  P.int_bytes = align_up(off, 256);
+  P.off_part_o = P.int_bytes;
+  P.off_part_lse = align_up(P.off_part_o + (size_t)n_prows * a.d * 4, 256);
+  P.total_bytes = align_up(P.off_part_lse + (size_t)std::max(n_prows, 1) * 4, 256);
+
+  P.int_image.assign(P.int_bytes, 0);
+  auto put = [&](size_t o, const std::vector<int32_t>& v) {
+    if (!v.empty()) std::memcpy(P.int_image.data() + o, v.data(), v.size() * 4);
+  };
+  put(P.off_p_q_indptr, P.p.q_indptr);
+  put(P.off_p_kv_indptr, P.p.kv_indptr);
+  put(P.off_p_kv_indices, P.p.kv_indices);
+  put(P.off_p_kv_len, P.p.kv_len);
+  put(P.off_d_q_indptr, P.dd.q_indptr);
+  put(P.off_d_kv_indptr, P.dd.kv_indptr);
+  put(P.off_d_kv_indices, P.dd.kv_indices);
+  put(P.off_d_kv_len, P.dd.kv_len);
+  put(P.off_ptiles, P.ptiles);
+  put(P.off_ditems, P.ditems);
+  put(P.off_cta_ptr, P.cta_ptr);
+  put(P.off_cta_list, P.cta_list);
+  put(P.off_mgroups, P.mgroups);
+  put(P.off_mrow_ptr, P.mrow_ptr);
+
+  P.summary.assign(S_COUNT, 0);
+  int32_t* s = P.summary.data();
+  s[S_H] = P.H; s[S_HK] = P.Hk; s[S_D] = P.d; s[S_PS] = P.ps; s[S_CAUSAL] = P.causal;
+  s[S_WINDOW] = P.window_left; s[S_DTYPE] = P.dtype; s[S_SINKS] = P.has_sinks;
+  s[S_NUM_SMS] = P.num_sms; s[S_GRID] = P.grid; s[S_NP_CTAS] = P.n_p_ctas;
+  s[S_ND_CTAS] = P.n_d_ctas; s[S_NTILES] = n_tiles; s[S_NITEMS] = n_items;
+  s[S_NGROUPS] = (int32_t)(P.mgroups.size() / POD_REC); s[S_NMROWS] = P.n_mrows;
+  s[S_NPROWS] = P.n_prows; s[S_P_ROWS] = P.p.rows; s[S_D_ROWS] = P.dd.rows;
+  s[S_P_BATCH] = P.p.batch; s[S_D_BATCH] = P.dd.batch; s[S_DECODE_CHUNK] = chunk;
+  s[S_WS_LO] = (int32_t)(P.total_bytes & 0x7fffffff);
+  s[S_WS_HI] = (int32_t)(P.total_bytes >> 31);
+  return 0;
+}

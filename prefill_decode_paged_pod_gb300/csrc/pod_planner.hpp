@@ -1,0 +1,47 @@
+// pod_planner.hpp — host-side POD planner (no CUDA dependency).
+#pragma once
+#include <stddef.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "pod_plan.h"
+
+struct PodHalfHost {
+  int batch = 0, num_pages = 0, rows = 0;
+  std::vector<int32_t> q_indptr, kv_indptr, kv_indices, last_page_len, kv_len, q_len;
+};
+
+struct PodPlanHost {
+  // configuration
+  int H = 0, Hk = 0, G = 0, d = 0, ps = 0, causal = 0, window_left = -1, dtype = 0,
+      has_sinks = 0, num_sms = 0;
+  float sm_scale = 0.f, scale_log2 = 0.f;
+  PodHalfHost p, dd;
+  // schedule
+  int grid = 0, n_p_ctas = 0, n_d_ctas = 0, decode_chunk = 0;
+  std::vector<int32_t> ptiles, ditems, cta_ptr, cta_list, mgroups, mrow_ptr;
+  int n_prows = 0, n_mrows = 0;
+  // workspace layout (byte offsets from the workspace base)
+  size_t off_status = 0, off_p_q_indptr = 0, off_p_kv_indptr = 0, off_p_kv_indices = 0,
+         off_p_kv_len = 0, off_d_q_indptr = 0, off_d_kv_indptr = 0, off_d_kv_indices = 0,
+         off_d_kv_len = 0, off_ptiles = 0, off_ditems = 0, off_cta_ptr = 0, off_cta_list = 0,
+         off_mgroups = 0, off_mrow_ptr = 0, int_bytes = 0, off_part_o = 0, off_part_lse = 0,
+         total_bytes = 0;
+  std::vector<uint8_t> int_image;   // bytes [0, int_bytes) of the workspace
+  std::vector<int32_t> summary;
+};
+
+struct PodPlanArgs {
+  const int32_t *p_q_indptr, *p_kv_indptr, *p_kv_indices, *p_last_page_len;
+  int p_batch, p_num_pages;
+  const int32_t *d_q_indptr, *d_kv_indptr, *d_kv_indices, *d_last_page_len;
+  int d_batch, d_num_pages;
+  int H, Hk, d, ps, causal, window_left;
+  float sm_scale;
+  int dtype, has_sinks, num_sms;
+};
+
+// Returns 0 on success, else a pod_status code with *err set.
+int pod_build_plan(const PodPlanArgs& a, PodPlanHost& plan, std::string* err);

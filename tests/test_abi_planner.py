@@ -1,0 +1,207 @@
+"""CPU tests of the C-ABI library: it loads, exports every declared symbol, and
+its host planner matches the plain restatement in oracle/planner_ref.py bit for
+bit. No GPU is needed: plans are made host-only (workspace NULL, num_sms given).
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import planner_ref
+import prefill_decode_paged_pod_gb300 as pod
+from prefill_decode_paged_pod_gb300 import _build
+from pod_workloads import make_config, make_custom
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+REC = 8
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return pod.load_library()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "pod.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pod_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    syms = declared_symbols()
+    assert "pod_plan" in syms and "pod_run" in syms and len(syms) >= 8
+    for s in syms:
+        assert hasattr(lib, s), f"{s} is declared in include/pod.h but not exported"
+
+
+def plan_host(inp, num_sms=152):
+    return pod.plan_inputs(inp, workspace=None, num_sms=num_sms)
+
+
+def check_against_reference(inp, h):
+    s = pod.plan_summary(h)
+    # kv_len: library == oracle C == python restatement
+    for half, which in (("p", 6), ("d", 7)):
+        hh = inp.p if half == "p" else inp.d
+        got = pod.pod_plan_table(h, which)
+        if hh.batch == 0:
+            continue
+        assert np.array_equal(got, oracle.seq_lens(hh.kv_indptr, hh.last_page_len, inp.page_size))
+        assert np.array_equal(got, planner_ref.seq_lens(hh.kv_indptr, hh.last_page_len, inp.page_size))
+    H, Hk = inp.num_qo_heads, inp.num_kv_heads
+    kvl_p = planner_ref.seq_lens(inp.p.kv_indptr, inp.p.last_page_len, inp.page_size)
+    kvl_d = planner_ref.seq_lens(inp.d.kv_indptr, inp.d.last_page_len, inp.page_size)
+    # prefill tiles: bit-exact, in order
+    tiles = pod.pod_plan_table(h, 1).reshape(-1, REC)
+    ref = planner_ref.prefill_tiles(inp.p.q_indptr, kvl_p, H, Hk, inp.causal, inp.window_left)
+    assert tiles.shape[0] == len(ref) == s["n_tiles"]
+    if len(ref):
+        assert np.array_equal(tiles[:, :6], np.array(ref, dtype=np.int32))
+        assert np.all(tiles[:, 6] == -1)
+    # decode items: per unit, the chunks partition [lo, hi) in order
+    items = pod.pod_plan_table(h, 2).reshape(-1, REC)
+    units = planner_ref.decode_units(inp.d.q_indptr, kvl_d, H, Hk, inp.causal, inp.window_left)
+    groups = pod.pod_plan_table(h, 5).reshape(-1, REC)
+    G = H // Hk
+    i = 0
+    gi = 0
+    prows = 0
+    for (r, g, t0, nt, lo, hi) in units:
+        start = i
+        k = lo
+        while i < len(items) and tuple(items[i, :4]) == (r, g, t0, nt) and items[i, 4] == k:
+            assert items[i, 5] > items[i, 4]
+            k = int(items[i, 5])
+            i += 1
+            if k == hi:
+                break
+        assert k == hi, f"unit {(r, g, t0, nt, lo, hi)} not covered"
+        n = i - start
+        inner = [int(items[j, 4]) for j in range(start + 1, i)]
+        assert all(b % 64 == 0 for b in inner)
+        if n == 1:
+            assert items[start, 6] == -1
+        else:
+            R = nt * G
+            assert tuple(groups[gi]) == (1, r, g, t0, nt, prows, n, R)
+            for j in range(n):
+                assert items[start + j, 6] == prows + j * R
+            prows += n * R
+            gi += 1
+    assert i == len(items) == s["n_items"]
+    assert gi == len(groups) == s["n_groups"]
+    assert prows == s["n_prows"]
+    # CTA lists: every record exactly once, prefill CTAs first
+    ptr = pod.pod_plan_table(h, 3)
+    lst = pod.pod_plan_table(h, 4)
+    npc, ndc = s["n_p_ctas"], s["n_d_ctas"]
+    assert len(ptr) == s["grid"] + 1 and s["grid"] == npc + ndc
+    assert sorted(lst[: ptr[npc]].tolist()) == list(range(s["n_tiles"]))
+    assert sorted(lst[ptr[npc]:].tolist()) == list(range(s["n_items"]))
+    assert s["grid"] <= 2 * s["num_sms"]
+    return s
+
+
+@pytest.mark.parametrize("name", ["c1", "c2"])
+def test_planner_small_configs(lib, name):
+    inp = make_config(name)
+    h = plan_host(inp)
+    s = check_against_reference(inp, h)
+    assert s["p_rows"] == inp.p.rows and s["d_rows"] == inp.d.rows
+    pod.pod_destroy(h)
+
+
+def test_planner_docstring_kv_lens(lib):
+    inp = make_config("c2")
+    h = plan_host(inp)
+    assert pod.pod_plan_table(h, 7).tolist() == [257, 183, 238, 52, 275, 529, 448]
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_planner_random(lib, seed):
+    rng = np.random.default_rng(seed)
+    G = int(rng.choice([1, 2, 4, 8]))
+    Hk = int(rng.choice([1, 2, 8]))
+    ps = int(rng.choice([1, 3, 16]))
+    causal = bool(rng.integers(0, 2))
+    window = int(rng.choice([-1, 0, 100, 4096]))
+    pb, db = int(rng.integers(0, 4)), int(rng.integers(0, 40))
+    pkv = rng.integers(1, 3000, size=pb)
+    pq = [int(rng.integers(1, k + 1)) if causal else int(rng.integers(1, 3000)) for k in pkv]
+    dkv = rng.integers(5, 20000, size=db)
+    dq = [int(rng.integers(1, min(5, k) + 1)) for k in dkv]
+    inp = make_custom("r", torch.float16, G * Hk, Hk, 64, ps, causal, window, pq, pkv, dq, dkv,
+                      seed=seed)
+    h = plan_host(inp, num_sms=int(rng.choice([8, 152])))
+    check_against_reference(inp, h)
+
+
+def test_planner_deterministic(lib):
+    inp = make_config("c1")
+    a = plan_host(inp)
+    b = plan_host(inp)
+    for w in range(6):
+        assert np.array_equal(pod.pod_plan_table(a, w), pod.pod_plan_table(b, w))
+
+
+def test_planner_large_configs_host_only(lib):
+    # c4: 256 decode requests of U[512,16384] keys; plan must split decode KV
+    inp = make_config("c4")
+    h = plan_host(inp)
+    s = check_against_reference(inp, h)
+    assert s["n_items"] >= s["n_d_ctas"] > 0 and s["n_p_ctas"] > 0
+
+
+def _bad(lib, **over):
+    inp = make_custom("v", torch.float16, 4, 2, 64, 4, True, -1, [3], [5], [1, 1], [6, 9], seed=0)
+    args = dict(p_q_indptr=inp.p.q_indptr, p_kv_indptr=inp.p.kv_indptr, p_kv_indices=inp.p.kv_indices,
+                p_last_page_len=inp.p.last_page_len, d_q_indptr=inp.d.q_indptr,
+                d_kv_indptr=inp.d.kv_indptr, d_kv_indices=inp.d.kv_indices,
+                d_last_page_len=inp.d.last_page_len, num_qo_heads=4, num_kv_heads=2, head_dim=64,
+                page_size=4, causal=True, window_left=-1, sm_scale=None, dtype=torch.float16,
+                p_num_pages=inp.p.num_pages, d_num_pages=inp.d.num_pages, num_sms=4)
+    args.update(over)
+    with pytest.raises(pod.PodError) as e:
+        pod.pod_plan(**args)
+    return e.value.code
+
+
+def test_plan_error_codes(lib):
+    assert _bad(lib, num_qo_heads=5) == 1                      # H % Hk != 0
+    assert _bad(lib, head_dim=96) == 2                         # unsupported head_dim
+    assert _bad(lib, d_last_page_len=np.array([5, 1])) == 1    # last_page_len > page_size
+    assert _bad(lib, d_last_page_len=np.array([0, 1])) == 1    # last_page_len < 1
+    assert _bad(lib, d_kv_indices=np.array([0, 1, 99])) == 1   # page outside the pool
+    assert _bad(lib, d_q_indptr=np.array([0, 2, 1])) == 1      # non-monotone indptr
+    assert _bad(lib, p_q_indptr=np.array([0, 9])) == 1         # kv_len < q_len under causal
+    assert _bad(lib, num_qo_heads=256, num_kv_heads=1) == 2    # group > 128
+    assert _bad(lib, num_qo_heads=128, num_kv_heads=2) == 2    # decode group > 32
+    assert _bad(lib, window_left=-2) == 1
+
+
+def test_reference_validation_agrees(lib):
+    """The restated validation rules reject exactly what the library rejects."""
+    rng = np.random.default_rng(3)
+    for trial in range(40):
+        b = int(rng.integers(1, 4))
+        ps = int(rng.choice([1, 4]))
+        q_indptr = np.concatenate([[0], np.cumsum(rng.integers(0, 4, size=b))]).astype(np.int32)
+        kv_indptr = np.concatenate([[0], np.cumsum(rng.integers(0, 3, size=b))]).astype(np.int32)
+        last = rng.integers(0, ps + 2, size=b).astype(np.int32)
+        npages = 6
+        idx = rng.integers(-1, npages + 1, size=int(kv_indptr[-1])).astype(np.int32)
+        reason = planner_ref.validate_half(q_indptr, kv_indptr, idx, last, npages, ps, True)
+        ok = True
+        try:
+            pod.pod_plan(None, None, None, None, q_indptr, kv_indptr, idx, last, 2, 1, 64, ps,
+                         True, -1, None, dtype=torch.float16, p_num_pages=1, d_num_pages=npages,
+                         num_sms=4)
+        except pod.PodError as e:
+            ok = False
+            assert e.code == 1
+        assert ok == (reason is None), (trial, reason)

@@ -1,0 +1,154 @@
+"""GPU parity: the POD library (through its C-ABI binding) against the fp64
+oracle on the same seeded inputs, element by element.
+
+Covers the five benchmark workloads (c1, c2 fully; c3-c5 at full size on a
+deterministic sample of rows), a randomized sweep shaped like the FlashInfer
+POD test grid (page size 1/16, GQA groups, decode batches 1/17/127, prefill
+lengths that are not tile multiples), edge cases, determinism and the tcgen05
+building blocks in isolation.
+"""
+import numpy as np
+import pytest
+import torch
+
+import prefill_decode_paged_pod_gb300 as pod
+from pod_workloads import make_config, make_custom
+from podtest_util import compare_half, run_pod, sample_rows, selftest_lib, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from prefill_decode_paged_pod_gb300 import _build
+    _build.build()
+    pod.load_library()
+
+
+# ------------------------------------------------------------- building blocks
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("bf16", [0, 1])
+@pytest.mark.parametrize("variant", [0, 1])
+def test_umma_building_blocks(d, bf16, variant):
+    L = selftest_lib()
+    dt = torch.bfloat16 if bf16 else torch.float16
+    g = torch.Generator().manual_seed(7 + d + bf16)
+    q = torch.randn(128, d, generator=g).to(dt).cuda()
+    k = torch.randn(64, d, generator=g).to(dt).cuda()
+    v = torch.randn(64, d, generator=g).to(dt).cuda()
+    p = torch.rand(128, 64, generator=g).to(dt).cuda()
+    s = torch.zeros(128, 64, device="cuda")
+    o = torch.zeros(128, d, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = L.umma_selftest(q.data_ptr(), k.data_ptr(), v.data_ptr(), p.data_ptr(), s.data_ptr(),
+                         o.data_ptr(), d, bf16, variant, st.data_ptr())
+    assert rc == 0 and int(st.item()) == 0
+    s_ref = q.float() @ k.float().T
+    o_ref = p.float() @ v.float()
+    assert torch.allclose(s, s_ref, atol=1e-2, rtol=1e-3), (s - s_ref).abs().max()
+    assert torch.allclose(o, o_ref, atol=1e-2, rtol=1e-3), (o - o_ref).abs().max()
+
+
+# ------------------------------------------------------------- workloads
+@pytest.mark.parametrize("name", ["c1", "c2"])
+def test_config_full(name):
+    inp = make_config(name)
+    (op, lp, od, ld), h, ws = run_pod(inp)
+    assert op.shape == (inp.p.rows, inp.num_qo_heads, inp.head_dim)
+    assert od.shape == (inp.d.rows, inp.num_qo_heads, inp.head_dim)
+    compare_half(inp, "p", op, lp, tag=name)
+    compare_half(inp, "d", od, ld, tag=name)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["c3", "c4", "c5"])
+def test_config_full_size_sampled(name):
+    inp = make_config(name)
+    (op, lp, od, ld), h, ws = run_pod(inp)
+    H = inp.num_qo_heads
+    st, sh = sample_rows(inp.p, H, 48, seed=1)
+    compare_half(inp, "p", op, lp, st, sh, tag=name)
+    st, sh = sample_rows(inp.d, H, 96, seed=2)
+    compare_half(inp, "d", od, ld, st, sh, tag=name)
+    assert np.isfinite(op).all() and np.isfinite(od).all()
+    assert np.isfinite(lp).all() and np.isfinite(ld).all()
+
+
+# ------------------------------------------------------------- sweep (M1-like)
+SWEEP = []
+for ps in (1, 16):
+    for G in (1, 4, 8):
+        for db in (1, 17, 127):
+            SWEEP.append((ps, G, db))
+
+
+@pytest.mark.parametrize("ps,G,db", SWEEP)
+def test_sweep(ps, G, db):
+    rng = np.random.default_rng(ps * 1000 + G * 10 + db)
+    Hk = 2
+    d = int(rng.choice([64, 128]))
+    dt = torch.bfloat16 if rng.integers(0, 2) else torch.float16
+    window = int(rng.choice([-1, -1, 37, 300]))
+    sinks = bool(rng.integers(0, 2))
+    pl = [int(x) for x in rng.choice([1, 127, 300], size=int(rng.integers(1, 3)))]
+    pkv = [q + int(rng.integers(0, 200)) for q in pl]
+    dkv = [int(x) for x in rng.integers(1, 700, size=db)]
+    dq = [int(min(k, rng.choice([1, 1, 3]))) for k in dkv]
+    inp = make_custom("sweep", dt, G * Hk, Hk, d, ps, True, window, pl, pkv, dq, dkv,
+                      seed=int(rng.integers(0, 1 << 30)), sinks=sinks, extra_pages=3)
+    (op, lp, od, ld), h, ws = run_pod(inp)
+    compare_half(inp, "p", op, lp, tag=f"ps{ps} G{G} db{db} d{d} w{window} ")
+    compare_half(inp, "d", od, ld, tag=f"ps{ps} G{G} db{db} d{d} w{window} ")
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_non_causal_and_long_decode_split(causal):
+    """Long decode KV on few SMs forces split chunks and the merge kernel."""
+    inp = make_custom("split", torch.bfloat16, 16, 2, 128, 16, causal, -1, [40], [300],
+                      [1, 2, 1], [5000, 7000, 3000], seed=11, sinks=True)
+    (op, lp, od, ld), h, ws = run_pod(inp, num_sms=4)
+    s = pod.plan_summary(h)
+    assert s["n_groups"] > 0, s
+    compare_half(inp, "p", op, lp)
+    compare_half(inp, "d", od, ld)
+
+
+# ------------------------------------------------------------- edge cases
+def test_empty_prefill_half():
+    inp = make_custom("ed", torch.float16, 8, 2, 128, 16, True, -1, [], [], [1, 1], [33, 1], seed=3)
+    (op, lp, od, ld), h, ws = run_pod(inp)
+    assert op.shape[0] == 0
+    compare_half(inp, "d", od, ld)
+
+
+def test_empty_decode_half():
+    inp = make_custom("ep", torch.bfloat16, 8, 8, 64, 1, True, 5, [65, 3], [70, 3], [], [], seed=4)
+    (op, lp, od, ld), h, ws = run_pod(inp)
+    assert od.shape[0] == 0
+    compare_half(inp, "p", op, lp)
+
+
+def test_zero_length_requests_and_tiny_kv():
+    # request 1 of each half has no queries; kv_len == 1 and kv_len == q_len cases
+    inp = make_custom("z", torch.float16, 4, 1, 64, 4, True, 0, [1, 0, 5], [1, 4, 5],
+                      [1, 0, 1], [1, 2, 9], seed=5, sinks=True)
+    (op, lp, od, ld), h, ws = run_pod(inp)
+    compare_half(inp, "p", op, lp)
+    compare_half(inp, "d", od, ld)
+
+
+def test_determinism():
+    inp = make_config("c1")
+    r1, h, ws = run_pod(inp)
+    r2, _, _ = run_pod(inp)
+    for x, y in zip(r1, r2):
+        assert np.array_equal(x, y)
+
+
+def test_run_many_times_one_plan():
+    """plan once, run many (the walkthrough's per-layer reuse)."""
+    inp = make_config("c1")
+    dev = to_dev(inp)
+    (op, lp, od, ld), h, ws = run_pod(inp, dev=dev, repeat=5)
+    compare_half(inp, "p", op, lp)
+    compare_half(inp, "d", od, ld)
