@@ -164,6 +164,41 @@ pod_status pod_read_device_status(pod_handle h, void* workspace, void* stream,
 pod_status pod_plan_table(pod_handle h, int32_t which, int32_t* out, int64_t capacity,
                           int64_t* count);
 
+/*
+ * pod_run_static_scratch — pod_run for callers that cannot allocate device
+ * memory. The paper has no counterpart: this entry point is a deployment aid
+ * of this library.
+ *
+ * Some callers cannot call cudaMalloc: plugins whose host application owns all
+ * device memory through its own pool, processes held to a fixed device-memory
+ * budget, and serving loops that cannot take the implicit synchronisation of
+ * cudaMalloc/cudaFree. This call needs no workspace from them: the scratch the
+ * kernels use (plan metadata, split partials, status word) is a fixed
+ * 32 MiB array inside the library (pod_static_scratch_capacity()), which every
+ * GPU that loads the library holds until the process exits. The caller still
+ * passes the input and output tensors, with the same meaning as for pod_run.
+ *
+ * Each call uploads the plan's metadata into that array (clearing the status
+ * word) and then runs the same kernels as pod_run. Every call on a device
+ * shares the one array, which keeps the last call's contents: calls that
+ * overlap on the GPU (other streams, other threads) race and must be
+ * serialised by the caller. The handle becomes bound to the array (a later
+ * pod_run on it must pass that array's address or re-bind with
+ * pod_bind_workspace). The first call on a device looks up the array's device
+ * address with that device current; make that first call before any stream
+ * capture. No device memory is allocated or freed.
+ *
+ * Errors: POD_ERR_WORKSPACE (with a message) when pod_workspace_size(h)
+ * exceeds the array; otherwise those of pod_bind_workspace and pod_run.
+ */
+pod_status pod_run_static_scratch(pod_handle h, const void* q_p, const void* kv_p,
+                                  const void* q_d, const void* kv_d, const float* sinks,
+                                  void* out_p, float* lse_p, void* out_d, float* lse_d,
+                                  void* stream);
+
+/* Size in bytes of the static scratch array used by pod_run_static_scratch. */
+size_t pod_static_scratch_capacity(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -29,6 +29,7 @@ __all__ = [
     "POD_OK", "PodError", "load_library", "pod_plan", "pod_run", "pod_destroy",
     "pod_workspace_size", "pod_bind_workspace", "pod_last_error", "pod_read_device_status",
     "pod_plan_table", "PodHandle", "LIB_PATH", "DEFAULT_WORKSPACE_BYTES",
+    "pod_run_static_scratch", "pod_static_scratch_capacity",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -77,6 +78,10 @@ def load_library(path: Optional[str] = None):
     lib.pod_read_device_status.argtypes = [V, V, V, ctypes.POINTER(I32)]
     lib.pod_plan_table.restype = ctypes.c_int
     lib.pod_plan_table.argtypes = [V, I32, V, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]
+    lib.pod_run_static_scratch.restype = ctypes.c_int
+    lib.pod_run_static_scratch.argtypes = [V, V, V, V, V, V, V, V, V, V, V]
+    lib.pod_static_scratch_capacity.restype = SZ
+    lib.pod_static_scratch_capacity.argtypes = []
     if path is None:
         _lib = lib
     return lib
@@ -224,6 +229,40 @@ def pod_run(h: PodHandle, q_p, kv_p, q_d, kv_d, workspace, sinks=None,
                        None if p_empty else _ptr(out_p), None if p_empty else _ptr(lse_p),
                        None if d_empty else _ptr(out_d), None if d_empty else _ptr(lse_d),
                        _stream(stream))
+    _check(code)
+    return out_p, lse_p, out_d, lse_d
+
+
+def pod_static_scratch_capacity() -> int:
+    return int(load_library().pod_static_scratch_capacity())
+
+
+def pod_run_static_scratch(h: PodHandle, q_p, kv_p, q_d, kv_d, sinks=None,
+                           out_p=None, lse_p=None, out_d=None, lse_d=None, stream=None):
+    """Like pod_run, but the kernels' scratch is the library's fixed device
+    array instead of a caller-allocated workspace (for callers that cannot
+    allocate device memory). Output tensors are allocated here when not given;
+    pass them to keep the call free of allocations. Calls sharing a device must
+    not overlap on the GPU."""
+    import torch
+    lib = load_library()
+    H, d = h.num_qo_heads, h.head_dim
+    dev = q_p.device if q_p is not None else (q_d.device if q_d is not None else None)
+    if out_p is None:
+        out_p = torch.empty((h.p_rows, H, d), dtype=h.dtype, device=dev)
+    if lse_p is None:
+        lse_p = torch.empty((h.p_rows, H), dtype=torch.float32, device=dev)
+    if out_d is None:
+        out_d = torch.empty((h.d_rows, H, d), dtype=h.dtype, device=dev)
+    if lse_d is None:
+        lse_d = torch.empty((h.d_rows, H), dtype=torch.float32, device=dev)
+    p_empty, d_empty = h.p_rows == 0, h.d_rows == 0
+    code = lib.pod_run_static_scratch(
+        ctypes.c_void_p(h.ptr),
+        None if p_empty else _ptr(q_p), None if p_empty else _ptr(kv_p),
+        None if d_empty else _ptr(q_d), None if d_empty else _ptr(kv_d), _ptr(sinks),
+        None if p_empty else _ptr(out_p), None if p_empty else _ptr(lse_p),
+        None if d_empty else _ptr(out_d), None if d_empty else _ptr(lse_d), _stream(stream))
     _check(code)
     return out_p, lse_p, out_d, lse_d
 

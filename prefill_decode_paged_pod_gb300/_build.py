@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libpod_gb300.so")
-SOURCES = ["pod_kernels.cu", "pod_api.cu", "pod_planner.cpp"]
+SOURCES = ["pod_kernels.cu", "pod_api.cu", "pod_planner.cpp", "pod_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -64,6 +64,10 @@ pod_status upload(pod_plan_s* h, void* ws, size_t bytes, void* stream) {
 
 }  // namespace
 
+// Lets other translation units of the library report a message through
+// pod_last_error().
+void pod_set_last_error(const std::string& msg) { g_err = msg; }
+
 extern "C" {
 
 pod_status pod_plan(const int32_t* p_q_indptr, const int32_t* p_kv_indptr,
