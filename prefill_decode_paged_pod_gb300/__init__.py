@@ -295,7 +295,8 @@ def pod_plan_table(h: PodHandle, which: int) -> np.ndarray:
 # summary indices of pod_plan_table(h, 0), mirroring enum PodSummary in csrc/pod_plan.h
 SUMMARY_FIELDS = ("H", "Hk", "d", "ps", "causal", "window", "dtype", "sinks", "num_sms", "grid",
                   "n_p_ctas", "n_d_ctas", "n_tiles", "n_items", "n_groups", "n_mrows", "n_prows",
-                  "p_rows", "d_rows", "p_batch", "d_batch", "decode_chunk", "ws_lo", "ws_hi")
+                  "p_rows", "d_rows", "p_batch", "d_batch", "decode_chunk", "ws_lo", "ws_hi",
+                  "p_tma", "d_tma")
 
 
 def plan_summary(h: PodHandle) -> dict:

@@ -3,10 +3,13 @@
 // Host-side only: argument checks, the planner call, the one metadata upload
 // and the kernel launches. Every step of the attention itself runs in the
 // kernels of pod_kernels.cu.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdio.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include <new>
 #include <string>
@@ -19,6 +22,9 @@ struct pod_plan_s {
   PodPlanHost plan;
   void* workspace = nullptr;      // bound device workspace (nullptr = host-only plan)
   size_t workspace_bytes = 0;
+  // TMA descriptors of the last run, re-encoded only when a tensor pointer changes
+  const void* tm_ptr[4] = {nullptr, nullptr, nullptr, nullptr};
+  CUtensorMap tm[4];
 };
 
 namespace {
@@ -59,6 +65,63 @@ pod_status upload(pod_plan_s* h, void* ws, size_t bytes, void* stream) {
   if (e != cudaSuccess) return cuda_err(e, "cudaStreamSynchronize(plan metadata)");
   h->workspace = ws;
   h->workspace_bytes = bytes;
+  return POD_OK;
+}
+
+// ---- TMA descriptors (driver entry point fetched through the runtime) --------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Q viewed as [rows][H][d]; box = 64 elements x G heads x `tokens` rows.
+pod_status encode_q(CUtensorMap* m, const void* ptr, int rows, int H, int d, int G, int tokens,
+                    int dtype) {
+  auto fn = encode_fn();
+  if (!fn) return set_err(POD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15u) != 0)
+    return set_err(POD_ERR_INVALID_ARG, "q tensors must be 16-byte aligned");
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)tokens};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, dtype ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                  const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_err(POD_ERR_CUDA, "cuTensorMapEncodeTiled(q) failed: " + std::to_string((int)r));
+  return POD_OK;
+}
+
+// Paged cache viewed as [pages][2][ps][Hk][d]; box = 64 elements x 1 head x
+// min(ps, 64) slots x 1 x 1 page, or 64 x 1 x ps x 1 x (8 / ps) pages for ps < 8.
+pod_status encode_kv(CUtensorMap* m, const void* ptr, int num_pages, int ps, int Hk, int d,
+                     int dtype) {
+  auto fn = encode_fn();
+  if (!fn) return set_err(POD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15u) != 0)
+    return set_err(POD_ERR_INVALID_ARG, "kv caches must be 16-byte aligned");
+  cuuint64_t dims[5] = {(cuuint64_t)d, (cuuint64_t)Hk, (cuuint64_t)ps, 2, (cuuint64_t)num_pages};
+  cuuint64_t row = (cuuint64_t)d * 2;
+  cuuint64_t strides[4] = {row, row * Hk, row * Hk * ps, row * Hk * ps * 2};
+  cuuint32_t box[5] = {64, 1, (cuuint32_t)(ps >= 8 ? (ps < 64 ? ps : 64) : ps), 1,
+                       (cuuint32_t)(ps >= 8 ? 1 : 8 / ps)};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, dtype ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5,
+                  const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_err(POD_ERR_CUDA, "cuTensorMapEncodeTiled(kv) failed: " + std::to_string((int)r));
   return POD_OK;
 }
 
@@ -153,8 +216,39 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
   if (!P.has_sinks && sinks)
     return set_err(POD_ERR_INVALID_ARG, "sinks given but the plan was made without sinks");
 
+  // TMA descriptors for the tensors of this call (cached while pointers repeat)
+  const void* ptrs[4] = {q_p, kv_p, q_d, kv_d};
+  for (int i = 0; i < 4; ++i) {
+    const bool pre = i < 2;
+    const PodHalfHost& hh = pre ? P.p : P.dd;
+    if (hh.rows == 0) continue;
+    if (i % 2 == 1 && !(pre ? P.p_tma : P.d_tma)) continue;
+    if (h->tm_ptr[i] == ptrs[i]) continue;
+    pod_status st = (i % 2 == 0)
+        ? encode_q(&h->tm[i], ptrs[i], hh.rows, P.H, P.d, P.G, pre ? P.tq : P.tu, P.dtype)
+        : encode_kv(&h->tm[i], ptrs[i], hh.num_pages, P.ps, P.Hk, P.d, P.dtype);
+    if (st != POD_OK) return st;
+    h->tm_ptr[i] = ptrs[i];
+  }
+
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   PodParams K;
+  memset(&K, 0, sizeof(K));
+  if (P.p.rows) {
+    K.tm_q_p = h->tm[0];
+    if (P.p_tma) K.tm_kv_p = h->tm[1];
+  }
+  if (P.dd.rows) {
+    K.tm_q_d = h->tm[2];
+    if (P.d_tma) K.tm_kv_d = h->tm[3];
+  }
+  K.p_tma = P.p_tma;
+  K.d_tma = P.d_tma;
+  K.kbx = P.ps >= 8 ? (P.ps < 64 ? P.ps : 64) : 8;
+  K.p_num_pages = P.p.num_pages;
+  K.d_num_pages = P.dd.num_pages;
+  K.tq = P.tq;
+  K.tu = P.tu;
   K.H = P.H; K.Hk = P.Hk; K.G = P.G; K.d = P.d; K.ps = P.ps;
   K.ps_shift = -1;
   for (int s = 0; s < 31; ++s)

@@ -6,20 +6,23 @@
 // two share the SMs instead of leaving gaps between two launches).
 //
 //  prefill tile (128 query rows = ntok tokens x G qo heads of one KV head):
-//    warps 5-7  cp.async loaders: Q tile once, then 64-key K/V blocks gathered
-//               through the page table into two 128B-swizzled stages;
+//    warps 5-6  TMA producers (one thread each): the Q tile, then 64-key K
+//               blocks (3-stage ring) and V blocks (2-stage ring) as page
+//               boxes through the page table, 128B-swizzled by the hardware
+//               (warps 5-7 gather with cp.async when the page table does not
+//               allow page boxes);
 //    warp 4     one thread issues tcgen05.mma: S = Q K^T into TMEM (double
-//               buffered), later O += P V into TMEM;
+//               buffered), then O += P V with P read from TMEM;
 //    warps 0-3  one TMEM lane (= one query row) per thread: tcgen05.ld of S,
 //               bottom-right causal / window mask, online softmax in base 2
-//               with lazy rescaling of O, P written to shared memory as the
-//               A operand of the next MMA, final O / (l + sink) and LSE.
+//               with lazy rescaling of O, P packed to 16 bits and stored over
+//               the S columns it came from, final O / (l + sink) and LSE.
 //  decode item (<= 32 rows = q tokens x G heads, keys [k0, k1) of one chunk):
-//    all 8 warps stream 64-key K/V stages with cp.async (3 stages); warp w
-//    owns m-tile w/4 and keys 16*(w%4).. of each stage and runs mma.sync
-//    m16n8k16 for Q K^T and P V with an online softmax in registers; warps
-//    combine through shared memory and write the final output, or an fp32
-//    partial (o, lse) when the plan split the KV range.
+//    a 3-stage ring of 64-key K/V stages fed by TMA page boxes (or cp.async);
+//    warp w owns m-tile w/4 and keys 16*(w%4).. of each stage and runs
+//    mma.sync m16n8k16 for Q K^T and P V with an online softmax in registers;
+//    warps combine through shared memory and write the final output, or an
+//    fp32 partial (o, lse) when the plan split the KV range.
 //
 // K2 `pod_merge_kernel`: merges the split partials of each row with base-2
 // LSE weights, adds the sink, writes out and LSE (flashinfer.cudnn page,
@@ -44,31 +47,34 @@ struct PLayout {                                   // prefill shared memory
   static constexpr int NKB = D / 64;               // 64-element K blocks of head_dim
   static constexpr int QBLK = POD_TILE_ROWS * 128; // 128 rows x 128 B
   static constexpr int KVBLK = POD_KBLOCK * 128;   // 64 rows x 128 B
+  static constexpr int KSTAGE = NKB * KVBLK;       // one 64-key K or V block
+  static constexpr int NK = 3, NV = 2;             // K and V stage rings
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + NKB * QBLK;
-  static constexpr int V_OFF = K_OFF + 2 * NKB * KVBLK;
-  static constexpr int P_OFF = V_OFF + 2 * NKB * KVBLK;
-  static constexpr int BAR_OFF = P_OFF + POD_TILE_ROWS * 128;
+  static constexpr int V_OFF = K_OFF + NK * KSTAGE;
+  static constexpr int BAR_OFF = V_OFF + NV * KSTAGE;
   static constexpr int TOTAL = BAR_OFF + 256;
-  static constexpr int TMEM_COLS = 256;            // S[2] (2 x 64) + O (<= 128)
+  static constexpr int TMEM_COLS = 256;            // S/P[2] (2 x 64) + O (<= 128)
   static constexpr int TM_S = 0, TM_O = 128;
 };
 
 template <int D>
 struct DLayout {                                   // decode shared memory
-  static constexpr int ROWB = D * 2;
-  static constexpr int NCH = D / 8;
-  static constexpr int KEYS = POD_DECODE_STAGE;
-  static constexpr int Q_OFF = 0;
-  static constexpr int STAGE_OFF = POD_DECODE_ROWS * ROWB;
-  static constexpr int KBYTES = KEYS * ROWB;
-  static constexpr int STAGE_BYTES = 2 * KBYTES;
+  static constexpr int NKB = D / 64;
+  static constexpr int QDH = POD_DECODE_ROWS * 128; // one 64-column half of Q: 32 rows x 128 B
+  static constexpr int KDH = POD_DECODE_STAGE * 128;// one half of a 64-key K or V block
+  static constexpr int KBYTES = NKB * KDH;
+  static constexpr int STAGE_BYTES = 2 * KBYTES;    // K then V
   static constexpr int NSTAGE = 3;
-  static constexpr int TOTAL = STAGE_OFF + NSTAGE * STAGE_BYTES;
+  static constexpr int Q_OFF = 0;
+  static constexpr int STAGE_OFF = NKB * QDH;
+  static constexpr int BAR_OFF = STAGE_OFF + NSTAGE * STAGE_BYTES;
+  static constexpr int TOTAL = BAR_OFF + 128;
   // combine scratch (reuses the stages): 8 warps x 16 rows x D floats, then m/l
   static constexpr int SCR_O = STAGE_OFF;
   static constexpr int SCR_ML = STAGE_OFF + 8 * 16 * D * 4;
-  static_assert(SCR_ML + 8 * 16 * 2 * 4 <= TOTAL, "combine scratch must fit in the stages");
+  static_assert(SCR_ML + 8 * 16 * 2 * 4 <= BAR_OFF, "combine scratch must fit in the stages");
+  static_assert(STAGE_OFF % 1024 == 0, "stages must be 1024-byte aligned");
 };
 
 template <int D>
@@ -86,32 +92,49 @@ POD_DEV bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) 
 }
 
 // ============================================================ prefill role
+// Barrier slots (8 bytes each) at PLayout::BAR_OFF.
 enum {
-  B_QFULL = 0, B_QEMPTY = 1, B_KVFULL = 2, B_KVEMPTY = 4, B_SFULL = 6, B_SEMPTY = 8,
-  B_PFULL = 10, B_PVDONE = 11, B_FINAL = 12
+  B_QFULL = 0, B_QEMPTY = 1,
+  B_KFULL = 2,                     // [NK]
+  B_KEMPTY = B_KFULL + 3,          // [NK]
+  B_VFULL = B_KEMPTY + 3,          // [NV]
+  B_VEMPTY = B_VFULL + 2,          // [NV]
+  B_SFULL = B_VEMPTY + 2,          // [2] S_j of buffer j%2 computed
+  B_PFULL = B_SFULL + 2,           // [2] P_j of buffer j%2 written into TMEM
+  B_PVDONE = B_PFULL + 2,          // [2] PV_j (A = P_j) finished
+  B_FINAL = B_PVDONE + 2,
+  B_COUNT = B_FINAL + 1
 };
 
 template <typename T, int D>
 __device__ void prefill_role(const PodParams& P, uint8_t* smem, int cta) {
   using L = PLayout<D>;
+  constexpr int NK = L::NK, NV = L::NV;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + L::BAR_OFF;
   auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + 128);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR_OFF + 132);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + 224);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR_OFF + 228);
+  static_assert(B_COUNT * 8 <= 224, "barriers overlap the TMEM slot");
 
   if (tid == 0) {
-    mbar_init(BAR(B_QFULL), 96);
+    const uint32_t kv_arrivals = P.p_tma ? 1u : 96u;  // TMA: one expect_tx arrive
+    mbar_init(BAR(B_QFULL), 1);
     mbar_init(BAR(B_QEMPTY), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(BAR(B_KVFULL + s), 96);
-      mbar_init(BAR(B_KVEMPTY + s), 1);
-      mbar_init(BAR(B_SFULL + s), 1);
-      mbar_init(BAR(B_SEMPTY + s), 128);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(BAR(B_KFULL + s), kv_arrivals);
+      mbar_init(BAR(B_KEMPTY + s), 1);
     }
-    mbar_init(BAR(B_PFULL), 128);
-    mbar_init(BAR(B_PVDONE), 1);
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(BAR(B_VFULL + s), kv_arrivals);
+      mbar_init(BAR(B_VEMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(BAR(B_SFULL + b), 1);
+      mbar_init(BAR(B_PFULL + b), 128);
+      mbar_init(BAR(B_PVDONE + b), 1);
+    }
     mbar_init(BAR(B_FINAL), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -129,85 +152,163 @@ __device__ void prefill_role(const PodParams& P, uint8_t* smem, int cta) {
 
   if (warp >= 5) {
     // ------------------------------------------------------------ loaders
-    const int lt = tid - 160;  // 0..95
-    const T* __restrict__ qg = reinterpret_cast<const T*>(P.q_p);
-    const T* __restrict__ kvg = reinterpret_cast<const T*>(P.kv_p);
-    int kv_fill = 0, q_fill = 0;
+    int kfill = 0, vfill = 0, qfill = 0;
     bool ok = true;
-    for (int w = w_begin; w < w_end && ok; ++w) {
-      const int32_t* rec = P.ptiles + POD_REC * P.cta_list[w];
-      const int req = rec[0], g = rec[1], tok0 = rec[2], ntok = rec[3], lo = rec[4], hi = rec[5];
-      const int q_base = P.p_q_indptr[req];
-      const int page_base = P.p_kv_indptr[req];
-      const int nrows = ntok * G;
-      if (!mbar_wait(BAR(B_QEMPTY), (q_fill & 1) ^ 1, abort_flag)) { ok = false; break; }
-      constexpr int QCH = POD_TILE_ROWS * (D / 8);
-      for (int idx = lt; idx < QCH; idx += 96) {
-        const int r = idx / (D / 8), c = idx % (D / 8);
-        const bool valid = r < nrows;
-        const int tok = valid ? tok0 + r / G : tok0;
-        const int head = valid ? g * G + r % G : g * G;
-        const T* src = qg + ((size_t)(q_base + tok) * H + head) * D + c * 8;
-        const uint32_t dst = sbase + L::Q_OFF + (c >> 3) * L::QBLK + sw128_off(r, c & 7);
-        cp_async16(dst, src, valid ? 16u : 0u);
-      }
-      cp_async_mbar_arrive(BAR(B_QFULL));
-      ++q_fill;
-      const int b0 = (lo / POD_KBLOCK) * POD_KBLOCK;
-      for (int kb = b0; kb < hi; kb += POD_KBLOCK) {
-        const int s = kv_fill & 1;
-        if (!mbar_wait(BAR(B_KVEMPTY + s), ((kv_fill >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
-        constexpr int KCH = POD_KBLOCK * (D / 8);
-        for (int idx = lt; idx < 2 * KCH; idx += 96) {
-          const int kv = idx / KCH, rem = idx % KCH;
-          const int key = rem / (D / 8), c = rem % (D / 8);
-          const int t = kb + key;
-          const bool valid = t < hi;
-          const int tt = valid ? t : kb;
-          const int pg_i = P.ps_shift >= 0 ? (tt >> P.ps_shift) : (tt / P.ps);
-          const int slot = P.ps_shift >= 0 ? (tt & (P.ps - 1)) : (tt % P.ps);
-          const int page = __ldg(P.p_kv_indices + page_base + pg_i);
-          const T* src = kvg + ((((size_t)page * 2 + kv) * P.ps + slot) * P.Hk + g) * D + c * 8;
-          const uint32_t base = sbase + (kv ? L::V_OFF : L::K_OFF) + s * (L::NKB * L::KVBLK);
-          const uint32_t dst = base + (c >> 3) * L::KVBLK + sw128_off(key, c & 7);
-          cp_async16(dst, src, valid ? 16u : 0u);
+    const uint32_t q_bytes = (uint32_t)(L::NKB * 128 * G * P.tq);
+    if (P.p_tma) {
+      // warp 5 fetches Q and K, warp 6 fetches V, each running ahead on its own
+      // ring. Lane i looks up the page of box group i and issues its boxes, so
+      // the page-table reads of one block overlap. Page ids beyond the request
+      // map to an out-of-range page coordinate, which TMA fills with zeros.
+      if (warp == 5 || warp == 6) {
+        const bool is_v = warp == 6;
+        const void* tkv = &P.tm_kv_p;
+        if (lane == 0) tma_prefetch_desc(tkv);
+        const int ngroups = POD_KBLOCK / P.kbx;
+        for (int w = w_begin; w < w_end && ok; ++w) {
+          const int32_t* rec = P.ptiles + POD_REC * P.cta_list[w];
+          const int req = rec[0], g = rec[1], tok0 = rec[2], lo = rec[4], hi = rec[5];
+          const int page_base = P.p_kv_indptr[req];
+          const int npages = P.p_kv_indptr[req + 1] - page_base;
+          if (!is_v) {
+            if (!warp_wait(BAR(B_QEMPTY), (qfill & 1) ^ 1, abort_flag)) { ok = false; break; }
+            if (lane == 0) {
+              mbar_arrive_expect_tx(BAR(B_QFULL), q_bytes);
+              for (int dh = 0; dh < L::NKB; ++dh)
+                tma_load_3d(sbase + L::Q_OFF + dh * L::QBLK, &P.tm_q_p, dh * 64, g * G,
+                            P.p_q_indptr[req] + tok0, BAR(B_QFULL));
+            }
+            ++qfill;
+          }
+          const int b0 = (lo / POD_KBLOCK) * POD_KBLOCK;
+          const int nb = (hi - b0 + POD_KBLOCK - 1) / POD_KBLOCK;
+          for (int j = 0; j < nb; ++j) {
+            const int NS = is_v ? NV : NK;
+            const int fill = is_v ? vfill : kfill;
+            const int s = fill % NS;
+            const int empty = (is_v ? B_VEMPTY : B_KEMPTY) + s, full = (is_v ? B_VFULL : B_KFULL) + s;
+            if (!warp_wait(BAR(empty), ((fill / NS) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            if (lane == 0) mbar_arrive_expect_tx(BAR(full), (uint32_t)L::KSTAGE);
+            __syncwarp();
+            const uint32_t dst0 = sbase + (is_v ? L::V_OFF : L::K_OFF) + s * L::KSTAGE;
+            const int kb = b0 + j * POD_KBLOCK;
+            for (int gi = lane; gi < ngroups; gi += 32) {
+              const int o = gi * P.kbx;
+              const int t = kb + o;
+              const int pidx = t >> P.ps_shift;
+              const int page = pidx < npages ? __ldg(P.p_kv_indices + page_base + pidx) : P.p_num_pages;
+              const int tin = P.ps >= 8 ? (t & (P.ps - 1)) : 0;
+              for (int dh = 0; dh < L::NKB; ++dh)
+                tma_load_5d(dst0 + dh * L::KVBLK + o * 128, tkv, dh * 64, g, tin, is_v ? 1 : 0, page,
+                            BAR(full));
+            }
+            if (is_v) ++vfill; else ++kfill;
+          }
         }
-        cp_async_mbar_arrive(BAR(B_KVFULL + s));
-        ++kv_fill;
       }
+    } else {
+      // cp.async gather by warps 5-7 (96 threads); Q still comes by TMA
+      const int lt = tid - 160;  // 0..95
+      const T* __restrict__ kvg = reinterpret_cast<const T*>(P.kv_p);
+      const size_t vstride = (size_t)P.ps * P.Hk * D;   // K row -> V row of the same page
+      constexpr int KCH = POD_KBLOCK * (D / 8);
+      constexpr int PER = (KCH + 95) / 96;
+      for (int w = w_begin; w < w_end && ok; ++w) {
+        const int32_t* rec = P.ptiles + POD_REC * P.cta_list[w];
+        const int req = rec[0], g = rec[1], tok0 = rec[2], lo = rec[4], hi = rec[5];
+        const int page_base = P.p_kv_indptr[req];
+        if (lt == 0) {
+          if (!mbar_wait(BAR(B_QEMPTY), (qfill & 1) ^ 1, abort_flag)) ok = false;
+          if (ok) {
+            mbar_arrive_expect_tx(BAR(B_QFULL), q_bytes);
+            for (int dh = 0; dh < L::NKB; ++dh)
+              tma_load_3d(sbase + L::Q_OFF + dh * L::QBLK, &P.tm_q_p, dh * 64, g * G,
+                          P.p_q_indptr[req] + tok0, BAR(B_QFULL));
+          }
+        }
+        ++qfill;
+        if (!ok) break;
+        const int b0 = (lo / POD_KBLOCK) * POD_KBLOCK;
+        const int nb = (hi - b0 + POD_KBLOCK - 1) / POD_KBLOCK;
+        // one K or V block: page ids first (independent loads), then the copies
+        auto load_block = [&](int j, bool is_v, uint32_t dst_base) {
+          const int kb = b0 + j * POD_KBLOCK;
+          int pages[PER];
+#pragma unroll
+          for (int i = 0; i < PER; ++i) {
+            const int idx = lt + 96 * i;
+            const int key = (idx < KCH ? idx : 0) / (D / 8);
+            const int t = kb + key;
+            const int tt = t < hi ? t : kb;
+            const int pg_i = P.ps_shift >= 0 ? (tt >> P.ps_shift) : (tt / P.ps);
+            pages[i] = __ldg(P.p_kv_indices + page_base + pg_i);
+          }
+#pragma unroll
+          for (int i = 0; i < PER; ++i) {
+            const int idx = lt + 96 * i;
+            if (idx < KCH) {
+              const int key = idx / (D / 8), c = idx % (D / 8);
+              const int t = kb + key;
+              const bool valid = t < hi;
+              const int tt = valid ? t : kb;
+              const int slot = P.ps_shift >= 0 ? (tt & (P.ps - 1)) : (tt % P.ps);
+              const T* src = kvg + (((size_t)pages[i] * 2 * P.ps + slot) * P.Hk + g) * D + c * 8;
+              cp_async16(dst_base + (c >> 3) * L::KVBLK + sw128_off(key, c & 7),
+                         is_v ? src + vstride : src, valid ? 16u : 0u);
+            }
+          }
+        };
+        for (int st = 0; st <= nb && ok; ++st) {
+          if (st < nb) {
+            const int s = kfill % NK;
+            if (!mbar_wait(BAR(B_KEMPTY + s), ((kfill / NK) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            load_block(st, false, sbase + L::K_OFF + s * L::KSTAGE);
+            cp_async_mbar_arrive(BAR(B_KFULL + s));
+            ++kfill;
+          }
+          if (st > 0) {
+            const int s = vfill % NV;
+            if (!mbar_wait(BAR(B_VEMPTY + s), ((vfill / NV) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            load_block(st - 1, true, sbase + L::V_OFF + s * L::KSTAGE);
+            cp_async_mbar_arrive(BAR(B_VFULL + s));
+            ++vfill;
+          }
+        }
+      }
+      cp_async_wait_all();
     }
     if (!ok) {
       *abort_flag = 1;
       raise_status(P.status, POD_STATUS_TIMEOUT);
     }
-    cp_async_wait_all();
   } else if (warp == 4) {
     // ------------------------------------------------------------ MMA issuer
+    // Order per tile: QK_0, [QK_1, PV_0], [QK_2, PV_1], ..., PV_{nb-1}. QK_{j+2}
+    // reuses the TMEM columns of S_j / P_j; it is issued after PV_j by this one
+    // thread, and MMAs issued by one thread run in order.
     if (lane == 0) {
       const bool bf16 = Pack<T>::kBF16;
       const uint32_t id_qk = idesc_f16(bf16, 128, POD_KBLOCK, false, false);
       const uint32_t id_pv = idesc_f16(bf16, 128, D, false, true);
-      int kv_fill = 0, q_fill = 0, s_cnt = 0, p_cnt = 0;
+      int kuse = 0, vuse = 0, qfill = 0, sc0 = 0;
       bool ok = true;
       for (int w = w_begin; w < w_end && ok; ++w) {
         const int32_t* rec = P.ptiles + POD_REC * P.cta_list[w];
-        const int lo = rec[4], hi = rec[5];
+        const int req = rec[0], lo = rec[4], hi = rec[5];
+        const int kv_len = P.p_kv_len[req];
         const int b0 = (lo / POD_KBLOCK) * POD_KBLOCK;
         const int nb = (hi - b0 + POD_KBLOCK - 1) / POD_KBLOCK;
-        if (!mbar_wait(BAR(B_QFULL), q_fill & 1, abort_flag)) { ok = false; break; }
-        ++q_fill;
+        if (!mbar_wait(BAR(B_QFULL), qfill & 1, abort_flag)) { ok = false; break; }
+        ++qfill;
         for (int j = 0; j <= nb && ok; ++j) {
           if (j < nb) {
-            const int f = kv_fill + j;
-            const int s = f & 1;
-            if (!mbar_wait(BAR(B_KVFULL + s), (f >> 1) & 1, abort_flag)) { ok = false; break; }
-            const int sc = s_cnt + j;
-            const int b = sc & 1;
-            if (!mbar_wait(BAR(B_SEMPTY + b), ((sc >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            const int s = kuse % NK;
+            if (!mbar_wait(BAR(B_KFULL + s), (kuse / NK) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
             fence_proxy_async();
+            const int b = (sc0 + j) & 1;
             const uint32_t qa = sbase + L::Q_OFF;
-            const uint32_t ka = sbase + L::K_OFF + s * (L::NKB * L::KVBLK);
+            const uint32_t ka = sbase + L::K_OFF + s * L::KSTAGE;
 #pragma unroll
             for (int k = 0; k < D / 16; ++k) {
               const uint64_t ad = sdesc_sw128(qa + (k >> 2) * L::QBLK + (k & 3) * 32, 16, 1024);
@@ -215,29 +316,47 @@ __device__ void prefill_role(const PodParams& P, uint8_t* smem, int cta) {
               mma_f16_ss(tmem + L::TM_S + b * POD_KBLOCK, ad, bd, id_qk, k > 0 ? 1u : 0u);
             }
             mma_commit(BAR(B_SFULL + b));
+            mma_commit(BAR(B_KEMPTY + s));
             if (j == nb - 1) mma_commit(BAR(B_QEMPTY));
+            ++kuse;
           }
           if (j > 0) {
-            // O += P_{j-1} V_{j-1}
-            if (!mbar_wait(BAR(B_PFULL), p_cnt & 1, abort_flag)) { ok = false; break; }
-            ++p_cnt;
+            // O += P_{j-1} V_{j-1}, P_{j-1} read from TMEM (columns of S_{j-1})
+            const int i = j - 1;
+            const int sc = sc0 + i;
+            const int b = sc & 1;
+            const int s = vuse % NV;
+            if (!mbar_wait(BAR(B_VFULL + s), (vuse / NV) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(BAR(B_PFULL + b), (sc >> 1) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            fence_proxy_async();
-            const int s = (kv_fill + j - 1) & 1;
-            const uint32_t pa = sbase + L::P_OFF;
-            const uint32_t va = sbase + L::V_OFF + s * (L::NKB * L::KVBLK);
-#pragma unroll
-            for (int k = 0; k < POD_KBLOCK / 16; ++k) {
-              const uint64_t ad = sdesc_sw128(pa + k * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(va + k * 2048, L::KVBLK, 1024);
-              mma_f16_ss(tmem + L::TM_O, ad, bd, id_pv, (j > 1 || k > 0) ? 1u : 0u);
+            const uint32_t va = sbase + L::V_OFF + s * L::KSTAGE;
+            // 16-key steps past hi carry P = 0 for every row: skip them. Rows at
+            // or past kv_len inside the last step come from unused slots of the
+            // request's last page (TMA copies whole pages): zero them so that
+            // P = 0 never meets a non-finite value.
+            const int kb_i = b0 + i * POD_KBLOCK;
+            const int ksteps = (min(hi, kb_i + POD_KBLOCK) - kb_i + 15) >> 4;
+            if (P.p_tma && kb_i + ksteps * 16 > kv_len) {
+              for (int rr = kv_len - kb_i; rr < ksteps * 16; ++rr)
+                for (int dh = 0; dh < L::NKB; ++dh)
+                  for (int c = 0; c < 8; ++c)
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(
+                                     va + dh * L::KVBLK + sw128_off(rr, c)),
+                                 "r"(0u)
+                                 : "memory");
             }
-            mma_commit(BAR(B_PVDONE));
-            mma_commit(BAR(B_KVEMPTY + s));
+            fence_proxy_async();
+            for (int k = 0; k < ksteps; ++k) {
+              const uint64_t bd = sdesc_sw128(va + k * 2048, L::KVBLK, 1024);
+              mma_f16_ts(tmem + L::TM_O, tmem + L::TM_S + b * POD_KBLOCK + k * 8, bd, id_pv,
+                         (i > 0 || k > 0) ? 1u : 0u);
+            }
+            mma_commit(BAR(B_PVDONE + b));
+            mma_commit(BAR(B_VEMPTY + s));
+            ++vuse;
           }
         }
-        kv_fill += nb;
-        s_cnt += nb;
+        sc0 += nb;
       }
       if (!ok) {
         *abort_flag = 1;
@@ -250,7 +369,7 @@ __device__ void prefill_role(const PodParams& P, uint8_t* smem, int cta) {
     const int r = tid;  // query row of the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     T* __restrict__ outg = reinterpret_cast<T*>(P.out_p);
-    int s_cnt = 0, pv_cnt = 0;
+    int sc0 = 0;
     bool ok = true;
     const float NEG_INF = -INFINITY;
     for (int w = w_begin; w < w_end && ok; ++w) {
@@ -271,20 +390,19 @@ __device__ void prefill_role(const PodParams& P, uint8_t* smem, int cta) {
       float m_ref = NEG_INF, l = 0.f;
       for (int j = 0; j < nb; ++j) {
         const int kb = b0 + j * POD_KBLOCK;
-        const int sc = s_cnt + j;
+        const int sc = sc0 + j;
         const int b = sc & 1;
         if (!warp_wait(BAR(B_SFULL + b), (sc >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
+        const uint32_t s_addr = tmem + lane_base + L::TM_S + b * POD_KBLOCK;
         float s[POD_KBLOCK];
-        tmem_ld32(tmem + lane_base + L::TM_S + b * POD_KBLOCK, s);
-        tmem_ld32(tmem + lane_base + L::TM_S + b * POD_KBLOCK + 32, s + 32);
-        tc_fence_before();
-        mbar_arrive(BAR(B_SEMPTY + b));
+        tmem_ld32(s_addr, s);
+        tmem_ld32(s_addr + 32, s + 32);
         const bool full = (kb >= row_lo) && (kb + POD_KBLOCK <= row_hi);
         float bmax = NEG_INF;
 #pragma unroll
         for (int i = 0; i < POD_KBLOCK; ++i) {
-          float x = s[i] * P.scale_log2;
+          float x = s[i];
           if (!full) {
             const int t = kb + i;
             if (t < row_lo || t >= row_hi) x = NEG_INF;
@@ -292,59 +410,51 @@ __device__ void prefill_role(const PodParams& P, uint8_t* smem, int cta) {
           s[i] = x;
           bmax = fmaxf(bmax, x);
         }
-        const float m_new = fmaxf(m_ref, bmax);
+        const float scale = P.scale_log2;
+        const float m_new = fmaxf(m_ref, bmax * scale);
         const bool rescale = m_new > m_ref + 8.0f;   // also true for the first finite max
         const float m_use = rescale ? m_new : m_ref;
         const float m_sub = (m_use == NEG_INF) ? 0.f : m_use;
         float rs = 0.f;
+        uint32_t pk[POD_KBLOCK / 2];
 #pragma unroll
-        for (int i = 0; i < POD_KBLOCK; ++i) {
-          s[i] = ex2(s[i] - m_sub);
-          rs += s[i];
+        for (int i = 0; i < POD_KBLOCK; i += 2) {
+          const float e0 = ex2(fmaf(s[i], scale, -m_sub)), e1 = ex2(fmaf(s[i + 1], scale, -m_sub));
+          rs += e0 + e1;
+          pk[i / 2] = Pack<T>::two(e0, e1);
         }
-        if (j > 0) {
-          // PV of the previous block must finish before P is overwritten or O rescaled
-          if (!warp_wait(BAR(B_PVDONE), pv_cnt & 1, abort_flag)) { ok = false; break; }
-          ++pv_cnt;
+        const bool need = rescale && (m_ref != NEG_INF) && j > 0;
+        if (__any_sync(0xffffffffu, need)) {
+          // O holds PV up to block j-1: wait for PV_{j-1}, then rescale it in TMEM
+          const int sp = sc - 1;
+          if (!warp_wait(BAR(B_PVDONE + (sp & 1)), (sp >> 1) & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const bool need = rescale && (m_ref != NEG_INF);
-          if (__any_sync(0xffffffffu, need)) {
-            const float alpha = need ? ex2(m_ref - m_use) : 1.f;
+          const float alpha = need ? ex2(m_ref - m_use) : 1.f;
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-              float o[32];
-              tmem_ld32(tmem + lane_base + L::TM_O + c, o);
+          for (int c = 0; c < D; c += 32) {
+            float o[32];
+            tmem_ld32(tmem + lane_base + L::TM_O + c, o);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] *= alpha;
-              tmem_st32(tmem + lane_base + L::TM_O + c, o);
-            }
-            tmem_wait_st();
-            l *= alpha;
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(tmem + lane_base + L::TM_O + c, o);
           }
+          l *= alpha;
         }
         m_ref = m_use;
         l += rs;
-        // P row -> shared memory (A operand of the PV MMA), 128B swizzle
-        const uint32_t prow_addr = sbase + L::P_OFF;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t u0 = Pack<T>::two(s[8 * c + 0], s[8 * c + 1]);
-          uint32_t u1 = Pack<T>::two(s[8 * c + 2], s[8 * c + 3]);
-          uint32_t u2 = Pack<T>::two(s[8 * c + 4], s[8 * c + 5]);
-          uint32_t u3 = Pack<T>::two(s[8 * c + 6], s[8 * c + 7]);
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(prow_addr + sw128_off(r, c)),
-                       "r"(u0), "r"(u1), "r"(u2), "r"(u3)
-                       : "memory");
-        }
-        fence_proxy_async();
+        // P_j (packed 16-bit pairs) over the first 32 columns of S_j: A operand of PV_j
+        tmem_st32u(s_addr, pk);
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(BAR(B_PFULL));
+        mbar_arrive(BAR(B_PFULL + b));
       }
       if (!ok) break;
-      if (!warp_wait(BAR(B_PVDONE), pv_cnt & 1, abort_flag)) { ok = false; break; }
-      ++pv_cnt;
+      {
+        const int sl = sc0 + nb - 1;
+        if (!warp_wait(BAR(B_PVDONE + (sl & 1)), (sl >> 1) & 1, abort_flag)) { ok = false; break; }
+      }
       tc_fence_after();
-      s_cnt += nb;
+      sc0 += nb;
       // epilogue: every lane loads (tcgen05.ld is warp-collective), valid rows store
       float denom = l;
       if (P.has_sinks && prow < 0) denom += ex2(P.sinks[head] * 1.4426950408889634f - m_ref);
@@ -409,17 +519,32 @@ template <typename T, int D>
 __device__ void decode_role(const PodParams& P, uint8_t* smem, int cta) {
   using L = DLayout<D>;
   constexpr bool BF16 = Pack<T>::kBF16;
+  constexpr int NKB = L::NKB;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int mt = warp >> 2, ks = warp & 3;
   const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L::BAR_OFF;   // full[NSTAGE]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR_OFF + 64);
   const int G = P.G, H = P.H;
-  const T* __restrict__ qg = reinterpret_cast<const T*>(P.q_d);
-  const T* __restrict__ kvg = reinterpret_cast<const T*>(P.kv_d);
   T* __restrict__ outg = reinterpret_cast<T*>(P.out_d);
   const float NEG_INF = -INFINITY;
   const int w_begin = P.cta_ptr[cta], w_end = P.cta_ptr[cta + 1];
 
-  for (int w = w_begin; w < w_end; ++w) {
+  if (tid == 0) {
+    for (int s = 0; s < L::NSTAGE; ++s) mbar_init(bar0 + 8 * s, P.d_tma ? 1u : (uint32_t)kThreads);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (P.d_tma && tid == 0) {
+    tma_prefetch_desc(&P.tm_kv_d);
+    tma_prefetch_desc(&P.tm_q_d);
+  }
+  const uint32_t q_bytes = (uint32_t)(NKB * 128 * G * P.tu);
+  int fills = 0;
+  bool ok = true;
+
+  for (int w = w_begin; w < w_end && ok; ++w) {
     const int32_t* rec = P.ditems + POD_REC * P.cta_list[w];
     const int req = rec[0], g = rec[1], tok0 = rec[2], ntok = rec[3], k0 = rec[4], k1 = rec[5];
     const int prow = rec[6];
@@ -429,39 +554,87 @@ __device__ void decode_role(const PodParams& P, uint8_t* smem, int cta) {
     const int q_base = P.d_q_indptr[req];
     const int q_len = P.d_q_indptr[req + 1] - q_base;
     const int page_base = P.d_kv_indptr[req];
-    const int nst = (k1 - k0 + L::KEYS - 1) / L::KEYS;
+    const int npages = P.d_kv_indptr[req + 1] - page_base;
+    const int kb0 = (k0 / POD_DECODE_STAGE) * POD_DECODE_STAGE;
+    const int nst = (k1 - kb0 + POD_DECODE_STAGE - 1) / POD_DECODE_STAGE;
 
-    // Q rows (zero beyond R) go with the first stage's commit group
-    for (int idx = tid; idx < POD_DECODE_ROWS * L::NCH; idx += kThreads) {
-      const int r = idx / L::NCH, c = idx % L::NCH;
-      const bool valid = r < R;
-      const int tok = tok0 + (valid ? r / G : 0);
-      const int head = g * G + (valid ? r % G : 0);
-      const T* src = qg + ((size_t)(q_base + tok) * H + head) * D + c * 8;
-      cp_async16(sbase + L::Q_OFF + r * L::ROWB + ((c ^ (r & 7)) << 4), src, valid ? 16u : 0u);
-    }
-    auto issue_stage = [&](int st) {
-      const int kbase = k0 + st * L::KEYS;
-      const uint32_t sb = sbase + L::STAGE_OFF + (st % L::NSTAGE) * L::STAGE_BYTES;
-      constexpr int CH = L::KEYS * L::NCH;
-      for (int idx = tid; idx < 2 * CH; idx += kThreads) {
-        const int kv = idx / CH, rem = idx % CH;
-        const int key = rem / L::NCH, c = rem % L::NCH;
-        const int t = kbase + key;
-        const bool valid = t < k1;
-        const int tt = valid ? t : k0;
-        const int pg_i = P.ps_shift >= 0 ? (tt >> P.ps_shift) : (tt / P.ps);
-        const int slot = P.ps_shift >= 0 ? (tt & (P.ps - 1)) : (tt % P.ps);
-        const int page = __ldg(P.d_kv_indices + page_base + pg_i);
-        const T* src = kvg + ((((size_t)page * 2 + kv) * P.ps + slot) * P.Hk + g) * D + c * 8;
-        cp_async16(sb + kv * L::KBYTES + key * L::ROWB + ((c ^ (key & 7)) << 4), src,
-                   valid ? 16u : 0u);
+    // fill stage st of this item (Q travels with stage 0) into ring slot (fills + st) % 3
+    auto issue = [&](int st) {
+      const int f = fills + st;
+      const int buf = f % L::NSTAGE;
+      const uint32_t full = bar0 + 8 * buf;
+      const uint32_t sk = sbase + L::STAGE_OFF + buf * L::STAGE_BYTES;
+      const uint32_t sv = sk + L::KBYTES;
+      const int kb = kb0 + st * POD_DECODE_STAGE;
+      if (P.d_tma) {
+        // warp 0: lane 0 registers the bytes, lane i fetches box group i
+        if (warp == 0) {
+          fence_proxy_async();  // earlier generic accesses to the slot come first
+          if (lane == 0) {
+            mbar_arrive_expect_tx(full, 2u * L::KBYTES + (st == 0 ? q_bytes : 0u));
+            if (st == 0)
+              for (int dh = 0; dh < NKB; ++dh)
+                tma_load_3d(sbase + L::Q_OFF + dh * L::QDH, &P.tm_q_d, dh * 64, g * G, q_base + tok0,
+                            full);
+          }
+          __syncwarp();
+          for (int gi = lane; gi < POD_DECODE_STAGE / P.kbx; gi += 32) {
+            const int o = gi * P.kbx;
+            const int t = kb + o;
+            const int pidx = t >> P.ps_shift;
+            const int page = pidx < npages ? __ldg(P.d_kv_indices + page_base + pidx) : P.d_num_pages;
+            const int tin = P.ps >= 8 ? (t & (P.ps - 1)) : 0;
+            for (int dh = 0; dh < NKB; ++dh) {
+              tma_load_5d(sk + dh * L::KDH + o * 128, &P.tm_kv_d, dh * 64, g, tin, 0, page, full);
+              tma_load_5d(sv + dh * L::KDH + o * 128, &P.tm_kv_d, dh * 64, g, tin, 1, page, full);
+            }
+          }
+        }
+      } else {
+        const T* __restrict__ qg = reinterpret_cast<const T*>(P.q_d);
+        const T* __restrict__ kvg = reinterpret_cast<const T*>(P.kv_d);
+        if (st == 0) {
+          for (int idx = tid; idx < POD_DECODE_ROWS * (D / 8); idx += kThreads) {
+            const int r = idx / (D / 8), c = idx % (D / 8);
+            const bool valid = r < R;
+            const int tok = tok0 + (valid ? r / G : 0);
+            const int head = g * G + (valid ? r % G : 0);
+            const T* src = qg + ((size_t)(q_base + tok) * H + head) * D + c * 8;
+            cp_async16(sbase + L::Q_OFF + (c >> 3) * L::QDH + sw128_off(r, c & 7), src,
+                       valid ? 16u : 0u);
+          }
+        }
+        constexpr int CH = POD_DECODE_STAGE * (D / 8);
+        constexpr int PER = CH / kThreads;
+        static_assert(CH % kThreads == 0, "stage chunks must divide evenly");
+        int pages[PER];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          const int key = (tid + kThreads * i) / (D / 8);
+          const int t = kb + key;
+          const int tt = (t >= k0 && t < k1) ? t : k0;
+          const int pg_i = P.ps_shift >= 0 ? (tt >> P.ps_shift) : (tt / P.ps);
+          pages[i] = __ldg(P.d_kv_indices + page_base + pg_i);
+        }
+        const size_t vstride = (size_t)P.ps * P.Hk * D;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          const int idx = tid + kThreads * i;
+          const int key = idx / (D / 8), c = idx % (D / 8);
+          const int t = kb + key;
+          const bool valid = t >= k0 && t < k1;
+          const int tt = valid ? t : k0;
+          const int slot = P.ps_shift >= 0 ? (tt & (P.ps - 1)) : (tt % P.ps);
+          const T* src = kvg + (((size_t)pages[i] * 2 * P.ps + slot) * P.Hk + g) * D + c * 8;
+          const uint32_t off = (c >> 3) * L::KDH + sw128_off(key, c & 7);
+          cp_async16(sk + off, src, valid ? 16u : 0u);
+          cp_async16(sv + off, src + vstride, valid ? 16u : 0u);
+        }
+        cp_async_mbar_arrive(full);
       }
     };
-    issue_stage(0);
-    cp_async_commit();
-    if (nst > 1) issue_stage(1);
-    cp_async_commit();
+    const int npre = nst < L::NSTAGE ? nst : L::NSTAGE;
+    for (int st = 0; st < npre; ++st) issue(st);
 
     // rows of this thread inside its m-tile: r0 = 16 mt + lane/4, r1 = r0 + 8
     int row_lo[2], row_hi[2];
@@ -470,45 +643,45 @@ __device__ void decode_role(const PodParams& P, uint8_t* smem, int cta) {
       const int rr = mt * 16 + (lane >> 2) + 8 * h2;
       const int tok = tok0 + (rr < R ? rr / G : 0);
       const int pd = kv_len - q_len + tok;
-      row_hi[h2] = P.causal ? min(pd + 1, kv_len) : kv_len;
-      row_lo[h2] = P.window_left >= 0 ? max(pd - P.window_left, 0) : 0;
+      row_hi[h2] = min(P.causal ? min(pd + 1, kv_len) : kv_len, k1);
+      row_lo[h2] = max(P.window_left >= 0 ? max(pd - P.window_left, 0) : 0, k0);
     }
     float m[2] = {NEG_INF, NEG_INF}, l[2] = {0.f, 0.f};
     float o[D / 8][4];
 #pragma unroll
     for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     const bool active = mt < Mt;
+    const int mi = lane >> 3;
 
     for (int st = 0; st < nst; ++st) {
-      if (st + 2 < nst) issue_stage(st + 2);
-      cp_async_commit();
-      cp_async_wait<2>();
-      __syncthreads();
-      const int kbase = k0 + st * L::KEYS + ks * 16;
-      if (active && kbase < k1) {
+      const int f = fills + st;
+      const int buf = f % L::NSTAGE;
+      const bool got = mbar_wait(bar0 + 8 * buf, (f / L::NSTAGE) & 1, abort_flag);
+      const int kbase = kb0 + st * POD_DECODE_STAGE + ks * 16;
+      if (got && active && kbase < k1 && kbase + 16 > k0) {
         const uint32_t sq = sbase + L::Q_OFF;
-        const uint32_t sk = sbase + L::STAGE_OFF + (st % L::NSTAGE) * L::STAGE_BYTES;
+        const uint32_t sk = sbase + L::STAGE_OFF + buf * L::STAGE_BYTES;
         const uint32_t sv = sk + L::KBYTES;
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-        const int mi = lane >> 3;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           uint32_t a[4], b[4];
           {
             const int rr = mt * 16 + (lane & 7) + ((mi & 1) << 3);
             const int c = kk * 2 + (mi >> 1);
-            ldsm_x4(sq + rr * L::ROWB + ((c ^ (rr & 7)) << 4), a[0], a[1], a[2], a[3]);
+            ldsm_x4(sq + (c >> 3) * L::QDH + sw128_off(rr, c & 7), a[0], a[1], a[2], a[3]);
           }
           {
             const int key = ks * 16 + (lane & 7) + ((mi >> 1) << 3);
             const int c = kk * 2 + (mi & 1);
-            ldsm_x4(sk + key * L::ROWB + ((c ^ (key & 7)) << 4), b[0], b[1], b[2], b[3]);
+            ldsm_x4(sk + (c >> 3) * L::KDH + sw128_off(key, c & 7), b[0], b[1], b[2], b[3]);
           }
           mma16816<BF16>(s0, a, b[0], b[1]);
           mma16816<BF16>(s1, a, b[2], b[3]);
         }
-        // scale, mask, online softmax (rows h2 = 0: c0,c1; h2 = 1: c2,c3)
+        // mask, online softmax in base 2 (rows h2 = 0: c0,c1; h2 = 1: c2,c3)
         const int kq = kbase + 2 * (lane & 3);
+        const float scale = P.scale_log2;
         float mx[2];
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
@@ -519,16 +692,15 @@ __device__ void decode_role(const PodParams& P, uint8_t* smem, int cta) {
           float mm = NEG_INF;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            float x = *v[e] * P.scale_log2;
-            if (key[e] >= k1 || key[e] < row_lo[h2] || key[e] >= row_hi[h2]) x = NEG_INF;
+            float x = *v[e];
+            if (key[e] < row_lo[h2] || key[e] >= row_hi[h2]) x = NEG_INF;
             *v[e] = x;
             mm = fmaxf(mm, x);
           }
           mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, 1));
           mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, 2));
-          mx[h2] = mm;
+          mx[h2] = mm * scale;
         }
-        uint32_t pa[4];
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           const float m_new = fmaxf(m[h2], mx[h2]);
@@ -537,10 +709,10 @@ __device__ void decode_role(const PodParams& P, uint8_t* smem, int cta) {
           m[h2] = m_new;
           float* a0 = s0 + 2 * h2;
           float* a1 = s1 + 2 * h2;
-          a0[0] = ex2(a0[0] - m_sub);
-          a0[1] = ex2(a0[1] - m_sub);
-          a1[0] = ex2(a1[0] - m_sub);
-          a1[1] = ex2(a1[1] - m_sub);
+          a0[0] = ex2(fmaf(a0[0], scale, -m_sub));
+          a0[1] = ex2(fmaf(a0[1], scale, -m_sub));
+          a1[0] = ex2(fmaf(a1[0], scale, -m_sub));
+          a1[1] = ex2(fmaf(a1[1], scale, -m_sub));
           l[h2] = l[h2] * alpha + (a0[0] + a0[1] + a1[0] + a1[1]);
 #pragma unroll
           for (int i = 0; i < D / 8; ++i) {
@@ -548,24 +720,33 @@ __device__ void decode_role(const PodParams& P, uint8_t* smem, int cta) {
             o[i][2 * h2 + 1] *= alpha;
           }
         }
+        uint32_t pa[4];
         pa[0] = Pack<T>::two(s0[0], s0[1]);
         pa[1] = Pack<T>::two(s0[2], s0[3]);
         pa[2] = Pack<T>::two(s1[0], s1[1]);
         pa[3] = Pack<T>::two(s1[2], s1[3]);
+        // V rows at or past kv_len may be unused slots of the last page: zero
+        // them in the fragments so that P = 0 never meets a non-finite value
+        uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+        if (kbase + 16 > kv_len) {
+          vm0 = (kq < kv_len ? 0x0000ffffu : 0u) | (kq + 1 < kv_len ? 0xffff0000u : 0u);
+          vm1 = (kq + 8 < kv_len ? 0x0000ffffu : 0u) | (kq + 9 < kv_len ? 0xffff0000u : 0u);
+        }
 #pragma unroll
         for (int j = 0; j < D / 16; ++j) {
           uint32_t b[4];
           const int key = ks * 16 + (lane & 7) + ((mi & 1) << 3);
           const int c = 2 * j + (mi >> 1);
-          ldsm_x4_t(sv + key * L::ROWB + ((c ^ (key & 7)) << 4), b[0], b[1], b[2], b[3]);
-          mma16816<BF16>(o[2 * j], pa, b[0], b[1]);
-          mma16816<BF16>(o[2 * j + 1], pa, b[2], b[3]);
+          ldsm_x4_t(sv + (c >> 3) * L::KDH + sw128_off(key, c & 7), b[0], b[1], b[2], b[3]);
+          mma16816<BF16>(o[2 * j], pa, b[0] & vm0, b[1] & vm1);
+          mma16816<BF16>(o[2 * j + 1], pa, b[2] & vm0, b[3] & vm1);
         }
       }
-      __syncthreads();
+      if (!__syncthreads_and(got)) { ok = false; break; }
+      if (st + L::NSTAGE < nst) issue(st + L::NSTAGE);
     }
-    cp_async_wait_all();
-    __syncthreads();
+    fills += nst;
+    if (!ok) break;
 
     // ---- combine the 4 key slices of each m-tile through shared memory
     float* scr_o = reinterpret_cast<float*>(smem + L::SCR_O);
@@ -634,20 +815,25 @@ __device__ void decode_role(const PodParams& P, uint8_t* smem, int cta) {
     }
     __syncthreads();
   }
+  if (!ok) {
+    *abort_flag = 1;
+    if (tid == 0) raise_status(P.status, POD_STATUS_TIMEOUT);
+  }
+  cp_async_wait_all();
 }
 
 // ============================================================ kernels
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, POD_CTAS_PER_SM) pod_kernel(const PodParams P) {
+__global__ void __launch_bounds__(kThreads, POD_CTAS_PER_SM) pod_kernel(const __grid_constant__ PodParams P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   // the merge kernel may start its prologue now; it waits for this grid's completion
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int cta = blockIdx.x;
+  if ((smem_u32(smem) & 1023u) != 0u) {  // 128B-swizzle atoms need 1024-byte alignment
+    if (threadIdx.x == 0) raise_status(P.status, POD_STATUS_ALIGN);
+    return;
+  }
   if (cta < P.n_p_ctas) {
-    if ((smem_u32(smem) & 1023u) != 0u) {  // 128B-swizzle atoms need 1024-byte alignment
-      if (threadIdx.x == 0) raise_status(P.status, POD_STATUS_ALIGN);
-      return;
-    }
     prefill_role<T, D>(P, smem, cta);
   } else {
     decode_role<T, D>(P, smem, cta);
@@ -655,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, POD_CTAS_PER_SM) pod_kernel(const Po
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(256) pod_merge_kernel(const PodParams P) {
+__global__ void __launch_bounds__(256) pod_merge_kernel(const __grid_constant__ PodParams P) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;

@@ -21,6 +21,7 @@
 //   mrow_ptr[n_groups+1]: prefix sums of R over merge groups.
 //   summary (pod_plan_table which = 0): see PodSummary below.
 #pragma once
+#include <cuda.h>
 #include <stdint.h>
 
 #define POD_REC 8
@@ -34,11 +35,20 @@ enum PodSummary {
   S_H = 0, S_HK, S_D, S_PS, S_CAUSAL, S_WINDOW, S_DTYPE, S_SINKS, S_NUM_SMS, S_GRID,
   S_NP_CTAS, S_ND_CTAS, S_NTILES, S_NITEMS, S_NGROUPS, S_NMROWS, S_NPROWS,
   S_P_ROWS, S_D_ROWS, S_P_BATCH, S_D_BATCH, S_DECODE_CHUNK, S_WS_LO, S_WS_HI,
-  S_COUNT
+  S_P_TMA, S_D_TMA, S_COUNT
 };
 
-// Everything a kernel needs, passed by value at launch.
+// Everything a kernel needs, passed by value at launch (as a __grid_constant__
+// parameter, so that the tensor maps can be addressed by TMA instructions).
 struct PodParams {
+  // TMA descriptors: Q as [rows, H, d] (box 64 x G x tokens), the paged cache
+  // as [pages, 2, ps, Hk, d] (box 64 x 1 x rows x 1 x pages); valid when the
+  // half's *_tma flag is set (Q maps whenever the half is non-empty).
+  CUtensorMap tm_q_p, tm_kv_p, tm_q_d, tm_kv_d;
+  int p_tma, d_tma;          // K/V of the half are fetched with TMA page boxes
+  int kbx;                   // keys per K/V box: min(ps, 64) for ps >= 8, else 8
+  int p_num_pages, d_num_pages;
+  int tq, tu;                // tokens per prefill tile / per decode unit
   int H, Hk, G, d, ps, ps_shift, causal, window_left, has_sinks;
   float scale_log2;          // sm_scale * log2(e)
   int n_p_ctas, grid;

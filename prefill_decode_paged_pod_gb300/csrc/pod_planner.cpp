@@ -31,25 +31,44 @@ namespace {
 
 constexpr int kInvalid = 1, kUnsupported = 2;
 
-// ---- cost model (nanoseconds); constants calibrated on GB300 -------------
+// ---- cost model; constants measured on GB300 ------------------------------
+// A CTA's speed depends on what shares its SM: the fused launch runs two CTAs
+// per SM, and CTA c sits on SM c mod num_sms (the first num_sms CTAs take one
+// slot of every SM, the next num_sms the second slot).
 struct CostModel {
-  double p_block_ns;     // one 64-key block of one 128-row prefill tile, one CTA
+  double p_block_ns[3];  // one 64-key block of a 128-row tile; SM shared with
+                         // [0] nothing, [1] a decode CTA, [2] another prefill CTA
   double p_tile_ns;      // per-tile setup + epilogue
-  double p_flops_per_s;  // whole-GPU prefill rate floor
-  double d_key_ns;       // one key (K+V rows) of one decode item, one CTA
-  double d_item_ns;      // per-item setup, pipeline drain and partial write
-  double d_bytes_per_s;  // whole-GPU HBM rate floor
+  double p_flops_per_ns; // whole-GPU prefill ceiling
+  double d_bytes_per_ns[3];  // decode stream of one CTA; SM shared with
+                             // [0] nothing, [1] a prefill CTA, [2] another decode CTA
+  double d_item_ns;      // per-item setup, pipeline fill and drain, output
+  double hbm_bytes_per_ns;   // whole-GPU decode ceiling
 };
 
 CostModel cost_model(int d) {
   CostModel c;
-  c.p_block_ns = 420.0 + 730.0 * d / 128.0;
+  const double f = 0.4 + 0.6 * d / 128.0;   // head_dim 64 halves the MMA work
+  c.p_block_ns[0] = 1100.0 * f;
+  c.p_block_ns[1] = 1300.0 * f;
+  c.p_block_ns[2] = 1700.0 * f;
   c.p_tile_ns = 1500.0;
-  c.p_flops_per_s = 1.10e15;
-  c.d_key_ns = (4.0 * d) / 40.0;      // 2 rows x d x 2 B at ~40 GB/s per CTA
+  c.p_flops_per_ns = 1.2e6;
+  c.d_bytes_per_ns[0] = 40.0;
+  c.d_bytes_per_ns[1] = 36.0;
+  c.d_bytes_per_ns[2] = 22.0;
   c.d_item_ns = 2500.0;
-  c.d_bytes_per_s = 5.6e12;
+  c.hbm_bytes_per_ns = 5600.0;
   return c;
+}
+
+// Co-residency class of CTA c (0 alone, 1 other role, 2 same role) when CTAs
+// [0, n_p) run prefill and [n_p, n_p + n_d) decode.
+int neighbour_class(int c, int n_p, int n_d, int S) {
+  const int other = c < S ? c + S : c - S;
+  if (other >= n_p + n_d) return 0;
+  const bool me_p = c < n_p, other_p = other < n_p;
+  return me_p == other_p ? 2 : 1;
 }
 
 int fail(std::string* err, int code, const std::string& msg) {
@@ -138,27 +157,51 @@ int64_t nblocks(int lo, int hi) {
   return (hi - b0 + POD_KBLOCK - 1) / POD_KBLOCK;
 }
 
-// Longest-processing-time-first list scheduling. Returns the makespan and, if
-// `assign` is given, the CTA of each job. Ties: larger cost first, then lower
-// job index; the least-loaded CTA with the lowest index wins.
-double lpt(const std::vector<double>& cost, int n_cta, std::vector<int>* order,
-           std::vector<int>* assign) {
-  if (n_cta <= 0 || cost.empty()) return 0.0;
-  std::vector<int> idx(cost.size());
+// Longest-processing-time-first list scheduling on CTAs of different speeds:
+// jobs in decreasing size go to the CTA that would finish them first. `work`
+// is in work units, `rate[c]` units per ns, `overhead` ns per job. Returns the
+// makespan (ns) and, if `assign` is given, the CTA of each job. CTAs of equal
+// rate form one class (a min-heap on load, ties to the lowest index), so a job
+// costs one probe per class. Ties between jobs: larger first, then lower index.
+double lpt(const std::vector<double>& work, double overhead, const std::vector<double>& rate,
+           std::vector<int>* order, std::vector<int>* assign) {
+  const int n_cta = (int)rate.size();
+  if (n_cta <= 0 || work.empty()) return 0.0;
+  std::vector<int> idx(work.size());
   for (size_t i = 0; i < idx.size(); ++i) idx[i] = (int)i;
-  std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return cost[a] > cost[b]; });
+  std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return work[a] > work[b]; });
   typedef std::pair<double, int> Slot;
-  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-  for (int c = 0; c < n_cta; ++c) heap.push(Slot(0.0, c));
-  if (assign) assign->assign(cost.size(), -1);
+  typedef std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> Heap;
+  std::vector<double> rates;
+  std::vector<Heap> heaps;
+  for (int c = 0; c < n_cta; ++c) {
+    size_t k = 0;
+    while (k < rates.size() && rates[k] != rate[c]) ++k;
+    if (k == rates.size()) {
+      rates.push_back(rate[c]);
+      heaps.emplace_back();
+    }
+    heaps[k].push(Slot(0.0, c));
+  }
+  if (assign) assign->assign(work.size(), -1);
   double makespan = 0.0;
   for (int j : idx) {
-    Slot s = heap.top();
-    heap.pop();
-    s.first += cost[j];
+    int best = -1;
+    double best_t = 0.0;
+    for (size_t k = 0; k < heaps.size(); ++k) {
+      const Slot& s = heaps[k].top();
+      const double t = s.first + overhead + work[j] / rates[k];
+      if (best < 0 || t < best_t || (t == best_t && s.second < heaps[best].top().second)) {
+        best = (int)k;
+        best_t = t;
+      }
+    }
+    Slot s = heaps[best].top();
+    heaps[best].pop();
+    s.first = best_t;
     makespan = std::max(makespan, s.first);
     if (assign) (*assign)[j] = s.second;
-    heap.push(s);
+    heaps[best].push(s);
   }
   if (order) *order = idx;
   return makespan;
@@ -194,30 +237,33 @@ struct DecodeChoice {
   int chunk = 0;
 };
 
-double decode_time(const std::vector<DecodeUnit>& units, int n_cta, int chunk, int G, int d,
-                   const CostModel& cm, double total_bytes) {
-  std::vector<double> cost;
+// bytes of K/V a decode item streams: keys x 2 rows (K, V) x d x 2 bytes
+double item_bytes(int keys, int d) { return 4.0 * d * (double)keys; }
+
+double decode_time(const std::vector<DecodeUnit>& units, const std::vector<double>& rate,
+                   int chunk, int G, int d, const CostModel& cm, double total_bytes) {
+  std::vector<double> work;
   std::vector<std::pair<int, int>> parts;
   double split_bytes = 0.0;
   for (const DecodeUnit& u : units) {
     split_range(u.lo, u.hi, chunk, parts);
-    for (auto& pr : parts) cost.push_back(cm.d_item_ns + cm.d_key_ns * (pr.second - pr.first));
+    for (auto& pr : parts) work.push_back(item_bytes(pr.second - pr.first, d));
     if (parts.size() > 1) split_bytes += (double)parts.size() * u.ntok * G * (d + 1) * 4.0 * 2.0;
   }
-  double t = lpt(cost, n_cta, nullptr, nullptr);
-  t = std::max(t, 1e9 * total_bytes / cm.d_bytes_per_s);
-  if (split_bytes > 0) t += 3000.0 + 1e9 * split_bytes / cm.d_bytes_per_s;
+  double t = lpt(work, cm.d_item_ns, rate, nullptr, nullptr);
+  t = std::max(t, total_bytes / cm.hbm_bytes_per_ns);
+  if (split_bytes > 0) t += 3000.0 + split_bytes / cm.hbm_bytes_per_ns;
   return t;
 }
 
-DecodeChoice best_decode(const std::vector<DecodeUnit>& units, int n_cta, int G, int d,
-                         const CostModel& cm, double total_bytes) {
+DecodeChoice best_decode(const std::vector<DecodeUnit>& units, const std::vector<double>& rate,
+                         int G, int d, const CostModel& cm, double total_bytes) {
   DecodeChoice best;
   best.time = -1.0;
   // 0 = no split; then 16 Ki .. 256 keys
   const int cands[] = {0, 16384, 8192, 4096, 2048, 1024, 512, 256};
   for (int c : cands) {
-    double t = decode_time(units, n_cta, c, G, d, cm, total_bytes);
+    double t = decode_time(units, rate, c, G, d, cm, total_bytes);
     if (best.time < 0 || t < best.time * (1.0 - 1e-9)) {
       best.time = t;
       best.chunk = c;
@@ -227,6 +273,23 @@ DecodeChoice best_decode(const std::vector<DecodeUnit>& units, int n_cta, int G,
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Can the half's K/V be fetched with TMA boxes of whole pages (page_size >= 8,
+// a power of two) or of 8-key runs of consecutive pages (page_size 1, 2, 4)?
+int tma_eligible(const PodHalfHost& h, int ps) {
+  if (ps <= 0 || (ps & (ps - 1)) != 0 || ps > 256) return 0;
+  if (ps >= 8) return 1;
+  const int n = 8 / ps;  // pages per 8-key box
+  for (int r = 0; r < h.batch; ++r) {
+    const int base = h.kv_indptr[r], np = h.kv_indptr[r + 1] - h.kv_indptr[r];
+    for (int g0 = 0; g0 < np; g0 += n) {
+      const int m = std::min(n, np - g0);
+      for (int i = 1; i < m; ++i)
+        if (h.kv_indices[base + g0 + i] != h.kv_indices[base + g0] + i) return 0;
+    }
+  }
+  return 1;
+}
 
 }  // namespace
 
@@ -273,15 +336,19 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
       for (int g = 0; g < P.Hk; ++g) {
         int32_t rec[POD_REC] = {r, g, t0, nt, lo, hi, -1, 0};
         P.ptiles.insert(P.ptiles.end(), rec, rec + POD_REC);
-        tile_cost.push_back(cm.p_tile_ns + cm.p_block_ns * (double)nblocks(lo, hi));
+        tile_cost.push_back((double)nblocks(lo, hi));
         p_flops += 4.0 * a.d * (double)nt * G * (double)(hi - lo);
       }
     }
   }
   const int n_tiles = (int)tile_cost.size();
+  P.tq = Tq;
 
   // ---- decode units ---------------------------------------------------------
   const int Tu = std::max(1, POD_DECODE_ROWS / G);
+  P.tu = Tu;
+  P.p_tma = tma_eligible(P.p, a.ps);
+  P.d_tma = tma_eligible(P.dd, a.ps);
   std::vector<DecodeUnit> units;
   double d_bytes = 0.0;
   for (int r = 0; r < P.dd.batch; ++r) {
@@ -298,25 +365,39 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   }
 
   // ---- CTA split between the halves ----------------------------------------
-  const int grid_max = a.num_sms * POD_CTAS_PER_SM;
+  const int S = a.num_sms;
+  const int grid_max = S * POD_CTAS_PER_SM;
+  // per-CTA rates for a split: prefill in blocks per ns, decode in bytes per ns
+  auto rates = [&](int n_p, int n_d, std::vector<double>& rp, std::vector<double>& rd) {
+    rp.resize(n_p);
+    rd.resize(n_d);
+    for (int c = 0; c < n_p; ++c) rp[c] = 1.0 / cm.p_block_ns[neighbour_class(c, n_p, n_d, S)];
+    for (int c = 0; c < n_d; ++c) rd[c] = cm.d_bytes_per_ns[neighbour_class(n_p + c, n_p, n_d, S)];
+  };
+  auto t_p = [&](int n_p, int n_d) {
+    std::vector<double> rp, rd;
+    rates(n_p, n_d, rp, rd);
+    return std::max(lpt(tile_cost, cm.p_tile_ns, rp, nullptr, nullptr), p_flops / cm.p_flops_per_ns);
+  };
+  auto t_d = [&](int n_p, int n_d) {
+    std::vector<double> rp, rd;
+    rates(n_p, n_d, rp, rd);
+    return best_decode(units, rd, G, a.d, cm, d_bytes).time;
+  };
   int n_p = 0;
   if (n_tiles > 0 && units.empty()) {
     n_p = std::min(grid_max, n_tiles);
   } else if (n_tiles > 0) {
-    auto t_p = [&](int n) {
-      return std::max(lpt(tile_cost, n, nullptr, nullptr), 1e9 * p_flops / cm.p_flops_per_s);
-    };
-    auto t_d = [&](int n) { return best_decode(units, n, G, a.d, cm, d_bytes).time; };
-    int lo = 1, hi = std::max(1, std::min(grid_max - 1, n_tiles));
     // smallest n_p whose prefill time fits under the decode time of the rest
+    int lo = 1, hi = std::max(1, std::min(grid_max - 1, n_tiles));
     while (lo < hi) {
       int mid = (lo + hi) / 2;
-      if (t_p(mid) <= t_d(grid_max - mid)) hi = mid; else lo = mid + 1;
+      if (t_p(mid, grid_max - mid) <= t_d(mid, grid_max - mid)) hi = mid; else lo = mid + 1;
     }
     n_p = lo;
     if (n_p > 1) {
-      double a1 = std::max(t_p(n_p), t_d(grid_max - n_p));
-      double a0 = std::max(t_p(n_p - 1), t_d(grid_max - n_p + 1));
+      double a1 = std::max(t_p(n_p, grid_max - n_p), t_d(n_p, grid_max - n_p));
+      double a0 = std::max(t_p(n_p - 1, grid_max - n_p + 1), t_d(n_p - 1, grid_max - n_p + 1));
       if (a0 < a1) n_p = n_p - 1;
     }
   }
@@ -324,7 +405,9 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   int chunk = 0;
   if (!units.empty()) {
     if (n_d_max <= 0) { n_p = grid_max - 1; n_d_max = 1; }
-    chunk = best_decode(units, n_d_max, G, a.d, cm, d_bytes).chunk;
+    std::vector<double> rp, rd;
+    rates(n_p, n_d_max, rp, rd);
+    chunk = best_decode(units, rd, G, a.d, cm, d_bytes).chunk;
   }
 
   // ---- decode items, partial rows, merge groups -------------------------------
@@ -350,7 +433,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
       int32_t rec[POD_REC] = {u.req, u.kv_head, u.tok0, u.ntok, parts[j].first, parts[j].second,
                               prow, 0};
       P.ditems.insert(P.ditems.end(), rec, rec + POD_REC);
-      item_cost.push_back(cm.d_item_ns + cm.d_key_ns * (parts[j].second - parts[j].first));
+      item_cost.push_back(item_bytes(parts[j].second - parts[j].first, a.d));
     }
   }
   const int n_items = (int)item_cost.size();
@@ -369,12 +452,14 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   {
     std::vector<int> order, assign;
     std::vector<std::vector<int>> lists(P.grid);
+    std::vector<double> rp, rd;
+    rates(n_p, n_d, rp, rd);
     if (n_p > 0) {
-      lpt(tile_cost, n_p, &order, &assign);
+      lpt(tile_cost, cm.p_tile_ns, rp, &order, &assign);
       for (int j : order) lists[assign[j]].push_back(j);
     }
     if (n_d > 0) {
-      lpt(item_cost, n_d, &order, &assign);
+      lpt(item_cost, cm.d_item_ns, rd, &order, &assign);
       for (int j : order) lists[n_p + assign[j]].push_back(j);
     }
     for (int c = 0; c < P.grid; ++c) {
@@ -441,5 +526,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   s[S_P_BATCH] = P.p.batch; s[S_D_BATCH] = P.dd.batch; s[S_DECODE_CHUNK] = chunk;
   s[S_WS_LO] = (int32_t)(P.total_bytes & 0x7fffffff);
   s[S_WS_HI] = (int32_t)(P.total_bytes >> 31);
+  s[S_P_TMA] = P.p_tma;
+  s[S_D_TMA] = P.d_tma;
   return 0;
 }

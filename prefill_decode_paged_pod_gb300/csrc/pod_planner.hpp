@@ -21,6 +21,8 @@ struct PodPlanHost {
   PodHalfHost p, dd;
   // schedule
   int grid = 0, n_p_ctas = 0, n_d_ctas = 0, decode_chunk = 0;
+  int p_tma = 0, d_tma = 0;   // K/V of the half can be fetched with TMA page boxes
+  int tq = 0, tu = 0;         // tokens per prefill tile / decode unit
   std::vector<int32_t> ptiles, ditems, cta_ptr, cta_list, mgroups, mrow_ptr;
   int n_prows = 0, n_mrows = 0;
   // workspace layout (byte offsets from the workspace base)

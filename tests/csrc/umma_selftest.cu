@@ -6,7 +6,8 @@
 //   O = P V     (M = 128, N = D, K = 64; V is MN-major)
 // and writes S and O in fp32 so a test can compare them with torch matmuls.
 // variant 0: O with one N = D MMA per k-step; variant 1: one N = 64 MMA per
-// 64-column block of D.
+// 64-column block of D; variant 2: P is written into TMEM (tcgen05.st, two
+// 16-bit values per column) and read from there as the A operand.
 #include <cuda_runtime.h>
 
 #include "pod_device.cuh"
@@ -58,6 +59,16 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(const uint16_t* q, c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  if (variant == 2) {
+    // row `tid` of P -> TMEM lane tid, columns 64..95 (S uses columns 0..63)
+    uint32_t u[32];
+    for (int i = 0; i < 32; ++i) u[i] = (uint32_t)p[tid * 64 + 2 * i] | ((uint32_t)p[tid * 64 + 2 * i + 1] << 16);
+    tmem_st32u(tmem + ((uint32_t)(warp * 32) << 16) + 64, u);
+    tmem_wait_st();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
   if (tid == 0) {
     const uint32_t id_qk = idesc_f16(BF16, 128, 64, false, false);
     for (int kk = 0; kk < D / 16; ++kk) {
@@ -66,7 +77,13 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(const uint16_t* q, c
       mma_f16_ss(tmem + 0, ad, bd, id_qk, kk > 0);
     }
     mma_commit(bar);
-    if (variant == 0) {
+    if (variant == 2) {
+      const uint32_t id_pv = idesc_f16(BF16, 128, D, false, true);
+      for (int kk = 0; kk < 4; ++kk) {
+        uint64_t bd = sdesc_sw128(sV + kk * 2048, KVBLK, 1024);
+        mma_f16_ts(tmem + 128, tmem + 64 + kk * 8, bd, id_pv, kk > 0);
+      }
+    } else if (variant == 0) {
       const uint32_t id_pv = idesc_f16(BF16, 128, D, false, true);
       for (int kk = 0; kk < 4; ++kk) {
         uint64_t ad = sdesc_sw128(sP + kk * 32, 16, 1024);

@@ -28,7 +28,7 @@ def built():
 # ------------------------------------------------------------- building blocks
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("bf16", [0, 1])
-@pytest.mark.parametrize("variant", [0, 1])
+@pytest.mark.parametrize("variant", [0, 1, 2])
 def test_umma_building_blocks(d, bf16, variant):
     L = selftest_lib()
     dt = torch.bfloat16 if bf16 else torch.float16
@@ -99,6 +99,37 @@ def test_sweep(ps, G, db):
     (op, lp, od, ld), h, ws = run_pod(inp)
     compare_half(inp, "p", op, lp, tag=f"ps{ps} G{G} db{db} d{d} w{window} ")
     compare_half(inp, "d", od, ld, tag=f"ps{ps} G{G} db{db} d{d} w{window} ")
+
+
+@pytest.mark.parametrize("ps,pages", [(1, "contig"), (2, "contig"), (4, "perm"), (3, "perm"),
+                                      (8, "perm"), (32, "perm"), (128, "perm")])
+def test_page_layouts(ps, pages):
+    """Every page geometry: TMA page boxes (ps >= 8), TMA runs of consecutive
+    pages (ps 1, 2 contiguous), and the cp.async gather (ps 3, ps 4 permuted)."""
+    inp = make_custom("pl", torch.bfloat16, 16, 2, 128, ps, True, -1, [130, 67], [200, 67],
+                      [1, 3, 1, 2], [1000, 517, 96, 33], seed=ps, sinks=True, pages=pages,
+                      extra_pages=5)
+    (op, lp, od, ld), h, ws = run_pod(inp)
+    s = pod.plan_summary(h)
+    want_tma = int(ps in (1, 2, 8, 32, 128))
+    assert s["p_tma"] == want_tma and s["d_tma"] == want_tma, s
+    compare_half(inp, "p", op, lp, tag=f"ps{ps} ")
+    compare_half(inp, "d", od, ld, tag=f"ps{ps} ")
+
+
+def test_unused_page_slots_do_not_leak():
+    """Slots past kv_len in a request's last page hold non-finite values; TMA
+    copies whole pages, so the kernels must keep them out of the result."""
+    inp = make_custom("nan", torch.float16, 16, 2, 64, 16, True, -1, [40, 7], [45, 7],
+                      [1, 2], [37, 70], seed=3, pages="perm")
+    for h in (inp.p, inp.d):
+        for r in range(h.batch):
+            last = int(h.kv_indices[h.kv_indptr[r + 1] - 1])
+            n = int(h.last_page_len[r])
+            h.kv[last, :, n:] = float("nan")
+    (op, lp, od, ld), h, ws = run_pod(inp)
+    compare_half(inp, "p", op, lp)
+    compare_half(inp, "d", od, ld)
 
 
 @pytest.mark.parametrize("causal", [True, False])
