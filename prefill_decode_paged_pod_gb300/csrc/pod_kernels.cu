@@ -396,20 +396,25 @@ __device__ void prefill_role(const PodParams& P, uint8_t* smem, int cta) {
         tc_fence_after();
         const uint32_t s_addr = tmem + lane_base + L::TM_S + b * POD_KBLOCK;
         float s[POD_KBLOCK];
-        tmem_ld32(s_addr, s);
-        tmem_ld32(s_addr + 32, s + 32);
+        tmem_ld64(s_addr, s);
         const bool full = (kb >= row_lo) && (kb + POD_KBLOCK <= row_hi);
-        float bmax = NEG_INF;
+        if (!full) {
 #pragma unroll
-        for (int i = 0; i < POD_KBLOCK; ++i) {
-          float x = s[i];
-          if (!full) {
+          for (int i = 0; i < POD_KBLOCK; ++i) {
             const int t = kb + i;
-            if (t < row_lo || t >= row_hi) x = NEG_INF;
+            if (t < row_lo || t >= row_hi) s[i] = NEG_INF;
           }
-          s[i] = x;
-          bmax = fmaxf(bmax, x);
         }
+        // row max with three-input max: four independent chains
+        float c0 = s[0], c1 = s[1], c2 = s[2], c3 = s[3];
+#pragma unroll
+        for (int i = 4; i < POD_KBLOCK; i += 8) {
+          c0 = max3(c0, s[i], s[i + 1]);
+          c1 = max3(c1, s[i + 2], s[i + 3]);
+          c2 = max3(c2, s[i + 4], s[i + 5]);
+          c3 = max3(c3, s[i + 6], s[i + 7]);
+        }
+        const float bmax = max3(fmaxf(c0, c1), c2, c3);
         const float scale = P.scale_log2;
         const float m_new = fmaxf(m_ref, bmax * scale);
         const bool rescale = m_new > m_ref + 8.0f;   // also true for the first finite max
@@ -530,6 +535,9 @@ __device__ void decode_role(const PodParams& P, uint8_t* smem, int cta) {
   const float NEG_INF = -INFINITY;
   const int w_begin = P.cta_ptr[cta], w_end = P.cta_ptr[cta + 1];
 
+  // Decode CTAs never allocate TMEM; giving up the allocation permit at once
+  // lets the SM take a second CTA of this kernel while this one runs.
+  if (warp == 0) tmem_relinquish();
   if (tid == 0) {
     for (int s = 0; s < L::NSTAGE; ++s) mbar_init(bar0 + 8 * s, P.d_tma ? 1u : (uint32_t)kThreads);
     *abort_flag = 0;
