@@ -47,18 +47,20 @@ struct CostModel {
 };
 
 CostModel cost_model(int d) {
+  // Measured on GB300 with the c3-c5 workloads: per-CTA time of a 64-key
+  // prefill block and per-CTA decode stream, by what shares the SM.
   CostModel c;
   const double f = 0.4 + 0.6 * d / 128.0;   // head_dim 64 halves the MMA work
-  c.p_block_ns[0] = 1100.0 * f;
-  c.p_block_ns[1] = 1300.0 * f;
-  c.p_block_ns[2] = 1700.0 * f;
+  c.p_block_ns[0] = 900.0 * f;
+  c.p_block_ns[1] = 1220.0 * f;
+  c.p_block_ns[2] = 1300.0 * f;
   c.p_tile_ns = 1500.0;
   c.p_flops_per_ns = 1.2e6;
-  c.d_bytes_per_ns[0] = 40.0;
-  c.d_bytes_per_ns[1] = 36.0;
-  c.d_bytes_per_ns[2] = 22.0;
+  c.d_bytes_per_ns[0] = 26.0;   // items of <= 16 rows; 32-row items cost 1.25x
+  c.d_bytes_per_ns[1] = 21.0;
+  c.d_bytes_per_ns[2] = 20.5;
   c.d_item_ns = 2500.0;
-  c.hbm_bytes_per_ns = 5600.0;
+  c.hbm_bytes_per_ns = 6200.0;
   return c;
 }
 
@@ -239,6 +241,11 @@ struct DecodeChoice {
 
 // bytes of K/V a decode item streams: keys x 2 rows (K, V) x d x 2 bytes
 double item_bytes(int keys, int d) { return 4.0 * d * (double)keys; }
+// scheduling weight of a decode item: its bytes, times 1.25 when its rows
+// fill two mma m-tiles (more compute per byte streamed)
+double item_work(int keys, int d, int rows) {
+  return item_bytes(keys, d) * (rows > 16 ? 1.25 : 1.0);
+}
 
 double decode_time(const std::vector<DecodeUnit>& units, const std::vector<double>& rate,
                    int chunk, int G, int d, const CostModel& cm, double total_bytes) {
@@ -247,7 +254,7 @@ double decode_time(const std::vector<DecodeUnit>& units, const std::vector<doubl
   double split_bytes = 0.0;
   for (const DecodeUnit& u : units) {
     split_range(u.lo, u.hi, chunk, parts);
-    for (auto& pr : parts) work.push_back(item_bytes(pr.second - pr.first, d));
+    for (auto& pr : parts) work.push_back(item_work(pr.second - pr.first, d, u.ntok * G));
     if (parts.size() > 1) split_bytes += (double)parts.size() * u.ntok * G * (d + 1) * 4.0 * 2.0;
   }
   double t = lpt(work, cm.d_item_ns, rate, nullptr, nullptr);
@@ -433,7 +440,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
       int32_t rec[POD_REC] = {u.req, u.kv_head, u.tok0, u.ntok, parts[j].first, parts[j].second,
                               prow, 0};
       P.ditems.insert(P.ditems.end(), rec, rec + POD_REC);
-      item_cost.push_back(item_bytes(parts[j].second - parts[j].first, a.d));
+      item_cost.push_back(item_work(parts[j].second - parts[j].first, a.d, R));
     }
   }
   const int n_items = (int)item_cost.size();
