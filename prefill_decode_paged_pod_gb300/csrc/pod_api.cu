@@ -11,6 +11,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <new>
 #include <string>
 
@@ -103,10 +104,11 @@ pod_status encode_q(CUtensorMap* m, const void* ptr, int rows, int H, int d, int
   return POD_OK;
 }
 
-// Paged cache viewed as [pages][2][ps][Hk][d]; box = 64 elements x 1 head x
-// min(ps, 64) slots x 1 x 1 page, or 64 x 1 x ps x 1 x (8 / ps) pages for ps < 8.
+// Paged cache viewed as [pages][2][ps][Hk][d]; a box holds `kbx` keys:
+// 64 elements x 1 head x kbx slots x 1 x 1 page when ps >= 8 (kbx <= ps), or
+// 64 x 1 x ps slots x 1 x (kbx / ps) pages when ps < 8.
 pod_status encode_kv(CUtensorMap* m, const void* ptr, int num_pages, int ps, int Hk, int d,
-                     int dtype) {
+                     int kbx, int dtype) {
   auto fn = encode_fn();
   if (!fn) return set_err(POD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   if ((reinterpret_cast<uintptr_t>(ptr) & 15u) != 0)
@@ -114,8 +116,8 @@ pod_status encode_kv(CUtensorMap* m, const void* ptr, int num_pages, int ps, int
   cuuint64_t dims[5] = {(cuuint64_t)d, (cuuint64_t)Hk, (cuuint64_t)ps, 2, (cuuint64_t)num_pages};
   cuuint64_t row = (cuuint64_t)d * 2;
   cuuint64_t strides[4] = {row, row * Hk, row * Hk * ps, row * Hk * ps * 2};
-  cuuint32_t box[5] = {64, 1, (cuuint32_t)(ps >= 8 ? (ps < 64 ? ps : 64) : ps), 1,
-                       (cuuint32_t)(ps >= 8 ? 1 : 8 / ps)};
+  cuuint32_t box[5] = {64, 1, (cuuint32_t)(ps >= 8 ? kbx : ps), 1,
+                       (cuuint32_t)(ps >= 8 ? 1 : kbx / ps)};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = fn(m, dtype ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5,
                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -226,7 +228,8 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
     if (h->tm_ptr[i] == ptrs[i]) continue;
     pod_status st = (i % 2 == 0)
         ? encode_q(&h->tm[i], ptrs[i], hh.rows, P.H, P.d, P.G, pre ? P.tq : P.tu, P.dtype)
-        : encode_kv(&h->tm[i], ptrs[i], hh.num_pages, P.ps, P.Hk, P.d, P.dtype);
+        : encode_kv(&h->tm[i], ptrs[i], hh.num_pages, P.ps, P.Hk, P.d,
+                    pre ? P.p_tma : P.d_tma, P.dtype);
     if (st != POD_OK) return st;
     h->tm_ptr[i] = ptrs[i];
   }
@@ -244,7 +247,6 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
   }
   K.p_tma = P.p_tma;
   K.d_tma = P.d_tma;
-  K.kbx = P.ps >= 8 ? (P.ps < 64 ? P.ps : 64) : 8;
   K.p_num_pages = P.p.num_pages;
   K.d_num_pages = P.dd.num_pages;
   K.tq = P.tq;
@@ -266,6 +268,8 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
   K.ptiles = I(P.off_ptiles); K.ditems = I(P.off_ditems);
   K.cta_ptr = I(P.off_cta_ptr); K.cta_list = I(P.off_cta_list);
   K.mgroups = I(P.off_mgroups); K.mrow_ptr = I(P.off_mrow_ptr);
+  K.pqueue = I(P.off_pqueue); K.dqueue = I(P.off_dqueue);
+  K.n_tiles = (int)P.pqueue.size(); K.n_items = (int)P.dqueue.size();
   K.part_o = reinterpret_cast<float*>(ws + P.off_part_o);
   K.part_lse = reinterpret_cast<float*>(ws + P.off_part_lse);
   K.status = reinterpret_cast<int32_t*>(ws + P.off_status);
@@ -319,6 +323,8 @@ pod_status pod_plan_table(pod_handle h, int32_t which, int32_t* out, int64_t cap
     case 5: v = &P.mgroups; break;
     case 6: v = &P.p.kv_len; break;
     case 7: v = &P.dd.kv_len; break;
+    case 8: v = &P.pqueue; break;
+    case 9: v = &P.dqueue; break;
     default: return set_err(POD_ERR_INVALID_ARG, "unknown plan table");
   }
   if (count) *count = (int64_t)v->size();

@@ -53,7 +53,10 @@ struct PLayout {                                   // prefill shared memory
   static constexpr int K_OFF = Q_OFF + NKB * QBLK;
   static constexpr int V_OFF = K_OFF + NK * KSTAGE;
   static constexpr int BAR_OFF = V_OFF + NV * KSTAGE;
-  static constexpr int TOTAL = BAR_OFF + 256;
+  // BAR_OFF + 0: mbarriers, +224: TMEM address, +228: abort flag,
+  // +256: tile-id ring [8], +288: published count, +320: per-warp read counts [8]
+  static constexpr int TQ_OFF = BAR_OFF + 256;
+  static constexpr int TOTAL = BAR_OFF + 384;
   static constexpr int TMEM_COLS = 256;            // S/P[2] (2 x 64) + O (<= 128)
   static constexpr int TM_S = 0, TM_O = 128;
 };
@@ -106,17 +109,59 @@ enum {
   B_COUNT = B_FINAL + 1
 };
 
+// Runs prefill tiles from the shared queue until it is empty. Warp 5 takes
+// tiles from the global queue and publishes them in order on a small ring in
+// shared memory; every other warp that walks tiles reads the same sequence.
+// Returns false when a wait ran out (the status word then says so).
 template <typename T, int D>
-__device__ void prefill_role(const PodParams& P, uint8_t* smem, int cta) {
+__device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
   using L = PLayout<D>;
   constexpr int NK = L::NK, NV = L::NV;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + L::BAR_OFF;
   auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + 224);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR_OFF + 228);
   static_assert(B_COUNT * 8 <= 224, "barriers overlap the TMEM slot");
+  volatile int* tq_ring = reinterpret_cast<volatile int*>(smem + L::TQ_OFF);
+  volatile int* tq_pub = tq_ring + 8;
+  volatile int* tq_used = tq_ring + 16;
+  constexpr int kNever = 1 << 30;
+
+  // warp 5: take the next tile of the global queue and publish it as number seq
+  // (-1: queue empty, -2: gave up waiting for a reader)
+  auto fetch_tile = [&](int seq) -> int {
+    int id = -1;
+    if (lane == 0) {
+      const int idx = atomicAdd(P.status + 8, 1);
+      id = idx < P.n_tiles ? __ldg(P.pqueue + idx) : -1;
+      const uint64_t t0 = globaltimer();
+      for (int r = 0; r < 8 && id != -2; ++r)
+        while (tq_used[r] < seq - 7)
+          if (*abort_flag || globaltimer() - t0 > POD_WAIT_TIMEOUT_NS) { id = -2; break; }
+      if (id != -2) {
+        tq_ring[seq & 7] = id;
+        __threadfence_block();
+        *tq_pub = seq + 1;
+      }
+    }
+    return __shfl_sync(0xffffffffu, id, 0);
+  };
+  // any other warp: the tile published as number seq (lane 0 reads, the warp shares)
+  auto read_tile = [&](int seq, bool lone_lane) -> int {
+    int id = -1;
+    if (lane == 0) {
+      const uint64_t t0 = globaltimer();
+      while (*tq_pub <= seq)
+        if (*abort_flag || globaltimer() - t0 > POD_WAIT_TIMEOUT_NS) { id = -2; break; }
+      if (id != -2) {
+        __threadfence_block();
+        id = tq_ring[seq & 7];
+        tq_used[warp] = seq + 1;
+      }
+    }
+    return lone_lane ? id : __shfl_sync(0xffffffffu, id, 0);
+  };
 
   if (tid == 0) {
     const uint32_t kv_arrivals = P.p_tma ? 1u : 96u;  // TMA: one expect_tx arrive
@@ -137,21 +182,20 @@ __device__ void prefill_role(const PodParams& P, uint8_t* smem, int cta) {
     }
     mbar_init(BAR(B_FINAL), 1);
     *abort_flag = 0;
+    *tq_pub = 0;
+    for (int r = 0; r < 8; ++r) tq_used[r] = 0;
+    tq_used[5] = kNever;                       // the fetcher itself
+    if (P.p_tma) tq_used[7] = kNever;          // idle when TMA feeds the tiles
     fence_mbar_init();
-  }
-  if (warp == 4) {
-    tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
-    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const int w_begin = P.cta_ptr[cta], w_end = P.cta_ptr[cta + 1];
   const int G = P.G, H = P.H;
 
   if (warp >= 5) {
     // ------------------------------------------------------------ loaders
+    fence_proxy_async();  // generic accesses of an earlier decode phase come first
     int kfill = 0, vfill = 0, qfill = 0;
     bool ok = true;
     const uint32_t q_bytes = (uint32_t)(L::NKB * 128 * G * P.tq);
@@ -164,9 +208,12 @@ __device__ void prefill_role(const PodParams& P, uint8_t* smem, int cta) {
         const bool is_v = warp == 6;
         const void* tkv = &P.tm_kv_p;
         if (lane == 0) tma_prefetch_desc(tkv);
-        const int ngroups = POD_KBLOCK / P.kbx;
-        for (int w = w_begin; w < w_end && ok; ++w) {
-          const int32_t* rec = P.ptiles + POD_REC * P.cta_list[w];
+        const int ngroups = POD_KBLOCK / P.p_tma;
+        for (int seq = 0; ok; ++seq) {
+          const int tile = is_v ? read_tile(seq, false) : fetch_tile(seq);
+          if (tile == -2) { ok = false; break; }
+          if (tile < 0) break;
+          const int32_t* rec = P.ptiles + POD_REC * tile;
           const int req = rec[0], g = rec[1], tok0 = rec[2], lo = rec[4], hi = rec[5];
           const int page_base = P.p_kv_indptr[req];
           const int npages = P.p_kv_indptr[req + 1] - page_base;
@@ -193,7 +240,7 @@ __device__ void prefill_role(const PodParams& P, uint8_t* smem, int cta) {
             const uint32_t dst0 = sbase + (is_v ? L::V_OFF : L::K_OFF) + s * L::KSTAGE;
             const int kb = b0 + j * POD_KBLOCK;
             for (int gi = lane; gi < ngroups; gi += 32) {
-              const int o = gi * P.kbx;
+              const int o = gi * P.p_tma;
               const int t = kb + o;
               const int pidx = t >> P.ps_shift;
               const int page = pidx < npages ? __ldg(P.p_kv_indices + page_base + pidx) : P.p_num_pages;
@@ -213,8 +260,11 @@ __device__ void prefill_role(const PodParams& P, uint8_t* smem, int cta) {
       const size_t vstride = (size_t)P.ps * P.Hk * D;   // K row -> V row of the same page
       constexpr int KCH = POD_KBLOCK * (D / 8);
       constexpr int PER = (KCH + 95) / 96;
-      for (int w = w_begin; w < w_end && ok; ++w) {
-        const int32_t* rec = P.ptiles + POD_REC * P.cta_list[w];
+      for (int seq = 0; ok; ++seq) {
+        const int tile = warp == 5 ? fetch_tile(seq) : read_tile(seq, false);
+        if (tile == -2) { ok = false; break; }
+        if (tile < 0) break;
+        const int32_t* rec = P.ptiles + POD_REC * tile;
         const int req = rec[0], g = rec[1], tok0 = rec[2], lo = rec[4], hi = rec[5];
         const int page_base = P.p_kv_indptr[req];
         if (lt == 0) {
@@ -292,8 +342,11 @@ __device__ void prefill_role(const PodParams& P, uint8_t* smem, int cta) {
       const uint32_t id_pv = idesc_f16(bf16, 128, D, false, true);
       int kuse = 0, vuse = 0, qfill = 0, sc0 = 0;
       bool ok = true;
-      for (int w = w_begin; w < w_end && ok; ++w) {
-        const int32_t* rec = P.ptiles + POD_REC * P.cta_list[w];
+      for (int seq = 0; ok; ++seq) {
+        const int tile = read_tile(seq, true);
+        if (tile == -2) { ok = false; break; }
+        if (tile < 0) break;
+        const int32_t* rec = P.ptiles + POD_REC * tile;
         const int req = rec[0], lo = rec[4], hi = rec[5];
         const int kv_len = P.p_kv_len[req];
         const int b0 = (lo / POD_KBLOCK) * POD_KBLOCK;
@@ -372,8 +425,11 @@ __device__ void prefill_role(const PodParams& P, uint8_t* smem, int cta) {
     int sc0 = 0;
     bool ok = true;
     const float NEG_INF = -INFINITY;
-    for (int w = w_begin; w < w_end && ok; ++w) {
-      const int32_t* rec = P.ptiles + POD_REC * P.cta_list[w];
+    for (int seq = 0; ok; ++seq) {
+      const int tile = read_tile(seq, false);
+      if (tile == -2) { ok = false; break; }
+      if (tile < 0) break;
+      const int32_t* rec = P.ptiles + POD_REC * tile;
       const int req = rec[0], g = rec[1], tok0 = rec[2], ntok = rec[3], lo = rec[4], hi = rec[5];
       const int prow = rec[6];
       const int kv_len = P.p_kv_len[req];
@@ -507,6 +563,8 @@ __device__ void prefill_role(const PodParams& P, uint8_t* smem, int cta) {
   }
 
   // ------------------------------------------------------------ teardown
+  // every MMA of this role has finished before the CTA moves on (TMEM and the
+  // shared memory may be reused)
   tc_fence_before();
   __syncthreads();
   if (warp == 4) {
@@ -515,13 +573,19 @@ __device__ void prefill_role(const PodParams& P, uint8_t* smem, int cta) {
     int never = 0;  // wait for the MMAs even after an abort, still bounded by the timeout
     mbar_wait(BAR(B_FINAL), 0, (volatile int*)&never);
     tc_fence_after();
-    tmem_dealloc(tmem, L::TMEM_COLS);
   }
+  __syncthreads();
+  const bool clean = *abort_flag == 0;
+  if (tid == 0 && clean)
+    for (int i = 0; i < B_COUNT; ++i) mbar_inval(BAR(i));
+  return clean;
 }
 
 // ============================================================ decode role
+// Runs decode items from the shared queue until it is empty. Returns false
+// when a wait ran out (the status word then says so).
 template <typename T, int D>
-__device__ void decode_role(const PodParams& P, uint8_t* smem, int cta) {
+__device__ bool decode_role(const PodParams& P, uint8_t* smem) {
   using L = DLayout<D>;
   constexpr bool BF16 = Pack<T>::kBF16;
   constexpr int NKB = L::NKB;
@@ -533,11 +597,8 @@ __device__ void decode_role(const PodParams& P, uint8_t* smem, int cta) {
   const int G = P.G, H = P.H;
   T* __restrict__ outg = reinterpret_cast<T*>(P.out_d);
   const float NEG_INF = -INFINITY;
-  const int w_begin = P.cta_ptr[cta], w_end = P.cta_ptr[cta + 1];
+  volatile int* item_slot = reinterpret_cast<volatile int*>(smem + L::BAR_OFF + 96);
 
-  // Decode CTAs never allocate TMEM; giving up the allocation permit at once
-  // lets the SM take a second CTA of this kernel while this one runs.
-  if (warp == 0) tmem_relinquish();
   if (tid == 0) {
     for (int s = 0; s < L::NSTAGE; ++s) mbar_init(bar0 + 8 * s, P.d_tma ? 1u : (uint32_t)kThreads);
     *abort_flag = 0;
@@ -552,8 +613,16 @@ __device__ void decode_role(const PodParams& P, uint8_t* smem, int cta) {
   int fills = 0;
   bool ok = true;
 
-  for (int w = w_begin; w < w_end && ok; ++w) {
-    const int32_t* rec = P.ditems + POD_REC * P.cta_list[w];
+  for (;;) {
+    // thread 0 takes the next item of the global queue; every thread reads it
+    if (tid == 0) {
+      const int idx = atomicAdd(P.status + 9, 1);
+      *item_slot = idx < P.n_items ? __ldg(P.dqueue + idx) : -1;
+    }
+    __syncthreads();
+    const int item = *item_slot;
+    if (item < 0 || !ok) break;
+    const int32_t* rec = P.ditems + POD_REC * item;
     const int req = rec[0], g = rec[1], tok0 = rec[2], ntok = rec[3], k0 = rec[4], k1 = rec[5];
     const int prow = rec[6];
     const int R = ntok * G;
@@ -586,8 +655,8 @@ __device__ void decode_role(const PodParams& P, uint8_t* smem, int cta) {
                             full);
           }
           __syncwarp();
-          for (int gi = lane; gi < POD_DECODE_STAGE / P.kbx; gi += 32) {
-            const int o = gi * P.kbx;
+          for (int gi = lane; gi < POD_DECODE_STAGE / P.d_tma; gi += 32) {
+            const int o = gi * P.d_tma;
             const int t = kb + o;
             const int pidx = t >> P.ps_shift;
             const int page = pidx < npages ? __ldg(P.d_kv_indices + page_base + pidx) : P.d_num_pages;
@@ -828,6 +897,9 @@ __device__ void decode_role(const PodParams& P, uint8_t* smem, int cta) {
     if (tid == 0) raise_status(P.status, POD_STATUS_TIMEOUT);
   }
   cp_async_wait_all();
+  if (ok && tid == 0)  // every filled stage was waited on: no transfer is pending
+    for (int s = 0; s < L::NSTAGE; ++s) mbar_inval(bar0 + 8 * s);
+  return ok;
 }
 
 // ============================================================ kernels
@@ -836,15 +908,48 @@ __global__ void __launch_bounds__(kThreads, POD_CTAS_PER_SM) pod_kernel(const __
   extern __shared__ __align__(1024) uint8_t smem[];
   // the merge kernel may start its prologue now; it waits for this grid's completion
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int cta = blockIdx.x;
-  if ((smem_u32(smem) & 1023u) != 0u) {  // 128B-swizzle atoms need 1024-byte alignment
-    if (threadIdx.x == 0) raise_status(P.status, POD_STATUS_ALIGN);
-    return;
-  }
-  if (cta < P.n_p_ctas) {
-    prefill_role<T, D>(P, smem, cta);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  bool aligned = (smem_u32(smem) & 1023u) == 0u;  // 128B-swizzle atoms need 1024-byte alignment
+  if (!aligned) {
+    if (tid == 0) raise_status(P.status, POD_STATUS_ALIGN);
   } else {
-    decode_role<T, D>(P, smem, cta);
+    // Every CTA holds 256 TMEM columns for its life (two CTAs fill an SM's
+    // 512); giving up the allocation permit at once lets the second CTA in.
+    const uint32_t tslot = smem_u32(smem) + PLayout<D>::BAR_OFF + 224;
+    if (warp == 4) {
+      tmem_alloc(tslot, PLayout<D>::TMEM_COLS);
+      tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + PLayout<D>::BAR_OFF + 224);
+    // Both queues are drained by every CTA: its own role's queue first (the
+    // plan sizes the split), then the other one, so whichever half finishes
+    // early helps with the rest.
+    const bool p_first = (int)blockIdx.x < P.n_p_ctas;
+    bool ok = true;
+    for (int phase = 0; phase < 2 && ok; ++phase) {
+      const bool do_prefill = (phase == 0) == p_first;
+      if (do_prefill ? P.n_tiles == 0 : P.n_items == 0) continue;
+      // shared memory changes hands between the generic and the async proxy
+      fence_proxy_async();
+      __syncthreads();
+      ok = do_prefill ? prefill_role<T, D>(P, smem, tmem) : decode_role<T, D>(P, smem);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 4) tmem_dealloc(tmem, PLayout<D>::TMEM_COLS);
+  }
+  // the last CTA to finish rewinds the queue counters for the next launch
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(P.status + 10, 1) == (int)gridDim.x - 1) {
+      atomicExch(P.status + 8, 0);
+      atomicExch(P.status + 9, 0);
+      atomicExch(P.status + 10, 0);
+    }
   }
 }
 

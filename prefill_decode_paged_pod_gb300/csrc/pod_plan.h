@@ -15,9 +15,17 @@
 //   merge group   : half (0 prefill, 1 decode), req, kv_head, tok0, ntok,
 //                   prow0, nsplit, R   with R = ntok * G; split j, row r of the
 //                   group is partial row prow0 + j * R + r.
-//   cta_ptr[grid+1], cta_list[]: CTA c runs the records cta_list[cta_ptr[c] ..
-//                   cta_ptr[c+1]) — prefill tiles when c < n_prefill_ctas,
-//                   decode items otherwise.
+//   cta_ptr[grid+1], cta_list[]: the planner's static assignment, CTA c taking
+//                   cta_list[cta_ptr[c] .. cta_ptr[c+1]) (prefill tiles when
+//                   c < n_prefill_ctas, decode items otherwise); it sizes the
+//                   CTA split and is kept for inspection.
+//   pqueue[n_tiles], dqueue[n_items]: the work queues the kernel serves, every
+//                   tile / item in decreasing cost. CTAs c < n_prefill_ctas
+//                   take prefill tiles first, the others decode items first;
+//                   a CTA whose queue runs dry helps with the other one. The
+//                   queue heads are three counters in the status block
+//                   (status[8] tiles, status[9] items, status[10] CTAs done);
+//                   the last CTA to finish resets them to zero.
 //   mrow_ptr[n_groups+1]: prefix sums of R over merge groups.
 //   summary (pod_plan_table which = 0): see PodSummary below.
 #pragma once
@@ -45,8 +53,7 @@ struct PodParams {
   // as [pages, 2, ps, Hk, d] (box 64 x 1 x rows x 1 x pages); valid when the
   // half's *_tma flag is set (Q maps whenever the half is non-empty).
   CUtensorMap tm_q_p, tm_kv_p, tm_q_d, tm_kv_d;
-  int p_tma, d_tma;          // K/V of the half are fetched with TMA page boxes
-  int kbx;                   // keys per K/V box: min(ps, 64) for ps >= 8, else 8
+  int p_tma, d_tma;          // keys per TMA K/V box of the half; 0 = cp.async gather
   int p_num_pages, d_num_pages;
   int tq, tu;                // tokens per prefill tile / per decode unit
   int H, Hk, G, d, ps, ps_shift, causal, window_left, has_sinks;
@@ -57,6 +64,8 @@ struct PodParams {
   const int32_t *p_q_indptr, *p_kv_indptr, *p_kv_indices, *p_kv_len;
   const int32_t *d_q_indptr, *d_kv_indptr, *d_kv_indices, *d_kv_len;
   const int32_t *ptiles, *ditems, *cta_ptr, *cta_list, *mgroups, *mrow_ptr;
+  const int32_t *pqueue, *dqueue;
+  int n_tiles, n_items;
   float* part_o;             // [n_prows, d]
   float* part_lse;           // [n_prows]
   int32_t* status;           // device status word

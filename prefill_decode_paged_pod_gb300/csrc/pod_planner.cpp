@@ -281,21 +281,28 @@ DecodeChoice best_decode(const std::vector<DecodeUnit>& units, const std::vector
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Can the half's K/V be fetched with TMA boxes of whole pages (page_size >= 8,
-// a power of two) or of 8-key runs of consecutive pages (page_size 1, 2, 4)?
-int tma_eligible(const PodHalfHost& h, int ps) {
+// Keys per TMA box for the half's K/V, or 0 when page boxes do not fit the
+// page table (then the kernel gathers with cp.async). page_size >= 8 (a power
+// of two): one page (at most 64 slots) per box. page_size 1, 2, 4: the longest
+// run of 64, 32, 16 or 8 keys such that every aligned run of that many keys of
+// every request lies on consecutive pages, so one box covers kbx / ps pages.
+int tma_box_keys(const PodHalfHost& h, int ps) {
   if (ps <= 0 || (ps & (ps - 1)) != 0 || ps > 256) return 0;
-  if (ps >= 8) return 1;
-  const int n = 8 / ps;  // pages per 8-key box
-  for (int r = 0; r < h.batch; ++r) {
-    const int base = h.kv_indptr[r], np = h.kv_indptr[r + 1] - h.kv_indptr[r];
-    for (int g0 = 0; g0 < np; g0 += n) {
-      const int m = std::min(n, np - g0);
-      for (int i = 1; i < m; ++i)
-        if (h.kv_indices[base + g0 + i] != h.kv_indices[base + g0] + i) return 0;
+  if (ps >= 8) return ps < 64 ? ps : 64;
+  for (int kbx = 64; kbx >= 8; kbx /= 2) {
+    const int n = kbx / ps;  // pages per box
+    bool ok = true;
+    for (int r = 0; r < h.batch && ok; ++r) {
+      const int base = h.kv_indptr[r], np = h.kv_indptr[r + 1] - h.kv_indptr[r];
+      for (int g0 = 0; g0 < np && ok; g0 += n) {
+        const int m = std::min(n, np - g0);
+        for (int i = 1; i < m; ++i)
+          if (h.kv_indices[base + g0 + i] != h.kv_indices[base + g0] + i) { ok = false; break; }
+      }
     }
+    if (ok) return kbx;
   }
-  return 1;
+  return 0;
 }
 
 }  // namespace
@@ -354,8 +361,8 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   // ---- decode units ---------------------------------------------------------
   const int Tu = std::max(1, POD_DECODE_ROWS / G);
   P.tu = Tu;
-  P.p_tma = tma_eligible(P.p, a.ps);
-  P.d_tma = tma_eligible(P.dd, a.ps);
+  P.p_tma = tma_box_keys(P.p, a.ps);
+  P.d_tma = tma_box_keys(P.dd, a.ps);
   std::vector<DecodeUnit> units;
   double d_bytes = 0.0;
   for (int r = 0; r < P.dd.batch; ++r) {
@@ -461,13 +468,18 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
     std::vector<std::vector<int>> lists(P.grid);
     std::vector<double> rp, rd;
     rates(n_p, n_d, rp, rd);
+    // the kernel's work queues: every tile / item, largest first
+    P.pqueue.clear();
+    P.dqueue.clear();
     if (n_p > 0) {
       lpt(tile_cost, cm.p_tile_ns, rp, &order, &assign);
       for (int j : order) lists[assign[j]].push_back(j);
+      P.pqueue.assign(order.begin(), order.end());
     }
     if (n_d > 0) {
       lpt(item_cost, cm.d_item_ns, rd, &order, &assign);
       for (int j : order) lists[n_p + assign[j]].push_back(j);
+      P.dqueue.assign(order.begin(), order.end());
     }
     for (int c = 0; c < P.grid; ++c) {
       P.cta_ptr[c] = (int32_t)P.cta_list.size();
@@ -498,6 +510,8 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   P.off_cta_list = place(P.cta_list.size());
   P.off_mgroups = place(P.mgroups.size());
   P.off_mrow_ptr = place(P.mrow_ptr.size());
+  P.off_pqueue = place(P.pqueue.size());
+  P.off_dqueue = place(P.dqueue.size());
   P.int_bytes = align_up(off, 256);
   P.off_part_o = P.int_bytes;
   P.off_part_lse = align_up(P.off_part_o + (size_t)n_prows * a.d * 4, 256);
@@ -521,6 +535,8 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   put(P.off_cta_list, P.cta_list);
   put(P.off_mgroups, P.mgroups);
   put(P.off_mrow_ptr, P.mrow_ptr);
+  put(P.off_pqueue, P.pqueue);
+  put(P.off_dqueue, P.dqueue);
 
   P.summary.assign(S_COUNT, 0);
   int32_t* s = P.summary.data();

@@ -104,6 +104,10 @@ def check_against_reference(inp, h):
     assert sorted(lst[: ptr[npc]].tolist()) == list(range(s["n_tiles"]))
     assert sorted(lst[ptr[npc]:].tolist()) == list(range(s["n_items"]))
     assert s["grid"] <= 2 * s["num_sms"]
+    # work queues: each a permutation of its records (the kernel serves both
+    # through atomic counters, so every record runs exactly once)
+    assert sorted(pod.pod_plan_table(h, 8).tolist()) == list(range(s["n_tiles"]))
+    assert sorted(pod.pod_plan_table(h, 9).tolist()) == list(range(s["n_items"]))
     return s
 
 

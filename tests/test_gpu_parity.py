@@ -111,8 +111,8 @@ def test_page_layouts(ps, pages):
                       extra_pages=5)
     (op, lp, od, ld), h, ws = run_pod(inp)
     s = pod.plan_summary(h)
-    want_tma = int(ps in (1, 2, 8, 32, 128))
-    assert s["p_tma"] == want_tma and s["d_tma"] == want_tma, s
+    want_tma = ps in (1, 2, 8, 32, 128)
+    assert bool(s["p_tma"]) == want_tma and bool(s["d_tma"]) == want_tma, s
     compare_half(inp, "p", op, lp, tag=f"ps{ps} ")
     compare_half(inp, "d", od, ld, tag=f"ps{ps} ")
 
