@@ -127,6 +127,41 @@ pod_status encode_kv(CUtensorMap* m, const void* ptr, int num_pages, int ps, int
   return POD_OK;
 }
 
+// Decode view of the paged cache: one box holds `kbx` keys of one head with
+// both 64-element halves of head_dim, landing in shared memory as
+// [half][key][64] (each half a run of kbx 128-byte rows). Dims, innermost
+// first: page_size >= 8: [64][ps][d/64][Hk][2 * pages] (K/V and page merged:
+// coordinate 2 * page + kv); page_size 1: [64][pages][d/64][Hk][2].
+pod_status encode_kv_decode(CUtensorMap* m, const void* ptr, int num_pages, int ps, int Hk, int d,
+                            int kbx, int dtype) {
+  auto fn = encode_fn();
+  if (!fn) return set_err(POD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15u) != 0)
+    return set_err(POD_ERR_INVALID_ARG, "kv caches must be 16-byte aligned");
+  const cuuint64_t row = (cuuint64_t)d * 2, nh = (cuuint64_t)d / 64;
+  cuuint64_t dims[5], strides[4];
+  if (ps >= 8) {
+    cuuint64_t d5[5] = {64, (cuuint64_t)ps, nh, (cuuint64_t)Hk, 2 * (cuuint64_t)num_pages};
+    cuuint64_t s4[4] = {row * Hk, 128, row, row * Hk * ps};
+    memcpy(dims, d5, sizeof(d5));
+    memcpy(strides, s4, sizeof(s4));
+  } else {
+    cuuint64_t d5[5] = {64, (cuuint64_t)num_pages, nh, (cuuint64_t)Hk, 2};
+    cuuint64_t s4[4] = {row * Hk * 2, 128, row, row * Hk};
+    memcpy(dims, d5, sizeof(d5));
+    memcpy(strides, s4, sizeof(s4));
+  }
+  cuuint32_t box[5] = {64, (cuuint32_t)kbx, (cuuint32_t)nh, 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, dtype ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5,
+                  const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_err(POD_ERR_CUDA, "cuTensorMapEncodeTiled(kv, decode) failed: " + std::to_string((int)r));
+  return POD_OK;
+}
+
 }  // namespace
 
 // Lets other translation units of the library report a message through
@@ -228,8 +263,9 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
     if (h->tm_ptr[i] == ptrs[i]) continue;
     pod_status st = (i % 2 == 0)
         ? encode_q(&h->tm[i], ptrs[i], hh.rows, P.H, P.d, P.G, pre ? P.tq : P.tu, P.dtype)
-        : encode_kv(&h->tm[i], ptrs[i], hh.num_pages, P.ps, P.Hk, P.d,
-                    pre ? P.p_tma : P.d_tma, P.dtype);
+        : pre ? encode_kv(&h->tm[i], ptrs[i], hh.num_pages, P.ps, P.Hk, P.d, P.p_tma, P.dtype)
+              : encode_kv_decode(&h->tm[i], ptrs[i], hh.num_pages, P.ps, P.Hk, P.d, P.d_tma,
+                                 P.dtype);
     if (st != POD_OK) return st;
     h->tm_ptr[i] = ptrs[i];
   }

@@ -358,7 +358,9 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
             const int s = kuse % NK;
             if (!mbar_wait(BAR(B_KFULL + s), (kuse / NK) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            fence_proxy_async();
+            // cp.async writes belong to the generic proxy: make them visible to
+            // the MMA (async proxy). TMA writes need no fence.
+            if (!P.p_tma) fence_proxy_async();
             const int b = (sc0 + j) & 1;
             const uint32_t qa = sbase + L::Q_OFF;
             const uint32_t ka = sbase + L::K_OFF + s * L::KSTAGE;
@@ -389,7 +391,8 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
             // P = 0 never meets a non-finite value.
             const int kb_i = b0 + i * POD_KBLOCK;
             const int ksteps = (min(hi, kb_i + POD_KBLOCK) - kb_i + 15) >> 4;
-            if (P.p_tma && kb_i + ksteps * 16 > kv_len) {
+            const bool zero_tail = P.p_tma && kb_i + ksteps * 16 > kv_len;
+            if (zero_tail) {
               for (int rr = kv_len - kb_i; rr < ksteps * 16; ++rr)
                 for (int dh = 0; dh < L::NKB; ++dh)
                   for (int c = 0; c < 8; ++c)
@@ -398,7 +401,8 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
                                  "r"(0u)
                                  : "memory");
             }
-            fence_proxy_async();
+            // generic writes (cp.async stage, zeroed tail) -> visible to the MMA
+            if (!P.p_tma || zero_tail) fence_proxy_async();
             for (int k = 0; k < ksteps; ++k) {
               const uint64_t bd = sdesc_sw128(va + k * 2048, L::KVBLK, 1024);
               mma_f16_ts(tmem + L::TM_O, tmem + L::TM_S + b * POD_KBLOCK + k * 8, bd, id_pv,
@@ -610,6 +614,15 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
     tma_prefetch_desc(&P.tm_q_d);
   }
   const uint32_t q_bytes = (uint32_t)(NKB * 128 * G * P.tu);
+  // K/V stage layout: [key / kbx][d half][key % kbx][64 elements] in 128-byte
+  // swizzled rows, kbx = keys per TMA box (64 on the cp.async path, where it
+  // is [d half][key][64]). Row offset of key k in its d half 0:
+  const int kshift = P.d_tma ? 31 - __clz(P.d_tma) : 6;
+  const uint32_t half_stride = 128u << kshift;  // bytes between the d halves of a box
+  auto key_row = [&](int k) -> uint32_t {
+    return (uint32_t)((k >> kshift) << kshift) * (NKB * 128u) +
+           (uint32_t)(k & ((1 << kshift) - 1)) * 128u;
+  };
   int fills = 0;
   bool ok = true;
 
@@ -635,8 +648,16 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
     const int kb0 = (k0 / POD_DECODE_STAGE) * POD_DECODE_STAGE;
     const int nst = (k1 - kb0 + POD_DECODE_STAGE - 1) / POD_DECODE_STAGE;
 
-    // fill stage st of this item (Q travels with stage 0) into ring slot (fills + st) % 3
-    auto issue = [&](int st) {
+    // TMA path: page of box `lane` of stage st (lane < 64 / d_tma <= 8); an id
+    // past the request's last page is the out-of-range page TMA fills with zeros
+    auto page_for = [&](int st) -> int {
+      const int pidx = (kb0 + st * POD_DECODE_STAGE + lane * P.d_tma) >> P.ps_shift;
+      return pidx < npages ? __ldg(P.d_kv_indices + page_base + pidx) : P.d_num_pages;
+    };
+    // fill stage st of this item (Q travels with stage 0) into ring slot
+    // (fills + st) % 3; TMA path: `page` = page_for(st) of this lane, or -1
+    // to look it up here
+    auto issue = [&](int st, int page) {
       const int f = fills + st;
       const int buf = f % L::NSTAGE;
       const uint32_t full = bar0 + 8 * buf;
@@ -646,7 +667,6 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
       if (P.d_tma) {
         // warp 0: lane 0 registers the bytes, lane i fetches box group i
         if (warp == 0) {
-          fence_proxy_async();  // earlier generic accesses to the slot come first
           if (lane == 0) {
             mbar_arrive_expect_tx(full, 2u * L::KBYTES + (st == 0 ? q_bytes : 0u));
             if (st == 0)
@@ -655,15 +675,17 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
                             full);
           }
           __syncwarp();
-          for (int gi = lane; gi < POD_DECODE_STAGE / P.d_tma; gi += 32) {
-            const int o = gi * P.d_tma;
-            const int t = kb + o;
-            const int pidx = t >> P.ps_shift;
-            const int page = pidx < npages ? __ldg(P.d_kv_indices + page_base + pidx) : P.d_num_pages;
-            const int tin = P.ps >= 8 ? (t & (P.ps - 1)) : 0;
-            for (int dh = 0; dh < NKB; ++dh) {
-              tma_load_5d(sk + dh * L::KDH + o * 128, &P.tm_kv_d, dh * 64, g, tin, 0, page, full);
-              tma_load_5d(sv + dh * L::KDH + o * 128, &P.tm_kv_d, dh * 64, g, tin, 1, page, full);
+          if (lane < POD_DECODE_STAGE / P.d_tma) {
+            if (page < 0) page = page_for(st);
+            const int o = lane * P.d_tma;
+            const uint32_t dst = (uint32_t)o * (NKB * 128u);
+            if (P.ps >= 8) {  // coordinates (x, slot, half, head, 2 * page + kv)
+              const int tin = (kb + o) & (P.ps - 1);
+              tma_load_5d(sk + dst, &P.tm_kv_d, 0, tin, 0, g, 2 * page, full);
+              tma_load_5d(sv + dst, &P.tm_kv_d, 0, tin, 0, g, 2 * page + 1, full);
+            } else {          // page_size 1: (x, page, half, head, kv)
+              tma_load_5d(sk + dst, &P.tm_kv_d, 0, page, 0, g, 0, full);
+              tma_load_5d(sv + dst, &P.tm_kv_d, 0, page, 0, g, 1, full);
             }
           }
         }
@@ -711,7 +733,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
       }
     };
     const int npre = nst < L::NSTAGE ? nst : L::NSTAGE;
-    for (int st = 0; st < npre; ++st) issue(st);
+    for (int st = 0; st < npre; ++st) issue(st, -1);
 
     // rows of this thread inside its m-tile: r0 = 16 mt + lane/4, r1 = r0 + 8
     int row_lo[2], row_hi[2];
@@ -733,6 +755,10 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
     for (int st = 0; st < nst; ++st) {
       const int f = fills + st;
       const int buf = f % L::NSTAGE;
+      // look up the pages of the stage this one's slot is refilled with now, so
+      // that the load latency hides behind the compute
+      const int next_page =
+          (P.d_tma && warp == 0 && st + L::NSTAGE < nst) ? page_for(st + L::NSTAGE) : -1;
       const bool got = mbar_wait(bar0 + 8 * buf, (f / L::NSTAGE) & 1, abort_flag);
       const int kbase = kb0 + st * POD_DECODE_STAGE + ks * 16;
       if (got && active && kbase < k1 && kbase + 16 > k0) {
@@ -751,7 +777,8 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
           {
             const int key = ks * 16 + (lane & 7) + ((mi >> 1) << 3);
             const int c = kk * 2 + (mi & 1);
-            ldsm_x4(sk + (c >> 3) * L::KDH + sw128_off(key, c & 7), b[0], b[1], b[2], b[3]);
+            ldsm_x4(sk + key_row(key) + (c >> 3) * half_stride + (((c & 7) ^ (lane & 7)) << 4), b[0],
+                    b[1], b[2], b[3]);
           }
           mma16816<BF16>(s0, a, b[0], b[1]);
           mma16816<BF16>(s1, a, b[2], b[3]);
@@ -814,13 +841,14 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
           uint32_t b[4];
           const int key = ks * 16 + (lane & 7) + ((mi & 1) << 3);
           const int c = 2 * j + (mi >> 1);
-          ldsm_x4_t(sv + (c >> 3) * L::KDH + sw128_off(key, c & 7), b[0], b[1], b[2], b[3]);
+          ldsm_x4_t(sv + key_row(key) + (c >> 3) * half_stride + (((c & 7) ^ (lane & 7)) << 4), b[0],
+                    b[1], b[2], b[3]);
           mma16816<BF16>(o[2 * j], pa, b[0] & vm0, b[1] & vm1);
           mma16816<BF16>(o[2 * j + 1], pa, b[2] & vm0, b[3] & vm1);
         }
       }
       if (!__syncthreads_and(got)) { ok = false; break; }
-      if (st + L::NSTAGE < nst) issue(st + L::NSTAGE);
+      if (st + L::NSTAGE < nst) issue(st + L::NSTAGE, next_page);
     }
     fills += nst;
     if (!ok) break;
@@ -890,6 +918,10 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
         if (c4 == 0) P.part_lse[prow + rr] = wsum > 0.f ? M + log2f(wsum) : NEG_INF;
       }
     }
+    // the combine's generic accesses to the stage area come before the next
+    // item's TMA writes into it (stage reads within an item are ordered by the
+    // per-stage barrier)
+    fence_proxy_async();
     __syncthreads();
   }
   if (!ok) {

@@ -362,7 +362,9 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   const int Tu = std::max(1, POD_DECODE_ROWS / G);
   P.tu = Tu;
   P.p_tma = tma_box_keys(P.p, a.ps);
-  P.d_tma = tma_box_keys(P.dd, a.ps);
+  // decode boxes hold both 64-element halves of head_dim; they are laid out
+  // for page_size >= 8 (a page per box) and 1 (runs of pages) only
+  P.d_tma = (a.ps == 1 || a.ps >= 8) ? tma_box_keys(P.dd, a.ps) : 0;
   std::vector<DecodeUnit> units;
   double d_bytes = 0.0;
   for (int r = 0; r < P.dd.batch; ++r) {

@@ -105,14 +105,15 @@ def test_sweep(ps, G, db):
                                       (8, "perm"), (32, "perm"), (128, "perm")])
 def test_page_layouts(ps, pages):
     """Every page geometry: TMA page boxes (ps >= 8), TMA runs of consecutive
-    pages (ps 1, 2 contiguous), and the cp.async gather (ps 3, ps 4 permuted)."""
+    pages (ps 1 both halves, ps 2 prefill only), and the cp.async gather (ps 3,
+    ps 4 permuted, ps 2 decode)."""
     inp = make_custom("pl", torch.bfloat16, 16, 2, 128, ps, True, -1, [130, 67], [200, 67],
                       [1, 3, 1, 2], [1000, 517, 96, 33], seed=ps, sinks=True, pages=pages,
                       extra_pages=5)
     (op, lp, od, ld), h, ws = run_pod(inp)
     s = pod.plan_summary(h)
-    want_tma = ps in (1, 2, 8, 32, 128)
-    assert bool(s["p_tma"]) == want_tma and bool(s["d_tma"]) == want_tma, s
+    assert bool(s["p_tma"]) == (ps in (1, 2, 8, 32, 128)), s
+    assert bool(s["d_tma"]) == (ps in (1, 8, 32, 128)), s  # decode boxes: ps 1 runs or ps >= 8
     compare_half(inp, "p", op, lp, tag=f"ps{ps} ")
     compare_half(inp, "d", od, ld, tag=f"ps{ps} ")
 
