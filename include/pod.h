@@ -157,7 +157,9 @@ pod_status pod_read_device_status(pod_handle h, void* workspace, void* stream,
  * pod_plan_table — host copy of one plan table, for inspection and tests.
  * which: 0 = summary ints, 1 = prefill tiles, 2 = decode items, 3 = CTA work
  * offsets, 4 = CTA work list, 5 = merge groups, 6 = p kv_len, 7 = d kv_len,
- * 8 = prefill tile queue, 9 = decode item queue.
+ * 8 = prefill tile queue, 9 = decode item queue, 10 = decode queue records
+ * (16 ints per queue position: the item record, then kv_len, first query row,
+ * q_len, first page-table entry, page count of its request).
  * Copies min(count, capacity) int32 values into `out` (may be NULL to query
  * *count). Each table's record format is documented beside the planner
  * (csrc/pod_plan.h in the library sources).

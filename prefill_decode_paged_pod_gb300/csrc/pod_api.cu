@@ -304,7 +304,7 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
   K.ptiles = I(P.off_ptiles); K.ditems = I(P.off_ditems);
   K.cta_ptr = I(P.off_cta_ptr); K.cta_list = I(P.off_cta_list);
   K.mgroups = I(P.off_mgroups); K.mrow_ptr = I(P.off_mrow_ptr);
-  K.pqueue = I(P.off_pqueue); K.dqueue = I(P.off_dqueue);
+  K.pqueue = I(P.off_pqueue); K.dqueue = I(P.off_dqueue); K.dqrec = I(P.off_dqrec);
   K.n_tiles = (int)P.pqueue.size(); K.n_items = (int)P.dqueue.size();
   K.part_o = reinterpret_cast<float*>(ws + P.off_part_o);
   K.part_lse = reinterpret_cast<float*>(ws + P.off_part_lse);
@@ -361,6 +361,7 @@ pod_status pod_plan_table(pod_handle h, int32_t which, int32_t* out, int64_t cap
     case 7: v = &P.dd.kv_len; break;
     case 8: v = &P.pqueue; break;
     case 9: v = &P.dqueue; break;
+    case 10: v = &P.dqrec; break;
     default: return set_err(POD_ERR_INVALID_ARG, "unknown plan table");
   }
   if (count) *count = (int64_t)v->size();

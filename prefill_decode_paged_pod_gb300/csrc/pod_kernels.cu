@@ -627,24 +627,24 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
   bool ok = true;
 
   for (;;) {
-    // thread 0 takes the next item of the global queue; every thread reads it
+    // thread 0 takes the next queue position; its record carries everything
+    // the item needs, so the claim costs one dependent load
     if (tid == 0) {
       const int idx = atomicAdd(P.status + 9, 1);
-      *item_slot = idx < P.n_items ? __ldg(P.dqueue + idx) : -1;
+      *item_slot = idx < P.n_items ? idx : -1;
     }
     __syncthreads();
-    const int item = *item_slot;
-    if (item < 0 || !ok) break;
-    const int32_t* rec = P.ditems + POD_REC * item;
-    const int req = rec[0], g = rec[1], tok0 = rec[2], ntok = rec[3], k0 = rec[4], k1 = rec[5];
-    const int prow = rec[6];
+    const int pos = *item_slot;
+    if (pos < 0 || !ok) break;
+    const int32_t* rec = P.dqrec + POD_DQREC * pos;
+    const int g = rec[1], tok0 = rec[2], ntok = rec[3], k0 = rec[4], k1 = rec[5];
     const int R = ntok * G;
     const int Mt = (R + 15) >> 4;
-    const int kv_len = P.d_kv_len[req];
-    const int q_base = P.d_q_indptr[req];
-    const int q_len = P.d_q_indptr[req + 1] - q_base;
-    const int page_base = P.d_kv_indptr[req];
-    const int npages = P.d_kv_indptr[req + 1] - page_base;
+    const int kv_len = rec[8];
+    const int q_base = rec[9];
+    const int q_len = rec[10];
+    const int page_base = rec[11];
+    const int npages = rec[12];
     const int kb0 = (k0 / POD_DECODE_STAGE) * POD_DECODE_STAGE;
     const int nst = (k1 - kb0 + POD_DECODE_STAGE - 1) / POD_DECODE_STAGE;
 
@@ -854,6 +854,11 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
     if (!ok) break;
 
     // ---- combine the 4 key slices of each m-tile through shared memory
+    // (the output placement is read from the record again rather than kept
+    // live in registers across the stage loop)
+    const int32_t* crec = P.dqrec + POD_DQREC * pos;
+    const int cg = __ldg(crec + 1), ctok0 = __ldg(crec + 2), prow = __ldg(crec + 6);
+    const int cq_base = __ldg(crec + 9);
     float* scr_o = reinterpret_cast<float*>(smem + L::SCR_O);
     float* scr_ml = reinterpret_cast<float*>(smem + L::SCR_ML);
 #pragma unroll
@@ -899,13 +904,13 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
         acc.z += wgt * v.z;
         acc.w += wgt * v.w;
       }
-      const int tok = tok0 + rr / G;
-      const int head = g * G + rr % G;
+      const int tok = ctok0 + rr / G;
+      const int head = cg * G + rr % G;
       if (prow < 0) {
         float denom = wsum;
         if (P.has_sinks) denom += ex2(P.sinks[head] * 1.4426950408889634f - Ms);
         const float inv = denom > 0.f ? 1.f / denom : 0.f;
-        const size_t orow = (size_t)(q_base + tok) * H + head;
+        const size_t orow = (size_t)(cq_base + tok) * H + head;
         uint2 v;
         v.x = Pack<T>::two(acc.x * inv, acc.y * inv);
         v.y = Pack<T>::two(acc.z * inv, acc.w * inv);

@@ -26,6 +26,12 @@
 //                   queue heads are three counters in the status block
 //                   (status[8] tiles, status[9] items, status[10] CTAs done);
 //                   the last CTA to finish resets them to zero.
+//   dqrec[n_items][16]: the decode queue again, one self-contained record per
+//                   position: the item's record (8 ints), then kv_len,
+//                   q_base (first query row), q_len, page_base (kv_indptr of
+//                   the request), npages, 0, 0, 0. A CTA that takes queue
+//                   position i reads only this record, so claiming an item
+//                   costs one dependent load.
 //   mrow_ptr[n_groups+1]: prefix sums of R over merge groups.
 //   summary (pod_plan_table which = 0): see PodSummary below.
 #pragma once
@@ -33,6 +39,7 @@
 #include <stdint.h>
 
 #define POD_REC 8
+#define POD_DQREC 16
 #define POD_TILE_ROWS 128      // prefill tile rows (tcgen05 M)
 #define POD_KBLOCK 64          // keys per prefill KV block
 #define POD_DECODE_ROWS 32     // max rows of a decode item (2 mma.sync m16 tiles)
@@ -64,7 +71,7 @@ struct PodParams {
   const int32_t *p_q_indptr, *p_kv_indptr, *p_kv_indices, *p_kv_len;
   const int32_t *d_q_indptr, *d_kv_indptr, *d_kv_indices, *d_kv_len;
   const int32_t *ptiles, *ditems, *cta_ptr, *cta_list, *mgroups, *mrow_ptr;
-  const int32_t *pqueue, *dqueue;
+  const int32_t *pqueue, *dqueue, *dqrec;
   int n_tiles, n_items;
   float* part_o;             // [n_prows, d]
   float* part_lse;           // [n_prows]

@@ -483,6 +483,16 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
       for (int j : order) lists[n_p + assign[j]].push_back(j);
       P.dqueue.assign(order.begin(), order.end());
     }
+    P.dqrec.clear();
+    for (int j : P.dqueue) {
+      const int32_t* rec = &P.ditems[(size_t)j * POD_REC];
+      const int r = rec[0];
+      P.dqrec.insert(P.dqrec.end(), rec, rec + POD_REC);
+      const int32_t ext[POD_DQREC - POD_REC] = {P.dd.kv_len[r], P.dd.q_indptr[r], P.dd.q_len[r],
+                                               P.dd.kv_indptr[r],
+                                               P.dd.kv_indptr[r + 1] - P.dd.kv_indptr[r], 0, 0, 0};
+      P.dqrec.insert(P.dqrec.end(), ext, ext + POD_DQREC - POD_REC);
+    }
     for (int c = 0; c < P.grid; ++c) {
       P.cta_ptr[c] = (int32_t)P.cta_list.size();
       P.cta_list.insert(P.cta_list.end(), lists[c].begin(), lists[c].end());
@@ -514,6 +524,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   P.off_mrow_ptr = place(P.mrow_ptr.size());
   P.off_pqueue = place(P.pqueue.size());
   P.off_dqueue = place(P.dqueue.size());
+  P.off_dqrec = place(P.dqrec.size());
   P.int_bytes = align_up(off, 256);
   P.off_part_o = P.int_bytes;
   P.off_part_lse = align_up(P.off_part_o + (size_t)n_prows * a.d * 4, 256);
@@ -539,6 +550,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   put(P.off_mrow_ptr, P.mrow_ptr);
   put(P.off_pqueue, P.pqueue);
   put(P.off_dqueue, P.dqueue);
+  put(P.off_dqrec, P.dqrec);
 
   P.summary.assign(S_COUNT, 0);
   int32_t* s = P.summary.data();

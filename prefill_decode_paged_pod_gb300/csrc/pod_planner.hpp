@@ -23,13 +23,13 @@ struct PodPlanHost {
   int grid = 0, n_p_ctas = 0, n_d_ctas = 0, decode_chunk = 0;
   int p_tma = 0, d_tma = 0;   // keys per TMA K/V box of the half (0 = cp.async gather)
   int tq = 0, tu = 0;         // tokens per prefill tile / decode unit
-  std::vector<int32_t> ptiles, ditems, cta_ptr, cta_list, mgroups, mrow_ptr, pqueue, dqueue;
+  std::vector<int32_t> ptiles, ditems, cta_ptr, cta_list, mgroups, mrow_ptr, pqueue, dqueue, dqrec;
   int n_prows = 0, n_mrows = 0;
   // workspace layout (byte offsets from the workspace base)
   size_t off_status = 0, off_p_q_indptr = 0, off_p_kv_indptr = 0, off_p_kv_indices = 0,
          off_p_kv_len = 0, off_d_q_indptr = 0, off_d_kv_indptr = 0, off_d_kv_indices = 0,
          off_d_kv_len = 0, off_ptiles = 0, off_ditems = 0, off_cta_ptr = 0, off_cta_list = 0,
-         off_mgroups = 0, off_mrow_ptr = 0, off_pqueue = 0, off_dqueue = 0, int_bytes = 0, off_part_o = 0, off_part_lse = 0,
+         off_mgroups = 0, off_mrow_ptr = 0, off_pqueue = 0, off_dqueue = 0, off_dqrec = 0, int_bytes = 0, off_part_o = 0, off_part_lse = 0,
          total_bytes = 0;
   std::vector<uint8_t> int_image;   // bytes [0, int_bytes) of the workspace
   std::vector<int32_t> summary;

@@ -107,7 +107,21 @@ def check_against_reference(inp, h):
     # work queues: each a permutation of its records (the kernel serves both
     # through atomic counters, so every record runs exactly once)
     assert sorted(pod.pod_plan_table(h, 8).tolist()) == list(range(s["n_tiles"]))
-    assert sorted(pod.pod_plan_table(h, 9).tolist()) == list(range(s["n_items"]))
+    dq = pod.pod_plan_table(h, 9)
+    assert sorted(dq.tolist()) == list(range(s["n_items"]))
+    # decode queue records: the item record, then its request's fields, in queue order
+    dqrec = pod.pod_plan_table(h, 10).reshape(-1, 16)
+    assert dqrec.shape[0] == s["n_items"]
+    if len(dq):
+        assert np.array_equal(dqrec[:, :REC], items[dq])
+        r = dqrec[:, 0]
+        d = inp.d
+        assert np.array_equal(dqrec[:, 8], kvl_d[r])
+        assert np.array_equal(dqrec[:, 9], d.q_indptr[r])
+        assert np.array_equal(dqrec[:, 10], d.q_indptr[r + 1] - d.q_indptr[r])
+        assert np.array_equal(dqrec[:, 11], d.kv_indptr[r])
+        assert np.array_equal(dqrec[:, 12], d.kv_indptr[r + 1] - d.kv_indptr[r])
+        assert np.all(dqrec[:, 13:] == 0)
     return s
 
 
