@@ -532,6 +532,58 @@ def run_ours(args, ws, rank, local):
     return 0
 
 
+def run_profile(args):
+    """Launch one variant of the workload --warmup + --steps times with nothing
+    else on the GPU (no flush, no timing beyond a summary line): the command
+    the ncu captures under profiles/ run. fused = both halves; prefill or
+    decode = that half alone, planned as the single-half runs of run_ours."""
+    import copy
+    import torch
+    import prefill_decode_paged_pod_gb300 as pod
+    from prefill_decode_paged_pod_gb300 import _build
+    from pod_workloads import make_config
+
+    _build.build()
+    pod.load_library()
+    torch.cuda.set_device(0)
+    idx = ["c1", "c2", "c3", "c4", "c5"].index(args.workload) + 1
+    inp = make_config(args.workload, seed=idx)
+    sub = copy.copy(inp)
+    if args.profile != "fused":
+        empty = copy.copy(inp.d if args.profile == "prefill" else inp.p)
+        empty.q_indptr = np.zeros(1, np.int32)
+        empty.kv_indptr = np.zeros(1, np.int32)
+        empty.kv_indices = np.zeros(0, np.int32)
+        empty.last_page_len = np.zeros(0, np.int32)
+        if args.profile == "prefill":
+            sub.d = empty
+        else:
+            sub.p = empty
+    use_p, use_d = sub.p.rows > 0, sub.d.rows > 0
+    q_p = inp.p.q.cuda() if use_p else None
+    kv_p = inp.p.kv.cuda() if use_p else None
+    q_d = inp.d.q.cuda() if use_d else None
+    kv_d = inp.d.kv.cuda() if use_d else None
+    sinks = inp.sinks.cuda() if inp.sinks is not None else None
+    h = pod.plan_inputs(sub)
+    wsb = torch.empty(pod.pod_workspace_size(h), dtype=torch.uint8, device="cuda")
+    pod.pod_bind_workspace(h, wsb)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup + args.steps):
+        if i == args.warmup:
+            torch.cuda.synchronize()
+            s.record()
+        pod.pod_run(h, q_p, kv_p, q_d, kv_d, wsb, sinks=sinks)
+    e.record()
+    torch.cuda.synchronize()
+    status = pod.pod_read_device_status(h, wsb)
+    summ = pod.plan_summary(h)
+    print(json.dumps({"profile": args.profile, "workload": args.workload,
+                      "launch_us_mean": s.elapsed_time(e) * 1e3 / max(args.steps, 1),
+                      "grid": summ["grid"], "status": status}), flush=True)
+    return 0 if status == 0 else 1
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -541,7 +593,11 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--profile", choices=["fused", "prefill", "decode"], default=None,
+                    help="only launch this variant (for ncu captures); prints a summary line")
     args = ap.parse_args(argv)
+    if args.profile:
+        return run_profile(args)
     if args.warmup < 3:
         args.warmup = 3
     ws, rank, local = dist_env()

@@ -51,16 +51,16 @@ CostModel cost_model(int d) {
   // prefill block and per-CTA decode stream, by what shares the SM.
   CostModel c;
   const double f = 0.4 + 0.6 * d / 128.0;   // head_dim 64 halves the MMA work
-  c.p_block_ns[0] = 900.0 * f;
-  c.p_block_ns[1] = 1220.0 * f;
-  c.p_block_ns[2] = 1300.0 * f;
+  c.p_block_ns[0] = 800.0 * f;
+  c.p_block_ns[1] = 1080.0 * f;
+  c.p_block_ns[2] = 1150.0 * f;
   c.p_tile_ns = 1500.0;
   c.p_flops_per_ns = 1.2e6;
-  c.d_bytes_per_ns[0] = 26.0;   // items of <= 16 rows; 32-row items cost 1.25x
-  c.d_bytes_per_ns[1] = 21.0;
-  c.d_bytes_per_ns[2] = 20.5;
+  c.d_bytes_per_ns[0] = 30.0;   // items of <= 16 rows; 32-row items cost 1.25x
+  c.d_bytes_per_ns[1] = 24.0;
+  c.d_bytes_per_ns[2] = 23.5;
   c.d_item_ns = 2500.0;
-  c.hbm_bytes_per_ns = 6200.0;
+  c.hbm_bytes_per_ns = 7000.0;
   return c;
 }
 
@@ -259,7 +259,8 @@ double decode_time(const std::vector<DecodeUnit>& units, const std::vector<doubl
   }
   double t = lpt(work, cm.d_item_ns, rate, nullptr, nullptr);
   t = std::max(t, total_bytes / cm.hbm_bytes_per_ns);
-  if (split_bytes > 0) t += 3000.0 + split_bytes / cm.hbm_bytes_per_ns;
+  // splitting costs the partial rows' round trip and the merge launch
+  if (split_bytes > 0) t += 8000.0 + split_bytes / cm.hbm_bytes_per_ns;
   return t;
 }
 
@@ -390,40 +391,80 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
     for (int c = 0; c < n_p; ++c) rp[c] = 1.0 / cm.p_block_ns[neighbour_class(c, n_p, n_d, S)];
     for (int c = 0; c < n_d; ++c) rd[c] = cm.d_bytes_per_ns[neighbour_class(n_p + c, n_p, n_d, S)];
   };
-  auto t_p = [&](int n_p, int n_d) {
-    std::vector<double> rp, rd;
-    rates(n_p, n_d, rp, rd);
-    return std::max(lpt(tile_cost, cm.p_tile_ns, rp, nullptr, nullptr), p_flops / cm.p_flops_per_ns);
-  };
-  auto t_d = [&](int n_p, int n_d) {
-    std::vector<double> rp, rd;
-    rates(n_p, n_d, rp, rd);
-    return best_decode(units, rd, G, a.d, cm, d_bytes).time;
-  };
   int n_p = 0;
+  int chunk = 0;
   if (n_tiles > 0 && units.empty()) {
     n_p = std::min(grid_max, n_tiles);
-  } else if (n_tiles > 0) {
-    // smallest n_p whose prefill time fits under the decode time of the rest
-    int lo = 1, hi = std::max(1, std::min(grid_max - 1, n_tiles));
-    while (lo < hi) {
-      int mid = (lo + hi) / 2;
-      if (t_p(mid, grid_max - mid) <= t_d(mid, grid_max - mid)) hi = mid; else lo = mid + 1;
-    }
-    n_p = lo;
-    if (n_p > 1) {
-      double a1 = std::max(t_p(n_p, grid_max - n_p), t_d(n_p, grid_max - n_p));
-      double a0 = std::max(t_p(n_p - 1, grid_max - n_p + 1), t_d(n_p - 1, grid_max - n_p + 1));
-      if (a0 < a1) n_p = n_p - 1;
-    }
+  } else if (!units.empty()) {
+    // decode chunk size for the decode share of the CTAs, estimated from the
+    // total CTA-time of each half at same-role rates
+    double p_total = 0.0, d_total = 0.0;
+    for (double b : tile_cost) p_total += cm.p_tile_ns + b * cm.p_block_ns[2];
+    for (const DecodeUnit& u : units)
+      d_total += cm.d_item_ns + item_work(u.hi - u.lo, a.d, u.ntok * G) / cm.d_bytes_per_ns[2];
+    n_p = n_tiles > 0 ? (int)std::lround(grid_max * p_total / (p_total + d_total)) : 0;
+    n_p = std::min(std::max(n_p, n_tiles > 0 ? 1 : 0), std::min(grid_max - 1, n_tiles));
+    std::vector<double> rp, rd;
+    rates(n_p, grid_max - n_p, rp, rd);
+    chunk = best_decode(units, rd, G, a.d, cm, d_bytes).chunk;
   }
   int n_d_max = grid_max - n_p;
-  int chunk = 0;
-  if (!units.empty()) {
-    if (n_d_max <= 0) { n_p = grid_max - 1; n_d_max = 1; }
-    std::vector<double> rp, rd;
-    rates(n_p, n_d_max, rp, rd);
-    chunk = best_decode(units, rd, G, a.d, cm, d_bytes).chunk;
+  // The kernel serves both queues to every CTA, so the split only sets where
+  // each CTA starts. Choose it on a simulation of the two queues: long
+  // prefill tiles that start late can set the makespan (c4: 128 tiles of 128
+  // blocks against 256 long decode requests).
+  if (n_tiles > 0 && !units.empty()) {
+    std::vector<double> tile_ns(tile_cost.size());
+    for (size_t t = 0; t < tile_cost.size(); ++t) tile_ns[t] = tile_cost[t];
+    std::sort(tile_ns.begin(), tile_ns.end(), std::greater<double>());
+    std::vector<double> item_b;
+    std::vector<std::pair<int, int>> parts;
+    for (const DecodeUnit& u : units) {
+      split_range(u.lo, u.hi, chunk, parts);
+      for (auto& pr : parts) item_b.push_back(item_work(pr.second - pr.first, a.d, u.ntok * G));
+    }
+    std::sort(item_b.begin(), item_b.end(), std::greater<double>());
+    // makespan when CTAs [0, np) start on tiles and the rest on items; a CTA
+    // takes the next job of its queue when free, the other queue's once its
+    // own is empty
+    auto queue_makespan = [&](int np) {
+      typedef std::pair<double, int> Slot;
+      std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+      for (int c = 0; c < grid_max; ++c) heap.push(Slot(0.0, c));
+      size_t it = 0, id = 0;
+      double makespan = 0.0;
+      while (it < tile_ns.size() || id < item_b.size()) {
+        Slot sl = heap.top();
+        heap.pop();
+        const int c = sl.second;
+        const int cls = neighbour_class(c, np, grid_max - np, S);
+        const bool want_p = c < np ? it < tile_ns.size() : id >= item_b.size();
+        double cost;
+        if (want_p) cost = cm.p_tile_ns + tile_ns[it++] * cm.p_block_ns[cls];
+        else cost = cm.d_item_ns + item_b[id++] / cm.d_bytes_per_ns[cls];
+        sl.first += cost;
+        makespan = std::max(makespan, sl.first);
+        heap.push(sl);
+      }
+      return std::max(makespan, std::max(p_flops / cm.p_flops_per_ns, d_bytes / cm.hbm_bytes_per_ns));
+    };
+    const double share_t = queue_makespan(n_p);
+    int best_np = n_p;
+    double best_t = share_t;
+    const int hi_np = std::min(grid_max - 1, n_tiles);
+    const int step = std::max(1, hi_np / 32);
+    for (int np = 1; np <= hi_np; np += step) {
+      const double t = queue_makespan(np);
+      if (t < best_t * (1.0 - 1e-9)) { best_t = t; best_np = np; }
+    }
+    for (int np = std::max(1, best_np - step); np <= std::min(hi_np, best_np + step); ++np) {
+      const double t = queue_makespan(np);
+      if (t < best_t * (1.0 - 1e-9)) { best_t = t; best_np = np; }
+    }
+    // the model is coarse: leave the balanced split unless the queues are
+    // predicted to finish at least 1 % earlier another way
+    if (best_t < 0.99 * share_t) n_p = best_np;
+    n_d_max = grid_max - n_p;
   }
 
   // ---- decode items, partial rows, merge groups -------------------------------
@@ -453,7 +494,10 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
     }
   }
   const int n_items = (int)item_cost.size();
-  int n_d = std::min(n_d_max, n_items);
+  // decode-first CTAs beyond the item count still pay off while there are
+  // prefill tiles left for them (they go straight to that queue); no more
+  // CTAs than jobs
+  int n_d = std::min(n_d_max, std::max(n_items, n_tiles + n_items - n_p));
   if (n_items == 0) n_d = 0;
   P.n_p_ctas = n_p;
   P.n_d_ctas = n_d;
