@@ -184,3 +184,56 @@ def test_run_many_times_one_plan():
     (op, lp, od, ld), h, ws = run_pod(inp, dev=dev, repeat=5)
     compare_half(inp, "p", op, lp)
     compare_half(inp, "d", od, ld)
+
+
+def test_cuda_graph_capture_and_replan_in_place():
+    """pod_run captured in a CUDA graph, then the graph replayed after a new
+    plan was written into the same workspace: same lengths, a different page
+    permutation and new cache contents in the same buffers (the serving loop's
+    fixed-batch mode: plan outside the graph, replay inside it)."""
+    def inputs(seed):
+        return make_custom("graph", torch.bfloat16, 16, 2, 128, 16, True, -1, [77, 300], [90, 300],
+                           [1, 4, 1, 2, 1], [1000, 517, 96, 33, 2500], seed=seed, sinks=True)
+    a, b = inputs(21), inputs(22)
+    assert not np.array_equal(a.d.kv_indices, b.d.kv_indices)
+    dev = to_dev(a)
+    h = pod.plan_inputs(a)
+    ws = torch.empty(pod.pod_workspace_size(h), dtype=torch.uint8, device="cuda")
+    pod.pod_bind_workspace(h, ws)
+    H, d = a.num_qo_heads, a.head_dim
+    outs = dict(out_p=torch.empty((a.p.rows, H, d), dtype=a.dtype, device="cuda"),
+                lse_p=torch.empty((a.p.rows, H), dtype=torch.float32, device="cuda"),
+                out_d=torch.empty((a.d.rows, H, d), dtype=a.dtype, device="cuda"),
+                lse_d=torch.empty((a.d.rows, H), dtype=torch.float32, device="cuda"))
+
+    def run():
+        pod.pod_run(h, dev["q_p"], dev["kv_p"], dev["q_d"], dev["kv_d"], ws, sinks=dev["sinks"],
+                    **outs)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run()  # warm-up outside the capture (function attributes, tensor maps)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for inp in (a, b):
+        if inp is b:
+            # new contents in the captured buffers, new tables in the same workspace
+            for k, t in (("q_p", b.p.q), ("kv_p", b.p.kv), ("q_d", b.d.q), ("kv_d", b.d.kv),
+                         ("sinks", b.sinks)):
+                dev[k].copy_(t.to("cuda"))
+            h2 = pod.plan_inputs(b, workspace=ws)
+            assert pod.pod_workspace_size(h2) == pod.pod_workspace_size(h)
+            for which in (0, 1, 8, 9):
+                assert np.array_equal(pod.pod_plan_table(h2, which), pod.pod_plan_table(h, which))
+            torch.cuda.synchronize()
+        for o in outs.values():
+            o.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert pod.pod_read_device_status(h, ws) == 0
+        op, lp, od, ld = [outs[k].double().cpu().numpy() for k in ("out_p", "lse_p", "out_d", "lse_d")]
+        compare_half(inp, "p", op, lp, tag="graph ")
+        compare_half(inp, "d", od, ld, tag="graph ")
