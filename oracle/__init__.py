@@ -15,6 +15,9 @@ Parity status per function (see the pins in tests/test_oracle_pins.py):
                                     forms, hand-worked example, split/merge)
   merge                             pinned (split/merge identity)
   seq_lens                          pinned (closed form from the page tables)
+  FP8 (E4M3) cache path             pinned (exhaustive decoder check against the
+                                    format's definition and torch; dequantized
+                                    brute force; scale folding identities)
   sink-in-LSE convention            pinned to the reading taken (sink excluded)
 """
 from __future__ import annotations
@@ -72,6 +75,15 @@ def lib():
             _lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
             _lib.oracle_bf16_to_f64.restype = ctypes.c_double
             _lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+            _lib.oracle_e4m3_to_f64.restype = ctypes.c_double
+            _lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            _lib.oracle_attention_rows_kv.restype = ctypes.c_int
+            _lib.oracle_attention_rows_kv.argtypes = [
+                P, P, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double,
+                P, P, P, P, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                P, ctypes.c_int64, P, P, P, P, P, P, ctypes.c_int]
         return _lib
 
 
@@ -87,6 +99,21 @@ def _codes(t) -> np.ndarray:
     return np.ascontiguousarray(t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
 
 
+def is_fp8(t) -> bool:
+    """True for an FP8 E4M3 torch tensor (the cache format the oracle reads
+    as E4M3 codes)."""
+    import torch
+    return getattr(t, "dtype", None) == torch.float8_e4m3fn
+
+
+def _codes8(t) -> np.ndarray:
+    """8-bit codes of an E4M3 torch tensor (or numpy uint8 array)."""
+    if isinstance(t, np.ndarray):
+        return np.ascontiguousarray(t.view(np.uint8))
+    import torch
+    return np.ascontiguousarray(t.detach().cpu().contiguous().view(torch.uint8).numpy())
+
+
 def dtype_code(t) -> int:
     import torch
     if t.dtype == torch.float16:
@@ -100,13 +127,16 @@ def attention_rows(q, kv, q_indptr, kv_indptr, kv_indices, last_page_len,
                    num_qo_heads, num_kv_heads, head_dim, page_size,
                    causal, window_left, sm_scale, sinks=None,
                    sel_token=None, sel_head=None, key_lo=None, key_hi=None,
-                   nthreads: Optional[int] = None, dtype: Optional[int] = None):
+                   nthreads: Optional[int] = None, dtype: Optional[int] = None,
+                   k_scale: float = 1.0, v_scale: float = 1.0):
     """fp64 outputs for selected (token, head) pairs; all pairs if no selection.
+    An E4M3 ``kv`` is read as codes times ``k_scale`` (K) / ``v_scale`` (V).
 
     Returns (out [n, d] float64, lse [n] float64, status int).
     """
     qc = _codes(q)
-    kvc = _codes(kv)
+    kv_fp8 = is_fp8(kv)
+    kvc = _codes8(kv) if kv_fp8 else _codes(kv)
     if dtype is None:
         dtype = dtype_code(q)
     q_indptr = np.ascontiguousarray(q_indptr, dtype=np.int32)
@@ -135,8 +165,8 @@ def attention_rows(q, kv, q_indptr, kv_indptr, kv_indices, last_page_len,
     num_pages = int(kvc.shape[0]) if kvc.ndim >= 1 else 0
     if nthreads is None:
         nthreads = os.cpu_count() or 1
-    st = lib().oracle_attention_rows(
-        _ptr(qc), _ptr(kvc), int(dtype),
+    st = lib().oracle_attention_rows_kv(
+        _ptr(qc), _ptr(kvc), int(dtype), int(kv_fp8), float(k_scale), float(v_scale),
         _ptr(q_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(last_page_len),
         batch, num_pages, H, int(num_kv_heads), d, int(page_size),
         int(bool(causal)), int(window_left), float(sm_scale),
@@ -148,10 +178,14 @@ def attention_rows(q, kv, q_indptr, kv_indptr, kv_indices, last_page_len,
 def attention_half(inp, half: str, sel_token=None, sel_head=None, nthreads=None, **kw):
     """Oracle for one half ("p" or "d") of a ``pod_workloads.PODInputs``."""
     h = inp.p if half == "p" else inp.d
+    scales = {}
+    if is_fp8(h.kv):
+        scales = dict(k_scale=getattr(inp, "k_scale", 1.0), v_scale=getattr(inp, "v_scale", 1.0))
     return attention_rows(h.q, h.kv, h.q_indptr, h.kv_indptr, h.kv_indices, h.last_page_len,
                           inp.num_qo_heads, inp.num_kv_heads, inp.head_dim, inp.page_size,
                           inp.causal, inp.window_left, inp.sm_scale, sinks=inp.sinks,
-                          sel_token=sel_token, sel_head=sel_head, nthreads=nthreads, **kw)
+                          sel_token=sel_token, sel_head=sel_head, nthreads=nthreads,
+                          **scales, **kw)
 
 
 def merge(o_parts: np.ndarray, lse_parts: np.ndarray, sink: Optional[float] = None):
@@ -181,3 +215,7 @@ def f16_to_f64(code: int) -> float:
 
 def bf16_to_f64(code: int) -> float:
     return lib().oracle_bf16_to_f64(int(code))
+
+
+def e4m3_to_f64(code: int) -> float:
+    return lib().oracle_e4m3_to_f64(int(code))

@@ -33,7 +33,10 @@
  *
  * Inputs are the same rounded fp16/bf16 values the GPU reads, widened to
  * double by decoders written from the IEEE-754 binary16 and bfloat16 bit
- * layouts. Nothing is blocked, fused or reordered: keys are visited in order
+ * layouts. An FP8 (E4M3) cache is read as its codes decoded from the E4M3
+ * bit layout times a per-tensor scale for K and one for V: attention over the
+ * dequantized cache, which is what folding the K scale into the softmax scale
+ * and multiplying the output by the V scale compute. Nothing is blocked, fused or reordered: keys are visited in order
  * 0..kv_len-1.
  *
  * Parity pins (tests under tests/, run on the CPU): brute-force dense attention
@@ -82,6 +85,31 @@ static double widen(uint16_t v, int dtype)
     return dtype == 0 ? oracle_f16_to_f64(v) : oracle_bf16_to_f64(v);
 }
 
+/* FP8 E4M3 (the "fn" variant: 1 sign, 4 exponent bits with bias 7, 3 fraction
+ * bits, no infinities, S.1111.111 is NaN). */
+double oracle_e4m3_to_f64(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 0xf;
+    int f = c & 7;
+    double v;
+    if (e == 15 && f == 7) return NAN;
+    if (e == 0) {
+        v = ldexp((double)f, -9);                /* subnormal: f/8 * 2^-6 */
+    } else {
+        v = ldexp((double)(8 + f), e - 10);      /* (1 + f/8) * 2^(e-7) */
+    }
+    return sign ? -v : v;
+}
+
+/* one K or V element: 16-bit codes of `dtype`, or e4m3 codes times `scale`
+ * when kv_fp8 is set */
+static double kv_elem(const void* kv, int64_t idx, int dtype, int kv_fp8, double scale)
+{
+    if (kv_fp8) return oracle_e4m3_to_f64(((const uint8_t*)kv)[idx]) * scale;
+    return widen(((const uint16_t*)kv)[idx], dtype);
+}
+
 /* kv_len of request r from its page table (POD walkthrough, plan step 1). */
 int64_t oracle_kv_len(const int32_t* kv_indptr, const int32_t* last_page_len,
                       int r, int page_size)
@@ -115,16 +143,17 @@ static int find_request(const int32_t* q_indptr, int batch, int64_t token)
  *   out [n, d], lse [n]                   : fp64 results
  * Returns the first error code met (rows are still filled where possible).
  */
-int oracle_attention_rows(const uint16_t* q, const uint16_t* kv, int dtype,
-                          const int32_t* q_indptr, const int32_t* kv_indptr,
-                          const int32_t* kv_indices, const int32_t* last_page_len,
-                          int batch, int num_pages,
-                          int H, int Hk, int d, int page_size,
-                          int causal, int window_left, double sm_scale,
-                          const float* sinks,
-                          int64_t n_sel, const int64_t* sel_token, const int32_t* sel_head,
-                          const int64_t* key_lo, const int64_t* key_hi,
-                          double* out, double* lse, int nthreads)
+int oracle_attention_rows_kv(const uint16_t* q, const void* kv, int dtype,
+                             int kv_fp8, double k_scale, double v_scale,
+                             const int32_t* q_indptr, const int32_t* kv_indptr,
+                             const int32_t* kv_indices, const int32_t* last_page_len,
+                             int batch, int num_pages,
+                             int H, int Hk, int d, int page_size,
+                             int causal, int window_left, double sm_scale,
+                             const float* sinks,
+                             int64_t n_sel, const int64_t* sel_token, const int32_t* sel_head,
+                             const int64_t* key_lo, const int64_t* key_hi,
+                             double* out, double* lse, int nthreads)
 {
     if (H <= 0 || Hk <= 0 || H % Hk != 0 || d <= 0 || page_size <= 0) return ORACLE_BAD_ARG;
     int group = H / Hk;
@@ -175,9 +204,9 @@ int oracle_attention_rows(const uint16_t* q, const uint16_t* kv, int dtype,
                 status = ORACLE_BAD_ARG;
                 continue;
             }
-            const uint16_t* k = kv + (((page * 2 + 0) * page_size + slot) * Hk + hk) * (int64_t)d;
+            int64_t k0 = (((page * 2 + 0) * page_size + slot) * Hk + hk) * (int64_t)d;
             double dot = 0.0;
-            for (int e = 0; e < d; ++e) dot += qv[e] * widen(k[e], dtype);
+            for (int e = 0; e < d; ++e) dot += qv[e] * kv_elem(kv, k0 + e, dtype, kv_fp8, k_scale);
             logit[t] = sm_scale * dot;
             if (logit[t] > m) m = logit[t];
             ++n_allowed;
@@ -198,14 +227,32 @@ int oracle_attention_rows(const uint16_t* q, const uint16_t* kv, int dtype,
             if (!allowed[t]) continue;
             int64_t page = kv_indices[kv_indptr[r] + t / page_size];
             int64_t slot = t % page_size;
-            const uint16_t* v = kv + (((page * 2 + 1) * page_size + slot) * Hk + hk) * (int64_t)d;
+            int64_t v0 = (((page * 2 + 1) * page_size + slot) * Hk + hk) * (int64_t)d;
             double w = exp(logit[t] - m) / denom;
-            for (int e = 0; e < d; ++e) o[e] += w * widen(v[e], dtype);
+            for (int e = 0; e < d; ++e) o[e] += w * kv_elem(kv, v0 + e, dtype, kv_fp8, v_scale);
         }
         lse[s] = (m + log(z)) / log(2.0);
         free(qv); free(logit); free(allowed);
     }
     return status;
+}
+
+/* The 16-bit cache of `dtype`: oracle_attention_rows_kv without FP8. */
+int oracle_attention_rows(const uint16_t* q, const uint16_t* kv, int dtype,
+                          const int32_t* q_indptr, const int32_t* kv_indptr,
+                          const int32_t* kv_indices, const int32_t* last_page_len,
+                          int batch, int num_pages,
+                          int H, int Hk, int d, int page_size,
+                          int causal, int window_left, double sm_scale,
+                          const float* sinks,
+                          int64_t n_sel, const int64_t* sel_token, const int32_t* sel_head,
+                          const int64_t* key_lo, const int64_t* key_hi,
+                          double* out, double* lse, int nthreads)
+{
+    return oracle_attention_rows_kv(q, kv, dtype, 0, 1.0, 1.0, q_indptr, kv_indptr, kv_indices,
+                                    last_page_len, batch, num_pages, H, Hk, d, page_size, causal,
+                                    window_left, sm_scale, sinks, n_sel, sel_token, sel_head,
+                                    key_lo, key_hi, out, lse, nthreads);
 }
 
 /*

@@ -72,6 +72,9 @@ class PODInputs:
     p: HalfInputs
     d: HalfInputs
     sinks: Optional[torch.Tensor]   # fp32 [H] or None
+    # decode cache in FP8 E4M3: d.kv holds the codes; K = code * k_scale, V = code * v_scale
+    k_scale: float = 1.0
+    v_scale: float = 1.0
 
 
 def page_table_from_lens(kv_lens: Sequence[int], page_size: int):
@@ -191,3 +194,22 @@ def make_config(name: str, seed: Optional[int] = None, with_data: bool = True) -
         sinks = torch.randn(H, generator=gen, dtype=torch.float32)
         return PODInputs(name, dt, H, Hk, d, ps, True, 4096, 1.0 / math.sqrt(d), p, dd, sinks)
     raise ValueError(f"unknown workload {name!r}")
+
+
+def with_fp8_decode_cache(inp: PODInputs, k_scale: float = 0.02, v_scale: float = 0.03) -> PODInputs:
+    """The same inputs with the decode half's cache stored as FP8 E4M3 codes:
+    K / k_scale and V / v_scale rounded to E4M3 (torch's conversion), so the
+    dequantized cache code * scale is close to the 16-bit one. Returns a new
+    PODInputs; the prefill half is untouched."""
+    import copy
+    out = copy.copy(inp)
+    d = copy.copy(inp.d)
+    kv = inp.d.kv.float()
+    scaled = torch.empty_like(kv)
+    scaled[:, 0] = kv[:, 0] / k_scale
+    scaled[:, 1] = kv[:, 1] / v_scale
+    d.kv = scaled.to(torch.float8_e4m3fn)
+    out.d = d
+    out.k_scale = float(k_scale)
+    out.v_scale = float(v_scale)
+    return out

@@ -35,7 +35,7 @@ GOLDEN = os.path.join(HERE, "golden")
 
 def dense_kv(h: HalfInputs, r: int, ps: int):
     """Dense K, V [kv_len, Hk, d] of request r, gathered with numpy indexing."""
-    kv = h.kv.float().numpy().astype(np.float64)
+    kv = h.kv.double().numpy()
     lo, hi = int(h.kv_indptr[r]), int(h.kv_indptr[r + 1])
     pages = h.kv_indices[lo:hi]
     kvl = int(h.kv_lens[r])
@@ -284,8 +284,19 @@ def pin_split_merge(fn, merge=None):
                 assert abs(ml - l[tok, hh]) < 1e-12
 
 
+def pin_fp8(fn, seeds=range(6)):
+    """FP8 (E4M3) decode cache: the attention callable on codes and scales
+    equals textbook attention over the dequantized cache."""
+    for seed in seeds:
+        inp = _fp8_tiny(seed)
+        ref_out, ref_lse = brute_force_scaled(inp)
+        out, lse = run_oracle(inp, "d", fn=fn, k_scale=inp.k_scale, v_scale=inp.v_scale)
+        assert np.allclose(out, ref_out, atol=1e-12, rtol=1e-12), seed
+        assert np.allclose(lse, ref_lse, atol=1e-12, rtol=0), seed
+
+
 ALL_PINS = (pin_two_token, pin_brute_force, pin_closed_forms, pin_gqa, pin_page_invariance,
-            pin_split_merge)
+            pin_split_merge, pin_fp8)
 
 
 # --------------------------------------------------------------------------
@@ -377,6 +388,10 @@ MUTANTS = {
     "scale_dropped": ("logit[t] = sm_scale * dot;", "logit[t] = dot;"),
     "merge_natural_weights": ("double w = pow(2.0, lse_parts[i] - M);", "double w = exp(lse_parts[i] - M);"),
     "f16_bias": ("e - 25", "e - 24"),
+    "e4m3_bias": ("ldexp((double)(8 + f), e - 10)", "ldexp((double)(8 + f), e - 9)"),
+    "e4m3_subnormal": ("v = ldexp((double)f, -9);", "v = ldexp((double)f, -10);"),
+    "fp8_v_with_k_scale": ("kv_elem(kv, v0 + e, dtype, kv_fp8, v_scale)",
+                           "kv_elem(kv, v0 + e, dtype, kv_fp8, k_scale)"),
 }
 
 
@@ -395,6 +410,8 @@ def _mutant_fns(tmpdir, name, old, new):
         oracle._lib = L
         L.oracle_attention_rows.restype = ctypes.c_int
         L.oracle_attention_rows.argtypes = saved.oracle_attention_rows.argtypes
+        L.oracle_attention_rows_kv.restype = ctypes.c_int
+        L.oracle_attention_rows_kv.argtypes = saved.oracle_attention_rows_kv.argtypes
         L.oracle_merge.argtypes = saved.oracle_merge.argtypes
         L.oracle_merge.restype = None
         try:
@@ -432,3 +449,78 @@ def test_planted_mistakes(name):
             except AssertionError:
                 failures += 1
         assert failures > 0, f"mutant {name} passed every pin"
+
+
+# --------------------------------------------------------------------------
+# FP8 (E4M3) decode cache
+# --------------------------------------------------------------------------
+
+def test_e4m3_decoder_exhaustive():
+    """All 256 E4M3 codes against torch's float8_e4m3fn and against values the
+    format's definition fixes (bias 7, 3 fraction bits, S.1111.111 = NaN)."""
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([oracle.e4m3_to_f64(int(c)) for c in codes])
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    assert np.array_equal(ref[~np.isnan(ref)], got[~np.isnan(got)])
+    fixed = {0x38: 1.0, 0x40: 2.0, 0x7E: 448.0, 0x08: 2.0 ** -6, 0x01: 2.0 ** -9,
+             0x07: 7 * 2.0 ** -9, 0x3C: 1.5, 0xC0: -2.0, 0x00: 0.0}
+    for c, v in fixed.items():
+        assert oracle.e4m3_to_f64(c) == v, hex(c)
+    assert math.isnan(oracle.e4m3_to_f64(0x7F)) and math.isnan(oracle.e4m3_to_f64(0xFF))
+    assert math.copysign(1.0, oracle.e4m3_to_f64(0x80)) == -1.0
+
+
+def _fp8_tiny(seed):
+    from pod_workloads import with_fp8_decode_cache
+    base = tiny_case(seed, dtype=torch.bfloat16)
+    rng = np.random.default_rng(seed)
+    return with_fp8_decode_cache(base, k_scale=float(rng.choice([0.02, 0.5, 3.0])),
+                                 v_scale=float(rng.choice([0.03, 1.0, 4.0])))
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_fp8_cache_matches_dequantized_brute_force(seed):
+    """Textbook attention over code * scale (K and V dequantized separately)
+    equals the oracle's FP8 path."""
+    inp = _fp8_tiny(seed)
+    ref_out, ref_lse = brute_force_scaled(inp)
+    out, lse, st = oracle.attention_half(inp, "d", nthreads=2)
+    assert st == 0
+    h = inp.d
+    out = out.reshape(h.rows, inp.num_qo_heads, inp.head_dim)
+    lse = lse.reshape(h.rows, inp.num_qo_heads)
+    assert np.allclose(out, ref_out, atol=1e-12, rtol=1e-12)
+    assert np.allclose(lse, ref_lse, atol=1e-12, rtol=0)
+
+
+def brute_force_scaled(inp):
+    """brute_force over a copy of the decode half whose cache holds the
+    dequantized values (codes * k_scale for K, codes * v_scale for V) in fp64."""
+    import copy
+    h = copy.copy(inp.d)
+    kv = h.kv.double()
+    kv[:, 0] *= inp.k_scale
+    kv[:, 1] *= inp.v_scale
+    h.kv = kv
+    inp2 = copy.copy(inp)
+    inp2.d = h
+    return brute_force(inp2, "d")
+
+
+def test_fp8_scale_folding():
+    """k_scale acts as a factor on the logits (same result as folding it into
+    sm_scale with k_scale = 1); v_scale scales the output and leaves the LSE."""
+    inp = _fp8_tiny(3)
+    h = inp.d
+    args = (h.q, h.kv, h.q_indptr, h.kv_indptr, h.kv_indices, h.last_page_len,
+            inp.num_qo_heads, inp.num_kv_heads, inp.head_dim, inp.page_size, inp.causal,
+            inp.window_left)
+    o1, l1, _ = oracle.attention_rows(*args, inp.sm_scale, sinks=inp.sinks, k_scale=2.5,
+                                      v_scale=1.0, nthreads=2)
+    o2, l2, _ = oracle.attention_rows(*args, inp.sm_scale * 2.5, sinks=inp.sinks, k_scale=1.0,
+                                      v_scale=1.0, nthreads=2)
+    assert np.allclose(o1, o2, atol=1e-12, rtol=1e-12) and np.allclose(l1, l2, atol=1e-12)
+    o3, l3, _ = oracle.attention_rows(*args, inp.sm_scale, sinks=inp.sinks, k_scale=2.5,
+                                      v_scale=0.25, nthreads=2)
+    assert np.allclose(o3, 0.25 * o1, atol=1e-12, rtol=1e-12) and np.array_equal(l3, l1)
