@@ -76,13 +76,14 @@ def work(inp):
     el = 2
     out = {}
     for name, h in (("p", inp.p), ("d", inp.d)):
+        el_kv = h.kv.element_size() if hasattr(h.kv, "element_size") else el
         pairs = keys = 0
         for r in range(h.batch):
             ql, kl = int(h.q_lens[r]), int(h.kv_lens[r])
             pairs += allowed_keys(kl, ql, inp.causal, inp.window_left)
             keys += touched_keys(kl, ql, inp.causal, inp.window_left)
         flops = 4.0 * d * H * pairs
-        kv_bytes = keys * Hk * d * el * 2.0
+        kv_bytes = keys * Hk * d * el_kv * 2.0
         qo_bytes = h.rows * H * (d * el * 2 + 4)
         out[name] = dict(pairs=pairs, keys=keys, flops=flops, kv_bytes=kv_bytes,
                          bytes=kv_bytes + qo_bytes, rows=h.rows)
@@ -269,7 +270,7 @@ def run_reference(args, ws, rank):
     from pod_workloads import make_config
     if rank != 0:
         return 0
-    inp = make_config(args.workload)
+    inp = with_kv_option(make_config(args.workload), args)
     w = work(inp)
     nthreads = os.cpu_count() or 1
     per_step = max(1.0, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
@@ -291,6 +292,14 @@ def run_reference(args, ws, rank):
             "e2e": {"value": v, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def with_kv_option(inp, args):
+    """--kv-fp8: the decode half's cache as FP8 E4M3 codes (scales 0.05)."""
+    if getattr(args, "kv_fp8", False):
+        from pod_workloads import with_fp8_decode_cache
+        return with_fp8_decode_cache(inp, k_scale=0.05, v_scale=0.05)
+    return inp
 
 
 def time_loop(fn, steps, stream, per_launch=True, pre=None):
@@ -338,7 +347,7 @@ def run_ours(args, ws, rank, local):
     _build.build()
     pod.load_library()
     idx = ["c1", "c2", "c3", "c4", "c5"].index(args.workload) + 1
-    inp = make_config(args.workload, seed=idx + 1000 * rank)
+    inp = with_kv_option(make_config(args.workload, seed=idx + 1000 * rank), args)
     w = work(inp)
     stream = torch.cuda.current_stream(device)
     dev = dict(q_p=inp.p.q.to(device) if inp.p.rows else None,
@@ -360,7 +369,7 @@ def run_ours(args, ws, rank, local):
         pod.pod_run(h, dev["q_p"], dev["kv_p"], dev["q_d"], dev["kv_d"], wsb, sinks=dev["sinks"],
                     out_p=out_p, lse_p=lse_p, out_d=out_d, lse_d=lse_d)
 
-    kv_total = (inp.p.kv.numel() + inp.d.kv.numel()) * inp.p.kv.element_size()
+    kv_total = inp.p.kv.numel() * inp.p.kv.element_size() + inp.d.kv.numel() * inp.d.kv.element_size()
     l2_bytes = 129 * 1024 * 1024
     flush = flush_r = None
     if kv_total < 2 * l2_bytes:
@@ -514,7 +523,8 @@ def run_ours(args, ws, rank, local):
                    "prefill_rows": inp.p.rows, "decode_rows": inp.d.rows,
                    "l2": ("inputs larger than L2" if flush is None else
                           "L2 flushed (256 MB write + 256 MB read) between timed launches"),
-                   "kv_cache_bytes": kv_total, "parallelism": f"replicas x{ws} (independent batches)"},
+                   "kv_cache_bytes": kv_total, "parallelism": f"replicas x{ws} (independent batches)",
+                   "decode_kv": "fp8 e4m3 (k_scale 0.05, v_scale 0.05)" if args.kv_fp8 else "16-bit"},
         "roofline": roof, "cpu_baseline": cpu,
         "e2e": {"value": e2e_step_ms * 1e3, "unit": "us", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -547,7 +557,7 @@ def run_profile(args):
     pod.load_library()
     torch.cuda.set_device(0)
     idx = ["c1", "c2", "c3", "c4", "c5"].index(args.workload) + 1
-    inp = make_config(args.workload, seed=idx)
+    inp = with_kv_option(make_config(args.workload, seed=idx), args)
     sub = copy.copy(inp)
     if args.profile != "fused":
         empty = copy.copy(inp.d if args.profile == "prefill" else inp.p)
@@ -593,6 +603,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--kv-fp8", action="store_true",
+                    help="decode cache in FP8 E4M3 (per-tensor K and V scales)")
     ap.add_argument("--profile", choices=["fused", "prefill", "decode"], default=None,
                     help="only launch this variant (for ncu captures); prints a summary line")
     args = ap.parse_args(argv)

@@ -137,6 +137,22 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p,
                    void* workspace, void* out_p, float* lse_p,
                    void* out_d, float* lse_d, void* stream);
 
+/*
+ * pod_plan_set_decode_fp8 — the decode half's cache is FP8 E4M3 with
+ * per-tensor calibration scales (POD walkthrough, "Decode 侧参数与'plan 覆盖'
+ * 行为": q_scale and k_scale multiply the decode sm_scale, v_scale multiplies
+ * the decode output). From the next pod_run on, kv_d is read as
+ * [d_num_pages, 2, page_size, Hk, head_dim] one-byte E4M3 codes, K = code *
+ * k_scale and V = code * v_scale; fold a query scale into k_scale. The
+ * kernel folds k_scale into its softmax scale and multiplies the decode
+ * outputs (split partials included) by v_scale; the decode LSE is that of the
+ * scaled logits. q_d and out_d keep the plan's 16-bit dtype; the prefill half
+ * is unchanged. May be called again to change the scales. Errors:
+ * POD_ERR_UNSUPPORTED unless head_dim is 128; POD_ERR_INVALID_ARG for a NULL
+ * handle or scales that are not finite and positive.
+ */
+pod_status pod_plan_set_decode_fp8(pod_handle h, float k_scale, float v_scale);
+
 /* Release the handle (host memory only). NULL is accepted. */
 pod_status pod_destroy(pod_handle h);
 

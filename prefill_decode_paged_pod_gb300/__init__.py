@@ -82,6 +82,8 @@ def load_library(path: Optional[str] = None):
     lib.pod_run_static_scratch.argtypes = [V, V, V, V, V, V, V, V, V, V, V]
     lib.pod_static_scratch_capacity.restype = SZ
     lib.pod_static_scratch_capacity.argtypes = []
+    lib.pod_plan_set_decode_fp8.restype = ctypes.c_int
+    lib.pod_plan_set_decode_fp8.argtypes = [V, ctypes.c_float, ctypes.c_float]
     if path is None:
         _lib = lib
     return lib
@@ -142,6 +144,7 @@ class PodHandle:
     dtype: object
     has_sinks: bool
     workspace_ptr: Optional[int] = None
+    d_kv_fp8: bool = False      # set by pod_plan_set_decode_fp8
 
     def __del__(self):
         if self.ptr and _lib is not None:
@@ -219,8 +222,9 @@ def pod_run(h: PodHandle, q_p, kv_p, q_d, kv_d, workspace, sinks=None,
     if lse_d is None:
         lse_d = torch.empty((h.d_rows, H), dtype=torch.float32, device=dev)
     for name, t in (("q_p", q_p), ("kv_p", kv_p), ("q_d", q_d), ("kv_d", kv_d)):
-        if t is not None and (not t.is_contiguous() or t.dtype != h.dtype):
-            raise PodError(1, f"{name} must be contiguous {h.dtype}")
+        want = torch.float8_e4m3fn if (name == "kv_d" and h.d_kv_fp8) else h.dtype
+        if t is not None and (not t.is_contiguous() or t.dtype != want):
+            raise PodError(1, f"{name} must be contiguous {want}")
     p_empty, d_empty = h.p_rows == 0, h.d_rows == 0
     code = lib.pod_run(ctypes.c_void_p(h.ptr),
                        None if p_empty else _ptr(q_p), None if p_empty else _ptr(kv_p),
@@ -304,8 +308,25 @@ def plan_summary(h: PodHandle) -> dict:
     return {k: int(v) for k, v in zip(SUMMARY_FIELDS, s)}
 
 
+def pod_plan_set_decode_fp8(h: PodHandle, k_scale: float, v_scale: float):
+    """The decode cache is FP8 E4M3 codes; K = code * k_scale, V = code * v_scale."""
+    _check(load_library().pod_plan_set_decode_fp8(ctypes.c_void_p(h.ptr), float(k_scale),
+                                                  float(v_scale)))
+    h.d_kv_fp8 = True
+
+
 def plan_inputs(inp, workspace=None, num_sms=0, stream=None) -> PodHandle:
-    """pod_plan for a ``pod_workloads.PODInputs``-shaped object (tests, bench)."""
+    """pod_plan for a ``pod_workloads.PODInputs``-shaped object (tests, bench);
+    an FP8 (float8_e4m3fn) decode cache gets pod_plan_set_decode_fp8 with the
+    inputs' scales."""
+    h = _plan_inputs(inp, workspace, num_sms, stream)
+    import torch
+    if inp.d.rows and getattr(inp.d.kv, "dtype", None) == torch.float8_e4m3fn:
+        pod_plan_set_decode_fp8(h, inp.k_scale, inp.v_scale)
+    return h
+
+
+def _plan_inputs(inp, workspace, num_sms, stream) -> PodHandle:
     return pod_plan(inp.p.q_indptr, inp.p.kv_indptr, inp.p.kv_indices, inp.p.last_page_len,
                     inp.d.q_indptr, inp.d.kv_indptr, inp.d.kv_indices, inp.d.last_page_len,
                     inp.num_qo_heads, inp.num_kv_heads, inp.head_dim, inp.page_size,

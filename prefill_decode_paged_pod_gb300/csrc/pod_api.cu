@@ -12,6 +12,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cmath>
 #include <new>
 #include <string>
 
@@ -21,6 +22,9 @@
 
 struct pod_plan_s {
   PodPlanHost plan;
+  // decode cache stored as FP8 E4M3 codes with per-tensor K and V scales
+  int d_fp8 = 0;
+  float k_scale = 1.f, v_scale = 1.f;
   void* workspace = nullptr;      // bound device workspace (nullptr = host-only plan)
   size_t workspace_bytes = 0;
   // TMA descriptors of the last run, re-encoded only when a tensor pointer changes
@@ -162,6 +166,40 @@ pod_status encode_kv_decode(CUtensorMap* m, const void* ptr, int num_pages, int 
   return POD_OK;
 }
 
+// FP8 (E4M3) decode view of the paged cache: a key's head row is 128 bytes,
+// one 128-byte swizzle row; one box holds `kbx` keys of one head and lands as
+// [key][128]. Dims, innermost first: page_size >= 8:
+// [128][ps][Hk][2 * pages] (coordinate 2 * page + kv); page_size 1:
+// [128][pages][Hk][2].
+pod_status encode_kv_decode_fp8(CUtensorMap* m, const void* ptr, int num_pages, int ps, int Hk,
+                                int d, int kbx) {
+  auto fn = encode_fn();
+  if (!fn) return set_err(POD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15u) != 0)
+    return set_err(POD_ERR_INVALID_ARG, "kv caches must be 16-byte aligned");
+  const cuuint64_t row = (cuuint64_t)d;  // bytes per head row
+  cuuint64_t dims[4], strides[3];
+  if (ps >= 8) {
+    cuuint64_t d4[4] = {(cuuint64_t)d, (cuuint64_t)ps, (cuuint64_t)Hk, 2 * (cuuint64_t)num_pages};
+    cuuint64_t s3[3] = {row * Hk, row, row * Hk * ps};
+    memcpy(dims, d4, sizeof(d4));
+    memcpy(strides, s3, sizeof(s3));
+  } else {
+    cuuint64_t d4[4] = {(cuuint64_t)d, (cuuint64_t)num_pages, (cuuint64_t)Hk, 2};
+    cuuint64_t s3[3] = {row * Hk * 2, row, row * Hk};
+    memcpy(dims, d4, sizeof(d4));
+    memcpy(strides, s3, sizeof(s3));
+  }
+  cuuint32_t box[4] = {(cuuint32_t)d, (cuuint32_t)kbx, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_err(POD_ERR_CUDA, "cuTensorMapEncodeTiled(kv, decode fp8) failed: " + std::to_string((int)r));
+  return POD_OK;
+}
+
 }  // namespace
 
 // Lets other translation units of the library report a message through
@@ -264,8 +302,10 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
     pod_status st = (i % 2 == 0)
         ? encode_q(&h->tm[i], ptrs[i], hh.rows, P.H, P.d, P.G, pre ? P.tq : P.tu, P.dtype)
         : pre ? encode_kv(&h->tm[i], ptrs[i], hh.num_pages, P.ps, P.Hk, P.d, P.p_tma, P.dtype)
-              : encode_kv_decode(&h->tm[i], ptrs[i], hh.num_pages, P.ps, P.Hk, P.d, P.d_tma,
-                                 P.dtype);
+              : h->d_fp8
+                    ? encode_kv_decode_fp8(&h->tm[i], ptrs[i], hh.num_pages, P.ps, P.Hk, P.d, P.d_tma)
+                    : encode_kv_decode(&h->tm[i], ptrs[i], hh.num_pages, P.ps, P.Hk, P.d, P.d_tma,
+                                       P.dtype);
     if (st != POD_OK) return st;
     h->tm_ptr[i] = ptrs[i];
   }
@@ -293,6 +333,9 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
     if ((1 << s) == P.ps) K.ps_shift = s;
   K.causal = P.causal; K.window_left = P.window_left; K.has_sinks = P.has_sinks;
   K.scale_log2 = P.scale_log2;
+  K.d_fp8 = h->d_fp8;
+  K.d_scale_log2 = P.scale_log2 * h->k_scale;
+  K.v_scale = h->v_scale;
   K.n_p_ctas = P.n_p_ctas; K.grid = P.grid;
   K.n_groups = (int)(P.mgroups.size() / POD_REC); K.n_mrows = P.n_mrows;
   K.p_batch = P.p.batch; K.d_batch = P.dd.batch;
@@ -319,6 +362,20 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
 
 pod_status pod_destroy(pod_handle h) {
   delete h;
+  return POD_OK;
+}
+
+pod_status pod_plan_set_decode_fp8(pod_handle h, float k_scale, float v_scale) {
+  g_err.clear();
+  if (!h) return set_err(POD_ERR_INVALID_ARG, "handle is NULL");
+  if (h->plan.d != 128)
+    return set_err(POD_ERR_UNSUPPORTED, "an FP8 decode cache needs head_dim 128");
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return set_err(POD_ERR_INVALID_ARG, "k_scale and v_scale must be finite and positive");
+  h->d_fp8 = 1;
+  h->k_scale = k_scale;
+  h->v_scale = v_scale;
+  h->tm_ptr[3] = nullptr;  // the decode cache's tensor map changes format
   return POD_OK;
 }
 

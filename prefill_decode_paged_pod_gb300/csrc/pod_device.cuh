@@ -96,6 +96,14 @@ POD_DEV void tma_load_5d(uint32_t dst, const void* tmap, int c0, int c1, int c2,
       "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
       : "memory");
 }
+POD_DEV void tma_load_4d(uint32_t dst, const void* tmap, int c0, int c1, int c2, int c3,
+                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
 POD_DEV void tma_load_3d(uint32_t dst, const void* tmap, int c0, int c1, int c2, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
@@ -265,6 +273,25 @@ struct Pack<__half> {
   }
   static constexpr bool kBF16 = false;
 };
+
+// Two FP8 E4M3 codes (low byte first) -> two 16-bit values of T, exactly
+// (every E4M3 value is representable in fp16 and in bf16).
+template <typename T>
+POD_DEV uint32_t e4m3x2_to(uint16_t two);
+template <>
+POD_DEV uint32_t e4m3x2_to<__half>(uint16_t two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+  return h2;
+}
+template <>
+POD_DEV uint32_t e4m3x2_to<__nv_bfloat16>(uint16_t two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+  const float2 f = __half22float2(*reinterpret_cast<__half2*>(&h2));
+  __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
 
 // ---------------------------------------------------------------- mma.sync
 POD_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {

@@ -73,6 +73,14 @@ struct DLayout {                                   // decode shared memory
   static constexpr int STAGE_OFF = NKB * QDH;
   static constexpr int BAR_OFF = STAGE_OFF + NSTAGE * STAGE_BYTES;
   static constexpr int TOTAL = BAR_OFF + 128;
+  // FP8 (E4M3) cache, head_dim 128 only: the ring holds one-byte codes
+  // ([key][128 B] per K or V, 16 KB a stage) and each stage is widened into
+  // one 16-bit stage buffer (layout of the cp.async path) before the compute
+  static constexpr int F8_HALF = POD_DECODE_STAGE * 128;   // K or V of a stage
+  static constexpr int F8_STAGE = 2 * F8_HALF;
+  static constexpr int CONV_OFF = STAGE_OFF + NSTAGE * F8_STAGE;
+  static_assert(D != 128 || CONV_OFF + STAGE_BYTES <= STAGE_OFF + NSTAGE * STAGE_BYTES,
+                "the FP8 ring and its widened stage must fit the 16-bit ring");
   // combine scratch (reuses the stages): 8 warps x 16 rows x D floats, then m/l
   static constexpr int SCR_O = STAGE_OFF;
   static constexpr int SCR_ML = STAGE_OFF + 8 * 16 * D * 4;
@@ -617,7 +625,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
   // K/V stage layout: [key / kbx][d half][key % kbx][64 elements] in 128-byte
   // swizzled rows, kbx = keys per TMA box (64 on the cp.async path, where it
   // is [d half][key][64]). Row offset of key k in its d half 0:
-  const int kshift = P.d_tma ? 31 - __clz(P.d_tma) : 6;
+  const int kshift = (P.d_tma && !P.d_fp8) ? 31 - __clz(P.d_tma) : 6;
   const uint32_t half_stride = 128u << kshift;  // bytes between the d halves of a box
   auto key_row = [&](int k) -> uint32_t {
     return (uint32_t)((k >> kshift) << kshift) * (NKB * 128u) +
@@ -668,14 +676,28 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
         // warp 0: lane 0 registers the bytes, lane i fetches box group i
         if (warp == 0) {
           if (lane == 0) {
-            mbar_arrive_expect_tx(full, 2u * L::KBYTES + (st == 0 ? q_bytes : 0u));
+            mbar_arrive_expect_tx(full, (P.d_fp8 ? (uint32_t)L::F8_STAGE : 2u * L::KBYTES) +
+                                            (st == 0 ? q_bytes : 0u));
             if (st == 0)
               for (int dh = 0; dh < NKB; ++dh)
                 tma_load_3d(sbase + L::Q_OFF + dh * L::QDH, &P.tm_q_d, dh * 64, g * G, q_base + tok0,
                             full);
           }
           __syncwarp();
-          if (lane < POD_DECODE_STAGE / P.d_tma) {
+          if (P.d_fp8 && lane < POD_DECODE_STAGE / P.d_tma) {
+            // one-byte codes: a key's head row is one 128-byte row
+            if (page < 0) page = page_for(st);
+            const int o = lane * P.d_tma;
+            const uint32_t k8 = sbase + L::STAGE_OFF + buf * L::F8_STAGE + (uint32_t)o * 128u;
+            if (P.ps >= 8) {  // coordinates (x, slot, head, 2 * page + kv)
+              const int tin = (kb + o) & (P.ps - 1);
+              tma_load_4d(k8, &P.tm_kv_d, 0, tin, g, 2 * page, full);
+              tma_load_4d(k8 + L::F8_HALF, &P.tm_kv_d, 0, tin, g, 2 * page + 1, full);
+            } else {          // page_size 1: (x, page, head, kv)
+              tma_load_4d(k8, &P.tm_kv_d, 0, page, g, 0, full);
+              tma_load_4d(k8 + L::F8_HALF, &P.tm_kv_d, 0, page, g, 1, full);
+            }
+          } else if (lane < POD_DECODE_STAGE / P.d_tma) {
             if (page < 0) page = page_for(st);
             const int o = lane * P.d_tma;
             const uint32_t dst = (uint32_t)o * (NKB * 128u);
@@ -702,6 +724,36 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
             cp_async16(sbase + L::Q_OFF + (c >> 3) * L::QDH + sw128_off(r, c & 7), src,
                        valid ? 16u : 0u);
           }
+        }
+        if (P.d_fp8) {
+          // one-byte codes, [key][128 B] per K or V: 8 chunks of 16 B a key
+          const uint8_t* __restrict__ kv8 = reinterpret_cast<const uint8_t*>(P.kv_d);
+          const uint32_t k8 = sbase + L::STAGE_OFF + buf * L::F8_STAGE;
+          const size_t vstride8 = (size_t)P.ps * P.Hk * D;
+          constexpr int PER8 = POD_DECODE_STAGE * 8 / kThreads;
+          int pages8[PER8];
+#pragma unroll
+          for (int i = 0; i < PER8; ++i) {
+            const int t = kb + ((tid + kThreads * i) >> 3);
+            const int tt = (t >= k0 && t < k1) ? t : k0;
+            pages8[i] = __ldg(P.d_kv_indices + page_base +
+                              (P.ps_shift >= 0 ? (tt >> P.ps_shift) : (tt / P.ps)));
+          }
+#pragma unroll
+          for (int i = 0; i < PER8; ++i) {
+            const int idx = tid + kThreads * i;
+            const int key = idx >> 3, c = idx & 7;
+            const int t = kb + key;
+            const bool valid = t >= k0 && t < k1;
+            const int tt = valid ? t : k0;
+            const int slot = P.ps_shift >= 0 ? (tt & (P.ps - 1)) : (tt % P.ps);
+            const uint8_t* src = kv8 + (((size_t)pages8[i] * 2 * P.ps + slot) * P.Hk + g) * D + c * 16;
+            const uint32_t off = (uint32_t)key * 128u + (uint32_t)((c ^ (key & 7)) << 4);
+            cp_async16(k8 + off, src, valid ? 16u : 0u);
+            cp_async16(k8 + L::F8_HALF + off, src + vstride8, valid ? 16u : 0u);
+          }
+          cp_async_mbar_arrive(full);
+          return;
         }
         constexpr int CH = POD_DECODE_STAGE * (D / 8);
         constexpr int PER = CH / kThreads;
@@ -760,10 +812,41 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
       const int next_page =
           (P.d_tma && warp == 0 && st + L::NSTAGE < nst) ? page_for(st + L::NSTAGE) : -1;
       const bool got = mbar_wait(bar0 + 8 * buf, (f / L::NSTAGE) & 1, abort_flag);
+      uint32_t sk = sbase + L::STAGE_OFF + buf * L::STAGE_BYTES;
+      if (P.d_fp8) {
+        // widen the stage's E4M3 codes into the 16-bit stage buffer; the ring
+        // slot is free again once that is done, and is refilled at once
+        if (got) {
+          const uint8_t* src = smem + L::STAGE_OFF + buf * L::F8_STAGE;
+          uint8_t* dst = smem + L::CONV_OFF;
+          for (int j = tid; j < 2 * POD_DECODE_STAGE * 8; j += kThreads) {
+            const int isv = j / (POD_DECODE_STAGE * 8), idx = j % (POD_DECODE_STAGE * 8);
+            const int key = idx >> 3, c = idx & 7, x = key & 7;
+            const uint4 v = *reinterpret_cast<const uint4*>(src + isv * L::F8_HALF + key * 128 +
+                                                            ((c ^ x) << 4));
+            uint4 lo, hi;
+            lo.x = e4m3x2_to<T>((uint16_t)(v.x & 0xffffu));
+            lo.y = e4m3x2_to<T>((uint16_t)(v.x >> 16));
+            lo.z = e4m3x2_to<T>((uint16_t)(v.y & 0xffffu));
+            lo.w = e4m3x2_to<T>((uint16_t)(v.y >> 16));
+            hi.x = e4m3x2_to<T>((uint16_t)(v.z & 0xffffu));
+            hi.y = e4m3x2_to<T>((uint16_t)(v.z >> 16));
+            hi.z = e4m3x2_to<T>((uint16_t)(v.w & 0xffffu));
+            hi.w = e4m3x2_to<T>((uint16_t)(v.w >> 16));
+            // elements 16c .. 16c+15: d half c/4, 16-bit chunks 2(c%4) and 2(c%4)+1
+            uint8_t* row = dst + isv * L::KBYTES + (c >> 2) * L::KDH + key * 128;
+            const int cc = 2 * (c & 3);
+            *reinterpret_cast<uint4*>(row + ((cc ^ x) << 4)) = lo;
+            *reinterpret_cast<uint4*>(row + (((cc + 1) ^ x) << 4)) = hi;
+          }
+        }
+        if (!__syncthreads_and(got)) { ok = false; break; }
+        if (st + L::NSTAGE < nst) issue(st + L::NSTAGE, next_page);
+        sk = sbase + L::CONV_OFF;
+      }
       const int kbase = kb0 + st * POD_DECODE_STAGE + ks * 16;
       if (got && active && kbase < k1 && kbase + 16 > k0) {
         const uint32_t sq = sbase + L::Q_OFF;
-        const uint32_t sk = sbase + L::STAGE_OFF + buf * L::STAGE_BYTES;
         const uint32_t sv = sk + L::KBYTES;
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -785,7 +868,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
         }
         // mask, online softmax in base 2 (rows h2 = 0: c0,c1; h2 = 1: c2,c3)
         const int kq = kbase + 2 * (lane & 3);
-        const float scale = P.scale_log2;
+        const float scale = P.d_scale_log2;  // sm_scale * log2(e), times k_scale for FP8
         float mx[2];
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
@@ -848,7 +931,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
         }
       }
       if (!__syncthreads_and(got)) { ok = false; break; }
-      if (st + L::NSTAGE < nst) issue(st + L::NSTAGE, next_page);
+      if (!P.d_fp8 && st + L::NSTAGE < nst) issue(st + L::NSTAGE, next_page);
     }
     fills += nst;
     if (!ok) break;
@@ -909,7 +992,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
       if (prow < 0) {
         float denom = wsum;
         if (P.has_sinks) denom += ex2(P.sinks[head] * 1.4426950408889634f - Ms);
-        const float inv = denom > 0.f ? 1.f / denom : 0.f;
+        const float inv = denom > 0.f ? P.v_scale / denom : 0.f;
         const size_t orow = (size_t)(cq_base + tok) * H + head;
         uint2 v;
         v.x = Pack<T>::two(acc.x * inv, acc.y * inv);
@@ -917,7 +1000,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
         *reinterpret_cast<uint2*>(outg + orow * D + c4) = v;
         if (c4 == 0 && P.lse_d) P.lse_d[orow] = wsum > 0.f ? M + log2f(wsum) : NEG_INF;
       } else {
-        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+        const float inv = wsum > 0.f ? P.v_scale / wsum : 0.f;
         *reinterpret_cast<float4*>(P.part_o + (size_t)(prow + rr) * D + c4) =
             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         if (c4 == 0) P.part_lse[prow + rr] = wsum > 0.f ? M + log2f(wsum) : NEG_INF;

@@ -65,6 +65,10 @@ struct PodParams {
   int tq, tu;                // tokens per prefill tile / per decode unit
   int H, Hk, G, d, ps, ps_shift, causal, window_left, has_sinks;
   float scale_log2;          // sm_scale * log2(e)
+  // decode cache in FP8 E4M3 (head_dim 128): d_scale_log2 = scale_log2 * k_scale,
+  // outputs multiplied by v_scale
+  int d_fp8;
+  float d_scale_log2, v_scale;
   int n_p_ctas, grid;
   int n_groups, n_mrows;
   int p_batch, d_batch;

@@ -8,6 +8,10 @@
 // variant 0: O with one N = D MMA per k-step; variant 1: one N = 64 MMA per
 // 64-column block of D; variant 2: P is written into TMEM (tcgen05.st, two
 // 16-bit values per column) and read from there as the A operand.
+// e4m3_selftest widens every pair of FP8 E4M3 codes with the decode path's
+// conversion helper.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "pod_device.cuh"
@@ -138,6 +142,23 @@ extern "C" int umma_selftest(const void* q, const void* k, const void* v, const 
     if (bf16) launch(umma_selftest_kernel<64, true>);
     else launch(umma_selftest_kernel<64, false>);
   }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return (int)e;
+  return (int)cudaDeviceSynchronize();
+}
+
+__global__ void e4m3_selftest_kernel(const uint16_t* in, uint32_t* out_h, uint32_t* out_b, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) {
+    out_h[i] = e4m3x2_to<__half>(in[i]);
+    out_b[i] = e4m3x2_to<__nv_bfloat16>(in[i]);
+  }
+}
+
+// n pairs of E4M3 codes (low byte first) -> packed fp16 pairs and bf16 pairs
+extern "C" int e4m3_selftest(const void* in, void* out_h, void* out_b, int n) {
+  e4m3_selftest_kernel<<<(n + 255) / 256, 256>>>((const uint16_t*)in, (uint32_t*)out_h,
+                                                (uint32_t*)out_b, n);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return (int)e;
   return (int)cudaDeviceSynchronize();

@@ -115,5 +115,7 @@ def selftest_lib():
         L = ctypes.CDLL(so)
         L.umma_selftest.restype = ctypes.c_int
         L.umma_selftest.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_int] * 3 + [ctypes.c_void_p]
+        L.e4m3_selftest.restype = ctypes.c_int
+        L.e4m3_selftest.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int]
         _SELFTEST = L
     return _SELFTEST

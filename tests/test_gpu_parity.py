@@ -237,3 +237,78 @@ def test_cuda_graph_capture_and_replan_in_place():
         op, lp, od, ld = [outs[k].double().cpu().numpy() for k in ("out_p", "lse_p", "out_d", "lse_d")]
         compare_half(inp, "p", op, lp, tag="graph ")
         compare_half(inp, "d", od, ld, tag="graph ")
+
+
+# ------------------------------------------------------------- FP8 decode cache
+def test_e4m3_widening_against_torch():
+    """The decode path's E4M3 -> fp16 / bf16 widening, on every pair of codes
+    (NaN codes excepted), against torch's conversion."""
+    L = selftest_lib()
+    pairs = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    codes = pairs.view(torch.uint8).reshape(-1, 2)           # low byte first
+    src = pairs.cuda()
+    out_h = torch.empty(65536, dtype=torch.int32, device="cuda")
+    out_b = torch.empty(65536, dtype=torch.int32, device="cuda")
+    assert L.e4m3_selftest(src.data_ptr(), out_h.data_ptr(), out_b.data_ptr(), 65536) == 0
+    f8 = codes.contiguous().view(torch.float8_e4m3fn)
+    ref = f8.float()
+    gh = out_h.cpu().view(torch.float16).reshape(-1, 2).float()
+    gb = out_b.cpu().view(torch.bfloat16).reshape(-1, 2).float()
+    live = ~torch.isnan(ref)
+    assert torch.equal(gh[live], ref[live]) and torch.equal(gb[live], ref[live])
+    assert torch.isnan(gh[~live]).all() and torch.isnan(gb[~live]).all()
+
+
+FP8_CASES = [
+    # ps, pages, G, Hk, decode q_len, dtype, window, sinks, num_sms
+    (16, "perm", 8, 2, 4, torch.bfloat16, 4096, True, 0),     # TMA page boxes, 32-row items
+    (16, "perm", 4, 2, 1, torch.float16, -1, False, 0),
+    (1, "contig", 4, 2, 1, torch.bfloat16, -1, True, 0),       # TMA runs of pages
+    (3, "perm", 2, 2, 2, torch.bfloat16, 37, True, 0),         # cp.async gather
+    (16, "perm", 8, 2, 1, torch.bfloat16, -1, True, 4),        # split KV + merge
+    (32, "perm", 4, 1, 3, torch.float16, 300, False, 0),
+    (32, "perm", 4, 1, 3, torch.float16, -1, False, 4),
+]
+
+
+@pytest.mark.parametrize("ps,pages,G,Hk,ql,dt,window,sinks,nsm", FP8_CASES)
+def test_fp8_decode_cache(ps, pages, G, Hk, ql, dt, window, sinks, nsm):
+    from pod_workloads import with_fp8_decode_cache
+    rng = np.random.default_rng(ps * 100 + G * 10 + ql)
+    if nsm:   # few long requests on few SMs: the plan splits their keys
+        dkv = [9000, 12000, 7000]
+    else:
+        dkv = [int(x) for x in rng.integers(ql, 3000, size=9)]
+    base = make_custom("fp8", dt, G * Hk, Hk, 128, ps, True, window, [70], [90], [ql] * len(dkv),
+                       dkv, seed=ps + G, sinks=sinks, pages=pages, extra_pages=2)
+    inp = with_fp8_decode_cache(base, k_scale=0.05, v_scale=0.02)
+    (op, lp, od, ld), h, ws = run_pod(inp, num_sms=nsm)
+    s = pod.plan_summary(h)
+    if nsm:
+        assert s["n_groups"] > 0, s
+    compare_half(inp, "p", op, lp, tag="fp8 ")
+    compare_half(inp, "d", od, ld, tag=f"fp8 ps{ps} G{G} q{ql} ")
+
+
+def test_fp8_unused_page_slots_do_not_leak():
+    """E4M3 NaN codes in the unused slots of the last pages stay out."""
+    from pod_workloads import with_fp8_decode_cache
+    base = make_custom("nan8", torch.bfloat16, 16, 2, 128, 16, True, -1, [20], [20],
+                       [1, 2, 1], [37, 70, 5], seed=9, pages="perm")
+    inp = with_fp8_decode_cache(base, k_scale=0.1, v_scale=0.1)
+    raw = inp.d.kv.view(torch.uint8)
+    for r in range(inp.d.batch):
+        last = int(inp.d.kv_indices[inp.d.kv_indptr[r + 1] - 1])
+        raw[last, :, int(inp.d.last_page_len[r]):] = 0x7F
+    (op, lp, od, ld), h, ws = run_pod(inp)
+    compare_half(inp, "d", od, ld, tag="fp8 nan ")
+
+
+@pytest.mark.slow
+def test_fp8_decode_c5_full_size_sampled():
+    from pod_workloads import with_fp8_decode_cache
+    inp = with_fp8_decode_cache(make_config("c5"), k_scale=0.05, v_scale=0.05)
+    (op, lp, od, ld), h, ws = run_pod(inp)
+    st, sh = sample_rows(inp.d, inp.num_qo_heads, 96, seed=4)
+    compare_half(inp, "d", od, ld, st, sh, tag="fp8 c5 ")
+    assert np.isfinite(od).all() and np.isfinite(ld).all()
