@@ -223,3 +223,22 @@ def test_reference_validation_agrees(lib):
             ok = False
             assert e.code == 1
         assert ok == (reason is None), (trial, reason)
+
+
+def test_decode_fp8_switch_host_checks(lib):
+    """pod_plan_set_decode_fp8 accepts head_dim 128 with positive scales and
+    refuses the rest with the documented codes (host-only plans)."""
+    from pod_workloads import with_fp8_decode_cache
+    inp = with_fp8_decode_cache(make_custom("f8", torch.bfloat16, 16, 2, 128, 16, True, -1, [5], [9],
+                                            [1, 2], [40, 70], seed=1))
+    h = plan_host(inp, num_sms=4)
+    pod.pod_plan_set_decode_fp8(h, 0.5, 2.0)
+    for ks, vs in ((0.0, 1.0), (1.0, -1.0), (float("nan"), 1.0), (1.0, float("inf"))):
+        with pytest.raises(pod.PodError) as e:
+            pod.pod_plan_set_decode_fp8(h, ks, vs)
+        assert e.value.code == 1
+    inp64 = make_custom("f8", torch.bfloat16, 16, 2, 64, 16, True, -1, [5], [9], [1], [40], seed=1)
+    h64 = plan_host(inp64, num_sms=4)
+    with pytest.raises(pod.PodError) as e:
+        pod.pod_plan_set_decode_fp8(h64, 1.0, 1.0)
+    assert e.value.code == 2
