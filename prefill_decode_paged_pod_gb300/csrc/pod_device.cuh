@@ -293,6 +293,12 @@ POD_DEV uint32_t e4m3x2_to<__nv_bfloat16>(uint16_t two) {
   return *reinterpret_cast<uint32_t*>(&b);
 }
 
+POD_DEV uint2 ld_shared_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
 // ---------------------------------------------------------------- mma.sync
 POD_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"

@@ -73,14 +73,11 @@ struct DLayout {                                   // decode shared memory
   static constexpr int STAGE_OFF = NKB * QDH;
   static constexpr int BAR_OFF = STAGE_OFF + NSTAGE * STAGE_BYTES;
   static constexpr int TOTAL = BAR_OFF + 128;
-  // FP8 (E4M3) cache, head_dim 128 only: the ring holds one-byte codes
-  // ([key][128 B] per K or V, 16 KB a stage) and each stage is widened into
-  // one 16-bit stage buffer (layout of the cp.async path) before the compute
+  // FP8 (E4M3) cache, head_dim 128 only: the ring holds one-byte codes,
+  // [key][128 B] per K or V (16 KB a stage), widened in registers as the
+  // mma fragments are built
   static constexpr int F8_HALF = POD_DECODE_STAGE * 128;   // K or V of a stage
   static constexpr int F8_STAGE = 2 * F8_HALF;
-  static constexpr int CONV_OFF = STAGE_OFF + NSTAGE * F8_STAGE;
-  static_assert(D != 128 || CONV_OFF + STAGE_BYTES <= STAGE_OFF + NSTAGE * STAGE_BYTES,
-                "the FP8 ring and its widened stage must fit the 16-bit ring");
   // combine scratch (reuses the stages): 8 warps x 16 rows x D floats, then m/l
   static constexpr int SCR_O = STAGE_OFF;
   static constexpr int SCR_ML = STAGE_OFF + 8 * 16 * D * 4;
@@ -812,45 +809,46 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
       const int next_page =
           (P.d_tma && warp == 0 && st + L::NSTAGE < nst) ? page_for(st + L::NSTAGE) : -1;
       const bool got = mbar_wait(bar0 + 8 * buf, (f / L::NSTAGE) & 1, abort_flag);
-      uint32_t sk = sbase + L::STAGE_OFF + buf * L::STAGE_BYTES;
-      if (P.d_fp8) {
-        // widen the stage's E4M3 codes into the 16-bit stage buffer; the ring
-        // slot is free again once that is done, and is refilled at once
-        if (got) {
-          const uint8_t* src = smem + L::STAGE_OFF + buf * L::F8_STAGE;
-          uint8_t* dst = smem + L::CONV_OFF;
-          for (int j = tid; j < 2 * POD_DECODE_STAGE * 8; j += kThreads) {
-            const int isv = j / (POD_DECODE_STAGE * 8), idx = j % (POD_DECODE_STAGE * 8);
-            const int key = idx >> 3, c = idx & 7, x = key & 7;
-            const uint4 v = *reinterpret_cast<const uint4*>(src + isv * L::F8_HALF + key * 128 +
-                                                            ((c ^ x) << 4));
-            uint4 lo, hi;
-            lo.x = e4m3x2_to<T>((uint16_t)(v.x & 0xffffu));
-            lo.y = e4m3x2_to<T>((uint16_t)(v.x >> 16));
-            lo.z = e4m3x2_to<T>((uint16_t)(v.y & 0xffffu));
-            lo.w = e4m3x2_to<T>((uint16_t)(v.y >> 16));
-            hi.x = e4m3x2_to<T>((uint16_t)(v.z & 0xffffu));
-            hi.y = e4m3x2_to<T>((uint16_t)(v.z >> 16));
-            hi.z = e4m3x2_to<T>((uint16_t)(v.w & 0xffffu));
-            hi.w = e4m3x2_to<T>((uint16_t)(v.w >> 16));
-            // elements 16c .. 16c+15: d half c/4, 16-bit chunks 2(c%4) and 2(c%4)+1
-            uint8_t* row = dst + isv * L::KBYTES + (c >> 2) * L::KDH + key * 128;
-            const int cc = 2 * (c & 3);
-            *reinterpret_cast<uint4*>(row + ((cc ^ x) << 4)) = lo;
-            *reinterpret_cast<uint4*>(row + (((cc + 1) ^ x) << 4)) = hi;
-          }
-        }
-        if (!__syncthreads_and(got)) { ok = false; break; }
-        if (st + L::NSTAGE < nst) issue(st + L::NSTAGE, next_page);
-        sk = sbase + L::CONV_OFF;
-      }
+      // 16-bit cache: K of the stage (V follows at +KBYTES); FP8: its codes
+      const uint32_t sk = P.d_fp8 ? sbase + L::STAGE_OFF + buf * L::F8_STAGE
+                                  : sbase + L::STAGE_OFF + buf * L::STAGE_BYTES;
       const int kbase = kb0 + st * POD_DECODE_STAGE + ks * 16;
       if (got && active && kbase < k1 && kbase + 16 > k0) {
         const uint32_t sq = sbase + L::Q_OFF;
-        const uint32_t sv = sk + L::KBYTES;
+        const uint32_t sv = sk + (P.d_fp8 ? (uint32_t)L::F8_HALF : (uint32_t)L::KBYTES);
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        // FP8 rows are [key][128 one-byte codes]; ldmatrix reads them as 8x8
+        // tiles of byte pairs. Lane addresses: matrix i = lane/8 holds keys
+        // 8(i&1) + lane%8 of the warp's slice and 16-byte chunk 2j + i/2.
+        const int f8key = ks * 16 + (lane & 7) + ((mi & 1) << 3);
+        if (P.d_fp8) {
+          // A thread's K bytes are d 4t..4t+3 of a 16-d chunk (t = lane%4); the
+          // k16 step sums over d, so Q is read with the same order: a0/a1 =
+          // d 4t, 4t+1 and a2/a3 = d 4t+2, 4t+3 (rows g and g+8, g = lane/4).
+          const int rq = mt * 16 + (lane >> 2);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+          for (int j = 0; j < D / 32; ++j) {
+            uint32_t r[4];
+            ldsm_x4(sk + f8key * 128 + ((((2 * j + (mi >> 1)) ^ (f8key & 7))) << 4), r[0], r[1],
+                    r[2], r[3]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int d0 = 32 * j + 16 * h + 4 * (lane & 3);
+              const int e = d0 & 63, ch = e >> 3;
+              const uint32_t qa = sq + (d0 >> 6) * L::QDH + ((e & 7) << 1);
+              const uint2 q0 = ld_shared_v2(qa + rq * 128 + ((ch ^ (rq & 7)) << 4));
+              const uint2 q1 = ld_shared_v2(qa + (rq + 8) * 128 + ((ch ^ ((rq + 8) & 7)) << 4));
+              uint32_t a[4] = {q0.x, q1.x, q0.y, q1.y};
+              const uint32_t k0 = r[2 * h], k1 = r[2 * h + 1];   // keys 0-7 / 8-15 of the slice
+              mma16816<BF16>(s0, a, e4m3x2_to<T>((uint16_t)(k0 & 0xffffu)),
+                             e4m3x2_to<T>((uint16_t)(k0 >> 16)));
+              mma16816<BF16>(s1, a, e4m3x2_to<T>((uint16_t)(k1 & 0xffffu)),
+                             e4m3x2_to<T>((uint16_t)(k1 >> 16)));
+            }
+          }
+        }
+#pragma unroll
+        for (int kk = 0; kk < (P.d_fp8 ? 0 : D / 16); ++kk) {
           uint32_t a[4], b[4];
           {
             const int rr = mt * 16 + (lane & 7) + ((mi & 1) << 3);
@@ -907,11 +905,20 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
             o[i][2 * h2 + 1] *= alpha;
           }
         }
+        // P <= 1: with an FP8 cache the PV product runs in fp16 (V widens to
+        // fp16 in one conversion), otherwise in the plan's 16-bit type
         uint32_t pa[4];
-        pa[0] = Pack<T>::two(s0[0], s0[1]);
-        pa[1] = Pack<T>::two(s0[2], s0[3]);
-        pa[2] = Pack<T>::two(s1[0], s1[1]);
-        pa[3] = Pack<T>::two(s1[2], s1[3]);
+        if (P.d_fp8) {
+          pa[0] = Pack<__half>::two(s0[0], s0[1]);
+          pa[1] = Pack<__half>::two(s0[2], s0[3]);
+          pa[2] = Pack<__half>::two(s1[0], s1[1]);
+          pa[3] = Pack<__half>::two(s1[2], s1[3]);
+        } else {
+          pa[0] = Pack<T>::two(s0[0], s0[1]);
+          pa[1] = Pack<T>::two(s0[2], s0[3]);
+          pa[2] = Pack<T>::two(s1[0], s1[1]);
+          pa[3] = Pack<T>::two(s1[2], s1[3]);
+        }
         // V rows at or past kv_len may be unused slots of the last page: zero
         // them in the fragments so that P = 0 never meets a non-finite value
         uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
@@ -919,8 +926,31 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
           vm0 = (kq < kv_len ? 0x0000ffffu : 0u) | (kq + 1 < kv_len ? 0xffff0000u : 0u);
           vm1 = (kq + 8 < kv_len ? 0x0000ffffu : 0u) | (kq + 9 < kv_len ? 0xffff0000u : 0u);
         }
+        if (P.d_fp8) {
+          // transposed byte-pair tiles: a register holds V[2t][2g], V[2t][2g+1],
+          // V[2t+1][2g], V[2t+1][2g+1] (keys 2t, 2t+1; d pair g); the even-d
+          // and odd-d bytes make two n8 tiles: o[2q] holds d 16q + 4t + {0, 2},
+          // o[2q+1] d 16q + 4t + {1, 3} (columns 2t, 2t+1 of each tile)
 #pragma unroll
-        for (int j = 0; j < D / 16; ++j) {
+          for (int j = 0; j < D / 32; ++j) {
+            uint32_t r[4];
+            ldsm_x4_t(sv + f8key * 128 + ((((2 * j + (mi >> 1)) ^ (f8key & 7))) << 4), r[0], r[1],
+                      r[2], r[3]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t lo = r[2 * h], hi = r[2 * h + 1];   // keys 2t.. / 2t+8..
+              const uint32_t be0 = e4m3x2_to<__half>((uint16_t)((lo & 0xffu) | ((lo >> 8) & 0xff00u)));
+              const uint32_t bo0 = e4m3x2_to<__half>((uint16_t)(((lo >> 8) & 0xffu) | ((lo >> 16) & 0xff00u)));
+              const uint32_t be1 = e4m3x2_to<__half>((uint16_t)((hi & 0xffu) | ((hi >> 8) & 0xff00u)));
+              const uint32_t bo1 = e4m3x2_to<__half>((uint16_t)(((hi >> 8) & 0xffu) | ((hi >> 16) & 0xff00u)));
+              const int q = 2 * j + h;
+              mma16816<false>(o[2 * q], pa, be0 & vm0, be1 & vm1);
+              mma16816<false>(o[2 * q + 1], pa, bo0 & vm0, bo1 & vm1);
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < (P.d_fp8 ? 0 : D / 16); ++j) {
           uint32_t b[4];
           const int key = ks * 16 + (lane & 7) + ((mi & 1) << 3);
           const int c = 2 * j + (mi >> 1);
@@ -931,7 +961,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
         }
       }
       if (!__syncthreads_and(got)) { ok = false; break; }
-      if (!P.d_fp8 && st + L::NSTAGE < nst) issue(st + L::NSTAGE, next_page);
+      if (st + L::NSTAGE < nst) issue(st + L::NSTAGE, next_page);
     }
     fills += nst;
     if (!ok) break;
@@ -951,12 +981,23 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
     }
     if (active) {
       float* wo = scr_o + warp * 16 * D;
+      const int rl = lane >> 2;
+      if (P.d_fp8) {  // d 16q + 4t .. +3 from the even / odd tiles of chunk q
 #pragma unroll
-      for (int i = 0; i < D / 8; ++i) {
-        const int col = 8 * i + 2 * (lane & 3);
-        const int rl = lane >> 2;
-        *reinterpret_cast<float2*>(wo + rl * D + col) = make_float2(o[i][0], o[i][1]);
-        *reinterpret_cast<float2*>(wo + (rl + 8) * D + col) = make_float2(o[i][2], o[i][3]);
+        for (int q = 0; q < D / 16; ++q) {
+          const int col = 16 * q + 4 * (lane & 3);
+          *reinterpret_cast<float4*>(wo + rl * D + col) =
+              make_float4(o[2 * q][0], o[2 * q + 1][0], o[2 * q][1], o[2 * q + 1][1]);
+          *reinterpret_cast<float4*>(wo + (rl + 8) * D + col) =
+              make_float4(o[2 * q][2], o[2 * q + 1][2], o[2 * q][3], o[2 * q + 1][3]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) {
+          const int col = 8 * i + 2 * (lane & 3);
+          *reinterpret_cast<float2*>(wo + rl * D + col) = make_float2(o[i][0], o[i][1]);
+          *reinterpret_cast<float2*>(wo + (rl + 8) * D + col) = make_float2(o[i][2], o[i][3]);
+        }
       }
       if ((lane & 3) == 0) {
         const int rl = lane >> 2;
