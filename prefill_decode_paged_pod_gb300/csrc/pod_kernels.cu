@@ -593,7 +593,7 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
 // ============================================================ decode role
 // Runs decode items from the shared queue until it is empty. Returns false
 // when a wait ran out (the status word then says so).
-template <typename T, int D>
+template <typename T, int D, bool F8>
 __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
   using L = DLayout<D>;
   constexpr bool BF16 = Pack<T>::kBF16;
@@ -622,7 +622,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
   // K/V stage layout: [key / kbx][d half][key % kbx][64 elements] in 128-byte
   // swizzled rows, kbx = keys per TMA box (64 on the cp.async path, where it
   // is [d half][key][64]). Row offset of key k in its d half 0:
-  const int kshift = (P.d_tma && !P.d_fp8) ? 31 - __clz(P.d_tma) : 6;
+  const int kshift = (P.d_tma && !F8) ? 31 - __clz(P.d_tma) : 6;
   const uint32_t half_stride = 128u << kshift;  // bytes between the d halves of a box
   auto key_row = [&](int k) -> uint32_t {
     return (uint32_t)((k >> kshift) << kshift) * (NKB * 128u) +
@@ -673,7 +673,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
         // warp 0: lane 0 registers the bytes, lane i fetches box group i
         if (warp == 0) {
           if (lane == 0) {
-            mbar_arrive_expect_tx(full, (P.d_fp8 ? (uint32_t)L::F8_STAGE : 2u * L::KBYTES) +
+            mbar_arrive_expect_tx(full, (F8 ? (uint32_t)L::F8_STAGE : 2u * L::KBYTES) +
                                             (st == 0 ? q_bytes : 0u));
             if (st == 0)
               for (int dh = 0; dh < NKB; ++dh)
@@ -681,7 +681,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
                             full);
           }
           __syncwarp();
-          if (P.d_fp8 && lane < POD_DECODE_STAGE / P.d_tma) {
+          if (F8 && lane < POD_DECODE_STAGE / P.d_tma) {
             // one-byte codes: a key's head row is one 128-byte row
             if (page < 0) page = page_for(st);
             const int o = lane * P.d_tma;
@@ -722,7 +722,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
                        valid ? 16u : 0u);
           }
         }
-        if (P.d_fp8) {
+        if constexpr (F8) {
           // one-byte codes, [key][128 B] per K or V: 8 chunks of 16 B a key
           const uint8_t* __restrict__ kv8 = reinterpret_cast<const uint8_t*>(P.kv_d);
           const uint32_t k8 = sbase + L::STAGE_OFF + buf * L::F8_STAGE;
@@ -810,18 +810,18 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
           (P.d_tma && warp == 0 && st + L::NSTAGE < nst) ? page_for(st + L::NSTAGE) : -1;
       const bool got = mbar_wait(bar0 + 8 * buf, (f / L::NSTAGE) & 1, abort_flag);
       // 16-bit cache: K of the stage (V follows at +KBYTES); FP8: its codes
-      const uint32_t sk = P.d_fp8 ? sbase + L::STAGE_OFF + buf * L::F8_STAGE
+      const uint32_t sk = F8 ? sbase + L::STAGE_OFF + buf * L::F8_STAGE
                                   : sbase + L::STAGE_OFF + buf * L::STAGE_BYTES;
       const int kbase = kb0 + st * POD_DECODE_STAGE + ks * 16;
       if (got && active && kbase < k1 && kbase + 16 > k0) {
         const uint32_t sq = sbase + L::Q_OFF;
-        const uint32_t sv = sk + (P.d_fp8 ? (uint32_t)L::F8_HALF : (uint32_t)L::KBYTES);
+        const uint32_t sv = sk + (F8 ? (uint32_t)L::F8_HALF : (uint32_t)L::KBYTES);
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
         // FP8 rows are [key][128 one-byte codes]; ldmatrix reads them as 8x8
         // tiles of byte pairs. Lane addresses: matrix i = lane/8 holds keys
         // 8(i&1) + lane%8 of the warp's slice and 16-byte chunk 2j + i/2.
         const int f8key = ks * 16 + (lane & 7) + ((mi & 1) << 3);
-        if (P.d_fp8) {
+        if constexpr (F8) {
           // A thread's K bytes are d 4t..4t+3 of a 16-d chunk (t = lane%4); the
           // k16 step sums over d, so Q is read with the same order: a0/a1 =
           // d 4t, 4t+1 and a2/a3 = d 4t+2, 4t+3 (rows g and g+8, g = lane/4).
@@ -846,23 +846,24 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
                              e4m3x2_to<T>((uint16_t)(k1 >> 16)));
             }
           }
-        }
+        } else {
 #pragma unroll
-        for (int kk = 0; kk < (P.d_fp8 ? 0 : D / 16); ++kk) {
-          uint32_t a[4], b[4];
-          {
-            const int rr = mt * 16 + (lane & 7) + ((mi & 1) << 3);
-            const int c = kk * 2 + (mi >> 1);
-            ldsm_x4(sq + (c >> 3) * L::QDH + sw128_off(rr, c & 7), a[0], a[1], a[2], a[3]);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            uint32_t a[4], b[4];
+            {
+              const int rr = mt * 16 + (lane & 7) + ((mi & 1) << 3);
+              const int c = kk * 2 + (mi >> 1);
+              ldsm_x4(sq + (c >> 3) * L::QDH + sw128_off(rr, c & 7), a[0], a[1], a[2], a[3]);
+            }
+            {
+              const int key = ks * 16 + (lane & 7) + ((mi >> 1) << 3);
+              const int c = kk * 2 + (mi & 1);
+              ldsm_x4(sk + key_row(key) + (c >> 3) * half_stride + (((c & 7) ^ (lane & 7)) << 4), b[0],
+                      b[1], b[2], b[3]);
+            }
+            mma16816<BF16>(s0, a, b[0], b[1]);
+            mma16816<BF16>(s1, a, b[2], b[3]);
           }
-          {
-            const int key = ks * 16 + (lane & 7) + ((mi >> 1) << 3);
-            const int c = kk * 2 + (mi & 1);
-            ldsm_x4(sk + key_row(key) + (c >> 3) * half_stride + (((c & 7) ^ (lane & 7)) << 4), b[0],
-                    b[1], b[2], b[3]);
-          }
-          mma16816<BF16>(s0, a, b[0], b[1]);
-          mma16816<BF16>(s1, a, b[2], b[3]);
         }
         // mask, online softmax in base 2 (rows h2 = 0: c0,c1; h2 = 1: c2,c3)
         const int kq = kbase + 2 * (lane & 3);
@@ -908,7 +909,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
         // P <= 1: with an FP8 cache the PV product runs in fp16 (V widens to
         // fp16 in one conversion), otherwise in the plan's 16-bit type
         uint32_t pa[4];
-        if (P.d_fp8) {
+        if constexpr (F8) {
           pa[0] = Pack<__half>::two(s0[0], s0[1]);
           pa[1] = Pack<__half>::two(s0[2], s0[3]);
           pa[2] = Pack<__half>::two(s1[0], s1[1]);
@@ -926,7 +927,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
           vm0 = (kq < kv_len ? 0x0000ffffu : 0u) | (kq + 1 < kv_len ? 0xffff0000u : 0u);
           vm1 = (kq + 8 < kv_len ? 0x0000ffffu : 0u) | (kq + 9 < kv_len ? 0xffff0000u : 0u);
         }
-        if (P.d_fp8) {
+        if constexpr (F8) {
           // transposed byte-pair tiles: a register holds V[2t][2g], V[2t][2g+1],
           // V[2t+1][2g], V[2t+1][2g+1] (keys 2t, 2t+1; d pair g); the even-d
           // and odd-d bytes make two n8 tiles: o[2q] holds d 16q + 4t + {0, 2},
@@ -948,16 +949,17 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
               mma16816<false>(o[2 * q + 1], pa, bo0 & vm0, bo1 & vm1);
             }
           }
-        }
+        } else {
 #pragma unroll
-        for (int j = 0; j < (P.d_fp8 ? 0 : D / 16); ++j) {
-          uint32_t b[4];
-          const int key = ks * 16 + (lane & 7) + ((mi & 1) << 3);
-          const int c = 2 * j + (mi >> 1);
-          ldsm_x4_t(sv + key_row(key) + (c >> 3) * half_stride + (((c & 7) ^ (lane & 7)) << 4), b[0],
-                    b[1], b[2], b[3]);
-          mma16816<BF16>(o[2 * j], pa, b[0] & vm0, b[1] & vm1);
-          mma16816<BF16>(o[2 * j + 1], pa, b[2] & vm0, b[3] & vm1);
+          for (int j = 0; j < D / 16; ++j) {
+            uint32_t b[4];
+            const int key = ks * 16 + (lane & 7) + ((mi & 1) << 3);
+            const int c = 2 * j + (mi >> 1);
+            ldsm_x4_t(sv + key_row(key) + (c >> 3) * half_stride + (((c & 7) ^ (lane & 7)) << 4), b[0],
+                      b[1], b[2], b[3]);
+            mma16816<BF16>(o[2 * j], pa, b[0] & vm0, b[1] & vm1);
+            mma16816<BF16>(o[2 * j + 1], pa, b[2] & vm0, b[3] & vm1);
+          }
         }
       }
       if (!__syncthreads_and(got)) { ok = false; break; }
@@ -982,7 +984,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
     if (active) {
       float* wo = scr_o + warp * 16 * D;
       const int rl = lane >> 2;
-      if (P.d_fp8) {  // d 16q + 4t .. +3 from the even / odd tiles of chunk q
+      if constexpr (F8) {  // d 16q + 4t .. +3 from the even / odd tiles of chunk q
 #pragma unroll
         for (int q = 0; q < D / 16; ++q) {
           const int col = 16 * q + 4 * (lane & 3);
@@ -1064,7 +1066,8 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
 }
 
 // ============================================================ kernels
-template <typename T, int D>
+// F8: the decode half reads an FP8 (E4M3) cache (head_dim 128 only)
+template <typename T, int D, bool F8>
 __global__ void __launch_bounds__(kThreads, POD_CTAS_PER_SM) pod_kernel(const __grid_constant__ PodParams P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   // the merge kernel may start its prologue now; it waits for this grid's completion
@@ -1096,7 +1099,7 @@ __global__ void __launch_bounds__(kThreads, POD_CTAS_PER_SM) pod_kernel(const __
       // shared memory changes hands between the generic and the async proxy
       fence_proxy_async();
       __syncthreads();
-      ok = do_prefill ? prefill_role<T, D>(P, smem, tmem) : decode_role<T, D>(P, smem);
+      ok = do_prefill ? prefill_role<T, D>(P, smem, tmem) : decode_role<T, D, F8>(P, smem);
     }
     tc_fence_before();
     __syncthreads();
@@ -1162,23 +1165,32 @@ __global__ void __launch_bounds__(256) pod_merge_kernel(const __grid_constant__ 
   if (lane == 0 && lse) lse[orow] = wsum > 0.f ? M + log2f(wsum) : -INFINITY;
 }
 
-template <typename T, int D>
-cudaError_t launch_impl(const PodParams& P, cudaStream_t stream) {
+template <typename T, int D, bool F8>
+cudaError_t launch_pod(const PodParams& P, cudaStream_t stream) {
   constexpr int SMEM = smem_bytes<D>();
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(pod_kernel<T, D>,
+    cudaError_t e = cudaFuncSetAttribute(pod_kernel<T, D, F8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     // two CTAs per SM need the largest shared-memory carveout
-    e = cudaFuncSetAttribute(pod_kernel<T, D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(pod_kernel<T, D, F8>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
+  pod_kernel<T, D, F8><<<P.grid, kThreads, SMEM, stream>>>(P);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_impl(const PodParams& P, cudaStream_t stream) {
   if (P.grid > 0) {
-    pod_kernel<T, D><<<P.grid, kThreads, SMEM, stream>>>(P);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    if constexpr (D == 128)
+      e = P.d_fp8 ? launch_pod<T, D, true>(P, stream) : launch_pod<T, D, false>(P, stream);
+    else
+      e = launch_pod<T, D, false>(P, stream);
     if (e != cudaSuccess) return e;
   }
   if (P.n_mrows > 0) {
