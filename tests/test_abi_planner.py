@@ -242,3 +242,26 @@ def test_decode_fp8_switch_host_checks(lib):
     with pytest.raises(pod.PodError) as e:
         pod.pod_plan_set_decode_fp8(h64, 1.0, 1.0)
     assert e.value.code == 2
+
+
+def test_split_starts_long_prefill_tiles_at_once(lib):
+    """The CTA split is chosen on a simulation of the two work queues: with
+    128 prefill tiles of 8192 keys next to a long decode stream (c4), every
+    long tile gets a CTA that starts on it, instead of queueing behind the
+    few CTAs a CTA-time balance would give prefill."""
+    inp = make_config("c4", with_data=False)
+    h = plan_host(inp)
+    s = pod.plan_summary(h)
+    assert s["n_tiles"] == 128 and s["n_p_ctas"] >= 128, s
+    assert s["grid"] <= 2 * s["num_sms"] and s["n_d_ctas"] > 0
+
+
+def test_split_keeps_balanced_start_when_no_tile_dominates(lib):
+    """c5: no prefill tile is long next to the decode stream, so the split
+    stays near the CTA-time balance (a third to a half of the grid starts on
+    prefill) and every CTA has work (grid = 2 x SMs)."""
+    inp = make_config("c5", with_data=False)
+    h = plan_host(inp)
+    s = pod.plan_summary(h)
+    assert s["grid"] == 2 * s["num_sms"], s
+    assert 0.25 * s["grid"] <= s["n_p_ctas"] <= 0.5 * s["grid"], s
