@@ -337,28 +337,6 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
 
   const CostModel cm = cost_model(a.d);
 
-  // ---- prefill tiles --------------------------------------------------------
-  const int Tq = std::max(1, POD_TILE_ROWS / G);
-  P.ptiles.clear();
-  std::vector<double> tile_cost;
-  double p_flops = 0.0;
-  for (int r = 0; r < P.p.batch; ++r) {
-    int ql = P.p.q_len[r], kl = P.p.kv_len[r];
-    for (int t0 = 0; t0 < ql; t0 += Tq) {
-      int nt = std::min(Tq, ql - t0);
-      int lo, hi;
-      key_range(kl, ql, t0, nt, P.causal, P.window_left, &lo, &hi);
-      for (int g = 0; g < P.Hk; ++g) {
-        int32_t rec[POD_REC] = {r, g, t0, nt, lo, hi, -1, 0};
-        P.ptiles.insert(P.ptiles.end(), rec, rec + POD_REC);
-        tile_cost.push_back((double)nblocks(lo, hi));
-        p_flops += 4.0 * a.d * (double)nt * G * (double)(hi - lo);
-      }
-    }
-  }
-  const int n_tiles = (int)tile_cost.size();
-  P.tq = Tq;
-
   // ---- decode units ---------------------------------------------------------
   const int Tu = std::max(1, POD_DECODE_ROWS / G);
   P.tu = Tu;
@@ -380,6 +358,76 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
       }
     }
   }
+
+  // ---- prefill tiles --------------------------------------------------------
+  // A tile's key range is split into chunks (merged like decode splits) when
+  // the prefill half is small enough to share SMs with split CTAs: at most
+  // 1536 query rows, the batch plan's cutoff for colocated prefill CTAs
+  // (POD walkthrough, "Batch 版本 plan 的 colocated-CTA 调度细节"), too few
+  // tiles to give every CTA of the grid one, and a longest tile that would
+  // outlast the balanced makespan of both halves. Next to a long decode
+  // stream (c4) the tiles already finish early; a split there only adds the
+  // merge.
+  const int Tq = std::max(1, POD_TILE_ROWS / G);
+  const int grid_cap = a.num_sms * POD_CTAS_PER_SM;
+  struct TileUnit { int r, g, t0, nt, lo, hi; };
+  std::vector<TileUnit> tunits;
+  for (int r = 0; r < P.p.batch; ++r) {
+    int ql = P.p.q_len[r], kl = P.p.kv_len[r];
+    for (int t0 = 0; t0 < ql; t0 += Tq) {
+      int nt = std::min(Tq, ql - t0);
+      int lo, hi;
+      key_range(kl, ql, t0, nt, P.causal, P.window_left, &lo, &hi);
+      for (int g = 0; g < P.Hk; ++g) tunits.push_back({r, g, t0, nt, lo, hi});
+    }
+  }
+  int p_split = 1;
+  if (P.p.rows <= 1536 && !tunits.empty() && 2 * (int)tunits.size() <= grid_cap) {
+    double longest = 0.0, total = 0.0;
+    for (const TileUnit& u : tunits) {
+      const double t = cm.p_tile_ns + (double)nblocks(u.lo, u.hi) * cm.p_block_ns[2];
+      longest = std::max(longest, t);
+      total += t;
+    }
+    for (const DecodeUnit& u : units)
+      total += cm.d_item_ns + item_work(u.hi - u.lo, a.d, u.ntok * G) / cm.d_bytes_per_ns[2];
+    if (longest > total / grid_cap)
+      p_split = (grid_cap + (int)tunits.size() - 1) / (int)tunits.size();
+  }
+  P.ptiles.clear();
+  std::vector<int32_t> pgroups;
+  std::vector<int32_t> pgroup_rows;
+  std::vector<double> tile_cost;
+  double p_flops = 0.0;
+  int p_prows = 0;
+  {
+    std::vector<std::pair<int, int>> parts;
+    for (const TileUnit& u : tunits) {
+      const int len = u.hi - u.lo;
+      // chunks of at least 8 key blocks, 64-key aligned inside the range
+      const int n = std::max(1, std::min(p_split, len / (8 * POD_KBLOCK)));
+      const int chunk = n > 1 ? ((len + n - 1) / n + POD_KBLOCK - 1) / POD_KBLOCK * POD_KBLOCK : 0;
+      split_range(u.lo, u.hi, chunk, parts);
+      const int R = u.nt * G;
+      int prow0 = -1;
+      if (parts.size() > 1) {
+        prow0 = p_prows;
+        p_prows += (int)parts.size() * R;
+        int32_t grp[POD_REC] = {0, u.r, u.g, u.t0, u.nt, prow0, (int)parts.size(), R};
+        pgroups.insert(pgroups.end(), grp, grp + POD_REC);
+        pgroup_rows.push_back(R);
+      }
+      for (size_t j = 0; j < parts.size(); ++j) {
+        const int prow = prow0 < 0 ? -1 : prow0 + (int)j * R;
+        int32_t rec[POD_REC] = {u.r, u.g, u.t0, u.nt, parts[j].first, parts[j].second, prow, 0};
+        P.ptiles.insert(P.ptiles.end(), rec, rec + POD_REC);
+        tile_cost.push_back((double)nblocks(parts[j].first, parts[j].second));
+      }
+      p_flops += 4.0 * a.d * (double)u.nt * G * (double)len;
+    }
+  }
+  const int n_tiles = (int)tile_cost.size();
+  P.tq = Tq;
 
   // ---- CTA split between the halves ----------------------------------------
   const int S = a.num_sms;
@@ -469,10 +517,11 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
 
   // ---- decode items, partial rows, merge groups -------------------------------
   P.ditems.clear();
-  P.mgroups.clear();
+  P.mgroups = pgroups;      // prefill merge groups first, then decode ones
   P.mrow_ptr.assign(1, 0);
+  for (int R : pgroup_rows) P.mrow_ptr.push_back(P.mrow_ptr.back() + R);
   std::vector<double> item_cost;
-  int n_prows = 0;
+  int n_prows = p_prows;
   std::vector<std::pair<int, int>> parts;
   for (const DecodeUnit& u : units) {
     split_range(u.lo, u.hi, chunk, parts);

@@ -2,6 +2,7 @@
 its host planner matches the plain restatement in oracle/planner_ref.py bit for
 bit. No GPU is needed: plans are made host-only (workspace NULL, num_sms given).
 """
+import copy
 import ctypes
 import os
 import re
@@ -56,21 +57,42 @@ def check_against_reference(inp, h):
     H, Hk = inp.num_qo_heads, inp.num_kv_heads
     kvl_p = planner_ref.seq_lens(inp.p.kv_indptr, inp.p.last_page_len, inp.page_size)
     kvl_d = planner_ref.seq_lens(inp.d.kv_indptr, inp.d.last_page_len, inp.page_size)
-    # prefill tiles: bit-exact, in order
+    G = H // Hk
+    groups = pod.pod_plan_table(h, 5).reshape(-1, REC)
+    # prefill tiles: in the restated order; per tile, the chunks partition
+    # [lo, hi) in order (one chunk unless the planner split it, then with a
+    # merge group of half 0)
     tiles = pod.pod_plan_table(h, 1).reshape(-1, REC)
     ref = planner_ref.prefill_tiles(inp.p.q_indptr, kvl_p, H, Hk, inp.causal, inp.window_left)
-    assert tiles.shape[0] == len(ref) == s["n_tiles"]
-    if len(ref):
-        assert np.array_equal(tiles[:, :6], np.array(ref, dtype=np.int32))
-        assert np.all(tiles[:, 6] == -1)
-    # decode items: per unit, the chunks partition [lo, hi) in order
-    items = pod.pod_plan_table(h, 2).reshape(-1, REC)
-    units = planner_ref.decode_units(inp.d.q_indptr, kvl_d, H, Hk, inp.causal, inp.window_left)
-    groups = pod.pod_plan_table(h, 5).reshape(-1, REC)
-    G = H // Hk
     i = 0
     gi = 0
     prows = 0
+    for (r, g, t0, nt, lo, hi) in ref:
+        start = i
+        k = lo
+        while i < len(tiles) and tuple(tiles[i, :4]) == (r, g, t0, nt) and tiles[i, 4] == k:
+            assert tiles[i, 5] > tiles[i, 4] or lo == hi
+            k = int(tiles[i, 5])
+            i += 1
+            if k == hi:
+                break
+        assert k == hi and i > start, f"tile {(r, g, t0, nt, lo, hi)} not covered"
+        n = i - start
+        assert all(int(tiles[j, 4]) % 64 == 0 for j in range(start + 1, i))
+        if n == 1:
+            assert tiles[start, 6] == -1
+        else:
+            R = nt * G
+            assert tuple(groups[gi]) == (0, r, g, t0, nt, prows, n, R)
+            for j in range(n):
+                assert tiles[start + j, 6] == prows + j * R
+            prows += n * R
+            gi += 1
+    assert i == len(tiles) == s["n_tiles"]
+    # decode items: per unit, the chunks partition [lo, hi) in order
+    items = pod.pod_plan_table(h, 2).reshape(-1, REC)
+    units = planner_ref.decode_units(inp.d.q_indptr, kvl_d, H, Hk, inp.causal, inp.window_left)
+    i = 0
     for (r, g, t0, nt, lo, hi) in units:
         start = i
         k = lo
@@ -244,16 +266,49 @@ def test_decode_fp8_switch_host_checks(lib):
     assert e.value.code == 2
 
 
-def test_split_starts_long_prefill_tiles_at_once(lib):
-    """The CTA split is chosen on a simulation of the two work queues: with
-    128 prefill tiles of 8192 keys next to a long decode stream (c4), every
-    long tile gets a CTA that starts on it, instead of queueing behind the
-    few CTAs a CTA-time balance would give prefill."""
-    inp = make_config("c4", with_data=False)
-    h = plan_host(inp)
+def _without_decode(inp):
+    sub = copy.copy(inp)
+    empty = copy.copy(inp.d)
+    empty.q_indptr = np.zeros(1, np.int32)
+    empty.kv_indptr = np.zeros(1, np.int32)
+    empty.kv_indices = np.zeros(0, np.int32)
+    empty.last_page_len = np.zeros(0, np.int32)
+    sub.d = empty
+    return sub
+
+
+def test_small_prefill_alone_is_split_and_starts_at_once(lib):
+    """c4's prefill half alone: 512 rows (below the 1536-row colocation
+    cutoff) in 128 tiles of 8192 keys, whose longest tile outlasts the
+    balanced makespan. The planner splits every tile's key range into chunks
+    merged like decode splits (half-0 merge groups), so that the grid has
+    about one prefill job per CTA."""
+    h = plan_host(_without_decode(make_config("c4", with_data=False)))
     s = pod.plan_summary(h)
+    groups = pod.pod_plan_table(h, 5).reshape(-1, REC)
+    pgroups = groups[groups[:, 0] == 0]
+    assert len(pgroups) == 128 and np.all(pgroups[:, 6] >= 2), s
+    assert s["n_tiles"] == int(pgroups[:, 6].sum()) and s["n_p_ctas"] >= s["num_sms"], s
+
+
+def test_small_prefill_next_to_long_decode_is_not_split(lib):
+    """c4 fused: the decode stream (about 9 GB) sets the makespan and the
+    unsplit 8192-key tiles finish well inside it, so a split would only add
+    the merge. Every long tile still gets a CTA that starts on it."""
+    h = plan_host(make_config("c4", with_data=False))
+    s = pod.plan_summary(h)
+    groups = pod.pod_plan_table(h, 5).reshape(-1, REC)
+    assert not np.any(groups[:, 0] == 0) if len(groups) else True
     assert s["n_tiles"] == 128 and s["n_p_ctas"] >= 128, s
     assert s["grid"] <= 2 * s["num_sms"] and s["n_d_ctas"] > 0
+
+
+def test_large_prefill_is_not_split(lib):
+    """c3 and c5 have more than 1536 prefill rows: no prefill merge group."""
+    for name in ("c3", "c5"):
+        h = plan_host(make_config(name, with_data=False))
+        groups = pod.pod_plan_table(h, 5).reshape(-1, REC)
+        assert not np.any(groups[:, 0] == 0) if len(groups) else True
 
 
 def test_split_keeps_balanced_start_when_no_tile_dominates(lib):

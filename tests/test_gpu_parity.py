@@ -312,3 +312,28 @@ def test_fp8_decode_c5_full_size_sampled():
     st, sh = sample_rows(inp.d, inp.num_qo_heads, 96, seed=4)
     compare_half(inp, "d", od, ld, st, sh, tag="fp8 c5 ")
     assert np.isfinite(od).all() and np.isfinite(ld).all()
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_key_split_and_merge(causal):
+    """A small prefill half (few tiles, long keys) is split along the keys
+    and merged (half-0 merge groups), next to a decode half."""
+    inp = make_custom("psplit", torch.bfloat16, 16, 2, 128, 16, causal, -1, [200, 37], [3000, 1200],
+                      [1, 2], [500, 900], seed=13, sinks=True)
+    (op, lp, od, ld), h, ws = run_pod(inp)
+    groups = pod.pod_plan_table(h, 5).reshape(-1, 8)
+    assert np.any(groups[:, 0] == 0), "expected a prefill key split"
+    compare_half(inp, "p", op, lp, tag="psplit ")
+    compare_half(inp, "d", od, ld, tag="psplit ")
+
+
+def test_prefill_alone_split_at_c4_shape():
+    """c4's prefill half alone (32/8/128/16, 512 rows against 8192 keys):
+    every one of its 128 tiles is split along the keys and merged."""
+    inp = make_custom("p4", torch.bfloat16, 32, 8, 128, 16, True, -1, [512], [8192], [], [], seed=14)
+    (op, lp, od, ld), h, ws = run_pod(inp)
+    groups = pod.pod_plan_table(h, 5).reshape(-1, 8)
+    assert int((groups[:, 0] == 0).sum()) == 128
+    st, sh = sample_rows(inp.p, inp.num_qo_heads, 64, seed=5)
+    compare_half(inp, "p", op, lp, st, sh, tag="p4 ")
+    assert np.isfinite(op).all() and np.isfinite(lp).all()
