@@ -77,6 +77,13 @@ def lib():
             _lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
             _lib.oracle_e4m3_to_f64.restype = ctypes.c_double
             _lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            _lib.oracle_attention_rows_masked.restype = ctypes.c_int
+            _lib.oracle_attention_rows_masked.argtypes = [
+                P, P, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double,
+                P, P, P, P, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                P, P, ctypes.c_int64, P, P, P, P, P, P, ctypes.c_int]
             _lib.oracle_attention_rows_kv.restype = ctypes.c_int
             _lib.oracle_attention_rows_kv.argtypes = [
                 P, P, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double,
@@ -128,9 +135,11 @@ def attention_rows(q, kv, q_indptr, kv_indptr, kv_indices, last_page_len,
                    causal, window_left, sm_scale, sinks=None,
                    sel_token=None, sel_head=None, key_lo=None, key_hi=None,
                    nthreads: Optional[int] = None, dtype: Optional[int] = None,
-                   k_scale: float = 1.0, v_scale: float = 1.0):
+                   k_scale: float = 1.0, v_scale: float = 1.0, packed_mask=None):
     """fp64 outputs for selected (token, head) pairs; all pairs if no selection.
     An E4M3 ``kv`` is read as codes times ``k_scale`` (K) / ``v_scale`` (V).
+    ``packed_mask`` (uint8, little bit order) is a custom mask over every
+    request's [q_len, kv_len] matrix; it replaces the causal rule.
 
     Returns (out [n, d] float64, lse [n] float64, status int).
     """
@@ -165,12 +174,21 @@ def attention_rows(q, kv, q_indptr, kv_indptr, kv_indices, last_page_len,
     num_pages = int(kvc.shape[0]) if kvc.ndim >= 1 else 0
     if nthreads is None:
         nthreads = os.cpu_count() or 1
-    st = lib().oracle_attention_rows_kv(
+    pm = None
+    if packed_mask is not None:
+        pm = np.ascontiguousarray(np.asarray(packed_mask.cpu() if hasattr(packed_mask, "cpu")
+                                             else packed_mask, dtype=np.uint8))
+        npg = np.diff(kv_indptr).astype(np.int64)
+        kvl = np.where(npg > 0, (npg - 1) * int(page_size) + last_page_len, 0)
+        need = int(np.sum(np.diff(q_indptr).astype(np.int64) * kvl))
+        if pm.size * 8 < need:
+            raise ValueError(f"packed_mask holds {pm.size * 8} bits, the requests need {need}")
+    st = lib().oracle_attention_rows_masked(
         _ptr(qc), _ptr(kvc), int(dtype), int(kv_fp8), float(k_scale), float(v_scale),
         _ptr(q_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(last_page_len),
         batch, num_pages, H, int(num_kv_heads), d, int(page_size),
         int(bool(causal)), int(window_left), float(sm_scale),
-        _ptr(sk), n, _ptr(tok), _ptr(hd), _ptr(key_lo), _ptr(key_hi),
+        _ptr(sk), _ptr(pm), n, _ptr(tok), _ptr(hd), _ptr(key_lo), _ptr(key_hi),
         _ptr(out), _ptr(lse), int(nthreads))
     return out[:n], lse[:n], int(st)
 
@@ -181,6 +199,8 @@ def attention_half(inp, half: str, sel_token=None, sel_head=None, nthreads=None,
     scales = {}
     if is_fp8(h.kv):
         scales = dict(k_scale=getattr(inp, "k_scale", 1.0), v_scale=getattr(inp, "v_scale", 1.0))
+    if getattr(h, "packed_mask", None) is not None and "packed_mask" not in kw:
+        scales["packed_mask"] = h.packed_mask
     return attention_rows(h.q, h.kv, h.q_indptr, h.kv_indptr, h.kv_indices, h.last_page_len,
                           inp.num_qo_heads, inp.num_kv_heads, inp.head_dim, inp.page_size,
                           inp.causal, inp.window_left, inp.sm_scale, sinks=inp.sinks,

@@ -30,6 +30,13 @@
  *    (flashinfer.cudnn page, "LSE 契约").
  *  - Merge of split partials (o_i, lse_i): weights 2^(lse_i - max), the
  *    property that lets base-2 LSE feed a cascade merge (same section).
+ *  - Custom mask (POD walkthrough, run parameters custom_mask_p /
+ *    packed_custom_mask_p, packed with little bit order): one boolean per
+ *    (query row, key) of each request, the requests' [q_len, kv_len]
+ *    row-major matrices laid end to end, eight to a byte, the first element
+ *    in the least significant bit. Readings taken here: a set bit allows the
+ *    key; the mask replaces the causal rule (window_left still applies);
+ *    a row the mask leaves without keys has out = 0 and lse = -inf.
  *
  * Inputs are the same rounded fp16/bf16 values the GPU reads, widened to
  * double by decoders written from the IEEE-754 binary16 and bfloat16 bit
@@ -43,7 +50,9 @@
  * on tiny inputs, page-permutation and page-size invariance, split/merge
  * identity, the hand-worked two-token example, closed forms (q = 0,
  * window_left = 0, kv_len = 1, equal keys), GQA head duplication, exhaustive
- * checks of the two 16-bit decoders.
+ * checks of the two 16-bit decoders; for the custom mask, brute force over
+ * the bits numpy unpacks, single-bit masks (out = v_t) and the triangular and
+ * all-ones masks against the causal and non-causal rules.
  */
 #include <math.h>
 #include <stdint.h>
@@ -126,6 +135,12 @@ void oracle_seq_lens(const int32_t* kv_indptr, const int32_t* last_page_len,
         kv_len_out[r] = (int32_t)oracle_kv_len(kv_indptr, last_page_len, r, page_size);
 }
 
+/* Bit `pos` of a little-bit-order packed array. */
+static int mask_bit(const uint8_t* packed, int64_t pos)
+{
+    return (packed[pos >> 3] >> (int)(pos & 7)) & 1;
+}
+
 static int find_request(const int32_t* q_indptr, int batch, int64_t token)
 {
     for (int r = 0; r < batch; ++r)
@@ -140,20 +155,22 @@ static int find_request(const int32_t* q_indptr, int batch, int64_t token)
  *   key_lo/key_hi (may be NULL)           : extra restriction key in [lo, hi)
  *                                           per selection (split-KV partials)
  *   sinks (may be NULL)                   : fp32 [H] extra logit per qo head
+ *   packed_mask (may be NULL)             : custom mask bits (see the header);
+ *                                           when given, causal is not applied
  *   out [n, d], lse [n]                   : fp64 results
  * Returns the first error code met (rows are still filled where possible).
  */
-int oracle_attention_rows_kv(const uint16_t* q, const void* kv, int dtype,
-                             int kv_fp8, double k_scale, double v_scale,
-                             const int32_t* q_indptr, const int32_t* kv_indptr,
-                             const int32_t* kv_indices, const int32_t* last_page_len,
-                             int batch, int num_pages,
-                             int H, int Hk, int d, int page_size,
-                             int causal, int window_left, double sm_scale,
-                             const float* sinks,
-                             int64_t n_sel, const int64_t* sel_token, const int32_t* sel_head,
-                             const int64_t* key_lo, const int64_t* key_hi,
-                             double* out, double* lse, int nthreads)
+int oracle_attention_rows_masked(const uint16_t* q, const void* kv, int dtype,
+                                 int kv_fp8, double k_scale, double v_scale,
+                                 const int32_t* q_indptr, const int32_t* kv_indptr,
+                                 const int32_t* kv_indices, const int32_t* last_page_len,
+                                 int batch, int num_pages,
+                                 int H, int Hk, int d, int page_size,
+                                 int causal, int window_left, double sm_scale,
+                                 const float* sinks, const uint8_t* packed_mask,
+                                 int64_t n_sel, const int64_t* sel_token, const int32_t* sel_head,
+                                 const int64_t* key_lo, const int64_t* key_hi,
+                                 double* out, double* lse, int nthreads)
 {
     if (H <= 0 || Hk <= 0 || H % Hk != 0 || d <= 0 || page_size <= 0) return ORACLE_BAD_ARG;
     int group = H / Hk;
@@ -178,6 +195,14 @@ int oracle_attention_rows_kv(const uint16_t* q, const void* kv, int dtype,
         int64_t kv_len = oracle_kv_len(kv_indptr, last_page_len, r, page_size);
         int64_t p = kv_len - q_len + i;          /* bottom-right diagonal */
         int hk = h / group;                       /* GQA mapping */
+        /* first bit of this request's mask: the earlier requests' q_len * kv_len */
+        int64_t mask_row = 0;
+        if (packed_mask) {
+            for (int rr = 0; rr < r; ++rr)
+                mask_row += ((int64_t)q_indptr[rr + 1] - q_indptr[rr]) *
+                            oracle_kv_len(kv_indptr, last_page_len, rr, page_size);
+            mask_row += i * kv_len;
+        }
 
         double* qv = (double*)malloc(sizeof(double) * (size_t)d);
         double* logit = (double*)malloc(sizeof(double) * (size_t)(kv_len > 0 ? kv_len : 1));
@@ -190,7 +215,11 @@ int oracle_attention_rows_kv(const uint16_t* q, const void* kv, int dtype,
         int64_t n_allowed = 0;
         for (int64_t t = 0; t < kv_len; ++t) {
             int ok = 1;
-            if (causal && t > p) ok = 0;
+            if (packed_mask) {
+                if (!mask_bit(packed_mask, mask_row + t)) ok = 0;
+            } else if (causal && t > p) {
+                ok = 0;
+            }
             if (window_left >= 0 && t < p - window_left) ok = 0;
             if (key_lo && t < key_lo[s]) ok = 0;
             if (key_hi && t >= key_hi[s]) ok = 0;
@@ -212,8 +241,11 @@ int oracle_attention_rows_kv(const uint16_t* q, const void* kv, int dtype,
             ++n_allowed;
         }
         if (n_allowed == 0) {
+            /* out = 0, lse = -inf; only the custom mask may empty a row */
+            if (!packed_mask) {
 #pragma omp atomic write
-            status = ORACLE_EMPTY_ROW;
+                status = ORACLE_EMPTY_ROW;
+            }
             free(qv); free(logit); free(allowed);
             continue;
         }
@@ -235,6 +267,26 @@ int oracle_attention_rows_kv(const uint16_t* q, const void* kv, int dtype,
         free(qv); free(logit); free(allowed);
     }
     return status;
+}
+
+/* oracle_attention_rows_masked without a custom mask. */
+int oracle_attention_rows_kv(const uint16_t* q, const void* kv, int dtype,
+                             int kv_fp8, double k_scale, double v_scale,
+                             const int32_t* q_indptr, const int32_t* kv_indptr,
+                             const int32_t* kv_indices, const int32_t* last_page_len,
+                             int batch, int num_pages,
+                             int H, int Hk, int d, int page_size,
+                             int causal, int window_left, double sm_scale,
+                             const float* sinks,
+                             int64_t n_sel, const int64_t* sel_token, const int32_t* sel_head,
+                             const int64_t* key_lo, const int64_t* key_hi,
+                             double* out, double* lse, int nthreads)
+{
+    return oracle_attention_rows_masked(q, kv, dtype, kv_fp8, k_scale, v_scale, q_indptr,
+                                        kv_indptr, kv_indices, last_page_len, batch, num_pages,
+                                        H, Hk, d, page_size, causal, window_left, sm_scale, sinks,
+                                        NULL, n_sel, sel_token, sel_head, key_lo, key_hi, out, lse,
+                                        nthreads);
 }
 
 /* The 16-bit cache of `dtype`: oracle_attention_rows_kv without FP8. */

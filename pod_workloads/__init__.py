@@ -31,7 +31,7 @@ import numpy as np
 import torch
 
 __all__ = ["HalfInputs", "PODInputs", "make_half", "make_config", "make_custom",
-           "CONFIG_NAMES", "page_table_from_lens"]
+           "CONFIG_NAMES", "page_table_from_lens", "pack_mask", "with_prefill_custom_mask"]
 
 CONFIG_NAMES = ("c1", "c2", "c3", "c4", "c5")
 
@@ -48,6 +48,9 @@ class HalfInputs:
     kv: torch.Tensor              # [num_pages, 2, ps, Hk, d] fp16/bf16, CPU
     q_lens: np.ndarray = field(default=None)   # int32 [B]
     kv_lens: np.ndarray = field(default=None)  # int32 [B]
+    # custom mask (prefill half): uint8, the requests' [q_len, kv_len] boolean
+    # matrices laid end to end, packed eight to a byte, little bit order
+    packed_mask: Optional[np.ndarray] = None
 
     @property
     def batch(self) -> int:
@@ -212,4 +215,37 @@ def with_fp8_decode_cache(inp: PODInputs, k_scale: float = 0.02, v_scale: float 
     out.d = d
     out.k_scale = float(k_scale)
     out.v_scale = float(v_scale)
+    return out
+
+
+def pack_mask(mats: Sequence[np.ndarray]) -> np.ndarray:
+    """Boolean [q_len, kv_len] matrices, one per request, laid end to end in
+    row-major order and packed eight to a byte with the first element in the
+    least significant bit (numpy's little bit order)."""
+    flat = [np.asarray(m, dtype=bool).reshape(-1) for m in mats]
+    bits = np.concatenate(flat) if flat else np.zeros(0, dtype=bool)
+    return np.packbits(bits, bitorder="little")
+
+
+def with_prefill_custom_mask(inp: PODInputs, seed: int = 0, density: float = 0.5,
+                             empty_rows: int = 1, full_rows: int = 1) -> PODInputs:
+    """The same inputs with a random custom mask on the prefill half: each
+    (query row, key) allowed with probability ``density``; in every request
+    with enough rows, the first ``empty_rows`` rows allow no key and the next
+    ``full_rows`` rows allow every key. Returns a new PODInputs."""
+    import copy
+    gen = torch.Generator().manual_seed(int(seed))
+    mats = []
+    for r in range(inp.p.batch):
+        ql = int(inp.p.q_indptr[r + 1] - inp.p.q_indptr[r])
+        kl = int(inp.p.kv_lens[r])
+        m = (torch.rand((ql, kl), generator=gen) < density).numpy()
+        if ql > empty_rows + full_rows:
+            m[:empty_rows] = False
+            m[empty_rows:empty_rows + full_rows] = True
+        mats.append(m)
+    out = copy.copy(inp)
+    p = copy.copy(inp.p)
+    p.packed_mask = pack_mask(mats)
+    out.p = p
     return out

@@ -23,7 +23,8 @@ import torch
 from scipy.special import logsumexp, softmax
 
 import oracle
-from pod_workloads import HalfInputs, make_custom, page_table_from_lens
+from pod_workloads import (HalfInputs, make_custom, pack_mask, page_table_from_lens,
+                           with_prefill_custom_mask)
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 GOLDEN = os.path.join(HERE, "golden")
@@ -65,21 +66,34 @@ def brute_force(inp, half="d"):
         t = np.arange(kvl)[None, :]
         p = kvl - ql + i
         mask = np.ones((ql, kvl), dtype=bool)
-        if inp.causal:
+        if h.packed_mask is not None:
+            # custom mask: this request's bits of the little-bit-order array,
+            # unpacked by numpy; it takes the place of the causal rule
+            bits = np.unpackbits(h.packed_mask, bitorder="little").astype(bool)
+            off = int(sum(int(h.q_indptr[j + 1] - h.q_indptr[j]) * int(h.kv_lens[j])
+                          for j in range(r)))
+            mask &= bits[off:off + ql * kvl].reshape(ql, kvl)
+        elif inp.causal:
             mask &= t <= p
         if inp.window_left >= 0:
             mask &= t >= p - inp.window_left
+        live = mask.any(axis=1)          # rows a custom mask left with keys
         for hh in range(H):
             S = inp.sm_scale * (q[q0:q1, hh, :] @ K[:, hh // G, :].T)
-            S = np.where(mask, S, -np.inf)
-            lse[q0:q1, hh] = logsumexp(S, axis=1) / math.log(2.0)
+            S = np.where(mask, S, -np.inf)[live]
+            lse[q0:q1, hh] = -np.inf
+            out[q0:q1, hh] = 0.0
+            if not live.any():
+                continue
+            rows_idx = np.arange(q0, q1)[live]
+            lse[rows_idx, hh] = logsumexp(S, axis=1) / math.log(2.0)
             if inp.sinks is not None:
-                sink_col = np.full((ql, 1), float(inp.sinks[hh]))
+                sink_col = np.full((S.shape[0], 1), float(inp.sinks[hh]))
                 Vz = np.concatenate([V[:, hh // G, :], np.zeros((1, d))], axis=0)
                 P = softmax(np.concatenate([S, sink_col], axis=1), axis=1)
-                out[q0:q1, hh] = P @ Vz
+                out[rows_idx, hh] = P @ Vz
             else:
-                out[q0:q1, hh] = softmax(S, axis=1) @ V[:, hh // G, :]
+                out[rows_idx, hh] = softmax(S, axis=1) @ V[:, hh // G, :]
     return out, lse
 
 
@@ -295,8 +309,75 @@ def pin_fp8(fn, seeds=range(6)):
         assert np.allclose(lse, ref_lse, atol=1e-12, rtol=0), seed
 
 
+def _masked_tiny(seed, **kw):
+    inp = tiny_case(seed, **kw)
+    # the prefill half of the tiny cases is empty: move the requests there
+    inp.p, inp.d = inp.d, inp.p
+    return with_prefill_custom_mask(inp, seed=seed, density=0.6)
+
+
+def pin_custom_mask(fn, seeds=range(8)):
+    """Custom prefill mask (POD walkthrough, run parameters custom_mask_p /
+    packed_custom_mask_p, little bit order):
+    - random masks with empty and full rows against brute force over the
+      mask numpy unpacks;
+    - a mask with one set bit picks exactly that key: out = v_t and
+      lse = s_t / ln 2, which fixes the bit order and the row stride;
+    - the bottom-right lower-triangular mask reproduces the causal result and
+      the all-ones mask the non-causal one, bit for bit."""
+    for seed in seeds:
+        inp = _masked_tiny(seed)
+        ref_out, ref_lse = brute_force(inp, "p")
+        out, lse = run_oracle(inp, "p", fn=fn, packed_mask=inp.p.packed_mask)
+        assert np.allclose(out, ref_out, atol=1e-12, rtol=1e-12), seed
+        fin = np.isfinite(ref_lse)
+        assert np.array_equal(fin, np.isfinite(lse)), seed
+        assert np.allclose(lse[fin], ref_lse[fin], atol=1e-12, rtol=0), seed
+    # one set bit per request, at a chosen (row, key)
+    inp = _masked_tiny(3, causal=False, window=-1, sinks=False)
+    h = inp.p
+    mats, picks = [], []
+    for r in range(h.batch):
+        ql = int(h.q_indptr[r + 1] - h.q_indptr[r])
+        kl = int(h.kv_lens[r])
+        m = np.zeros((ql, kl), dtype=bool)
+        i, t = ql - 1, (7 * r + 5) % kl
+        m[i, t] = True
+        mats.append(m)
+        picks.append((r, i, t))
+    h.packed_mask = pack_mask(mats)
+    out, lse = run_oracle(inp, "p", fn=fn, packed_mask=h.packed_mask)
+    G = inp.num_qo_heads // inp.num_kv_heads
+    qf = h.q.double().numpy()
+    for r, i, t in picks:
+        K, V = dense_kv(h, r, inp.page_size)
+        row = int(h.q_indptr[r]) + i
+        for hh in range(inp.num_qo_heads):
+            assert np.array_equal(out[row, hh], V[t, hh // G]), (r, hh)
+            s_t = inp.sm_scale * float(qf[row, hh] @ K[t, hh // G])
+            assert abs(lse[row, hh] - s_t / math.log(2.0)) < 1e-12, (r, hh)
+    # triangular and all-ones masks against the mask-free rules
+    for seed in (1, 2, 5):
+        inp = _masked_tiny(seed, window=-1)
+        h = inp.p
+        tri, ones = [], []
+        for r in range(h.batch):
+            ql = int(h.q_indptr[r + 1] - h.q_indptr[r])
+            kl = int(h.kv_lens[r])
+            i = np.arange(ql)[:, None]
+            t = np.arange(kl)[None, :]
+            tri.append(t <= kl - ql + i)
+            ones.append(np.ones((ql, kl), dtype=bool))
+        for mats, causal in ((tri, True), (ones, False)):
+            inp.causal = causal
+            o_ref, l_ref = run_oracle(inp, "p", fn=fn)
+            inp.causal = not causal
+            o_m, l_m = run_oracle(inp, "p", fn=fn, packed_mask=pack_mask(mats))
+            assert np.array_equal(o_m, o_ref) and np.array_equal(l_m, l_ref), seed
+
+
 ALL_PINS = (pin_two_token, pin_brute_force, pin_closed_forms, pin_gqa, pin_page_invariance,
-            pin_split_merge, pin_fp8)
+            pin_split_merge, pin_fp8, pin_custom_mask)
 
 
 # --------------------------------------------------------------------------
@@ -374,7 +455,7 @@ def test_prefill_half_matches_brute_force():
 # --------------------------------------------------------------------------
 
 MUTANTS = {
-    "causal_off_by_one": ("if (causal && t > p) ok = 0;", "if (causal && t >= p) ok = 0;"),
+    "causal_off_by_one": ("} else if (causal && t > p) {", "} else if (causal && t >= p) {"),
     "window_excludes_diagonal_bound": ("t < p - window_left) ok = 0;", "t <= p - window_left) ok = 0;"),
     "gqa_modulo": ("int hk = h / group;", "int hk = h % Hk;"),
     "top_left_causal": ("int64_t p = kv_len - q_len + i;", "int64_t p = i;"),
@@ -392,6 +473,11 @@ MUTANTS = {
     "e4m3_subnormal": ("v = ldexp((double)f, -9);", "v = ldexp((double)f, -10);"),
     "fp8_v_with_k_scale": ("kv_elem(kv, v0 + e, dtype, kv_fp8, v_scale)",
                            "kv_elem(kv, v0 + e, dtype, kv_fp8, k_scale)"),
+    "mask_big_endian_bits": ("(packed[pos >> 3] >> (int)(pos & 7)) & 1",
+                             "(packed[pos >> 3] >> (int)(7 - (pos & 7))) & 1"),
+    "mask_no_request_offset": ("for (int rr = 0; rr < r; ++rr)", "for (int rr = 0; rr < 0; ++rr)"),
+    "mask_row_stride_q_len": ("mask_row += i * kv_len;", "mask_row += i * q_len;"),
+    "mask_and_causal": ("} else if (causal && t > p) {", "} if (causal && t > p) {"),
 }
 
 
@@ -412,6 +498,8 @@ def _mutant_fns(tmpdir, name, old, new):
         L.oracle_attention_rows.argtypes = saved.oracle_attention_rows.argtypes
         L.oracle_attention_rows_kv.restype = ctypes.c_int
         L.oracle_attention_rows_kv.argtypes = saved.oracle_attention_rows_kv.argtypes
+        L.oracle_attention_rows_masked.restype = ctypes.c_int
+        L.oracle_attention_rows_masked.argtypes = saved.oracle_attention_rows_masked.argtypes
         L.oracle_merge.argtypes = saved.oracle_merge.argtypes
         L.oracle_merge.restype = None
         try:
@@ -524,3 +612,38 @@ def test_fp8_scale_folding():
     o3, l3, _ = oracle.attention_rows(*args, inp.sm_scale, sinks=inp.sinks, k_scale=2.5,
                                       v_scale=0.25, nthreads=2)
     assert np.allclose(o3, 0.25 * o1, atol=1e-12, rtol=1e-12) and np.array_equal(l3, l1)
+
+
+# --------------------------------------------------------------------------
+# custom prefill mask
+# --------------------------------------------------------------------------
+
+def test_custom_mask_pins():
+    pin_custom_mask(oracle.attention_rows)
+
+
+def test_pack_mask_bit_order():
+    """pack_mask puts element k of the flattened masks at bit k % 8 of byte
+    k // 8 (little bit order), the layout the pages name."""
+    m = np.zeros((3, 5), dtype=bool)
+    m[0, 0] = m[1, 2] = m[2, 4] = True     # flat positions 0, 7, 14
+    b = pack_mask([m])
+    assert b.tolist() == [0b10000001, 0b01000000]
+
+
+def test_custom_mask_with_window_and_sinks():
+    """An all-ones mask with a window equals the non-causal windowed result;
+    sinks leave a row the mask empties at out = 0 (its only weight is on the
+    sink's zero value row) and lse = -inf."""
+    inp = _masked_tiny(4, window=2, sinks=True)
+    h = inp.p
+    ones = [np.ones((int(h.q_indptr[r + 1] - h.q_indptr[r]), int(h.kv_lens[r])), dtype=bool)
+            for r in range(h.batch)]
+    inp.causal = False
+    o_ref, l_ref = run_oracle(inp, "p")
+    inp.causal = True
+    o_m, l_m = run_oracle(inp, "p", packed_mask=pack_mask(ones))
+    assert np.array_equal(o_m, o_ref) and np.array_equal(l_m, l_ref)
+    zeros = [np.zeros_like(m) for m in ones]
+    o_z, l_z = run_oracle(inp, "p", packed_mask=pack_mask(zeros))
+    assert np.all(o_z == 0.0) and np.all(l_z == -np.inf)
