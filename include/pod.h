@@ -130,7 +130,8 @@ pod_status pod_bind_workspace(pod_handle h, void* workspace, size_t workspace_by
  * plan was bound to; it is read and written (plan metadata, split partials,
  * device status word); calls that share a workspace must not overlap.
  * Errors: POD_ERR_INVALID_ARG (NULL tensor for a non-empty half, sinks
- * mismatch, unbound handle), POD_ERR_CUDA (launch failure).
+ * mismatch, unbound handle, a custom prefill mask that is not device
+ * memory), POD_ERR_CUDA (launch failure).
  */
 pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p,
                    const void* q_d, const void* kv_d, const float* sinks,
@@ -152,6 +153,32 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p,
  * handle or scales that are not finite and positive.
  */
 pod_status pod_plan_set_decode_fp8(pod_handle h, float k_scale, float v_scale);
+
+/*
+ * pod_plan_set_prefill_mask — a custom mask on the prefill half (POD
+ * walkthrough, "run 参数详解", prefill parameters: custom_mask_p /
+ * packed_custom_mask_p, packed with little bit order; a custom mask takes
+ * precedence over causal).
+ *
+ * packed_mask: DEVICE pointer, caller-owned, read by every later pod_run
+ *   until replaced; it must stay valid while those runs execute. It holds
+ *   one bit per (query row, key) of every prefill request: request r's
+ *   [q_len_r, kv_len_r] matrix in row-major order, the requests end to end,
+ *   eight bits to a byte with the first in the least significant bit. A set
+ *   bit allows the key. mask_bytes is its size; it must cover
+ *   ceil(sum_r q_len_r * kv_len_r / 8) bytes, and no byte past mask_bytes is
+ *   read. NULL removes the mask (mask_bytes ignored).
+ * Semantics: on the prefill half the mask replaces the causal rule;
+ *   window_left still applies; the decode half is unchanged. A row the mask
+ *   leaves without keys gets out = 0 and lse = -inf.
+ * Switching the mask on or off plans the handle again from its own copies of
+ *   the page tables (prefill tiles then span every key the window allows):
+ *   any bound workspace is released, so call pod_workspace_size and
+ *   pod_bind_workspace again before the next pod_run. Replacing one mask
+ *   pointer by another keeps the plan and its workspace.
+ * Errors: POD_ERR_INVALID_ARG (NULL handle, mask_bytes too small).
+ */
+pod_status pod_plan_set_prefill_mask(pod_handle h, const void* packed_mask, int64_t mask_bytes);
 
 /* Release the handle (host memory only). NULL is accepted. */
 pod_status pod_destroy(pod_handle h);
@@ -175,7 +202,9 @@ pod_status pod_read_device_status(pod_handle h, void* workspace, void* stream,
  * offsets, 4 = CTA work list, 5 = merge groups, 6 = p kv_len, 7 = d kv_len,
  * 8 = prefill tile queue, 9 = decode item queue, 10 = decode queue records
  * (16 ints per queue position: the item record, then kv_len, first query row,
- * q_len, first page-table entry, page count of its request).
+ * q_len, first page-table entry, page count of its request), 11 = first
+ * custom-mask bit of each prefill request and the total, as int64 values
+ * stored as little-endian int32 pairs (empty without a custom mask).
  * Copies min(count, capacity) int32 values into `out` (may be NULL to query
  * *count). Each table's record format is documented beside the planner
  * (csrc/pod_plan.h in the library sources).

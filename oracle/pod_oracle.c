@@ -30,13 +30,14 @@
  *    (flashinfer.cudnn page, "LSE 契约").
  *  - Merge of split partials (o_i, lse_i): weights 2^(lse_i - max), the
  *    property that lets base-2 LSE feed a cascade merge (same section).
- *  - Custom mask (POD walkthrough, run parameters custom_mask_p /
- *    packed_custom_mask_p, packed with little bit order): one boolean per
- *    (query row, key) of each request, the requests' [q_len, kv_len]
- *    row-major matrices laid end to end, eight to a byte, the first element
- *    in the least significant bit. Readings taken here: a set bit allows the
- *    key; the mask replaces the causal rule (window_left still applies);
- *    a row the mask leaves without keys has out = 0 and lse = -inf.
+ *  - Custom mask (POD walkthrough, "run 参数详解", prefill parameters
+ *    custom_mask_p / packed_custom_mask_p, packed with little bit order; a
+ *    custom mask takes precedence over causal): one boolean per (query row,
+ *    key) of each request, the requests' [q_len, kv_len] row-major matrices
+ *    laid end to end, eight to a byte, the first element in the least
+ *    significant bit. Readings taken here: a set bit allows the key;
+ *    window_left still applies; a row the mask leaves without keys has
+ *    out = 0 and lse = -inf.
  *
  * Inputs are the same rounded fp16/bf16 values the GPU reads, widened to
  * double by decoders written from the IEEE-754 binary16 and bfloat16 bit

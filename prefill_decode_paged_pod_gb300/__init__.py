@@ -29,7 +29,8 @@ __all__ = [
     "POD_OK", "PodError", "load_library", "pod_plan", "pod_run", "pod_destroy",
     "pod_workspace_size", "pod_bind_workspace", "pod_last_error", "pod_read_device_status",
     "pod_plan_table", "PodHandle", "LIB_PATH", "DEFAULT_WORKSPACE_BYTES",
-    "pod_run_static_scratch", "pod_static_scratch_capacity",
+    "pod_run_static_scratch", "pod_static_scratch_capacity", "pod_plan_set_decode_fp8",
+    "pod_plan_set_prefill_mask",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -84,6 +85,8 @@ def load_library(path: Optional[str] = None):
     lib.pod_static_scratch_capacity.argtypes = []
     lib.pod_plan_set_decode_fp8.restype = ctypes.c_int
     lib.pod_plan_set_decode_fp8.argtypes = [V, ctypes.c_float, ctypes.c_float]
+    lib.pod_plan_set_prefill_mask.restype = ctypes.c_int
+    lib.pod_plan_set_prefill_mask.argtypes = [V, V, ctypes.c_int64]
     if path is None:
         _lib = lib
     return lib
@@ -145,6 +148,7 @@ class PodHandle:
     has_sinks: bool
     workspace_ptr: Optional[int] = None
     d_kv_fp8: bool = False      # set by pod_plan_set_decode_fp8
+    p_mask: object = None       # custom prefill mask, kept alive while the plan uses it
 
     def __del__(self):
         if self.ptr and _lib is not None:
@@ -225,6 +229,7 @@ def pod_run(h: PodHandle, q_p, kv_p, q_d, kv_d, workspace, sinks=None,
         want = torch.float8_e4m3fn if (name == "kv_d" and h.d_kv_fp8) else h.dtype
         if t is not None and (not t.is_contiguous() or t.dtype != want):
             raise PodError(1, f"{name} must be contiguous {want}")
+    _check_mask_device(h)
     p_empty, d_empty = h.p_rows == 0, h.d_rows == 0
     code = lib.pod_run(ctypes.c_void_p(h.ptr),
                        None if p_empty else _ptr(q_p), None if p_empty else _ptr(kv_p),
@@ -260,6 +265,7 @@ def pod_run_static_scratch(h: PodHandle, q_p, kv_p, q_d, kv_d, sinks=None,
         out_d = torch.empty((h.d_rows, H, d), dtype=h.dtype, device=dev)
     if lse_d is None:
         lse_d = torch.empty((h.d_rows, H), dtype=torch.float32, device=dev)
+    _check_mask_device(h)
     p_empty, d_empty = h.p_rows == 0, h.d_rows == 0
     code = lib.pod_run_static_scratch(
         ctypes.c_void_p(h.ptr),
@@ -300,7 +306,7 @@ def pod_plan_table(h: PodHandle, which: int) -> np.ndarray:
 SUMMARY_FIELDS = ("H", "Hk", "d", "ps", "causal", "window", "dtype", "sinks", "num_sms", "grid",
                   "n_p_ctas", "n_d_ctas", "n_tiles", "n_items", "n_groups", "n_mrows", "n_prows",
                   "p_rows", "d_rows", "p_batch", "d_batch", "decode_chunk", "ws_lo", "ws_hi",
-                  "p_tma", "d_tma")
+                  "p_tma", "d_tma", "p_mask")
 
 
 def plan_summary(h: PodHandle) -> dict:
@@ -315,14 +321,54 @@ def pod_plan_set_decode_fp8(h: PodHandle, k_scale: float, v_scale: float):
     h.d_kv_fp8 = True
 
 
+def pod_plan_set_prefill_mask(h: PodHandle, packed_mask):
+    """Custom prefill mask: uint8 bits (little bit order) of every prefill
+    request's [q_len, kv_len] matrix, end to end; None removes it. A CUDA
+    tensor for runs; a CPU tensor or numpy array serves host-only plans
+    (inspection), whose pointer the library never reads. Switching the mask
+    on or off re-plans the handle and releases its workspace: bind again."""
+    lib = load_library()
+    if packed_mask is None:
+        _check(lib.pod_plan_set_prefill_mask(ctypes.c_void_p(h.ptr), None, 0))
+        h.p_mask = None
+    else:
+        if isinstance(packed_mask, np.ndarray):
+            packed_mask = np.ascontiguousarray(packed_mask, dtype=np.uint8)
+            ptr, nbytes = packed_mask.ctypes.data, packed_mask.nbytes
+        else:
+            import torch
+            if packed_mask.dtype != torch.uint8 or not packed_mask.is_contiguous():
+                raise PodError(1, "packed_mask must be a contiguous uint8 tensor")
+            ptr, nbytes = packed_mask.data_ptr(), packed_mask.numel()
+        _check(lib.pod_plan_set_prefill_mask(ctypes.c_void_p(h.ptr), ptr, int(nbytes)))
+        h.p_mask = packed_mask
+    h.workspace_bytes = pod_workspace_size(h)
+    h.workspace_ptr = None
+
+
+def _check_mask_device(h: PodHandle):
+    m = h.p_mask
+    if m is not None and h.p_rows and not getattr(m, "is_cuda", False):
+        raise PodError(1, "the custom prefill mask must be a CUDA uint8 tensor to run")
+
+
 def plan_inputs(inp, workspace=None, num_sms=0, stream=None) -> PodHandle:
     """pod_plan for a ``pod_workloads.PODInputs``-shaped object (tests, bench);
     an FP8 (float8_e4m3fn) decode cache gets pod_plan_set_decode_fp8 with the
-    inputs' scales."""
-    h = _plan_inputs(inp, workspace, num_sms, stream)
+    inputs' scales, a packed custom mask on the prefill half
+    pod_plan_set_prefill_mask (moved to the GPU when there is one)."""
+    mask = getattr(inp.p, "packed_mask", None)
+    h = _plan_inputs(inp, None if mask is not None else workspace, num_sms, stream)
     import torch
     if inp.d.rows and getattr(inp.d.kv, "dtype", None) == torch.float8_e4m3fn:
         pod_plan_set_decode_fp8(h, inp.k_scale, inp.v_scale)
+    if mask is not None:
+        t = torch.from_numpy(np.ascontiguousarray(mask, dtype=np.uint8))
+        if torch.cuda.is_available():
+            t = t.cuda()
+        pod_plan_set_prefill_mask(h, t)
+        if workspace is not None:
+            pod_bind_workspace(h, workspace, stream)
     return h
 
 

@@ -25,6 +25,9 @@ struct pod_plan_s {
   // decode cache stored as FP8 E4M3 codes with per-tensor K and V scales
   int d_fp8 = 0;
   float k_scale = 1.f, v_scale = 1.f;
+  // custom prefill mask: caller-owned device bytes read by every run
+  const void* p_mask = nullptr;
+  int64_t p_mask_bytes = 0;
   void* workspace = nullptr;      // bound device workspace (nullptr = host-only plan)
   size_t workspace_bytes = 0;
   // TMA descriptors of the last run, re-encoded only when a tensor pointer changes
@@ -236,6 +239,7 @@ pod_status pod_plan(const int32_t* p_q_indptr, const int32_t* p_kv_indptr,
   a.H = num_qo_heads; a.Hk = num_kv_heads; a.d = head_dim; a.ps = page_size;
   a.causal = causal; a.window_left = window_left; a.sm_scale = sm_scale;
   a.dtype = (int)dtype; a.has_sinks = has_sinks; a.num_sms = num_sms;
+  a.p_custom_mask = 0;
 
   pod_plan_s* h = new (std::nothrow) pod_plan_s();
   if (!h) return set_err(POD_ERR_INVALID_ARG, "out of host memory");
@@ -290,6 +294,14 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
   if (P.has_sinks && !sinks) return set_err(POD_ERR_INVALID_ARG, "plan has sinks but sinks is NULL");
   if (!P.has_sinks && sinks)
     return set_err(POD_ERR_INVALID_ARG, "sinks given but the plan was made without sinks");
+  if (P.p_custom_mask && P.p.rows > 0) {
+    // the kernel reads the mask: it must be device (or managed) memory
+    cudaPointerAttributes pa;
+    cudaError_t e = cudaPointerGetAttributes(&pa, h->p_mask);
+    if (e != cudaSuccess) return cuda_err(e, "cudaPointerGetAttributes(prefill mask)");
+    if (pa.type != cudaMemoryTypeDevice && pa.type != cudaMemoryTypeManaged)
+      return set_err(POD_ERR_INVALID_ARG, "the custom prefill mask is not device memory");
+  }
 
   // TMA descriptors for the tensors of this call (cached while pointers repeat)
   const void* ptrs[4] = {q_p, kv_p, q_d, kv_d};
@@ -353,6 +365,11 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
   K.part_lse = reinterpret_cast<float*>(ws + P.off_part_lse);
   K.status = reinterpret_cast<int32_t*>(ws + P.off_status);
   K.q_p = q_p; K.kv_p = kv_p; K.q_d = q_d; K.kv_d = kv_d; K.sinks = sinks;
+  if (P.p_custom_mask && P.p.rows > 0) {
+    K.p_mask = static_cast<const uint8_t*>(h->p_mask);
+    K.p_mask_off = reinterpret_cast<const long long*>(ws + P.off_p_mask_off);
+    K.p_mask_bytes = (long long)h->p_mask_bytes;
+  }
   K.out_p = out_p; K.out_d = out_d; K.lse_p = lse_p; K.lse_d = lse_d;
 
   cudaError_t e = pod_launch(K, P.dtype, (cudaStream_t)stream);
@@ -376,6 +393,47 @@ pod_status pod_plan_set_decode_fp8(pod_handle h, float k_scale, float v_scale) {
   h->k_scale = k_scale;
   h->v_scale = v_scale;
   h->tm_ptr[3] = nullptr;  // the decode cache's tensor map changes format
+  return POD_OK;
+}
+
+pod_status pod_plan_set_prefill_mask(pod_handle h, const void* packed_mask, int64_t mask_bytes) {
+  g_err.clear();
+  if (!h) return set_err(POD_ERR_INVALID_ARG, "handle is NULL");
+  const PodPlanHost& O = h->plan;
+  const int want = packed_mask != nullptr ? 1 : 0;
+  if (want) {
+    int64_t bits = 0;
+    for (int r = 0; r < O.p.batch; ++r) bits += (int64_t)O.p.q_len[r] * O.p.kv_len[r];
+    if (mask_bytes < (bits + 7) / 8)
+      return set_err(POD_ERR_INVALID_ARG, "the mask holds " + std::to_string(mask_bytes) +
+                                              " bytes; the prefill requests need " +
+                                              std::to_string((bits + 7) / 8));
+  }
+  if (want != O.p_custom_mask) {
+    // plan again from the handle's own copies of the page tables: the prefill
+    // tiles now span every key the window allows
+    PodPlanArgs a;
+    a.p_q_indptr = O.p.q_indptr.data(); a.p_kv_indptr = O.p.kv_indptr.data();
+    a.p_kv_indices = O.p.kv_indices.data(); a.p_last_page_len = O.p.last_page_len.data();
+    a.p_batch = O.p.batch; a.p_num_pages = O.p.num_pages;
+    a.d_q_indptr = O.dd.q_indptr.data(); a.d_kv_indptr = O.dd.kv_indptr.data();
+    a.d_kv_indices = O.dd.kv_indices.data(); a.d_last_page_len = O.dd.last_page_len.data();
+    a.d_batch = O.dd.batch; a.d_num_pages = O.dd.num_pages;
+    a.H = O.H; a.Hk = O.Hk; a.d = O.d; a.ps = O.ps; a.causal = O.causal;
+    a.window_left = O.window_left; a.sm_scale = O.sm_scale; a.dtype = O.dtype;
+    a.has_sinks = O.has_sinks; a.num_sms = O.num_sms; a.p_custom_mask = want;
+    PodPlanHost fresh;
+    std::string err;
+    const int rc = pod_build_plan(a, fresh, &err);
+    if (rc != 0) return set_err((pod_status)rc, err);
+    h->plan = std::move(fresh);
+    // the layout may have changed: the caller binds a workspace again
+    h->workspace = nullptr;
+    h->workspace_bytes = 0;
+    for (int i = 0; i < 4; ++i) h->tm_ptr[i] = nullptr;
+  }
+  h->p_mask = packed_mask;
+  h->p_mask_bytes = want ? mask_bytes : 0;
   return POD_OK;
 }
 
@@ -419,6 +477,7 @@ pod_status pod_plan_table(pod_handle h, int32_t which, int32_t* out, int64_t cap
     case 8: v = &P.pqueue; break;
     case 9: v = &P.dqueue; break;
     case 10: v = &P.dqrec; break;
+    case 11: v = &P.p_mask_off; break;
     default: return set_err(POD_ERR_INVALID_ARG, "unknown plan table");
   }
   if (count) *count = (int64_t)v->size();

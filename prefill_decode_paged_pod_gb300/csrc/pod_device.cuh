@@ -299,6 +299,19 @@ POD_DEV uint2 ld_shared_v2(uint32_t addr) {
   return v;
 }
 
+// 64 bits of a little-bit-order packed array starting at bit `pos` (bit i of
+// the result = array bit pos + i); bytes at or past `nbytes` read as zero.
+POD_DEV uint64_t load_bits64(const uint8_t* m, long long nbytes, long long pos) {
+  const long long b0 = pos >> 3;
+  const int sh = (int)(pos & 7);
+  uint64_t lo = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    if (b0 + k < nbytes) lo |= (uint64_t)__ldg(m + b0 + k) << (8 * k);
+  const uint64_t hi = (b0 + 8 < nbytes) ? (uint64_t)__ldg(m + b0 + 8) : 0ull;
+  return sh ? (lo >> sh) | (hi << (64 - sh)) : lo;
+}
+
 // ---------------------------------------------------------------- mma.sync
 POD_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"

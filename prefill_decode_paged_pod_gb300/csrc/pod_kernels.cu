@@ -448,8 +448,11 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
       const int tok = tok0 + (valid ? r / G : ntok - 1);
       const int head = g * G + (valid ? r % G : 0);
       const int pdiag = kv_len - q_len + tok;
-      const int row_hi = P.causal ? min(pdiag + 1, kv_len) : kv_len;
+      // a custom mask takes the place of the causal rule
+      const bool masked = P.p_mask != nullptr;
+      const int row_hi = (P.causal && !masked) ? min(pdiag + 1, kv_len) : kv_len;
       const int row_lo = P.window_left >= 0 ? max(pdiag - P.window_left, 0) : 0;
+      const long long mrow = masked ? P.p_mask_off[req] + (long long)tok * kv_len : 0;
       const int b0 = (lo / POD_KBLOCK) * POD_KBLOCK;
       const int nb = (hi - b0 + POD_KBLOCK - 1) / POD_KBLOCK;
       float m_ref = NEG_INF, l = 0.f;
@@ -469,6 +472,13 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
             const int t = kb + i;
             if (t < row_lo || t >= row_hi) s[i] = NEG_INF;
           }
+        }
+        if (masked) {
+          // keys past kv_len read the next row's bits; row_hi has masked them
+          const uint64_t bits = load_bits64(P.p_mask, P.p_mask_bytes, mrow + kb);
+#pragma unroll
+          for (int i = 0; i < POD_KBLOCK; ++i)
+            if (!((bits >> i) & 1ull)) s[i] = NEG_INF;
         }
         // row max with three-input max: four independent chains
         float c0 = s[0], c1 = s[1], c2 = s[2], c3 = s[3];

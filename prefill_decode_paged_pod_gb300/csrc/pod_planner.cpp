@@ -322,6 +322,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
 
   P.H = a.H; P.Hk = a.Hk; P.G = G; P.d = a.d; P.ps = a.ps;
   P.causal = a.causal ? 1 : 0; P.window_left = a.window_left;
+  P.p_custom_mask = a.p_custom_mask ? 1 : 0;
   P.dtype = a.dtype; P.has_sinks = a.has_sinks ? 1 : 0; P.num_sms = a.num_sms;
   P.sm_scale = a.sm_scale > 0.f ? a.sm_scale : (float)(1.0 / std::sqrt((double)a.d));
   P.scale_log2 = (float)((double)P.sm_scale * 1.4426950408889634);
@@ -377,7 +378,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
     for (int t0 = 0; t0 < ql; t0 += Tq) {
       int nt = std::min(Tq, ql - t0);
       int lo, hi;
-      key_range(kl, ql, t0, nt, P.causal, P.window_left, &lo, &hi);
+      key_range(kl, ql, t0, nt, P.causal && !P.p_custom_mask, P.window_left, &lo, &hi);
       for (int g = 0; g < P.Hk; ++g) tunits.push_back({r, g, t0, nt, lo, hi});
     }
   }
@@ -593,6 +594,20 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
     P.cta_ptr[P.grid] = (int32_t)P.cta_list.size();
   }
 
+  // ---- custom-mask bit offsets: request r's [q_len, kv_len] bits start after
+  // those of the requests before it
+  P.p_mask_off.clear();
+  P.p_mask_bits = 0;
+  if (P.p_custom_mask) {
+    int64_t bit = 0;
+    for (int r = 0; r <= P.p.batch; ++r) {
+      P.p_mask_off.push_back((int32_t)(uint32_t)((uint64_t)bit & 0xffffffffu));
+      P.p_mask_off.push_back((int32_t)(uint32_t)((uint64_t)bit >> 32));
+      if (r < P.p.batch) bit += (int64_t)P.p.q_len[r] * P.p.kv_len[r];
+    }
+    P.p_mask_bits = bit;
+  }
+
   // ---- workspace layout -----------------------------------------------------------
   size_t off = 0;
   auto place = [&](size_t n_int32) {
@@ -618,6 +633,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   P.off_pqueue = place(P.pqueue.size());
   P.off_dqueue = place(P.dqueue.size());
   P.off_dqrec = place(P.dqrec.size());
+  P.off_p_mask_off = place(P.p_mask_off.size());
   P.int_bytes = align_up(off, 256);
   P.off_part_o = P.int_bytes;
   P.off_part_lse = align_up(P.off_part_o + (size_t)n_prows * a.d * 4, 256);
@@ -644,6 +660,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   put(P.off_pqueue, P.pqueue);
   put(P.off_dqueue, P.dqueue);
   put(P.off_dqrec, P.dqrec);
+  put(P.off_p_mask_off, P.p_mask_off);
 
   P.summary.assign(S_COUNT, 0);
   int32_t* s = P.summary.data();
@@ -658,5 +675,6 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   s[S_WS_HI] = (int32_t)(P.total_bytes >> 31);
   s[S_P_TMA] = P.p_tma;
   s[S_D_TMA] = P.d_tma;
+  s[S_P_MASK] = P.p_custom_mask;
   return 0;
 }

@@ -17,6 +17,12 @@ struct PodPlanHost {
   // configuration
   int H = 0, Hk = 0, G = 0, d = 0, ps = 0, causal = 0, window_left = -1, dtype = 0,
       has_sinks = 0, num_sms = 0;
+  // prefill half under a custom mask: its tiles span every key the window
+  // allows (the mask replaces the causal rule); p_mask_off holds each
+  // request's first mask bit as int64 (little-endian int32 pairs), B+1 of them
+  int p_custom_mask = 0;
+  int64_t p_mask_bits = 0;
+  std::vector<int32_t> p_mask_off;
   float sm_scale = 0.f, scale_log2 = 0.f;
   PodHalfHost p, dd;
   // schedule
@@ -29,8 +35,8 @@ struct PodPlanHost {
   size_t off_status = 0, off_p_q_indptr = 0, off_p_kv_indptr = 0, off_p_kv_indices = 0,
          off_p_kv_len = 0, off_d_q_indptr = 0, off_d_kv_indptr = 0, off_d_kv_indices = 0,
          off_d_kv_len = 0, off_ptiles = 0, off_ditems = 0, off_cta_ptr = 0, off_cta_list = 0,
-         off_mgroups = 0, off_mrow_ptr = 0, off_pqueue = 0, off_dqueue = 0, off_dqrec = 0, int_bytes = 0, off_part_o = 0, off_part_lse = 0,
-         total_bytes = 0;
+         off_mgroups = 0, off_mrow_ptr = 0, off_pqueue = 0, off_dqueue = 0, off_dqrec = 0,
+         off_p_mask_off = 0, int_bytes = 0, off_part_o = 0, off_part_lse = 0, total_bytes = 0;
   std::vector<uint8_t> int_image;   // bytes [0, int_bytes) of the workspace
   std::vector<int32_t> summary;
 };
@@ -43,6 +49,7 @@ struct PodPlanArgs {
   int H, Hk, d, ps, causal, window_left;
   float sm_scale;
   int dtype, has_sinks, num_sms;
+  int p_custom_mask;   // 1: a custom mask replaces the causal rule on the prefill half
 };
 
 // Returns 0 on success, else a pod_status code with *err set.

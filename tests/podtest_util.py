@@ -63,7 +63,10 @@ def compare_half(inp, half, out, lse, sel_token=None, sel_head=None, tag=""):
     gl = lse[sel_token, sel_head].astype(np.float64)
     err = np.abs(go - ro)
     bad = err > OUT_ATOL + OUT_RTOL * np.abs(ro)
-    lerr = np.abs(gl - rl)
+    # rows a custom mask leaves without keys: lse = -inf on both sides
+    fin = np.isfinite(rl)
+    assert np.array_equal(np.isneginf(gl), ~fin), f"{tag}{half}: -inf LSE rows differ"
+    lerr = np.abs(gl[fin] - rl[fin]) if fin.any() else np.zeros(1)
     msg = f"{tag}{half}: max|out err| {err.max():.3e}, max|lse err| {lerr.max():.3e}"
     if bad.any():
         i = np.argwhere(bad)[0]

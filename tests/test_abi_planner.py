@@ -63,7 +63,9 @@ def check_against_reference(inp, h):
     # [lo, hi) in order (one chunk unless the planner split it, then with a
     # merge group of half 0)
     tiles = pod.pod_plan_table(h, 1).reshape(-1, REC)
-    ref = planner_ref.prefill_tiles(inp.p.q_indptr, kvl_p, H, Hk, inp.causal, inp.window_left)
+    # a custom mask replaces the causal rule on the prefill half
+    p_causal = inp.causal and getattr(inp.p, "packed_mask", None) is None
+    ref = planner_ref.prefill_tiles(inp.p.q_indptr, kvl_p, H, Hk, p_causal, inp.window_left)
     i = 0
     gi = 0
     prows = 0
@@ -320,3 +322,55 @@ def test_split_keeps_balanced_start_when_no_tile_dominates(lib):
     s = pod.plan_summary(h)
     assert s["grid"] == 2 * s["num_sms"], s
     assert 0.25 * s["grid"] <= s["n_p_ctas"] <= 0.5 * s["grid"], s
+
+
+# ------------------------------------------------------------- custom prefill mask
+def _mask_offsets(inp):
+    ql = np.diff(inp.p.q_indptr).astype(np.int64)
+    kvl = planner_ref.seq_lens(inp.p.kv_indptr, inp.p.last_page_len, inp.page_size).astype(np.int64)
+    return np.concatenate([[0], np.cumsum(ql * kvl)])
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_custom_mask_plan(lib, seed):
+    """With a custom mask the prefill tiles span every key the window allows
+    (the restated planner run non-causal on that half), the decode half keeps
+    the causal rule, and plan table 11 holds each request's first mask bit."""
+    from pod_workloads import with_prefill_custom_mask
+    rng = np.random.default_rng(100 + seed)
+    window = int(rng.choice([-1, 50]))
+    pkv = rng.integers(1, 900, size=int(rng.integers(1, 4)))
+    pq = [int(rng.integers(1, k + 1)) for k in pkv]
+    inp = make_custom("m", torch.bfloat16, 16, 2, 128, int(rng.choice([1, 16])), True, window,
+                      pq, pkv, [1, 3], [300, 40], seed=seed)
+    inp = with_prefill_custom_mask(inp, seed=seed)
+    h = plan_host(inp, num_sms=int(rng.choice([8, 152])))
+    s = check_against_reference(inp, h)
+    assert s["p_mask"] == 1 and s["causal"] == 1
+    off = pod.pod_plan_table(h, 11).view(np.int64)
+    assert np.array_equal(off, _mask_offsets(inp))
+    # removing the mask gives the causal plan back
+    pod.pod_plan_set_prefill_mask(h, None)
+    inp.p.packed_mask = None
+    s = check_against_reference(inp, h)
+    assert s["p_mask"] == 0 and len(pod.pod_plan_table(h, 11)) == 0
+
+
+def test_custom_mask_host_checks(lib):
+    """A mask shorter than the prefill requests' bits is refused; switching
+    the mask on releases the bound workspace (host-only here: the size may
+    change, so the caller binds again)."""
+    inp = make_custom("m", torch.float16, 8, 2, 64, 16, True, -1, [70], [100],
+                      [1], [40], seed=1)
+    h = plan_host(inp, num_sms=4)
+    need = (70 * 100 + 7) // 8
+    with pytest.raises(pod.PodError) as e:
+        pod.pod_plan_set_prefill_mask(h, np.zeros(need - 1, np.uint8))
+    assert e.value.code == 1
+    causal_hi = sorted(set(pod.pod_plan_table(h, 1).reshape(-1, REC)[:, 5].tolist()))
+    pod.pod_plan_set_prefill_mask(h, np.zeros(need, np.uint8))
+    masked_hi = sorted(set(pod.pod_plan_table(h, 1).reshape(-1, REC)[:, 5].tolist()))
+    # tiles of 32 tokens (G = 4): causal ranges end at the tiles' last
+    # diagonals 62, 94, 100; under the mask every tile reads all 100 keys
+    assert causal_hi == [62, 94, 100] and masked_hi == [100]
+    assert h.workspace_ptr is None and pod.plan_summary(h)["p_mask"] == 1

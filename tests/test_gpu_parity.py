@@ -337,3 +337,37 @@ def test_prefill_alone_split_at_c4_shape():
     st, sh = sample_rows(inp.p, inp.num_qo_heads, 64, seed=5)
     compare_half(inp, "p", op, lp, st, sh, tag="p4 ")
     assert np.isfinite(op).all() and np.isfinite(lp).all()
+
+
+# ------------------------------------------------------------- custom prefill mask
+MASK_CASES = [
+    # name, dtype, H, Hk, d, ps, causal, window, sinks, p_q, p_kv, d_q, d_kv
+    ("mA", torch.float16, 8, 2, 128, 16, True, -1, False, [100, 37], [300, 37], [1, 2], [50, 60]),
+    ("mB", torch.bfloat16, 16, 2, 128, 1, True, 64, True, [200], [900], [4], [500]),
+    ("mC", torch.bfloat16, 4, 4, 64, 16, False, -1, True, [130, 1], [130, 260], [], []),
+    ("mD", torch.bfloat16, 16, 2, 128, 16, True, -1, True, [40], [6000], [1], [30]),
+]
+
+
+@pytest.mark.parametrize("case", MASK_CASES, ids=[c[0] for c in MASK_CASES])
+def test_custom_prefill_mask(case):
+    """A packed custom mask on the prefill half (random bits plus a row with
+    no key and a row with every key in each request), next to a decode half
+    that keeps the causal rule. mD is a small prefill with long keys whose
+    tiles the planner splits: merged partials of rows that some chunks
+    leave empty."""
+    from pod_workloads import with_prefill_custom_mask
+    name, dt, H, Hk, d, ps, causal, window, sinks, pq, pkv, dq, dkv = case
+    inp = make_custom(name, dt, H, Hk, d, ps, causal, window, pq, pkv, dq, dkv, seed=21,
+                      sinks=sinks)
+    inp = with_prefill_custom_mask(inp, seed=22, density=0.5)
+    (op, lp, od, ld), h, ws = run_pod(inp)
+    assert pod.plan_summary(h)["p_mask"] == 1
+    if name == "mD":
+        groups = pod.pod_plan_table(h, 5).reshape(-1, 8)
+        assert np.any(groups[:, 0] == 0), "expected a prefill key split"
+    compare_half(inp, "p", op, lp, tag=name + " ")
+    compare_half(inp, "d", od, ld, tag=name + " ")
+    # the first row of every request allows no key: out = 0, lse = -inf
+    first = inp.p.q_indptr[:-1][np.diff(inp.p.q_indptr) > 2]
+    assert np.all(op[first] == 0.0) and np.all(np.isneginf(lp[first]))
