@@ -84,6 +84,13 @@ def lib():
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_int, ctypes.c_double,
                 P, P, ctypes.c_int64, P, P, P, P, P, P, ctypes.c_int]
+            _lib.oracle_attention_rows_ext.restype = ctypes.c_int
+            _lib.oracle_attention_rows_ext.argtypes = [
+                P, P, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double,
+                P, P, P, P, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double, P,
+                P, P, ctypes.c_int64, P, P, P, P, P, P, ctypes.c_int]
             _lib.oracle_attention_rows_kv.restype = ctypes.c_int
             _lib.oracle_attention_rows_kv.argtypes = [
                 P, P, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double,
@@ -135,11 +142,15 @@ def attention_rows(q, kv, q_indptr, kv_indptr, kv_indices, last_page_len,
                    causal, window_left, sm_scale, sinks=None,
                    sel_token=None, sel_head=None, key_lo=None, key_hi=None,
                    nthreads: Optional[int] = None, dtype: Optional[int] = None,
-                   k_scale: float = 1.0, v_scale: float = 1.0, packed_mask=None):
+                   k_scale: float = 1.0, v_scale: float = 1.0, packed_mask=None,
+                   kv_layout: int = 0, soft_cap: float = 0.0, alibi_slopes=None):
     """fp64 outputs for selected (token, head) pairs; all pairs if no selection.
     An E4M3 ``kv`` is read as codes times ``k_scale`` (K) / ``v_scale`` (V).
     ``packed_mask`` (uint8, little bit order) is a custom mask over every
     request's [q_len, kv_len] matrix; it replaces the causal rule.
+    ``kv_layout`` 0 = NHD pages [2, ps, Hk, d], 1 = HND [2, Hk, ps, d];
+    ``soft_cap`` > 0 caps the scaled logits (cap * tanh(x / cap));
+    ``alibi_slopes`` [H] adds slope * (t - p) to each logit.
 
     Returns (out [n, d] float64, lse [n] float64, status int).
     """
@@ -183,11 +194,15 @@ def attention_rows(q, kv, q_indptr, kv_indptr, kv_indices, last_page_len,
         need = int(np.sum(np.diff(q_indptr).astype(np.int64) * kvl))
         if pm.size * 8 < need:
             raise ValueError(f"packed_mask holds {pm.size * 8} bits, the requests need {need}")
-    st = lib().oracle_attention_rows_masked(
+    al = None
+    if alibi_slopes is not None:
+        al = np.ascontiguousarray(np.asarray(alibi_slopes.cpu() if hasattr(alibi_slopes, "cpu")
+                                             else alibi_slopes, dtype=np.float32))
+    st = lib().oracle_attention_rows_ext(
         _ptr(qc), _ptr(kvc), int(dtype), int(kv_fp8), float(k_scale), float(v_scale),
         _ptr(q_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(last_page_len),
-        batch, num_pages, H, int(num_kv_heads), d, int(page_size),
-        int(bool(causal)), int(window_left), float(sm_scale),
+        batch, num_pages, H, int(num_kv_heads), d, int(page_size), int(kv_layout),
+        int(bool(causal)), int(window_left), float(sm_scale), float(soft_cap), _ptr(al),
         _ptr(sk), _ptr(pm), n, _ptr(tok), _ptr(hd), _ptr(key_lo), _ptr(key_hi),
         _ptr(out), _ptr(lse), int(nthreads))
     return out[:n], lse[:n], int(st)
@@ -201,6 +216,8 @@ def attention_half(inp, half: str, sel_token=None, sel_head=None, nthreads=None,
         scales = dict(k_scale=getattr(inp, "k_scale", 1.0), v_scale=getattr(inp, "v_scale", 1.0))
     if getattr(h, "packed_mask", None) is not None and "packed_mask" not in kw:
         scales["packed_mask"] = h.packed_mask
+    if getattr(h, "kv_layout", "NHD") == "HND" and "kv_layout" not in kw:
+        scales["kv_layout"] = 1
     return attention_rows(h.q, h.kv, h.q_indptr, h.kv_indptr, h.kv_indices, h.last_page_len,
                           inp.num_qo_heads, inp.num_kv_heads, inp.head_dim, inp.page_size,
                           inp.causal, inp.window_left, inp.sm_scale, sinks=inp.sinks,

@@ -30,6 +30,16 @@
  *    (flashinfer.cudnn page, "LSE 契约").
  *  - Merge of split partials (o_i, lse_i): weights 2^(lse_i - max), the
  *    property that lets base-2 LSE feed a cascade merge (same section).
+ *  - KV layout (FlashInfer guide, "快速上手", kv_layout: NHD or HND orders
+ *    the dimensions of the k/v tensors): NHD pages are [2, page_size, Hk, d],
+ *    HND pages [2, Hk, page_size, d]; the page pool is [num_pages, ...] either way.
+ *  - ALiBi (same section, pos_encoding_mode ALIBI; per-head slopes are an
+ *    input): the logit of key t for query row i gains slope[h] * (t - p),
+ *    p the row's bottom-right diagonal position (the published ALiBi bias
+ *    -m * distance, with the distance measured from the diagonal).
+ *  - Logits soft cap (same section, logits_soft_cap: cap * tanh(x / cap), 0
+ *    = off): x is the scaled logit sm_scale * q.k. With both, the ALiBi bias
+ *    is added after the cap (a reading: the pages do not combine them).
  *  - Custom mask (POD walkthrough, "run 参数详解", prefill parameters
  *    custom_mask_p / packed_custom_mask_p, packed with little bit order; a
  *    custom mask takes precedence over causal): one boolean per (query row,
@@ -53,7 +63,10 @@
  * window_left = 0, kv_len = 1, equal keys), GQA head duplication, exhaustive
  * checks of the two 16-bit decoders; for the custom mask, brute force over
  * the bits numpy unpacks, single-bit masks (out = v_t) and the triangular and
- * all-ones masks against the causal and non-causal rules.
+ * all-ones masks against the causal and non-causal rules; for HND pages,
+ * bit-identity with NHD and brute force over an HND gather; for ALiBi, brute
+ * force, the geometric-series lse of q = 0 and slope 0; for the soft cap,
+ * brute force, two saturated keys and a cap far above every logit.
  */
 #include <math.h>
 #include <stdint.h>
@@ -136,6 +149,15 @@ void oracle_seq_lens(const int32_t* kv_indptr, const int32_t* last_page_len,
         kv_len_out[r] = (int32_t)oracle_kv_len(kv_indptr, last_page_len, r, page_size);
 }
 
+/* Element offset of the K (kv = 0) or V (kv = 1) row of (page, slot, head). */
+static int64_t row_offset(int kv_layout, int64_t page, int kv, int64_t slot, int hk,
+                          int page_size, int Hk, int d)
+{
+    if (kv_layout == 1) /* HND */
+        return (((page * 2 + kv) * Hk + hk) * (int64_t)page_size + slot) * (int64_t)d;
+    return (((page * 2 + kv) * (int64_t)page_size + slot) * Hk + hk) * (int64_t)d;
+}
+
 /* Bit `pos` of a little-bit-order packed array. */
 static int mask_bit(const uint8_t* packed, int64_t pos)
 {
@@ -161,19 +183,21 @@ static int find_request(const int32_t* q_indptr, int batch, int64_t token)
  *   out [n, d], lse [n]                   : fp64 results
  * Returns the first error code met (rows are still filled where possible).
  */
-int oracle_attention_rows_masked(const uint16_t* q, const void* kv, int dtype,
-                                 int kv_fp8, double k_scale, double v_scale,
-                                 const int32_t* q_indptr, const int32_t* kv_indptr,
-                                 const int32_t* kv_indices, const int32_t* last_page_len,
-                                 int batch, int num_pages,
-                                 int H, int Hk, int d, int page_size,
-                                 int causal, int window_left, double sm_scale,
-                                 const float* sinks, const uint8_t* packed_mask,
-                                 int64_t n_sel, const int64_t* sel_token, const int32_t* sel_head,
-                                 const int64_t* key_lo, const int64_t* key_hi,
-                                 double* out, double* lse, int nthreads)
+int oracle_attention_rows_ext(const uint16_t* q, const void* kv, int dtype,
+                              int kv_fp8, double k_scale, double v_scale,
+                              const int32_t* q_indptr, const int32_t* kv_indptr,
+                              const int32_t* kv_indices, const int32_t* last_page_len,
+                              int batch, int num_pages,
+                              int H, int Hk, int d, int page_size, int kv_layout,
+                              int causal, int window_left, double sm_scale,
+                              double soft_cap, const float* alibi_slopes,
+                              const float* sinks, const uint8_t* packed_mask,
+                              int64_t n_sel, const int64_t* sel_token, const int32_t* sel_head,
+                              const int64_t* key_lo, const int64_t* key_hi,
+                              double* out, double* lse, int nthreads)
 {
     if (H <= 0 || Hk <= 0 || H % Hk != 0 || d <= 0 || page_size <= 0) return ORACLE_BAD_ARG;
+    if (kv_layout != 0 && kv_layout != 1) return ORACLE_BAD_ARG;
     int group = H / Hk;
     int status = ORACLE_OK;
     (void)nthreads;
@@ -234,10 +258,14 @@ int oracle_attention_rows_masked(const uint16_t* q, const void* kv, int dtype,
                 status = ORACLE_BAD_ARG;
                 continue;
             }
-            int64_t k0 = (((page * 2 + 0) * page_size + slot) * Hk + hk) * (int64_t)d;
+            int64_t k0 = row_offset(kv_layout, page, 0, slot, hk, page_size, Hk, d);
             double dot = 0.0;
             for (int e = 0; e < d; ++e) dot += qv[e] * kv_elem(kv, k0 + e, dtype, kv_fp8, k_scale);
-            logit[t] = sm_scale * dot;
+            if (soft_cap > 0.0)
+                logit[t] = soft_cap * tanh(sm_scale * dot / soft_cap);
+            else
+                logit[t] = sm_scale * dot;
+            if (alibi_slopes) logit[t] += (double)alibi_slopes[h] * (double)(t - p);
             if (logit[t] > m) m = logit[t];
             ++n_allowed;
         }
@@ -260,7 +288,7 @@ int oracle_attention_rows_masked(const uint16_t* q, const void* kv, int dtype,
             if (!allowed[t]) continue;
             int64_t page = kv_indices[kv_indptr[r] + t / page_size];
             int64_t slot = t % page_size;
-            int64_t v0 = (((page * 2 + 1) * page_size + slot) * Hk + hk) * (int64_t)d;
+            int64_t v0 = row_offset(kv_layout, page, 1, slot, hk, page_size, Hk, d);
             double w = exp(logit[t] - m) / denom;
             for (int e = 0; e < d; ++e) o[e] += w * kv_elem(kv, v0 + e, dtype, kv_fp8, v_scale);
         }
@@ -268,6 +296,26 @@ int oracle_attention_rows_masked(const uint16_t* q, const void* kv, int dtype,
         free(qv); free(logit); free(allowed);
     }
     return status;
+}
+
+/* oracle_attention_rows_ext with the NHD layout, no soft cap and no ALiBi. */
+int oracle_attention_rows_masked(const uint16_t* q, const void* kv, int dtype,
+                                 int kv_fp8, double k_scale, double v_scale,
+                                 const int32_t* q_indptr, const int32_t* kv_indptr,
+                                 const int32_t* kv_indices, const int32_t* last_page_len,
+                                 int batch, int num_pages,
+                                 int H, int Hk, int d, int page_size,
+                                 int causal, int window_left, double sm_scale,
+                                 const float* sinks, const uint8_t* packed_mask,
+                                 int64_t n_sel, const int64_t* sel_token, const int32_t* sel_head,
+                                 const int64_t* key_lo, const int64_t* key_hi,
+                                 double* out, double* lse, int nthreads)
+{
+    return oracle_attention_rows_ext(q, kv, dtype, kv_fp8, k_scale, v_scale, q_indptr, kv_indptr,
+                                     kv_indices, last_page_len, batch, num_pages, H, Hk, d,
+                                     page_size, 0, causal, window_left, sm_scale, 0.0, NULL,
+                                     sinks, packed_mask, n_sel, sel_token, sel_head, key_lo,
+                                     key_hi, out, lse, nthreads);
 }
 
 /* oracle_attention_rows_masked without a custom mask. */

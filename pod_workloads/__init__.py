@@ -31,7 +31,8 @@ import numpy as np
 import torch
 
 __all__ = ["HalfInputs", "PODInputs", "make_half", "make_config", "make_custom",
-           "CONFIG_NAMES", "page_table_from_lens", "pack_mask", "with_prefill_custom_mask"]
+           "CONFIG_NAMES", "page_table_from_lens", "pack_mask", "with_prefill_custom_mask",
+           "with_kv_layout", "alibi_slopes"]
 
 CONFIG_NAMES = ("c1", "c2", "c3", "c4", "c5")
 
@@ -51,6 +52,8 @@ class HalfInputs:
     # custom mask (prefill half): uint8, the requests' [q_len, kv_len] boolean
     # matrices laid end to end, packed eight to a byte, little bit order
     packed_mask: Optional[np.ndarray] = None
+    # page layout of kv: "NHD" [pages, 2, ps, Hk, d] or "HND" [pages, 2, Hk, ps, d]
+    kv_layout: str = "NHD"
 
     @property
     def batch(self) -> int:
@@ -249,3 +252,26 @@ def with_prefill_custom_mask(inp: PODInputs, seed: int = 0, density: float = 0.5
     p.packed_mask = pack_mask(mats)
     out.p = p
     return out
+
+
+def with_kv_layout(inp: PODInputs, layout: str = "HND", halves: str = "pd") -> PODInputs:
+    """The same inputs with the caches of ``halves`` ("p", "d" or "pd") stored
+    in ``layout``: the same keys and values, pages reordered from
+    [2, ps, Hk, d] (NHD) to [2, Hk, ps, d] (HND) or back. Returns a new
+    PODInputs."""
+    import copy
+    out = copy.copy(inp)
+    for name in halves:
+        h = copy.copy(getattr(inp, name))
+        if h.kv_layout != layout:
+            h.kv = h.kv.permute(0, 1, 3, 2, 4).contiguous()
+            h.kv_layout = layout
+        setattr(out, name, h)
+    return out
+
+
+def alibi_slopes(num_heads: int) -> torch.Tensor:
+    """The geometric head slopes of the ALiBi paper for a power-of-two head
+    count: 2^(-8 (h + 1) / H), h = 0..H-1 (fp32)."""
+    h = torch.arange(1, num_heads + 1, dtype=torch.float64)
+    return torch.pow(2.0, -8.0 * h / num_heads).to(torch.float32)

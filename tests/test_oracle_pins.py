@@ -23,8 +23,8 @@ import torch
 from scipy.special import logsumexp, softmax
 
 import oracle
-from pod_workloads import (HalfInputs, make_custom, pack_mask, page_table_from_lens,
-                           with_prefill_custom_mask)
+from pod_workloads import (HalfInputs, alibi_slopes, make_custom, pack_mask,
+                           page_table_from_lens, with_kv_layout, with_prefill_custom_mask)
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 GOLDEN = os.path.join(HERE, "golden")
@@ -35,7 +35,8 @@ GOLDEN = os.path.join(HERE, "golden")
 # --------------------------------------------------------------------------
 
 def dense_kv(h: HalfInputs, r: int, ps: int):
-    """Dense K, V [kv_len, Hk, d] of request r, gathered with numpy indexing."""
+    """Dense K, V [kv_len, Hk, d] of request r, gathered with numpy indexing
+    (NHD pages [2, ps, Hk, d] or HND pages [2, Hk, ps, d])."""
     kv = h.kv.double().numpy()
     lo, hi = int(h.kv_indptr[r]), int(h.kv_indptr[r + 1])
     pages = h.kv_indices[lo:hi]
@@ -43,11 +44,15 @@ def dense_kv(h: HalfInputs, r: int, ps: int):
     t = np.arange(kvl)
     pg = pages[t // ps]
     sl = t % ps
+    if h.kv_layout == "HND":
+        return kv[pg, 0, :, sl], kv[pg, 1, :, sl]
     return kv[pg, 0, sl], kv[pg, 1, sl]
 
 
-def brute_force(inp, half="d"):
-    """Textbook masked softmax(QK^T)V per request/head, all rows."""
+def brute_force(inp, half="d", soft_cap=0.0, alibi=None):
+    """Textbook masked softmax(QK^T)V per request/head, all rows; optional
+    logits soft cap (cap * tanh(x / cap) of the scaled logits) and ALiBi
+    bias slope * (t - p)."""
     h = inp.p if half == "p" else inp.d
     H, Hk, d = inp.num_qo_heads, inp.num_kv_heads, inp.head_dim
     G = H // Hk
@@ -80,6 +85,10 @@ def brute_force(inp, half="d"):
         live = mask.any(axis=1)          # rows a custom mask left with keys
         for hh in range(H):
             S = inp.sm_scale * (q[q0:q1, hh, :] @ K[:, hh // G, :].T)
+            if soft_cap > 0:
+                S = soft_cap * np.tanh(S / soft_cap)
+            if alibi is not None:
+                S = S + float(alibi[hh]) * (t - p)
             S = np.where(mask, S, -np.inf)[live]
             lse[q0:q1, hh] = -np.inf
             out[q0:q1, hh] = 0.0
@@ -376,8 +385,91 @@ def pin_custom_mask(fn, seeds=range(8)):
             assert np.array_equal(o_m, o_ref) and np.array_equal(l_m, l_ref), seed
 
 
+def pin_hnd_layout(fn, seeds=range(6)):
+    """HND pages ([2, Hk, ps, d]): the same keys stored the other way give the
+    NHD result bit for bit, and brute force over a gather written for HND."""
+    for seed in seeds:
+        inp = tiny_case(seed)
+        o_n, l_n = run_oracle(inp, "d", fn=fn)
+        hnd = with_kv_layout(inp, "HND")
+        o_h, l_h = run_oracle(hnd, "d", fn=fn, kv_layout=1)
+        assert np.array_equal(o_h, o_n) and np.array_equal(l_h, l_n), seed
+        if inp.num_kv_heads > 1 and inp.page_size > 1:
+            # reading HND pages as NHD must change the result
+            o_x, _ = run_oracle(hnd, "d", fn=fn, kv_layout=0)
+            assert not np.array_equal(o_x, o_n), seed
+        ref_o, ref_l = brute_force(hnd, "d")
+        assert np.allclose(o_h, ref_o, atol=1e-12, rtol=1e-12), seed
+        assert np.allclose(l_h, ref_l, atol=1e-12, rtol=0), seed
+
+
+def pin_alibi(fn, seeds=range(6)):
+    """ALiBi (pos_encoding_mode ALIBI): brute force with the bias
+    slope * (t - p); with q = 0 on a causal row the weights are
+    e^{-m (p - t)}, so the lse is log2 of the geometric sum
+    (1 - e^{-m (p + 1)}) / (1 - e^{-m}); slope 0 is the plain result."""
+    for seed in seeds:
+        inp = tiny_case(seed)
+        sl = alibi_slopes(inp.num_qo_heads)
+        ref_o, ref_l = brute_force(inp, "d", alibi=sl.numpy())
+        out, lse = run_oracle(inp, "d", fn=fn, alibi_slopes=sl)
+        assert np.allclose(out, ref_o, atol=1e-12, rtol=1e-12), seed
+        assert np.allclose(lse, ref_l, atol=1e-12, rtol=0), seed
+        o0, l0 = run_oracle(inp, "d", fn=fn, alibi_slopes=np.zeros(inp.num_qo_heads, np.float32))
+        o1, l1 = run_oracle(inp, "d", fn=fn)
+        assert np.array_equal(o0, o1) and np.array_equal(l0, l1), seed
+    inp = tiny_case(2, causal=True, window=-1, sinks=False)
+    inp.d.q = torch.zeros_like(inp.d.q)
+    sl = alibi_slopes(inp.num_qo_heads)
+    _, lse = run_oracle(inp, "d", fn=fn, alibi_slopes=sl)
+    h = inp.d
+    for r in range(h.batch):
+        ql = int(h.q_indptr[r + 1] - h.q_indptr[r])
+        kvl = int(h.kv_lens[r])
+        for i in range(ql):
+            p = kvl - ql + i
+            for hh in range(inp.num_qo_heads):
+                m = float(sl[hh])
+                z = (1.0 - math.exp(-m * (p + 1))) / (1.0 - math.exp(-m))
+                assert abs(lse[int(h.q_indptr[r]) + i, hh] - math.log2(z)) < 1e-12
+
+
+def pin_soft_cap(fn, seeds=range(6)):
+    """Logits soft cap (cap * tanh(x / cap) of the scaled logit x): brute
+    force; two keys whose scaled logits are +-L with L far above the cap get
+    weights 1 / (1 + e^{-2 cap}) and e^{-2 cap} / (1 + e^{-2 cap}); a cap far
+    above every logit leaves the result unchanged to 1e-9."""
+    for seed in seeds:
+        inp = tiny_case(seed)
+        ref_o, ref_l = brute_force(inp, "d", soft_cap=1.5)
+        out, lse = run_oracle(inp, "d", fn=fn, soft_cap=1.5)
+        assert np.allclose(out, ref_o, atol=1e-12, rtol=1e-12), seed
+        assert np.allclose(lse, ref_l, atol=1e-12, rtol=0), seed
+        o_big, l_big = run_oracle(inp, "d", fn=fn, soft_cap=1e7)
+        o_pl, l_pl = run_oracle(inp, "d", fn=fn)
+        assert np.allclose(o_big, o_pl, atol=1e-9) and np.allclose(l_big, l_pl, atol=1e-9), seed
+    # one request, two keys, d = 2: q = [1, 0], k0 = [L, 0], k1 = [-L, 0], sm_scale = 1
+    H = Hk = 1
+    q_indptr = np.array([0, 1], np.int32)
+    kv_indptr = np.array([0, 1], np.int32)
+    kv = torch.zeros((1, 2, 2, 1, 2), dtype=torch.float16)
+    L, cap = 1000.0, 2.0
+    kv[0, 0, 0, 0] = torch.tensor([L, 0.0])
+    kv[0, 0, 1, 0] = torch.tensor([-L, 0.0])
+    kv[0, 1, 0, 0] = torch.tensor([1.0, 0.0])
+    kv[0, 1, 1, 0] = torch.tensor([0.0, 1.0])
+    q = torch.tensor([[[1.0, 0.0]]], dtype=torch.float16)
+    out, lse, st = fn(q, kv, q_indptr, kv_indptr, np.array([0], np.int32), np.array([2], np.int32),
+                      H, Hk, 2, 2, False, -1, 1.0, nthreads=1, soft_cap=cap)
+    assert st == 0
+    c0, c1 = cap * math.tanh(L / cap), cap * math.tanh(-L / cap)   # = +-cap in fp64
+    w0 = 1.0 / (1.0 + math.exp(c1 - c0))
+    assert abs(out[0, 0] - w0) < 1e-15 and abs(out[0, 1] - (1.0 - w0)) < 1e-15
+    assert abs(lse[0] - (c0 + math.log1p(math.exp(c1 - c0))) / math.log(2.0)) < 1e-12
+
+
 ALL_PINS = (pin_two_token, pin_brute_force, pin_closed_forms, pin_gqa, pin_page_invariance,
-            pin_split_merge, pin_fp8, pin_custom_mask)
+            pin_split_merge, pin_fp8, pin_custom_mask, pin_hnd_layout, pin_alibi, pin_soft_cap)
 
 
 # --------------------------------------------------------------------------
@@ -463,10 +555,10 @@ MUTANTS = {
     "sink_in_lse": ("lse[s] = (m + log(z)) / log(2.0);", "lse[s] = (m + log(denom)) / log(2.0);"),
     "sink_dropped": ("if (sinks) denom += exp((double)sinks[h] - m);", ""),
     "sink_scaled": ("denom += exp((double)sinks[h] - m);", "denom += exp(sm_scale * (double)sinks[h] - m);"),
-    "k_for_v": ("(((page * 2 + 1) * page_size + slot) * Hk + hk)", "(((page * 2 + 0) * page_size + slot) * Hk + hk)"),
+    "k_for_v": ("row_offset(kv_layout, page, 1, slot", "row_offset(kv_layout, page, 0, slot"),
     "last_page_off": ("return (pages - 1) * (int64_t)page_size + last_page_len[r];",
                       "return pages * (int64_t)page_size;"),
-    "scale_dropped": ("logit[t] = sm_scale * dot;", "logit[t] = dot;"),
+    "scale_dropped": ("            logit[t] = sm_scale * dot;", "            logit[t] = dot;"),
     "merge_natural_weights": ("double w = pow(2.0, lse_parts[i] - M);", "double w = exp(lse_parts[i] - M);"),
     "f16_bias": ("e - 25", "e - 24"),
     "e4m3_bias": ("ldexp((double)(8 + f), e - 10)", "ldexp((double)(8 + f), e - 9)"),
@@ -478,6 +570,12 @@ MUTANTS = {
     "mask_no_request_offset": ("for (int rr = 0; rr < r; ++rr)", "for (int rr = 0; rr < 0; ++rr)"),
     "mask_row_stride_q_len": ("mask_row += i * kv_len;", "mask_row += i * q_len;"),
     "mask_and_causal": ("} else if (causal && t > p) {", "} if (causal && t > p) {"),
+    "hnd_read_as_nhd": ("return (((page * 2 + kv) * Hk + hk) * (int64_t)page_size + slot) * (int64_t)d;",
+                        "return (((page * 2 + kv) * (int64_t)page_size + slot) * Hk + hk) * (int64_t)d;"),
+    "alibi_sign": ("(double)alibi_slopes[h] * (double)(t - p)", "(double)alibi_slopes[h] * (double)(p - t)"),
+    "alibi_top_left": ("(double)alibi_slopes[h] * (double)(t - p)", "(double)alibi_slopes[h] * (double)(t - i)"),
+    "soft_cap_outside_scale": ("soft_cap * tanh(sm_scale * dot / soft_cap)",
+                               "sm_scale * soft_cap * tanh(dot / soft_cap)"),
 }
 
 
@@ -500,6 +598,8 @@ def _mutant_fns(tmpdir, name, old, new):
         L.oracle_attention_rows_kv.argtypes = saved.oracle_attention_rows_kv.argtypes
         L.oracle_attention_rows_masked.restype = ctypes.c_int
         L.oracle_attention_rows_masked.argtypes = saved.oracle_attention_rows_masked.argtypes
+        L.oracle_attention_rows_ext.restype = ctypes.c_int
+        L.oracle_attention_rows_ext.argtypes = saved.oracle_attention_rows_ext.argtypes
         L.oracle_merge.argtypes = saved.oracle_merge.argtypes
         L.oracle_merge.restype = None
         try:
@@ -647,3 +747,19 @@ def test_custom_mask_with_window_and_sinks():
     zeros = [np.zeros_like(m) for m in ones]
     o_z, l_z = run_oracle(inp, "p", packed_mask=pack_mask(zeros))
     assert np.all(o_z == 0.0) and np.all(l_z == -np.inf)
+
+
+# --------------------------------------------------------------------------
+# NEXT variants: HND layout, ALiBi, logits soft cap
+# --------------------------------------------------------------------------
+
+def test_hnd_layout_pins():
+    pin_hnd_layout(oracle.attention_rows)
+
+
+def test_alibi_pins():
+    pin_alibi(oracle.attention_rows)
+
+
+def test_soft_cap_pins():
+    pin_soft_cap(oracle.attention_rows)
