@@ -155,6 +155,19 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p,
 pod_status pod_plan_set_decode_fp8(pod_handle h, float k_scale, float v_scale);
 
 /*
+ * pod_plan_set_kv_layout — page layout of each half's cache (FlashInfer
+ * guide, "快速上手", kv_layout: NHD or HND orders the k/v dimensions; the
+ * POD run takes one layout per half).
+ * p_layout / d_layout: 0 = NHD, pages [2, page_size, Hk, head_dim] (the
+ *   default); 1 = HND, pages [2, Hk, page_size, head_dim]. The page pool is
+ *   [num_pages, ...] either way and the page tables are unchanged.
+ * Takes effect from the next pod_run; the plan and its workspace are kept.
+ * With an FP8 decode cache the same two layouts apply to the one-byte codes.
+ * Errors: POD_ERR_INVALID_ARG (NULL handle, a layout other than 0 or 1).
+ */
+pod_status pod_plan_set_kv_layout(pod_handle h, int32_t p_layout, int32_t d_layout);
+
+/*
  * pod_plan_set_prefill_mask — a custom mask on the prefill half (POD
  * walkthrough, "run 参数详解", prefill parameters: custom_mask_p /
  * packed_custom_mask_p, packed with little bit order; a custom mask takes

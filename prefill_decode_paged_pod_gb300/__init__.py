@@ -30,7 +30,7 @@ __all__ = [
     "pod_workspace_size", "pod_bind_workspace", "pod_last_error", "pod_read_device_status",
     "pod_plan_table", "PodHandle", "LIB_PATH", "DEFAULT_WORKSPACE_BYTES",
     "pod_run_static_scratch", "pod_static_scratch_capacity", "pod_plan_set_decode_fp8",
-    "pod_plan_set_prefill_mask",
+    "pod_plan_set_prefill_mask", "pod_plan_set_kv_layout",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -85,6 +85,8 @@ def load_library(path: Optional[str] = None):
     lib.pod_static_scratch_capacity.argtypes = []
     lib.pod_plan_set_decode_fp8.restype = ctypes.c_int
     lib.pod_plan_set_decode_fp8.argtypes = [V, ctypes.c_float, ctypes.c_float]
+    lib.pod_plan_set_kv_layout.restype = ctypes.c_int
+    lib.pod_plan_set_kv_layout.argtypes = [V, I32, I32]
     lib.pod_plan_set_prefill_mask.restype = ctypes.c_int
     lib.pod_plan_set_prefill_mask.argtypes = [V, V, ctypes.c_int64]
     if path is None:
@@ -346,6 +348,18 @@ def pod_plan_set_prefill_mask(h: PodHandle, packed_mask):
     h.workspace_ptr = None
 
 
+_LAYOUTS = {"NHD": 0, "HND": 1, 0: 0, 1: 1}
+
+
+def pod_plan_set_kv_layout(h: PodHandle, p_layout="NHD", d_layout="NHD"):
+    """Page layout of each half's cache: "NHD" [pages, 2, ps, Hk, d] or
+    "HND" [pages, 2, Hk, ps, d]."""
+    if p_layout not in _LAYOUTS or d_layout not in _LAYOUTS:
+        raise PodError(1, f"unknown kv layout {p_layout!r} / {d_layout!r}")
+    _check(load_library().pod_plan_set_kv_layout(ctypes.c_void_p(h.ptr), _LAYOUTS[p_layout],
+                                                 _LAYOUTS[d_layout]))
+
+
 def _check_mask_device(h: PodHandle):
     m = h.p_mask
     if m is not None and h.p_rows and not getattr(m, "is_cuda", False):
@@ -362,6 +376,9 @@ def plan_inputs(inp, workspace=None, num_sms=0, stream=None) -> PodHandle:
     import torch
     if inp.d.rows and getattr(inp.d.kv, "dtype", None) == torch.float8_e4m3fn:
         pod_plan_set_decode_fp8(h, inp.k_scale, inp.v_scale)
+    lp, ld = getattr(inp.p, "kv_layout", "NHD"), getattr(inp.d, "kv_layout", "NHD")
+    if (lp, ld) != ("NHD", "NHD"):
+        pod_plan_set_kv_layout(h, lp, ld)
     if mask is not None:
         t = torch.from_numpy(np.ascontiguousarray(mask, dtype=np.uint8))
         if torch.cuda.is_available():

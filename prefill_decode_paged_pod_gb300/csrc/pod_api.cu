@@ -25,6 +25,8 @@ struct pod_plan_s {
   // decode cache stored as FP8 E4M3 codes with per-tensor K and V scales
   int d_fp8 = 0;
   float k_scale = 1.f, v_scale = 1.f;
+  // page layout of each half's cache: 0 = NHD, 1 = HND
+  int p_layout = 0, d_layout = 0;
   // custom prefill mask: caller-owned device bytes read by every run
   const void* p_mask = nullptr;
   int64_t p_mask_bytes = 0;
@@ -111,18 +113,21 @@ pod_status encode_q(CUtensorMap* m, const void* ptr, int rows, int H, int d, int
   return POD_OK;
 }
 
-// Paged cache viewed as [pages][2][ps][Hk][d]; a box holds `kbx` keys:
+// Paged cache viewed as [pages][2][ps][Hk][d] (dims listed the same way for
+// an HND cache, [pages][2][Hk][ps][d] in memory, with its strides); a box holds `kbx` keys:
 // 64 elements x 1 head x kbx slots x 1 x 1 page when ps >= 8 (kbx <= ps), or
 // 64 x 1 x ps slots x 1 x (kbx / ps) pages when ps < 8.
 pod_status encode_kv(CUtensorMap* m, const void* ptr, int num_pages, int ps, int Hk, int d,
-                     int kbx, int dtype) {
+                     int kbx, int dtype, int hnd) {
   auto fn = encode_fn();
   if (!fn) return set_err(POD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   if ((reinterpret_cast<uintptr_t>(ptr) & 15u) != 0)
     return set_err(POD_ERR_INVALID_ARG, "kv caches must be 16-byte aligned");
   cuuint64_t dims[5] = {(cuuint64_t)d, (cuuint64_t)Hk, (cuuint64_t)ps, 2, (cuuint64_t)num_pages};
   cuuint64_t row = (cuuint64_t)d * 2;
-  cuuint64_t strides[4] = {row, row * Hk, row * Hk * ps, row * Hk * ps * 2};
+  // the same logical dims for both layouts; HND swaps the head and slot strides
+  cuuint64_t strides[4] = {hnd ? row * ps : row, hnd ? row : row * Hk, row * Hk * ps,
+                           row * Hk * ps * 2};
   cuuint32_t box[5] = {64, 1, (cuuint32_t)(ps >= 8 ? kbx : ps), 1,
                        (cuuint32_t)(ps >= 8 ? 1 : kbx / ps)};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
@@ -138,9 +143,10 @@ pod_status encode_kv(CUtensorMap* m, const void* ptr, int num_pages, int ps, int
 // both 64-element halves of head_dim, landing in shared memory as
 // [half][key][64] (each half a run of kbx 128-byte rows). Dims, innermost
 // first: page_size >= 8: [64][ps][d/64][Hk][2 * pages] (K/V and page merged:
-// coordinate 2 * page + kv); page_size 1: [64][pages][d/64][Hk][2].
+// coordinate 2 * page + kv); page_size 1: [64][pages][d/64][Hk][2] (an HND
+// cache has the same bytes there). HND swaps the slot and head strides.
 pod_status encode_kv_decode(CUtensorMap* m, const void* ptr, int num_pages, int ps, int Hk, int d,
-                            int kbx, int dtype) {
+                            int kbx, int dtype, int hnd) {
   auto fn = encode_fn();
   if (!fn) return set_err(POD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   if ((reinterpret_cast<uintptr_t>(ptr) & 15u) != 0)
@@ -149,7 +155,7 @@ pod_status encode_kv_decode(CUtensorMap* m, const void* ptr, int num_pages, int 
   cuuint64_t dims[5], strides[4];
   if (ps >= 8) {
     cuuint64_t d5[5] = {64, (cuuint64_t)ps, nh, (cuuint64_t)Hk, 2 * (cuuint64_t)num_pages};
-    cuuint64_t s4[4] = {row * Hk, 128, row, row * Hk * ps};
+    cuuint64_t s4[4] = {hnd ? row : row * Hk, 128, hnd ? row * ps : row, row * Hk * ps};
     memcpy(dims, d5, sizeof(d5));
     memcpy(strides, s4, sizeof(s4));
   } else {
@@ -175,7 +181,7 @@ pod_status encode_kv_decode(CUtensorMap* m, const void* ptr, int num_pages, int 
 // [128][ps][Hk][2 * pages] (coordinate 2 * page + kv); page_size 1:
 // [128][pages][Hk][2].
 pod_status encode_kv_decode_fp8(CUtensorMap* m, const void* ptr, int num_pages, int ps, int Hk,
-                                int d, int kbx) {
+                                int d, int kbx, int hnd) {
   auto fn = encode_fn();
   if (!fn) return set_err(POD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   if ((reinterpret_cast<uintptr_t>(ptr) & 15u) != 0)
@@ -184,7 +190,7 @@ pod_status encode_kv_decode_fp8(CUtensorMap* m, const void* ptr, int num_pages, 
   cuuint64_t dims[4], strides[3];
   if (ps >= 8) {
     cuuint64_t d4[4] = {(cuuint64_t)d, (cuuint64_t)ps, (cuuint64_t)Hk, 2 * (cuuint64_t)num_pages};
-    cuuint64_t s3[3] = {row * Hk, row, row * Hk * ps};
+    cuuint64_t s3[3] = {hnd ? row : row * Hk, hnd ? row * ps : row, row * Hk * ps};
     memcpy(dims, d4, sizeof(d4));
     memcpy(strides, s3, sizeof(s3));
   } else {
@@ -313,11 +319,13 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
     if (h->tm_ptr[i] == ptrs[i]) continue;
     pod_status st = (i % 2 == 0)
         ? encode_q(&h->tm[i], ptrs[i], hh.rows, P.H, P.d, P.G, pre ? P.tq : P.tu, P.dtype)
-        : pre ? encode_kv(&h->tm[i], ptrs[i], hh.num_pages, P.ps, P.Hk, P.d, P.p_tma, P.dtype)
+        : pre ? encode_kv(&h->tm[i], ptrs[i], hh.num_pages, P.ps, P.Hk, P.d, P.p_tma, P.dtype,
+                          h->p_layout)
               : h->d_fp8
-                    ? encode_kv_decode_fp8(&h->tm[i], ptrs[i], hh.num_pages, P.ps, P.Hk, P.d, P.d_tma)
+                    ? encode_kv_decode_fp8(&h->tm[i], ptrs[i], hh.num_pages, P.ps, P.Hk, P.d, P.d_tma,
+                                           h->d_layout)
                     : encode_kv_decode(&h->tm[i], ptrs[i], hh.num_pages, P.ps, P.Hk, P.d, P.d_tma,
-                                       P.dtype);
+                                       P.dtype, h->d_layout);
     if (st != POD_OK) return st;
     h->tm_ptr[i] = ptrs[i];
   }
@@ -344,6 +352,8 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
   for (int s = 0; s < 31; ++s)
     if ((1 << s) == P.ps) K.ps_shift = s;
   K.causal = P.causal; K.window_left = P.window_left; K.has_sinks = P.has_sinks;
+  K.p_hnd = h->p_layout;
+  K.d_hnd = h->d_layout;
   K.scale_log2 = P.scale_log2;
   K.d_fp8 = h->d_fp8;
   K.d_scale_log2 = P.scale_log2 * h->k_scale;
@@ -393,6 +403,18 @@ pod_status pod_plan_set_decode_fp8(pod_handle h, float k_scale, float v_scale) {
   h->k_scale = k_scale;
   h->v_scale = v_scale;
   h->tm_ptr[3] = nullptr;  // the decode cache's tensor map changes format
+  return POD_OK;
+}
+
+pod_status pod_plan_set_kv_layout(pod_handle h, int32_t p_layout, int32_t d_layout) {
+  g_err.clear();
+  if (!h) return set_err(POD_ERR_INVALID_ARG, "handle is NULL");
+  if ((p_layout != 0 && p_layout != 1) || (d_layout != 0 && d_layout != 1))
+    return set_err(POD_ERR_INVALID_ARG, "layouts must be 0 (NHD) or 1 (HND)");
+  if (p_layout != h->p_layout) h->tm_ptr[1] = nullptr;  // cache maps are re-encoded
+  if (d_layout != h->d_layout) h->tm_ptr[3] = nullptr;
+  h->p_layout = p_layout;
+  h->d_layout = d_layout;
   return POD_OK;
 }
 

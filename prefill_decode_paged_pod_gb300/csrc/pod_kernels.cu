@@ -307,7 +307,9 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
               const bool valid = t < hi;
               const int tt = valid ? t : kb;
               const int slot = P.ps_shift >= 0 ? (tt & (P.ps - 1)) : (tt % P.ps);
-              const T* src = kvg + (((size_t)pages[i] * 2 * P.ps + slot) * P.Hk + g) * D + c * 8;
+              const T* src = kvg + (P.p_hnd
+                  ? (((size_t)pages[i] * 2 * P.Hk + g) * P.ps + slot) * D + c * 8
+                  : (((size_t)pages[i] * 2 * P.ps + slot) * P.Hk + g) * D + c * 8);
               cp_async16(dst_base + (c >> 3) * L::KVBLK + sw128_off(key, c & 7),
                          is_v ? src + vstride : src, valid ? 16u : 0u);
             }
@@ -754,7 +756,9 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
             const bool valid = t >= k0 && t < k1;
             const int tt = valid ? t : k0;
             const int slot = P.ps_shift >= 0 ? (tt & (P.ps - 1)) : (tt % P.ps);
-            const uint8_t* src = kv8 + (((size_t)pages8[i] * 2 * P.ps + slot) * P.Hk + g) * D + c * 16;
+            const uint8_t* src = kv8 + (P.d_hnd
+                ? (((size_t)pages8[i] * 2 * P.Hk + g) * P.ps + slot) * D + c * 16
+                : (((size_t)pages8[i] * 2 * P.ps + slot) * P.Hk + g) * D + c * 16);
             const uint32_t off = (uint32_t)key * 128u + (uint32_t)((c ^ (key & 7)) << 4);
             cp_async16(k8 + off, src, valid ? 16u : 0u);
             cp_async16(k8 + L::F8_HALF + off, src + vstride8, valid ? 16u : 0u);
@@ -783,7 +787,9 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
           const bool valid = t >= k0 && t < k1;
           const int tt = valid ? t : k0;
           const int slot = P.ps_shift >= 0 ? (tt & (P.ps - 1)) : (tt % P.ps);
-          const T* src = kvg + (((size_t)pages[i] * 2 * P.ps + slot) * P.Hk + g) * D + c * 8;
+          const T* src = kvg + (P.d_hnd
+              ? (((size_t)pages[i] * 2 * P.Hk + g) * P.ps + slot) * D + c * 8
+              : (((size_t)pages[i] * 2 * P.ps + slot) * P.Hk + g) * D + c * 8);
           const uint32_t off = (c >> 3) * L::KDH + sw128_off(key, c & 7);
           cp_async16(sk + off, src, valid ? 16u : 0u);
           cp_async16(sv + off, src + vstride, valid ? 16u : 0u);

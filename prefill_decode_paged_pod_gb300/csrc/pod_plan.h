@@ -64,6 +64,10 @@ struct PodParams {
   int p_num_pages, d_num_pages;
   int tq, tu;                // tokens per prefill tile / per decode unit
   int H, Hk, G, d, ps, ps_shift, causal, window_left, has_sinks;
+  // page layout of each half's cache: 0 = NHD pages [2, ps, Hk, d],
+  // 1 = HND pages [2, Hk, ps, d] (only the cp.async gathers read it; the
+  // tensor maps carry the layout in their strides)
+  int p_hnd, d_hnd;
   float scale_log2;          // sm_scale * log2(e)
   // decode cache in FP8 E4M3 (head_dim 128): d_scale_log2 = scale_log2 * k_scale,
   // outputs multiplied by v_scale

@@ -374,3 +374,22 @@ def test_custom_mask_host_checks(lib):
     # diagonals 62, 94, 100; under the mask every tile reads all 100 keys
     assert causal_hi == [62, 94, 100] and masked_hi == [100]
     assert h.workspace_ptr is None and pod.plan_summary(h)["p_mask"] == 1
+
+
+def test_kv_layout_switch_host_checks(lib):
+    """pod_plan_set_kv_layout takes 0 (NHD) or 1 (HND) per half, leaves the
+    plan as it is (the page tables do not depend on the layout) and refuses
+    other codes."""
+    inp = make_custom("l", torch.bfloat16, 16, 2, 128, 16, True, -1, [40], [90], [1, 2], [60, 70],
+                      seed=2)
+    h = plan_host(inp, num_sms=8)
+    before = [pod.pod_plan_table(h, w).copy() for w in range(11)]
+    pod.pod_plan_set_kv_layout(h, "HND", "NHD")
+    pod.pod_plan_set_kv_layout(h, 1, 1)
+    assert all(np.array_equal(b, pod.pod_plan_table(h, w)) for w, b in enumerate(before))
+    L = pod.load_library()
+    for p_l, d_l in ((2, 0), (0, -1)):
+        assert L.pod_plan_set_kv_layout(ctypes.c_void_p(h.ptr), p_l, d_l) == 1
+    assert L.pod_plan_set_kv_layout(None, 0, 0) == 1
+    with pytest.raises(pod.PodError):
+        pod.pod_plan_set_kv_layout(h, "NDH", "NHD")

@@ -371,3 +371,44 @@ def test_custom_prefill_mask(case):
     # the first row of every request allows no key: out = 0, lse = -inf
     first = inp.p.q_indptr[:-1][np.diff(inp.p.q_indptr) > 2]
     assert np.all(op[first] == 0.0) and np.all(np.isneginf(lp[first]))
+
+
+# ------------------------------------------------------------- HND page layout
+HND_CASES = [
+    # name, dtype, H, Hk, d, ps, causal, window, sinks, p_q, p_kv, d_q, d_kv, layouts (p, d), fp8
+    ("h16", torch.bfloat16, 16, 2, 128, 16, True, -1, True, [100, 37], [300, 37], [1, 4], [500, 900],
+     ("HND", "HND"), False),
+    ("h4", torch.float16, 8, 2, 64, 4, True, 40, False, [70], [150], [1, 2, 1], [33, 64, 90],
+     ("HND", "HND"), False),
+    ("h3", torch.bfloat16, 8, 8, 128, 3, False, -1, False, [20], [50], [3], [77], ("HND", "HND"), False),
+    ("hmix", torch.bfloat16, 32, 8, 128, 16, True, -1, False, [64], [64], [1, 1], [129, 700],
+     ("NHD", "HND"), False),
+    ("h1", torch.float16, 4, 2, 64, 1, True, -1, False, [64], [64], [1, 1], [17, 29], ("HND", "HND"), False),
+    ("h1c", torch.bfloat16, 16, 2, 128, 1, True, -1, False, [80], [200], [2, 1], [300, 129],
+     ("HND", "HND"), False),
+    ("f8h16", torch.bfloat16, 16, 2, 128, 16, True, -1, True, [33], [33], [1, 4, 2], [700, 300, 64],
+     ("HND", "HND"), True),
+    ("f8h4", torch.bfloat16, 16, 2, 128, 4, True, -1, False, [], [], [1, 4], [200, 51],
+     ("NHD", "HND"), True),
+]
+
+
+@pytest.mark.parametrize("case", HND_CASES, ids=[c[0] for c in HND_CASES])
+def test_hnd_layout(case):
+    """Caches stored HND ([pages, 2, Hk, ps, d]) on either half: TMA page boxes
+    (page_size 16, and contiguous page_size 1 where both layouts are the
+    same bytes) and the cp.async gather (page sizes 1, 3 and 4), 16-bit and
+    FP8 decode caches."""
+    from pod_workloads import with_fp8_decode_cache, with_kv_layout
+    name, dt, H, Hk, d, ps, causal, window, sinks, pq, pkv, dq, dkv, (lp, ld), fp8 = case
+    inp = make_custom(name, dt, H, Hk, d, ps, causal, window, pq, pkv, dq, dkv, seed=31,
+                      sinks=sinks, pages="contig" if name == "h1c" else "perm")
+    if lp == "HND":
+        inp = with_kv_layout(inp, "HND", "p")
+    if ld == "HND":
+        inp = with_kv_layout(inp, "HND", "d")
+    if fp8:
+        inp = with_fp8_decode_cache(inp)
+    (op, lp_, od, ld_), h, ws = run_pod(inp)
+    compare_half(inp, "p", op, lp_, tag=name + " ")
+    compare_half(inp, "d", od, ld_, tag=name + " ")
