@@ -90,6 +90,7 @@ def lib():
                 P, P, P, P, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double, P,
+                ctypes.c_int, ctypes.c_double, ctypes.c_double,
                 P, P, ctypes.c_int64, P, P, P, P, P, P, ctypes.c_int]
             _lib.oracle_attention_rows_kv.restype = ctypes.c_int
             _lib.oracle_attention_rows_kv.argtypes = [
@@ -143,14 +144,16 @@ def attention_rows(q, kv, q_indptr, kv_indptr, kv_indices, last_page_len,
                    sel_token=None, sel_head=None, key_lo=None, key_hi=None,
                    nthreads: Optional[int] = None, dtype: Optional[int] = None,
                    k_scale: float = 1.0, v_scale: float = 1.0, packed_mask=None,
-                   kv_layout: int = 0, soft_cap: float = 0.0, alibi_slopes=None):
+                   kv_layout: int = 0, soft_cap: float = 0.0, alibi_slopes=None,
+                   rope: bool = False, rope_scale: float = 1.0, rope_theta: float = 1e4):
     """fp64 outputs for selected (token, head) pairs; all pairs if no selection.
     An E4M3 ``kv`` is read as codes times ``k_scale`` (K) / ``v_scale`` (V).
     ``packed_mask`` (uint8, little bit order) is a custom mask over every
     request's [q_len, kv_len] matrix; it replaces the causal rule.
     ``kv_layout`` 0 = NHD pages [2, ps, Hk, d], 1 = HND [2, Hk, ps, d];
     ``soft_cap`` > 0 caps the scaled logits (cap * tanh(x / cap));
-    ``alibi_slopes`` [H] adds slope * (t - p) to each logit.
+    ``alibi_slopes`` [H] adds slope * (t - p) to each logit;
+    ``rope`` rotates q (at p) and keys (at t) by the LLaMA rotary embedding.
 
     Returns (out [n, d] float64, lse [n] float64, status int).
     """
@@ -203,6 +206,7 @@ def attention_rows(q, kv, q_indptr, kv_indptr, kv_indices, last_page_len,
         _ptr(q_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(last_page_len),
         batch, num_pages, H, int(num_kv_heads), d, int(page_size), int(kv_layout),
         int(bool(causal)), int(window_left), float(sm_scale), float(soft_cap), _ptr(al),
+        int(bool(rope)), float(rope_scale), float(rope_theta),
         _ptr(sk), _ptr(pm), n, _ptr(tok), _ptr(hd), _ptr(key_lo), _ptr(key_hi),
         _ptr(out), _ptr(lse), int(nthreads))
     return out[:n], lse[:n], int(st)

@@ -40,6 +40,13 @@
  *  - Logits soft cap (same section, logits_soft_cap: cap * tanh(x / cap), 0
  *    = off): x is the scaled logit sm_scale * q.k. With both, the ALiBi bias
  *    is added after the cap (a reading: the pages do not combine them).
+ *  - ROPE_LLAMA (same section, pos_encoding_mode, rope_scale default 1,
+ *    rope_theta default 1e4): q and each key are rotated before the dot
+ *    product by the rotary embedding of their positions (p for the query,
+ *    t for key t; values are not rotated). Reading taken here: the LLaMA
+ *    half-split pairing, element j with j + d/2, turned by the angle
+ *    (pos / rope_scale) * rope_theta^(-2j/d) (rotary position embedding
+ *    with position interpolation by rope_scale).
  *  - Custom mask (POD walkthrough, "run 参数详解", prefill parameters
  *    custom_mask_p / packed_custom_mask_p, packed with little bit order; a
  *    custom mask takes precedence over causal): one boolean per (query row,
@@ -66,7 +73,9 @@
  * all-ones masks against the causal and non-causal rules; for HND pages,
  * bit-identity with NHD and brute force over an HND gather; for ALiBi, brute
  * force, the geometric-series lse of q = 0 and slope 0; for the soft cap,
- * brute force, two saturated keys and a cap far above every logit.
+ * brute force, two saturated keys and a cap far above every logit; for
+ * ROPE_LLAMA, closed-form logits cos/sin((p - t) f) of unit vectors, a
+ * request shifted five positions later, and position 0.
  */
 #include <math.h>
 #include <stdint.h>
@@ -158,6 +167,19 @@ static int64_t row_offset(int kv_layout, int64_t page, int kv, int64_t slot, int
     return (((page * 2 + kv) * (int64_t)page_size + slot) * Hk + hk) * (int64_t)d;
 }
 
+/* Rotary embedding of x[0..d) at position pos, pairs (j, j + d/2). */
+static void rope_rotate(double* x, int d, double pos, double rope_scale, double rope_theta)
+{
+    int half = d / 2;
+    for (int j = 0; j < half; ++j) {
+        double ang = (pos / rope_scale) * pow(rope_theta, -2.0 * (double)j / (double)d);
+        double c = cos(ang), sn = sin(ang);
+        double a = x[j], b = x[j + half];
+        x[j] = a * c - b * sn;
+        x[j + half] = b * c + a * sn;
+    }
+}
+
 /* Bit `pos` of a little-bit-order packed array. */
 static int mask_bit(const uint8_t* packed, int64_t pos)
 {
@@ -191,6 +213,7 @@ int oracle_attention_rows_ext(const uint16_t* q, const void* kv, int dtype,
                               int H, int Hk, int d, int page_size, int kv_layout,
                               int causal, int window_left, double sm_scale,
                               double soft_cap, const float* alibi_slopes,
+                              int rope, double rope_scale, double rope_theta,
                               const float* sinks, const uint8_t* packed_mask,
                               int64_t n_sel, const int64_t* sel_token, const int32_t* sel_head,
                               const int64_t* key_lo, const int64_t* key_hi,
@@ -198,6 +221,7 @@ int oracle_attention_rows_ext(const uint16_t* q, const void* kv, int dtype,
 {
     if (H <= 0 || Hk <= 0 || H % Hk != 0 || d <= 0 || page_size <= 0) return ORACLE_BAD_ARG;
     if (kv_layout != 0 && kv_layout != 1) return ORACLE_BAD_ARG;
+    if (rope && (d % 2 != 0 || !(rope_scale > 0.0) || !(rope_theta > 0.0))) return ORACLE_BAD_ARG;
     int group = H / Hk;
     int status = ORACLE_OK;
     (void)nthreads;
@@ -230,10 +254,12 @@ int oracle_attention_rows_ext(const uint16_t* q, const void* kv, int dtype,
         }
 
         double* qv = (double*)malloc(sizeof(double) * (size_t)d);
+        double* kr = (double*)malloc(sizeof(double) * (size_t)d);
         double* logit = (double*)malloc(sizeof(double) * (size_t)(kv_len > 0 ? kv_len : 1));
         char* allowed = (char*)malloc((size_t)(kv_len > 0 ? kv_len : 1));
         for (int e = 0; e < d; ++e)
             qv[e] = widen(q[(token * H + h) * (int64_t)d + e], dtype);
+        if (rope) rope_rotate(qv, d, (double)p, rope_scale, rope_theta);
 
         /* logits of the allowed keys */
         double m = -INFINITY;
@@ -259,8 +285,10 @@ int oracle_attention_rows_ext(const uint16_t* q, const void* kv, int dtype,
                 continue;
             }
             int64_t k0 = row_offset(kv_layout, page, 0, slot, hk, page_size, Hk, d);
+            for (int e = 0; e < d; ++e) kr[e] = kv_elem(kv, k0 + e, dtype, kv_fp8, k_scale);
+            if (rope) rope_rotate(kr, d, (double)t, rope_scale, rope_theta);
             double dot = 0.0;
-            for (int e = 0; e < d; ++e) dot += qv[e] * kv_elem(kv, k0 + e, dtype, kv_fp8, k_scale);
+            for (int e = 0; e < d; ++e) dot += qv[e] * kr[e];
             if (soft_cap > 0.0)
                 logit[t] = soft_cap * tanh(sm_scale * dot / soft_cap);
             else
@@ -275,7 +303,7 @@ int oracle_attention_rows_ext(const uint16_t* q, const void* kv, int dtype,
 #pragma omp atomic write
                 status = ORACLE_EMPTY_ROW;
             }
-            free(qv); free(logit); free(allowed);
+            free(qv); free(kr); free(logit); free(allowed);
             continue;
         }
         /* explicit softmax with an optional sink logit in the denominator */
@@ -293,7 +321,7 @@ int oracle_attention_rows_ext(const uint16_t* q, const void* kv, int dtype,
             for (int e = 0; e < d; ++e) o[e] += w * kv_elem(kv, v0 + e, dtype, kv_fp8, v_scale);
         }
         lse[s] = (m + log(z)) / log(2.0);
-        free(qv); free(logit); free(allowed);
+        free(qv); free(kr); free(logit); free(allowed);
     }
     return status;
 }
@@ -314,7 +342,8 @@ int oracle_attention_rows_masked(const uint16_t* q, const void* kv, int dtype,
     return oracle_attention_rows_ext(q, kv, dtype, kv_fp8, k_scale, v_scale, q_indptr, kv_indptr,
                                      kv_indices, last_page_len, batch, num_pages, H, Hk, d,
                                      page_size, 0, causal, window_left, sm_scale, 0.0, NULL,
-                                     sinks, packed_mask, n_sel, sel_token, sel_head, key_lo,
+                                     0, 1.0, 1e4, sinks, packed_mask, n_sel, sel_token, sel_head,
+                                     key_lo,
                                      key_hi, out, lse, nthreads);
 }
 

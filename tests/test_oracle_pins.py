@@ -468,8 +468,75 @@ def pin_soft_cap(fn, seeds=range(6)):
     assert abs(lse[0] - (c0 + math.log1p(math.exp(c1 - c0))) / math.log(2.0)) < 1e-12
 
 
+def _set_row(h, r, t, kind, vec):
+    """Write key/value vector of request r, position t (all kv heads), NHD."""
+    ps = h.kv.shape[2]
+    page = int(h.kv_indices[int(h.kv_indptr[r]) + t // ps])
+    h.kv[page, kind, t % ps, :, :] = torch.as_tensor(vec, dtype=h.kv.dtype)
+
+
+def _rope_closed_case(q, k, n, sm_scale=1.0):
+    """One request, one query at p = n - 1, n keys all equal to k, value row
+    t = (t, 1, ...); H = Hk = 1, d = len(q)."""
+    d = len(q)
+    inp = make_custom("rope", torch.float16, 1, 1, d, 4, True, -1, [], [], [1], [n], seed=0,
+                      sm_scale=sm_scale)
+    h = inp.d
+    h.q[0, 0] = torch.tensor(q, dtype=h.q.dtype)
+    for t in range(n):
+        _set_row(h, 0, t, 0, k)
+        v = np.zeros(d)
+        v[0], v[1] = t, 1.0
+        _set_row(h, 0, t, 1, v)
+    return inp
+
+
+def pin_rope(fn):
+    """ROPE_LLAMA: pins that do not restate the rotation.
+    - d = 4, q = k = e1 (pair 1: elements 1 and 3): the logit of key t is
+      cos((p - t) * theta^(-1/2) / rope_scale); q = k = e0 gives
+      cos((p - t) / rope_scale); q = e0, k = e2 gives sin((p - t) / rope_scale)
+      (fixes pairing, frequency exponent, scale and direction);
+    - a query and its keys moved 5 positions later give the same output
+      (only relative positions matter);
+    - at position 0 (kv_len = 1) the rotation is the identity."""
+    rs, th, n = 2.0, 100.0, 6
+    e = np.eye(4)
+    for qv, kv_, f in ((e[1], e[1], lambda x: math.cos(x * th ** -0.5 / rs)),
+                       (e[0], e[0], lambda x: math.cos(x / rs)),
+                       (e[0], e[2], lambda x: math.sin(x / rs))):
+        inp = _rope_closed_case(qv, kv_, n)
+        out, lse = run_oracle(inp, "d", fn=fn, rope=True, rope_scale=rs, rope_theta=th)
+        s_t = np.array([f(n - 1 - t) for t in range(n)])
+        w = np.exp(s_t - s_t.max())
+        w /= w.sum()
+        assert abs(out[0, 0, 0] - float(w @ np.arange(n))) < 1e-12
+        assert abs(out[0, 0, 1] - 1.0) < 1e-12
+        assert abs(lse[0, 0] - math.log2(np.exp(s_t).sum())) < 1e-12
+    # shift: request 1 = request 0 moved 5 positions later, a window hides the rest
+    inp = make_custom("ropeshift", torch.float16, 4, 2, 8, 4, True, 6, [], [], [1, 1], [7, 12],
+                      seed=5)
+    h = inp.d
+    h.q[1] = h.q[0]
+    for t in range(7):
+        for kind in (0, 1):
+            ps = inp.page_size
+            src = int(h.kv_indices[int(h.kv_indptr[0]) + t // ps])
+            _set_row(h, 1, t + 5, kind, h.kv[src, kind, t % ps].clone())
+    out, lse = run_oracle(inp, "d", fn=fn, rope=True, rope_scale=1.0, rope_theta=1e4)
+    assert np.allclose(out[1], out[0], atol=1e-12, rtol=0) and np.allclose(lse[1], lse[0], atol=1e-12)
+    plain_o, _ = run_oracle(inp, "d", fn=fn)
+    assert not np.allclose(plain_o[0], out[0], atol=1e-6)
+    # position 0
+    inp = make_custom("rope0", torch.float16, 2, 1, 8, 4, True, -1, [], [], [1], [1], seed=6)
+    o_r, l_r = run_oracle(inp, "d", fn=fn, rope=True, rope_scale=3.0, rope_theta=50.0)
+    o_p, l_p = run_oracle(inp, "d", fn=fn)
+    assert np.allclose(o_r, o_p, atol=1e-14) and np.allclose(l_r, l_p, atol=1e-14)
+
+
 ALL_PINS = (pin_two_token, pin_brute_force, pin_closed_forms, pin_gqa, pin_page_invariance,
-            pin_split_merge, pin_fp8, pin_custom_mask, pin_hnd_layout, pin_alibi, pin_soft_cap)
+            pin_split_merge, pin_fp8, pin_custom_mask, pin_hnd_layout, pin_alibi, pin_soft_cap,
+            pin_rope)
 
 
 # --------------------------------------------------------------------------
@@ -576,6 +643,13 @@ MUTANTS = {
     "alibi_top_left": ("(double)alibi_slopes[h] * (double)(t - p)", "(double)alibi_slopes[h] * (double)(t - i)"),
     "soft_cap_outside_scale": ("soft_cap * tanh(sm_scale * dot / soft_cap)",
                                "sm_scale * soft_cap * tanh(dot / soft_cap)"),
+    "rope_interleaved_pairs": ("double a = x[j], b = x[j + half];\n        x[j] = a * c - b * sn;\n        x[j + half] = b * c + a * sn;",
+                               "double a = x[2 * j], b = x[2 * j + 1];\n        x[2 * j] = a * c - b * sn;\n        x[2 * j + 1] = b * c + a * sn;"),
+    "rope_freq_exponent": ("-2.0 * (double)j / (double)d", "-1.0 * (double)j / (double)d"),
+    "rope_scale_multiplies": ("(pos / rope_scale)", "(pos * rope_scale)"),
+    "rope_query_at_row_index": ("rope_rotate(qv, d, (double)p,", "rope_rotate(qv, d, (double)i,"),
+    "rope_reverse_direction": ("x[j] = a * c - b * sn;\n        x[j + half] = b * c + a * sn;",
+                               "x[j] = a * c + b * sn;\n        x[j + half] = b * c - a * sn;"),
 }
 
 
@@ -763,3 +837,7 @@ def test_alibi_pins():
 
 def test_soft_cap_pins():
     pin_soft_cap(oracle.attention_rows)
+
+
+def test_rope_pins():
+    pin_rope(oracle.attention_rows)
