@@ -149,10 +149,29 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p,
  * outputs (split partials included) by v_scale; the decode LSE is that of the
  * scaled logits. q_d and out_d keep the plan's 16-bit dtype; the prefill half
  * is unchanged. May be called again to change the scales. Errors:
- * POD_ERR_UNSUPPORTED unless head_dim is 128; POD_ERR_INVALID_ARG for a NULL
- * handle or scales that are not finite and positive.
+ * POD_ERR_UNSUPPORTED unless head_dim is 128, or with a logits transform set
+ * (pod_plan_set_logits_transform); POD_ERR_INVALID_ARG for a NULL handle or
+ * scales that are not finite and positive.
  */
 pod_status pod_plan_set_decode_fp8(pod_handle h, float k_scale, float v_scale);
+
+/*
+ * pod_plan_set_logits_transform — a transform of every logit, applied by
+ * both halves before masking and softmax (FlashInfer guide, "快速上手":
+ * logits_soft_cap and pos_encoding_mode ALIBI; the POD plan keeps them).
+ * logits_soft_cap > 0: the scaled logit x = sm_scale * q.k becomes
+ *   cap * tanh(x / cap); 0 turns it off.
+ * alibi_slopes: DEVICE pointer to H fp32 slopes (caller-owned, read by every
+ *   later pod_run) or NULL: the logit of key t for a query at bottom-right
+ *   position p gains slope[head] * (t - p).
+ * Sinks stay plain logits; the LSE is that of the transformed logits.
+ * Takes effect from the next pod_run; the plan and workspace are kept.
+ * Errors: POD_ERR_INVALID_ARG (NULL handle, negative or non-finite cap),
+ * POD_ERR_UNSUPPORTED (both at once, or with an FP8 decode cache; pod_run
+ * also refuses slopes that are not device memory).
+ */
+pod_status pod_plan_set_logits_transform(pod_handle h, float logits_soft_cap,
+                                         const float* alibi_slopes);
 
 /*
  * pod_plan_set_kv_layout — page layout of each half's cache (FlashInfer

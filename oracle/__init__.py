@@ -222,6 +222,10 @@ def attention_half(inp, half: str, sel_token=None, sel_head=None, nthreads=None,
         scales["packed_mask"] = h.packed_mask
     if getattr(h, "kv_layout", "NHD") == "HND" and "kv_layout" not in kw:
         scales["kv_layout"] = 1
+    if getattr(inp, "soft_cap", 0.0) and "soft_cap" not in kw:
+        scales["soft_cap"] = float(inp.soft_cap)
+    if getattr(inp, "alibi", None) is not None and "alibi_slopes" not in kw:
+        scales["alibi_slopes"] = inp.alibi
     return attention_rows(h.q, h.kv, h.q_indptr, h.kv_indptr, h.kv_indices, h.last_page_len,
                           inp.num_qo_heads, inp.num_kv_heads, inp.head_dim, inp.page_size,
                           inp.causal, inp.window_left, inp.sm_scale, sinks=inp.sinks,

@@ -81,6 +81,9 @@ class PODInputs:
     # decode cache in FP8 E4M3: d.kv holds the codes; K = code * k_scale, V = code * v_scale
     k_scale: float = 1.0
     v_scale: float = 1.0
+    # logits transform of both halves: soft cap (> 0) or per-head ALiBi slopes [H] fp32
+    soft_cap: float = 0.0
+    alibi: Optional[torch.Tensor] = None
 
 
 def page_table_from_lens(kv_lens: Sequence[int], page_size: int):

@@ -30,7 +30,7 @@ __all__ = [
     "pod_workspace_size", "pod_bind_workspace", "pod_last_error", "pod_read_device_status",
     "pod_plan_table", "PodHandle", "LIB_PATH", "DEFAULT_WORKSPACE_BYTES",
     "pod_run_static_scratch", "pod_static_scratch_capacity", "pod_plan_set_decode_fp8",
-    "pod_plan_set_prefill_mask", "pod_plan_set_kv_layout",
+    "pod_plan_set_prefill_mask", "pod_plan_set_kv_layout", "pod_plan_set_logits_transform",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -85,6 +85,8 @@ def load_library(path: Optional[str] = None):
     lib.pod_static_scratch_capacity.argtypes = []
     lib.pod_plan_set_decode_fp8.restype = ctypes.c_int
     lib.pod_plan_set_decode_fp8.argtypes = [V, ctypes.c_float, ctypes.c_float]
+    lib.pod_plan_set_logits_transform.restype = ctypes.c_int
+    lib.pod_plan_set_logits_transform.argtypes = [V, ctypes.c_float, V]
     lib.pod_plan_set_kv_layout.restype = ctypes.c_int
     lib.pod_plan_set_kv_layout.argtypes = [V, I32, I32]
     lib.pod_plan_set_prefill_mask.restype = ctypes.c_int
@@ -151,6 +153,7 @@ class PodHandle:
     workspace_ptr: Optional[int] = None
     d_kv_fp8: bool = False      # set by pod_plan_set_decode_fp8
     p_mask: object = None       # custom prefill mask, kept alive while the plan uses it
+    alibi: object = None        # ALiBi slopes, kept alive while the plan uses them
 
     def __del__(self):
         if self.ptr and _lib is not None:
@@ -348,6 +351,22 @@ def pod_plan_set_prefill_mask(h: PodHandle, packed_mask):
     h.workspace_ptr = None
 
 
+def pod_plan_set_logits_transform(h: PodHandle, soft_cap: float = 0.0, alibi_slopes=None):
+    """Logits soft cap (cap * tanh(x / cap) of the scaled logit; 0 = off) or
+    ALiBi slopes (fp32 [H]; a CUDA tensor for runs, any tensor for host-only
+    plans), applied by both halves."""
+    ptr = None
+    if alibi_slopes is not None:
+        import torch
+        if alibi_slopes.dtype != torch.float32 or not alibi_slopes.is_contiguous() \
+                or alibi_slopes.numel() != h.num_qo_heads:
+            raise PodError(1, "alibi_slopes must be a contiguous float32 tensor of num_qo_heads")
+        ptr = alibi_slopes.data_ptr()
+    _check(load_library().pod_plan_set_logits_transform(ctypes.c_void_p(h.ptr), float(soft_cap),
+                                                        ptr))
+    h.alibi = alibi_slopes
+
+
 _LAYOUTS = {"NHD": 0, "HND": 1, 0: 0, 1: 1}
 
 
@@ -364,6 +383,8 @@ def _check_mask_device(h: PodHandle):
     m = h.p_mask
     if m is not None and h.p_rows and not getattr(m, "is_cuda", False):
         raise PodError(1, "the custom prefill mask must be a CUDA uint8 tensor to run")
+    if h.alibi is not None and not getattr(h.alibi, "is_cuda", False):
+        raise PodError(1, "the ALiBi slopes must be a CUDA float32 tensor to run")
 
 
 def plan_inputs(inp, workspace=None, num_sms=0, stream=None) -> PodHandle:
@@ -376,6 +397,11 @@ def plan_inputs(inp, workspace=None, num_sms=0, stream=None) -> PodHandle:
     import torch
     if inp.d.rows and getattr(inp.d.kv, "dtype", None) == torch.float8_e4m3fn:
         pod_plan_set_decode_fp8(h, inp.k_scale, inp.v_scale)
+    cap, slopes = float(getattr(inp, "soft_cap", 0.0) or 0.0), getattr(inp, "alibi", None)
+    if cap > 0 or slopes is not None:
+        if slopes is not None and torch.cuda.is_available():
+            slopes = slopes.to(device="cuda", dtype=torch.float32).contiguous()
+        pod_plan_set_logits_transform(h, cap, slopes)
     lp, ld = getattr(inp.p, "kv_layout", "NHD"), getattr(inp.d, "kv_layout", "NHD")
     if (lp, ld) != ("NHD", "NHD"):
         pod_plan_set_kv_layout(h, lp, ld)

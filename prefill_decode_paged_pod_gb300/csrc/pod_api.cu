@@ -27,6 +27,9 @@ struct pod_plan_s {
   float k_scale = 1.f, v_scale = 1.f;
   // page layout of each half's cache: 0 = NHD, 1 = HND
   int p_layout = 0, d_layout = 0;
+  // logits transform of both halves: soft cap (> 0) or ALiBi slopes (device [H])
+  float soft_cap = 0.f;
+  const float* alibi = nullptr;
   // custom prefill mask: caller-owned device bytes read by every run
   const void* p_mask = nullptr;
   int64_t p_mask_bytes = 0;
@@ -300,6 +303,13 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
   if (P.has_sinks && !sinks) return set_err(POD_ERR_INVALID_ARG, "plan has sinks but sinks is NULL");
   if (!P.has_sinks && sinks)
     return set_err(POD_ERR_INVALID_ARG, "sinks given but the plan was made without sinks");
+  if (h->alibi) {
+    cudaPointerAttributes pa;
+    cudaError_t e = cudaPointerGetAttributes(&pa, h->alibi);
+    if (e != cudaSuccess) return cuda_err(e, "cudaPointerGetAttributes(alibi slopes)");
+    if (pa.type != cudaMemoryTypeDevice && pa.type != cudaMemoryTypeManaged)
+      return set_err(POD_ERR_INVALID_ARG, "the ALiBi slopes are not device memory");
+  }
   if (P.p_custom_mask && P.p.rows > 0) {
     // the kernel reads the mask: it must be device (or managed) memory
     cudaPointerAttributes pa;
@@ -354,6 +364,10 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
   K.causal = P.causal; K.window_left = P.window_left; K.has_sinks = P.has_sinks;
   K.p_hnd = h->p_layout;
   K.d_hnd = h->d_layout;
+  K.lt = h->soft_cap > 0.f ? POD_LT_SOFTCAP : (h->alibi ? POD_LT_ALIBI : POD_LT_NONE);
+  K.lt_c = h->soft_cap / P.sm_scale;
+  K.lt_inv_scale = 1.f / P.sm_scale;
+  K.alibi = h->alibi;
   K.scale_log2 = P.scale_log2;
   K.d_fp8 = h->d_fp8;
   K.d_scale_log2 = P.scale_log2 * h->k_scale;
@@ -399,10 +413,27 @@ pod_status pod_plan_set_decode_fp8(pod_handle h, float k_scale, float v_scale) {
     return set_err(POD_ERR_UNSUPPORTED, "an FP8 decode cache needs head_dim 128");
   if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
     return set_err(POD_ERR_INVALID_ARG, "k_scale and v_scale must be finite and positive");
+  if (h->soft_cap > 0.f || h->alibi)
+    return set_err(POD_ERR_UNSUPPORTED, "an FP8 decode cache with a soft cap or ALiBi");
   h->d_fp8 = 1;
   h->k_scale = k_scale;
   h->v_scale = v_scale;
   h->tm_ptr[3] = nullptr;  // the decode cache's tensor map changes format
+  return POD_OK;
+}
+
+pod_status pod_plan_set_logits_transform(pod_handle h, float logits_soft_cap,
+                                         const float* alibi_slopes) {
+  g_err.clear();
+  if (!h) return set_err(POD_ERR_INVALID_ARG, "handle is NULL");
+  if (!std::isfinite(logits_soft_cap) || logits_soft_cap < 0.f)
+    return set_err(POD_ERR_INVALID_ARG, "logits_soft_cap must be finite and >= 0");
+  if (logits_soft_cap > 0.f && alibi_slopes)
+    return set_err(POD_ERR_UNSUPPORTED, "a soft cap and ALiBi together");
+  if ((logits_soft_cap > 0.f || alibi_slopes) && h->d_fp8)
+    return set_err(POD_ERR_UNSUPPORTED, "a soft cap or ALiBi with an FP8 decode cache");
+  h->soft_cap = logits_soft_cap;
+  h->alibi = alibi_slopes;
   return POD_OK;
 }
 

@@ -118,7 +118,7 @@ enum {
 // tiles from the global queue and publishes them in order on a small ring in
 // shared memory; every other warp that walks tiles reads the same sequence.
 // Returns false when a wait ran out (the status word then says so).
-template <typename T, int D>
+template <typename T, int D, int LT>
 __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
   using L = PLayout<D>;
   constexpr int NK = L::NK, NV = L::NV;
@@ -455,6 +455,9 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
       const int row_hi = (P.causal && !masked) ? min(pdiag + 1, kv_len) : kv_len;
       const int row_lo = P.window_left >= 0 ? max(pdiag - P.window_left, 0) : 0;
       const long long mrow = masked ? P.p_mask_off[req] + (long long)tok * kv_len : 0;
+      // ALiBi: slope of this row's head in raw q.k units
+      float a_slope = 0.f;
+      if constexpr (LT == POD_LT_ALIBI) a_slope = __ldg(P.alibi + head) * P.lt_inv_scale;
       const int b0 = (lo / POD_KBLOCK) * POD_KBLOCK;
       const int nb = (hi - b0 + POD_KBLOCK - 1) / POD_KBLOCK;
       float m_ref = NEG_INF, l = 0.f;
@@ -467,6 +470,17 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
         const uint32_t s_addr = tmem + lane_base + L::TM_S + b * POD_KBLOCK;
         float s[POD_KBLOCK];
         tmem_ld64(s_addr, s);
+        if constexpr (LT == POD_LT_SOFTCAP) {
+          // cap * tanh(x / cap) of the scaled logit, kept in raw q.k units
+          const float c = P.lt_c, ic = 1.f / P.lt_c;
+#pragma unroll
+          for (int i = 0; i < POD_KBLOCK; ++i) s[i] = soft_cap(s[i], c, ic);
+        }
+        if constexpr (LT == POD_LT_ALIBI) {
+          const float base = (float)(kb - pdiag);
+#pragma unroll
+          for (int i = 0; i < POD_KBLOCK; ++i) s[i] = fmaf(a_slope, base + (float)i, s[i]);
+        }
         const bool full = (kb >= row_lo) && (kb + POD_KBLOCK <= row_hi);
         if (!full) {
 #pragma unroll
@@ -605,7 +619,7 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
 // ============================================================ decode role
 // Runs decode items from the shared queue until it is empty. Returns false
 // when a wait ran out (the status word then says so).
-template <typename T, int D, bool F8>
+template <typename T, int D, bool F8, int LT>
 __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
   using L = DLayout<D>;
   constexpr bool BF16 = Pack<T>::kBF16;
@@ -802,6 +816,9 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
 
     // rows of this thread inside its m-tile: r0 = 16 mt + lane/4, r1 = r0 + 8
     int row_lo[2], row_hi[2];
+    // ALiBi only: the rows' slopes (raw q.k units) and diagonal positions
+    float a_slope[2] = {0.f, 0.f};
+    int a_pd[2] = {0, 0};
 #pragma unroll
     for (int h2 = 0; h2 < 2; ++h2) {
       const int rr = mt * 16 + (lane >> 2) + 8 * h2;
@@ -809,6 +826,10 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
       const int pd = kv_len - q_len + tok;
       row_hi[h2] = min(P.causal ? min(pd + 1, kv_len) : kv_len, k1);
       row_lo[h2] = max(P.window_left >= 0 ? max(pd - P.window_left, 0) : 0, k0);
+      if constexpr (LT == POD_LT_ALIBI) {
+        a_slope[h2] = __ldg(P.alibi + g * G + (rr < R ? rr % G : 0)) * P.lt_inv_scale;
+        a_pd[h2] = pd;
+      }
     }
     float m[2] = {NEG_INF, NEG_INF}, l[2] = {0.f, 0.f};
     float o[D / 8][4];
@@ -895,6 +916,8 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             float x = *v[e];
+            if constexpr (LT == POD_LT_SOFTCAP) x = soft_cap(x, P.lt_c, 1.f / P.lt_c);
+            if constexpr (LT == POD_LT_ALIBI) x = fmaf(a_slope[h2], (float)(key[e] - a_pd[h2]), x);
             if (key[e] < row_lo[h2] || key[e] >= row_hi[h2]) x = NEG_INF;
             *v[e] = x;
             mm = fmaxf(mm, x);
@@ -1082,8 +1105,9 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
 }
 
 // ============================================================ kernels
-// F8: the decode half reads an FP8 (E4M3) cache (head_dim 128 only)
-template <typename T, int D, bool F8>
+// F8: the decode half reads an FP8 (E4M3) cache (head_dim 128 only).
+// LT: logits transform of both halves (POD_LT_NONE, _SOFTCAP, _ALIBI).
+template <typename T, int D, bool F8, int LT>
 __global__ void __launch_bounds__(kThreads, POD_CTAS_PER_SM) pod_kernel(const __grid_constant__ PodParams P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   // the merge kernel may start its prologue now; it waits for this grid's completion
@@ -1115,7 +1139,7 @@ __global__ void __launch_bounds__(kThreads, POD_CTAS_PER_SM) pod_kernel(const __
       // shared memory changes hands between the generic and the async proxy
       fence_proxy_async();
       __syncthreads();
-      ok = do_prefill ? prefill_role<T, D>(P, smem, tmem) : decode_role<T, D, F8>(P, smem);
+      ok = do_prefill ? prefill_role<T, D, LT>(P, smem, tmem) : decode_role<T, D, F8, LT>(P, smem);
     }
     tc_fence_before();
     __syncthreads();
@@ -1181,21 +1205,22 @@ __global__ void __launch_bounds__(256) pod_merge_kernel(const __grid_constant__ 
   if (lane == 0 && lse) lse[orow] = wsum > 0.f ? M + log2f(wsum) : -INFINITY;
 }
 
-template <typename T, int D, bool F8>
+template <typename T, int D, bool F8, int LT>
 cudaError_t launch_pod(const PodParams& P, cudaStream_t stream) {
   constexpr int SMEM = smem_bytes<D>();
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(pod_kernel<T, D, F8>,
+    cudaError_t e = cudaFuncSetAttribute(pod_kernel<T, D, F8, LT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     // two CTAs per SM need the largest shared-memory carveout
-    e = cudaFuncSetAttribute(pod_kernel<T, D, F8>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(pod_kernel<T, D, F8, LT>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  pod_kernel<T, D, F8><<<P.grid, kThreads, SMEM, stream>>>(P);
+  pod_kernel<T, D, F8, LT><<<P.grid, kThreads, SMEM, stream>>>(P);
   return cudaGetLastError();
 }
 
@@ -1203,10 +1228,16 @@ template <typename T, int D>
 cudaError_t launch_impl(const PodParams& P, cudaStream_t stream) {
   if (P.grid > 0) {
     cudaError_t e;
-    if constexpr (D == 128)
-      e = P.d_fp8 ? launch_pod<T, D, true>(P, stream) : launch_pod<T, D, false>(P, stream);
+    // the host refuses a logits transform with an FP8 decode cache
+    if (P.lt == POD_LT_SOFTCAP)
+      e = launch_pod<T, D, false, POD_LT_SOFTCAP>(P, stream);
+    else if (P.lt == POD_LT_ALIBI)
+      e = launch_pod<T, D, false, POD_LT_ALIBI>(P, stream);
+    else if constexpr (D == 128)
+      e = P.d_fp8 ? launch_pod<T, D, true, POD_LT_NONE>(P, stream)
+                  : launch_pod<T, D, false, POD_LT_NONE>(P, stream);
     else
-      e = launch_pod<T, D, false>(P, stream);
+      e = launch_pod<T, D, false, POD_LT_NONE>(P, stream);
     if (e != cudaSuccess) return e;
   }
   if (P.n_mrows > 0) {

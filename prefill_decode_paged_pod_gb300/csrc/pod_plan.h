@@ -45,6 +45,10 @@
 #define POD_DECODE_ROWS 32     // max rows of a decode item (2 mma.sync m16 tiles)
 #define POD_DECODE_STAGE 64    // keys per decode pipeline stage
 #define POD_CTAS_PER_SM 2
+// logits transform applied by both halves before masking and softmax
+#define POD_LT_NONE 0
+#define POD_LT_SOFTCAP 1   // cap * tanh(x / cap) of the scaled logit x
+#define POD_LT_ALIBI 2     // + slope[head] * (t - p)
 
 enum PodSummary {
   S_H = 0, S_HK, S_D, S_PS, S_CAUSAL, S_WINDOW, S_DTYPE, S_SINKS, S_NUM_SMS, S_GRID,
@@ -68,6 +72,11 @@ struct PodParams {
   // 1 = HND pages [2, Hk, ps, d] (only the cp.async gathers read it; the
   // tensor maps carry the layout in their strides)
   int p_hnd, d_hnd;
+  // logits transform: lt = POD_LT_*; lt_c = cap / sm_scale (soft cap in raw
+  // q.k units); lt_inv_scale = 1 / sm_scale; alibi = device [H] slopes
+  int lt;
+  float lt_c, lt_inv_scale;
+  const float* alibi;
   float scale_log2;          // sm_scale * log2(e)
   // decode cache in FP8 E4M3 (head_dim 128): d_scale_log2 = scale_log2 * k_scale,
   // outputs multiplied by v_scale

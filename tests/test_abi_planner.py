@@ -393,3 +393,35 @@ def test_kv_layout_switch_host_checks(lib):
     assert L.pod_plan_set_kv_layout(None, 0, 0) == 1
     with pytest.raises(pod.PodError):
         pod.pod_plan_set_kv_layout(h, "NDH", "NHD")
+
+
+def test_logits_transform_host_checks(lib):
+    """pod_plan_set_logits_transform takes a non-negative finite soft cap or
+    ALiBi slopes, not both, and neither next to an FP8 decode cache."""
+    from pod_workloads import with_fp8_decode_cache
+    inp = make_custom("t", torch.bfloat16, 16, 2, 128, 16, True, -1, [5], [9], [1, 2], [40, 70],
+                      seed=1)
+    h = plan_host(inp, num_sms=4)
+    slopes = torch.full((16,), 0.5)
+    pod.pod_plan_set_logits_transform(h, 30.0)
+    pod.pod_plan_set_logits_transform(h, 0.0, slopes)
+    pod.pod_plan_set_logits_transform(h, 0.0)
+    for cap in (-1.0, float("nan"), float("inf")):
+        with pytest.raises(pod.PodError) as e:
+            pod.pod_plan_set_logits_transform(h, cap)
+        assert e.value.code == 1
+    with pytest.raises(pod.PodError) as e:
+        pod.pod_plan_set_logits_transform(h, 5.0, slopes)
+    assert e.value.code == 2
+    with pytest.raises(pod.PodError) as e:
+        pod.pod_plan_set_logits_transform(h, 0.0, torch.zeros(8))
+    assert e.value.code == 1
+    # FP8 decode cache: either order is refused
+    pod.pod_plan_set_logits_transform(h, 5.0)
+    with pytest.raises(pod.PodError) as e:
+        pod.pod_plan_set_decode_fp8(h, 1.0, 1.0)
+    assert e.value.code == 2
+    h8 = plan_host(with_fp8_decode_cache(inp), num_sms=4)
+    with pytest.raises(pod.PodError) as e:
+        pod.pod_plan_set_logits_transform(h8, 5.0)
+    assert e.value.code == 2

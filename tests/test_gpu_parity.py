@@ -412,3 +412,38 @@ def test_hnd_layout(case):
     (op, lp_, od, ld_), h, ws = run_pod(inp)
     compare_half(inp, "p", op, lp_, tag=name + " ")
     compare_half(inp, "d", od, ld_, tag=name + " ")
+
+
+# ------------------------------------------------------------- logits soft cap and ALiBi
+LT_CASES = [
+    # name, dtype, H, Hk, d, ps, causal, window, sinks, p_q, p_kv, d_q, d_kv, cap, alibi, num_sms
+    ("cap30", torch.bfloat16, 16, 2, 128, 16, True, -1, True, [100, 37], [300, 37], [1, 4],
+     [500, 900], 30.0, False, 0),
+    ("cap5", torch.float16, 8, 2, 64, 16, False, 64, False, [70], [150], [1, 2, 1], [33, 64, 90],
+     5.0, False, 0),
+    ("capsplit", torch.bfloat16, 32, 8, 128, 16, True, -1, False, [64], [64], [1, 4], [9000, 12000],
+     20.0, False, 16),
+    ("alibi", torch.bfloat16, 16, 2, 128, 16, True, -1, True, [100, 37], [300, 37], [1, 4],
+     [500, 900], 0.0, True, 0),
+    ("alibi64", torch.float16, 8, 8, 64, 1, False, -1, False, [70], [150], [3], [77], 0.0, True, 0),
+    ("alibisplit", torch.bfloat16, 32, 8, 128, 16, True, 4096, True, [], [], [1, 4], [9000, 7000],
+     0.0, True, 16),
+]
+
+
+@pytest.mark.parametrize("case", LT_CASES, ids=[c[0] for c in LT_CASES])
+def test_logits_transform(case):
+    """Logits soft cap (cap * tanh(x / cap) of the scaled logit) and ALiBi
+    (geometric head slopes, bias slope * (t - p)) on both halves, including
+    decode splits merged by the second kernel (few SMs, long keys)."""
+    from pod_workloads import alibi_slopes
+    name, dt, H, Hk, d, ps, causal, window, sinks, pq, pkv, dq, dkv, cap, alibi, nsm = case
+    inp = make_custom(name, dt, H, Hk, d, ps, causal, window, pq, pkv, dq, dkv, seed=41,
+                      sinks=sinks)
+    inp.soft_cap = cap
+    inp.alibi = alibi_slopes(H) if alibi else None
+    (op, lp, od, ld), h, ws = run_pod(inp, num_sms=nsm)
+    if name.endswith("split"):
+        assert pod.plan_summary(h)["n_groups"] > 0, "expected decode splits"
+    compare_half(inp, "p", op, lp, tag=name + " ")
+    compare_half(inp, "d", od, ld, tag=name + " ")
