@@ -286,7 +286,8 @@ def run_reference(args, ws, rank):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "us", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1000.0,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD_DESC[args.workload]},
+            "data": "synthetic", "config": {"workload": WORKLOAD_DESC[args.workload],
+                                            **variant_desc(args)},
             "cpu_baseline": {"value": v, "unit": "us", "cores": nthreads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -295,11 +296,39 @@ def run_reference(args, ws, rank):
 
 
 def with_kv_option(inp, args):
-    """--kv-fp8: the decode half's cache as FP8 E4M3 codes (scales 0.05)."""
+    """Variant switches of the same workload:
+    --kv-fp8: the decode half's cache as FP8 E4M3 codes (scales 0.05);
+    --kv-layout HND: both caches stored [pages, 2, Hk, ps, d];
+    --soft-cap C: logits soft cap C on both halves;
+    --alibi: geometric ALiBi slopes on both halves;
+    --prefill-mask P: a random custom prefill mask, each bit set with probability P."""
+    from pod_workloads import (alibi_slopes, with_fp8_decode_cache, with_kv_layout,
+                               with_prefill_custom_mask)
+    if getattr(args, "kv_layout", "NHD") == "HND":
+        inp = with_kv_layout(inp, "HND")
     if getattr(args, "kv_fp8", False):
-        from pod_workloads import with_fp8_decode_cache
-        return with_fp8_decode_cache(inp, k_scale=0.05, v_scale=0.05)
+        inp = with_fp8_decode_cache(inp, k_scale=0.05, v_scale=0.05)
+    if getattr(args, "soft_cap", 0.0):
+        inp.soft_cap = float(args.soft_cap)
+    if getattr(args, "alibi", False):
+        inp.alibi = alibi_slopes(inp.num_qo_heads)
+    if getattr(args, "prefill_mask", None) is not None:
+        inp = with_prefill_custom_mask(inp, seed=7, density=float(args.prefill_mask))
     return inp
+
+
+def variant_desc(args) -> dict:
+    """The variant switches of a run, for the JSON line's config."""
+    v = {"decode_kv": "fp8 e4m3 (k_scale 0.05, v_scale 0.05)" if args.kv_fp8 else "16-bit"}
+    if getattr(args, "kv_layout", "NHD") != "NHD":
+        v["kv_layout"] = args.kv_layout
+    if getattr(args, "soft_cap", 0.0):
+        v["logits_soft_cap"] = float(args.soft_cap)
+    if getattr(args, "alibi", False):
+        v["alibi"] = "geometric slopes 2^(-8h/H)"
+    if getattr(args, "prefill_mask", None) is not None:
+        v["prefill_custom_mask_density"] = float(args.prefill_mask)
+    return v
 
 
 def time_loop(fn, steps, stream, per_launch=True, pre=None):
@@ -524,7 +553,7 @@ def run_ours(args, ws, rank, local):
                    "l2": ("inputs larger than L2" if flush is None else
                           "L2 flushed (256 MB write + 256 MB read) between timed launches"),
                    "kv_cache_bytes": kv_total, "parallelism": f"replicas x{ws} (independent batches)",
-                   "decode_kv": "fp8 e4m3 (k_scale 0.05, v_scale 0.05)" if args.kv_fp8 else "16-bit"},
+                   **variant_desc(args)},
         "roofline": roof, "cpu_baseline": cpu,
         "e2e": {"value": e2e_step_ms * 1e3, "unit": "us", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -605,6 +634,12 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--kv-fp8", action="store_true",
                     help="decode cache in FP8 E4M3 (per-tensor K and V scales)")
+    ap.add_argument("--kv-layout", choices=["NHD", "HND"], default="NHD",
+                    help="page layout of both caches")
+    ap.add_argument("--soft-cap", type=float, default=0.0, help="logits soft cap (0 = off)")
+    ap.add_argument("--alibi", action="store_true", help="ALiBi with geometric head slopes")
+    ap.add_argument("--prefill-mask", type=float, default=None, metavar="DENSITY",
+                    help="random custom prefill mask with this fraction of allowed keys")
     ap.add_argument("--profile", choices=["fused", "prefill", "decode"], default=None,
                     help="only launch this variant (for ncu captures); prints a summary line")
     args = ap.parse_args(argv)

@@ -76,3 +76,24 @@ def test_reference_arm_json_contract():
         assert k in line
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_variant_switches_reach_the_inputs():
+    """bench.py's variant switches build the same workload with an HND cache,
+    a soft cap, ALiBi slopes or a custom prefill mask, and name them in the
+    JSON line's config."""
+    import argparse
+    from pod_workloads import make_config
+    args = argparse.Namespace(kv_fp8=False, kv_layout="HND", soft_cap=0.0, alibi=True,
+                              prefill_mask=0.3)
+    base = make_config("c1")
+    inp = bench.with_kv_option(make_config("c1"), args)
+    assert inp.p.kv_layout == inp.d.kv_layout == "HND"
+    assert tuple(inp.p.kv.shape) == (base.p.kv.shape[0], 2, base.num_kv_heads, base.page_size,
+                                      base.head_dim)
+    assert inp.alibi is not None and inp.alibi.shape == (base.num_qo_heads,)
+    bits = int(sum(int(q) * int(k) for q, k in zip(np.diff(inp.p.q_indptr), inp.p.kv_lens)))
+    assert inp.p.packed_mask.nbytes == (bits + 7) // 8
+    desc = bench.variant_desc(args)
+    assert desc["kv_layout"] == "HND" and "alibi" in desc
+    assert desc["prefill_custom_mask_density"] == 0.3
