@@ -12,7 +12,10 @@
  * run many times (for example once per transformer layer) with the same page
  * tables. Every policy (causal, window_left, sm_scale, sinks on/off, dtype) is
  * fixed at plan time, as the walkthrough's "plan 覆盖" rule does for the decode
- * side ("Decode 侧参数与'plan 覆盖'行为"); run takes tensors only.
+ * side ("Decode 侧参数与'plan 覆盖'行为"); run takes tensors only. Optional
+ * policies are set on the handle between pod_plan and pod_run:
+ * pod_plan_set_decode_fp8, pod_plan_set_kv_layout,
+ * pod_plan_set_logits_transform and pod_plan_set_prefill_mask.
  *
  * Conventions shared by every entry point
  *  - Errors are returned as pod_status codes; nothing aborts or throws.
@@ -27,7 +30,8 @@
  *  - q_p : [p_q_indptr[p_batch], H, d]    q_d : [d_q_indptr[d_batch], H, d]
  *  - kv_p: [p_num_pages, 2, page_size, Hk, d]   kv_d: [d_num_pages, 2, page_size, Hk, d]
  *    (NHD paged cache, index 0 = K, 1 = V; POD walkthrough single-request
- *    docstring example)
+ *    docstring example); per half [num_pages, 2, Hk, page_size, d] (HND)
+ *    after pod_plan_set_kv_layout
  *  - out_p / out_d: same shape and dtype as q_p / q_d
  *  - lse_p / lse_d: fp32 [rows, H], base 2 (flashinfer.cudnn page, "LSE 契约")
  *  - sinks: fp32 [H] or NULL (flashinfer.cudnn page, "Decode 能力矩阵与参数")

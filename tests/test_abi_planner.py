@@ -425,3 +425,21 @@ def test_logits_transform_host_checks(lib):
     with pytest.raises(pod.PodError) as e:
         pod.pod_plan_set_logits_transform(h8, 5.0)
     assert e.value.code == 2
+
+
+def test_plain_c_client(lib, tmp_path):
+    """include/pod.h compiles as strict C99, and a C program makes, inspects,
+    switches and destroys a host-only plan through the ABI alone."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(pod.LIB_PATH)
+    exe = str(tmp_path / "abi_c_client")
+    subprocess.check_call([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                           "-I", os.path.join(ROOT, "include"),
+                           os.path.join(ROOT, "tests", "csrc", "abi_c_client.c"),
+                           "-L", libdir, "-lpod_gb300", f"-Wl,-rpath,{libdir}", "-o", exe])
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
