@@ -360,6 +360,66 @@ def time_loop(fn, steps, stream, per_launch=True, pre=None):
     return start.elapsed_time(end), per
 
 
+def e2e_pipelined(pod, inp, h, wsb, dev, outs, hq, device, steps):
+    """End to end through the public API, steps overlapped on three streams:
+    while step i computes, the host->device copy of step i+1's queries and
+    the device->host copy of step i-1's outputs run on their own streams.
+    Two device buffer sets (and two plan handles on the one workspace, so
+    each keeps its tensor maps) alternate; events order every reuse. Every
+    step still copies its queries in and its outputs out inside the timed
+    region. Returns (ms per step, host outputs of the last step)."""
+    import torch
+    Ev = torch.cuda.Event
+    h_b = pod.plan_inputs(inp)
+    pod.pod_bind_workspace(h_b, wsb)
+    handles = (h, h_b)
+    like = lambda t: torch.empty_like(t) if t is not None else None
+    qbuf = [dict(q_p=dev["q_p"], q_d=dev["q_d"]), dict(q_p=like(dev["q_p"]), q_d=like(dev["q_d"]))]
+    obuf = [tuple(outs), tuple(torch.empty_like(t) for t in outs)]
+    hout = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs] for _ in range(2)]
+    s_in, s_c, s_out = (torch.cuda.Stream(device) for _ in range(3))
+    q_ready, q_free, done, out_free = ([Ev(), Ev()] for _ in range(4))
+
+    def one(i):
+        b = i & 1
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(q_free[b])          # step i-2 has read this buffer set
+            for k in ("q_p", "q_d"):
+                if hq[k] is not None:
+                    qbuf[b][k].copy_(hq[k], non_blocking=True)
+            q_ready[b].record(s_in)
+        with torch.cuda.stream(s_c):
+            s_c.wait_event(q_ready[b])
+            s_c.wait_event(out_free[b])         # step i-2's outputs have left
+            op, lp, od, ld = obuf[b]
+            pod.pod_run(handles[b], qbuf[b]["q_p"], dev["kv_p"], qbuf[b]["q_d"], dev["kv_d"], wsb,
+                        sinks=dev["sinks"], out_p=op, lse_p=lp, out_d=od, lse_d=ld)
+            q_free[b].record(s_c)
+            done[b].record(s_c)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done[b])
+            for dst, src in zip(hout[b], obuf[b]):
+                if src.numel():
+                    dst.copy_(src, non_blocking=True)
+            out_free[b].record(s_out)
+
+    for i in range(4):
+        one(i)
+    torch.cuda.synchronize()
+    main = torch.cuda.current_stream(device)
+    start, end = Ev(enable_timing=True), Ev(enable_timing=True)
+    start.record(main)
+    for st in (s_in, s_c, s_out):
+        st.wait_stream(main)
+    for i in range(steps):
+        one(i)
+    for st in (s_in, s_c, s_out):
+        main.wait_stream(st)
+    end.record(main)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps, hout[(steps - 1) & 1]
+
+
 def run_ours(args, ws, rank, local):
     import torch
     import prefill_decode_paged_pod_gb300 as pod
@@ -499,7 +559,23 @@ def run_ours(args, ws, rank, local):
     barrier(ws)
     e2e_ms, _ = time_loop(step_e2e, args.steps, stream, per_launch=False)
     barrier(ws)
-    e2e_step_ms = max_over_ranks(e2e_ms / args.steps, ws, device)
+    e2e_serial_ms = max_over_ranks(e2e_ms / args.steps, ws, device)
+    # the same, with the copies of neighbouring steps overlapping the compute;
+    # kept only if its outputs equal the serial loop's bit for bit
+    e2e_mode = "3-stream pipelined"
+    try:
+        pipe_ms, last = e2e_pipelined(pod, inp, h, wsb, dev, (out_p, lse_p, out_d, lse_d),
+                                      dict(q_p=hq_p, q_d=hq_d), device, args.steps)
+        if not all(torch.equal(a, b) for a, b in zip(last, ho)):
+            raise RuntimeError("pipelined outputs differ from the serial loop")
+    except Exception as ex:  # noqa: BLE001 - report and keep the serial figure
+        print(f"[bench] pipelined end-to-end not used: {ex!r}", file=sys.stderr)
+        pipe_ms = float("inf")
+    barrier(ws)
+    pipe_ms = max_over_ranks(pipe_ms, ws, device)
+    if pipe_ms == float("inf"):
+        e2e_mode, pipe_ms = "serial", e2e_serial_ms
+    e2e_step_ms = pipe_ms
     clk = clocks.stop()
     assert pod.pod_read_device_status(h, wsb) == 0
 
@@ -556,7 +632,8 @@ def run_ours(args, ws, rank, local):
                    **variant_desc(args)},
         "roofline": roof, "cpu_baseline": cpu,
         "e2e": {"value": e2e_step_ms * 1e3, "unit": "us", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "mode": e2e_mode,
+                "serial_value": e2e_serial_ms * 1e3},
         "gpu_launches": launches * args.steps, "clocks": clk,
         "plan": {k: summ[k] for k in ("grid", "n_p_ctas", "n_d_ctas", "n_tiles", "n_items",
                                        "n_groups", "decode_chunk")},
