@@ -21,6 +21,9 @@
 #include "pod_planner.hpp"
 
 #include <algorithm>
+#include <cstdlib>
+#include <limits>
+#include <thread>
 #include <cmath>
 #include <cstring>
 #include <functional>
@@ -30,6 +33,19 @@
 namespace {
 
 constexpr int kInvalid = 1, kUnsupported = 2;
+
+// Host threads the planner may use for its what-if simulations: the
+// POD_PLAN_THREADS environment variable (1..64), else the hardware's count
+// capped at 8. The plan does not depend on it.
+int plan_threads() {
+  static const int n = [] {
+    const char* e = getenv("POD_PLAN_THREADS");
+    if (e) return std::max(1, std::min(64, atoi(e)));
+    return std::max(1, std::min(8, (int)std::thread::hardware_concurrency()));
+  }();
+  return n;
+}
+
 
 // ---- cost model; constants measured on GB300 ------------------------------
 // A CTA's speed depends on what shares its SM: the fused launch runs two CTAs
@@ -209,6 +225,57 @@ double lpt(const std::vector<double>& work, double overhead, const std::vector<d
   return makespan;
 }
 
+// The makespan lpt() returns for jobs already in decreasing order, without
+// the schedule: each rate class is an array heap of (finish time, CTA index)
+// whose root is pushed down in place. Returns early, with the makespan so
+// far, once it reaches `bound`.
+double lpt_makespan(const std::vector<double>& sorted_work, double overhead,
+                    const std::vector<double>& rate, double bound) {
+  const int n_cta = (int)rate.size();
+  if (n_cta <= 0 || sorted_work.empty()) return 0.0;
+  struct Cls { double rate; std::vector<double> t; std::vector<int> c; };
+  std::vector<Cls> cls;
+  for (int c = 0; c < n_cta; ++c) {
+    size_t k = 0;
+    while (k < cls.size() && cls[k].rate != rate[c]) ++k;
+    if (k == cls.size()) cls.push_back(Cls{rate[c], {}, {}});
+    cls[k].t.push_back(0.0);   // CTAs join in index order: a valid heap
+    cls[k].c.push_back(c);
+  }
+  double makespan = 0.0;
+  for (double w : sorted_work) {
+    int best = -1;
+    double best_t = 0.0;
+    for (size_t k = 0; k < cls.size(); ++k) {
+      const double t = cls[k].t[0] + overhead + w / cls[k].rate;
+      if (best < 0 || t < best_t || (t == best_t && cls[k].c[0] < cls[best].c[0])) {
+        best = (int)k;
+        best_t = t;
+      }
+    }
+    makespan = std::max(makespan, best_t);
+    if (makespan >= bound) return makespan;
+    Cls& h = cls[best];
+    const int n = (int)h.t.size(), cid = h.c[0];
+    int i = 0;
+    for (;;) {
+      const int l = 2 * i + 1, r = l + 1;
+      int m = -1;
+      double mt = best_t;
+      int mc = cid;
+      if (l < n && (h.t[l] < mt || (h.t[l] == mt && h.c[l] < mc))) { m = l; mt = h.t[l]; mc = h.c[l]; }
+      if (r < n && (h.t[r] < mt || (h.t[r] == mt && h.c[r] < mc))) { m = r; mt = h.t[r]; mc = h.c[r]; }
+      if (m < 0) break;
+      h.t[i] = mt;
+      h.c[i] = mc;
+      i = m;
+    }
+    h.t[i] = best_t;
+    h.c[i] = cid;
+  }
+  return makespan;
+}
+
 struct DecodeUnit {
   int req, kv_head, tok0, ntok, lo, hi;
 };
@@ -247,34 +314,81 @@ double item_work(int keys, int d, int rows) {
   return item_bytes(keys, d) * (rows > 16 ? 1.25 : 1.0);
 }
 
+// Estimated decode time (ns) with key chunks of `chunk` (0 = no split). When
+// even the bandwidth floor plus the split's cost reaches `bound`, that lower
+// bound is returned without scheduling the items.
 double decode_time(const std::vector<DecodeUnit>& units, const std::vector<double>& rate,
-                   int chunk, int G, int d, const CostModel& cm, double total_bytes) {
-  std::vector<double> work;
+                   int chunk, int G, int d, const CostModel& cm, double total_bytes,
+                   double bound = std::numeric_limits<double>::infinity()) {
+  // item counts by key count, for items of <= 16 rows ([0]) and more ([1])
+  int max_keys = 0;
+  for (const DecodeUnit& u : units) max_keys = std::max(max_keys, u.hi - u.lo);
+  std::vector<int> cnt[2] = {std::vector<int>(max_keys + 1, 0), std::vector<int>(max_keys + 1, 0)};
   std::vector<std::pair<int, int>> parts;
   double split_bytes = 0.0;
+  size_t n_items = 0;
   for (const DecodeUnit& u : units) {
     split_range(u.lo, u.hi, chunk, parts);
-    for (auto& pr : parts) work.push_back(item_work(pr.second - pr.first, d, u.ntok * G));
+    const int f = u.ntok * G > 16 ? 1 : 0;
+    for (auto& pr : parts) ++cnt[f][pr.second - pr.first];
+    n_items += parts.size();
     if (parts.size() > 1) split_bytes += (double)parts.size() * u.ntok * G * (d + 1) * 4.0 * 2.0;
   }
-  double t = lpt(work, cm.d_item_ns, rate, nullptr, nullptr);
-  t = std::max(t, total_bytes / cm.hbm_bytes_per_ns);
   // splitting costs the partial rows' round trip and the merge launch
-  if (split_bytes > 0) t += 8000.0 + split_bytes / cm.hbm_bytes_per_ns;
-  return t;
+  const double extra = split_bytes > 0 ? 8000.0 + split_bytes / cm.hbm_bytes_per_ns : 0.0;
+  const double floor_t = total_bytes / cm.hbm_bytes_per_ns + extra;
+  if (floor_t >= bound) return floor_t;
+  // only the makespan is needed and equal jobs are interchangeable: the work
+  // values in decreasing order (the order lpt's index sort gives), merged
+  // from the two count tables
+  std::vector<double> work;
+  work.reserve(n_items);
+  int k0 = max_keys, k1 = max_keys;
+  for (;;) {
+    while (k0 >= 0 && cnt[0][k0] == 0) --k0;
+    while (k1 >= 0 && cnt[1][k1] == 0) --k1;
+    if (k0 < 0 && k1 < 0) break;
+    const double w0 = k0 >= 0 ? item_work(k0, d, 16) : -1.0;
+    const double w1 = k1 >= 0 ? item_work(k1, d, 32) : -1.0;
+    if (w0 >= w1) {
+      work.insert(work.end(), cnt[0][k0], w0);
+      cnt[0][k0] = 0;
+    } else {
+      work.insert(work.end(), cnt[1][k1], w1);
+      cnt[1][k1] = 0;
+    }
+  }
+  double t = lpt_makespan(work, cm.d_item_ns, rate, bound - extra);
+  t = std::max(t, total_bytes / cm.hbm_bytes_per_ns);
+  return t + extra;
 }
 
 DecodeChoice best_decode(const std::vector<DecodeUnit>& units, const std::vector<double>& rate,
                          int G, int d, const CostModel& cm, double total_bytes) {
   DecodeChoice best;
   best.time = -1.0;
-  // 0 = no split; then 16 Ki .. 256 keys
+  // 0 = no split; then 16 Ki .. 256 keys, each estimated on its own thread
   const int cands[] = {0, 16384, 8192, 4096, 2048, 1024, 512, 256};
-  for (int c : cands) {
-    double t = decode_time(units, rate, c, G, d, cm, total_bytes);
-    if (best.time < 0 || t < best.time * (1.0 - 1e-9)) {
-      best.time = t;
-      best.chunk = c;
+  constexpr int NC = (int)(sizeof(cands) / sizeof(cands[0]));
+  double times[NC];
+  // the unsplit estimate first: a candidate is taken only below
+  // best * (1 - 1e-9) <= times[0] * (1 - 1e-9), which bounds the others
+  times[0] = decode_time(units, rate, cands[0], G, d, cm, total_bytes);
+  const double bound = times[0] * (1.0 - 1e-9);
+  // threads pay off only for larger batches
+  const int nt = units.size() < 512 ? 1 : std::min(plan_threads(), NC - 1);
+  auto work = [&](int k) {
+    for (int j = 1 + k; j < NC; j += nt)
+      times[j] = decode_time(units, rate, cands[j], G, d, cm, total_bytes, bound);
+  };
+  std::vector<std::thread> pool;
+  for (int k = 1; k < nt; ++k) pool.emplace_back(work, k);
+  work(0);
+  for (auto& th : pool) th.join();
+  for (int j = 0; j < NC; ++j) {
+    if (best.time < 0 || times[j] < best.time * (1.0 - 1e-9)) {
+      best.time = times[j];
+      best.chunk = cands[j];
     }
   }
   return best;
@@ -475,41 +589,90 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
     std::sort(item_b.begin(), item_b.end(), std::greater<double>());
     // makespan when CTAs [0, np) start on tiles and the rest on items; a CTA
     // takes the next job of its queue when free, the other queue's once its
-    // own is empty
-    auto queue_makespan = [&](int np) {
-      typedef std::pair<double, int> Slot;
-      std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-      for (int c = 0; c < grid_max; ++c) heap.push(Slot(0.0, c));
+    // own is empty. CTAs are served in (finish time, index) order from a
+    // binary heap. The simulation stops as soon as a CTA's finish time reaches
+    // `bound` (the candidate can no longer win) and returns that time.
+    const double floor_t = std::max(p_flops / cm.p_flops_per_ns, d_bytes / cm.hbm_bytes_per_ns);
+    struct Scratch { std::vector<double> t, p_ns, d_rate; std::vector<int> c; };
+    auto queue_makespan = [&](int np, double bound, Scratch& w) {
+      if (floor_t >= bound) return floor_t;
+      const int n = grid_max;
+      w.t.assign(n, 0.0);
+      w.c.resize(n);
+      w.p_ns.resize(n);
+      w.d_rate.resize(n);
+      for (int c = 0; c < n; ++c) {
+        const int cls = neighbour_class(c, np, n - np, S);
+        w.p_ns[c] = cm.p_block_ns[cls];
+        w.d_rate[c] = cm.d_bytes_per_ns[cls];
+        w.c[c] = c;   // all loads zero: index order is a valid heap
+      }
+      double* ht = w.t.data();
+      int* hc = w.c.data();
       size_t it = 0, id = 0;
       double makespan = 0.0;
       while (it < tile_ns.size() || id < item_b.size()) {
-        Slot sl = heap.top();
-        heap.pop();
-        const int c = sl.second;
-        const int cls = neighbour_class(c, np, grid_max - np, S);
+        const int c = hc[0];
         const bool want_p = c < np ? it < tile_ns.size() : id >= item_b.size();
-        double cost;
-        if (want_p) cost = cm.p_tile_ns + tile_ns[it++] * cm.p_block_ns[cls];
-        else cost = cm.d_item_ns + item_b[id++] / cm.d_bytes_per_ns[cls];
-        sl.first += cost;
-        makespan = std::max(makespan, sl.first);
-        heap.push(sl);
+        const double cost = want_p ? cm.p_tile_ns + tile_ns[it++] * w.p_ns[c]
+                                   : cm.d_item_ns + item_b[id++] / w.d_rate[c];
+        const double tnew = ht[0] + cost;
+        makespan = std::max(makespan, tnew);
+        if (makespan >= bound) return makespan;
+        // the root grew: sift it down
+        int i = 0;
+        for (;;) {
+          const int l = 2 * i + 1, r = l + 1;
+          int m = -1;
+          double mt = tnew;
+          int mc = c;
+          if (l < n && (ht[l] < mt || (ht[l] == mt && hc[l] < mc))) { m = l; mt = ht[l]; mc = hc[l]; }
+          if (r < n && (ht[r] < mt || (ht[r] == mt && hc[r] < mc))) { m = r; mt = ht[r]; mc = hc[r]; }
+          if (m < 0) break;
+          ht[i] = mt;
+          hc[i] = mc;
+          i = m;
+        }
+        ht[i] = tnew;
+        hc[i] = c;
       }
-      return std::max(makespan, std::max(p_flops / cm.p_flops_per_ns, d_bytes / cm.hbm_bytes_per_ns));
+      return std::max(makespan, floor_t);
     };
-    const double share_t = queue_makespan(n_p);
+    // candidates are evaluated on a few host threads; each result does not
+    // depend on the others, and the choice below walks them in order
+    auto eval_all = [&](const std::vector<int>& nps, double bound, std::vector<double>& out) {
+      out.assign(nps.size(), 0.0);
+      const size_t jobs = tile_ns.size() + item_b.size();
+      const int nt = jobs < 2048 ? 1 : std::max(1, std::min<int>(plan_threads(), (int)nps.size()));
+      std::vector<Scratch> ws(nt);
+      auto work = [&](int k) {
+        for (size_t j = k; j < nps.size(); j += nt) out[j] = queue_makespan(nps[j], bound, ws[k]);
+      };
+      std::vector<std::thread> pool;
+      for (int k = 1; k < nt; ++k) pool.emplace_back(work, k);
+      work(0);
+      for (auto& th : pool) th.join();
+    };
+    Scratch w0;
+    const double share_t = queue_makespan(n_p, std::numeric_limits<double>::infinity(), w0);
     int best_np = n_p;
     double best_t = share_t;
     const int hi_np = std::min(grid_max - 1, n_tiles);
     const int step = std::max(1, hi_np / 32);
-    for (int np = 1; np <= hi_np; np += step) {
-      const double t = queue_makespan(np);
-      if (t < best_t * (1.0 - 1e-9)) { best_t = t; best_np = np; }
-    }
-    for (int np = std::max(1, best_np - step); np <= std::min(hi_np, best_np + step); ++np) {
-      const double t = queue_makespan(np);
-      if (t < best_t * (1.0 - 1e-9)) { best_t = t; best_np = np; }
-    }
+    // a candidate is taken only below best_t * (1 - 1e-9) <= share_t * (1 - 1e-9):
+    // no simulation needs to run past that
+    std::vector<int> nps;
+    std::vector<double> ts;
+    for (int np = 1; np <= hi_np; np += step) nps.push_back(np);
+    eval_all(nps, share_t * (1.0 - 1e-9), ts);
+    for (size_t j = 0; j < nps.size(); ++j)
+      if (ts[j] < best_t * (1.0 - 1e-9)) { best_t = ts[j]; best_np = nps[j]; }
+    nps.clear();
+    for (int np = std::max(1, best_np - step); np <= std::min(hi_np, best_np + step); ++np)
+      nps.push_back(np);
+    eval_all(nps, best_t * (1.0 - 1e-9), ts);
+    for (size_t j = 0; j < nps.size(); ++j)
+      if (ts[j] < best_t * (1.0 - 1e-9)) { best_t = ts[j]; best_np = nps[j]; }
     // the model is coarse: leave the balanced split unless the queues are
     // predicted to finish at least 1 % earlier another way
     if (best_t < 0.99 * share_t) n_p = best_np;

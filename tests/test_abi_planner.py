@@ -443,3 +443,30 @@ def test_plain_c_client(lib, tmp_path):
                            "-L", libdir, "-lpod_gb300", f"-Wl,-rpath,{libdir}", "-o", exe])
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
+
+
+def test_plan_independent_of_planner_threads(lib):
+    """The planner's what-if simulations run on POD_PLAN_THREADS host threads;
+    the plan is the same bit for bit with 1 and with 8 of them."""
+    import subprocess
+    import sys
+    code = (
+        "import hashlib, sys\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "import prefill_decode_paged_pod_gb300 as pod\n"
+        "from pod_workloads import make_config\n"
+        "pod.load_library()\n"
+        "h = hashlib.sha256()\n"
+        "for n in ('c3', 'c4', 'c5'):\n"
+        "    p = pod.plan_inputs(make_config(n, with_data=False), num_sms=152)\n"
+        "    for w in range(12):\n"
+        "        h.update(pod.pod_plan_table(p, w).tobytes())\n"
+        "print(h.hexdigest())\n")
+    digests = set()
+    for t in ("1", "8"):
+        env = dict(os.environ, POD_PLAN_THREADS=t)
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                           timeout=600)
+        assert r.returncode == 0, r.stderr
+        digests.add(r.stdout.strip())
+    assert len(digests) == 1
