@@ -31,7 +31,7 @@ def test_allowed_and_touched_keys_closed_forms():
     assert bench.allowed_keys(9, 5, False, -1) == 45
 
 
-def test_work_matches_survey_figures():
+def test_work_matches_workload_figures():
     inp = make_config("c3", with_data=False)
     w = bench.work(inp)
     # 2 requests x causal 2048^2 / 2 pairs x 64 heads x 4 d flops
