@@ -470,3 +470,21 @@ def test_plan_independent_of_planner_threads(lib):
         assert r.returncode == 0, r.stderr
         digests.add(r.stdout.strip())
     assert len(digests) == 1
+
+
+def test_binding_refuses_host_mask_and_slopes_before_launch(lib):
+    """A custom mask or ALiBi slopes that live in host memory serve host-only
+    plans, but pod_run refuses them before any launch (the kernels read them
+    from device memory)."""
+    from pod_workloads import alibi_slopes, with_prefill_custom_mask
+    inp = with_prefill_custom_mask(
+        make_custom("b", torch.bfloat16, 8, 2, 64, 16, True, -1, [5], [9], [1], [20], seed=3))
+    h = plan_host(inp, num_sms=4)          # the mask stays a CPU tensor without a GPU
+    q = inp.p.q
+    with pytest.raises(pod.PodError, match="CUDA uint8"):
+        pod.pod_run(h, q, inp.p.kv, inp.d.q, inp.d.kv, torch.empty(256, dtype=torch.uint8))
+    h2 = plan_host(make_custom("b", torch.bfloat16, 8, 2, 64, 16, True, -1, [5], [9], [1], [20],
+                               seed=3), num_sms=4)
+    pod.pod_plan_set_logits_transform(h2, 0.0, alibi_slopes(8))
+    with pytest.raises(pod.PodError, match="ALiBi"):
+        pod.pod_run(h2, q, inp.p.kv, inp.d.q, inp.d.kv, torch.empty(256, dtype=torch.uint8))
