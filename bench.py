@@ -301,7 +301,8 @@ def with_kv_option(inp, args):
     --kv-layout HND: both caches stored [pages, 2, Hk, ps, d];
     --soft-cap C: logits soft cap C on both halves;
     --alibi: geometric ALiBi slopes on both halves;
-    --prefill-mask P: a random custom prefill mask, each bit set with probability P."""
+    --prefill-mask P: a random custom prefill mask, each bit set with probability P;
+    --rope: ROPE_LLAMA (rope_scale 1, rope_theta 1e4) on both halves."""
     from pod_workloads import (alibi_slopes, with_fp8_decode_cache, with_kv_layout,
                                with_prefill_custom_mask)
     if getattr(args, "kv_layout", "NHD") == "HND":
@@ -314,6 +315,8 @@ def with_kv_option(inp, args):
         inp.alibi = alibi_slopes(inp.num_qo_heads)
     if getattr(args, "prefill_mask", None) is not None:
         inp = with_prefill_custom_mask(inp, seed=7, density=float(args.prefill_mask))
+    if getattr(args, "rope", False):
+        inp.rope = (1.0, 1e4)
     return inp
 
 
@@ -328,6 +331,8 @@ def variant_desc(args) -> dict:
         v["alibi"] = "geometric slopes 2^(-8h/H)"
     if getattr(args, "prefill_mask", None) is not None:
         v["prefill_custom_mask_density"] = float(args.prefill_mask)
+    if getattr(args, "rope", False):
+        v["pos_encoding"] = "ROPE_LLAMA (scale 1, theta 1e4), rotated-copy pre-pass"
     return v
 
 
@@ -717,6 +722,7 @@ def main(argv=None):
     ap.add_argument("--alibi", action="store_true", help="ALiBi with geometric head slopes")
     ap.add_argument("--prefill-mask", type=float, default=None, metavar="DENSITY",
                     help="random custom prefill mask with this fraction of allowed keys")
+    ap.add_argument("--rope", action="store_true", help="ROPE_LLAMA on both halves")
     ap.add_argument("--profile", choices=["fused", "prefill", "decode"], default=None,
                     help="only launch this variant (for ncu captures); prints a summary line")
     args = ap.parse_args(argv)

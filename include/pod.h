@@ -15,7 +15,8 @@
  * side ("Decode 侧参数与'plan 覆盖'行为"); run takes tensors only. Optional
  * policies are set on the handle between pod_plan and pod_run:
  * pod_plan_set_decode_fp8, pod_plan_set_kv_layout,
- * pod_plan_set_logits_transform and pod_plan_set_prefill_mask.
+ * pod_plan_set_logits_transform, pod_plan_set_rope and
+ * pod_plan_set_prefill_mask.
  *
  * Conventions shared by every entry point
  *  - Errors are returned as pod_status codes; nothing aborts or throws.
@@ -154,8 +155,9 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p,
  * scaled logits. q_d and out_d keep the plan's 16-bit dtype; the prefill half
  * is unchanged. May be called again to change the scales. Errors:
  * POD_ERR_UNSUPPORTED unless head_dim is 128, or with a logits transform set
- * (pod_plan_set_logits_transform); POD_ERR_INVALID_ARG for a NULL handle or
- * scales that are not finite and positive.
+ * (pod_plan_set_logits_transform) or RoPE (pod_plan_set_rope);
+ * POD_ERR_INVALID_ARG for a NULL handle or scales that are not finite and
+ * positive.
  */
 pod_status pod_plan_set_decode_fp8(pod_handle h, float k_scale, float v_scale);
 
@@ -176,6 +178,25 @@ pod_status pod_plan_set_decode_fp8(pod_handle h, float k_scale, float v_scale);
  */
 pod_status pod_plan_set_logits_transform(pod_handle h, float logits_soft_cap,
                                          const float* alibi_slopes);
+
+/*
+ * pod_plan_set_rope — rotary position encoding of both halves (FlashInfer
+ * guide, "快速上手": pos_encoding_mode ROPE_LLAMA with rope_scale, default
+ * 1, and rope_theta, default 1e4; the POD plan keeps them).
+ * Queries and keys are rotated before the dot product: a query row at its
+ * bottom-right position p = kv_len - q_len + i, key t at t; element j pairs
+ * with j + head_dim/2 and turns by (pos / rope_scale) * rope_theta^(-2j/d).
+ * Values are not rotated. rope_scale = 0 turns it off.
+ * Each pod_run first writes rotated copies of both halves' queries and of
+ * every page-table entry's page into the workspace (so the workspace grows
+ * by about the size of the pages the page tables name) and runs the kernels
+ * on them; the caller's tensors are only read.
+ * Switching it on, off or to other values plans the handle again: any bound
+ * workspace is released, bind again (the size changes).
+ * Errors: POD_ERR_INVALID_ARG (NULL handle, non-finite or non-positive
+ * values), POD_ERR_UNSUPPORTED (with an FP8 decode cache).
+ */
+pod_status pod_plan_set_rope(pod_handle h, float rope_scale, float rope_theta);
 
 /*
  * pod_plan_set_kv_layout — page layout of each half's cache (FlashInfer
@@ -240,7 +261,10 @@ pod_status pod_read_device_status(pod_handle h, void* workspace, void* stream,
  * (16 ints per queue position: the item record, then kv_len, first query row,
  * q_len, first page-table entry, page count of its request), 11 = first
  * custom-mask bit of each prefill request and the total, as int64 values
- * stored as little-endian int32 pairs (empty without a custom mask).
+ * stored as little-endian int32 pairs (empty without a custom mask); under
+ * RoPE, 12 / 13 = per page-table entry of the prefill / decode half the
+ * position of its slot 0 and its slots below kv_len (2 ints), 14 / 15 = the
+ * position of each prefill / decode query row (empty without RoPE).
  * Copies min(count, capacity) int32 values into `out` (may be NULL to query
  * *count). Each table's record format is documented beside the planner
  * (csrc/pod_plan.h in the library sources).

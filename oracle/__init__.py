@@ -226,6 +226,8 @@ def attention_half(inp, half: str, sel_token=None, sel_head=None, nthreads=None,
         scales["soft_cap"] = float(inp.soft_cap)
     if getattr(inp, "alibi", None) is not None and "alibi_slopes" not in kw:
         scales["alibi_slopes"] = inp.alibi
+    if getattr(inp, "rope", None) is not None and "rope" not in kw:
+        scales.update(rope=True, rope_scale=float(inp.rope[0]), rope_theta=float(inp.rope[1]))
     return attention_rows(h.q, h.kv, h.q_indptr, h.kv_indptr, h.kv_indices, h.last_page_len,
                           inp.num_qo_heads, inp.num_kv_heads, inp.head_dim, inp.page_size,
                           inp.causal, inp.window_left, inp.sm_scale, sinks=inp.sinks,

@@ -84,6 +84,8 @@ class PODInputs:
     # logits transform of both halves: soft cap (> 0) or per-head ALiBi slopes [H] fp32
     soft_cap: float = 0.0
     alibi: Optional[torch.Tensor] = None
+    # rotary position encoding of both halves: (rope_scale, rope_theta) or None
+    rope: Optional[tuple] = None
 
 
 def page_table_from_lens(kv_lens: Sequence[int], page_size: int):

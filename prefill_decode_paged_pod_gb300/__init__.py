@@ -31,6 +31,7 @@ __all__ = [
     "pod_plan_table", "PodHandle", "LIB_PATH", "DEFAULT_WORKSPACE_BYTES",
     "pod_run_static_scratch", "pod_static_scratch_capacity", "pod_plan_set_decode_fp8",
     "pod_plan_set_prefill_mask", "pod_plan_set_kv_layout", "pod_plan_set_logits_transform",
+    "pod_plan_set_rope",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -85,6 +86,8 @@ def load_library(path: Optional[str] = None):
     lib.pod_static_scratch_capacity.argtypes = []
     lib.pod_plan_set_decode_fp8.restype = ctypes.c_int
     lib.pod_plan_set_decode_fp8.argtypes = [V, ctypes.c_float, ctypes.c_float]
+    lib.pod_plan_set_rope.restype = ctypes.c_int
+    lib.pod_plan_set_rope.argtypes = [V, ctypes.c_float, ctypes.c_float]
     lib.pod_plan_set_logits_transform.restype = ctypes.c_int
     lib.pod_plan_set_logits_transform.argtypes = [V, ctypes.c_float, V]
     lib.pod_plan_set_kv_layout.restype = ctypes.c_int
@@ -311,7 +314,7 @@ def pod_plan_table(h: PodHandle, which: int) -> np.ndarray:
 SUMMARY_FIELDS = ("H", "Hk", "d", "ps", "causal", "window", "dtype", "sinks", "num_sms", "grid",
                   "n_p_ctas", "n_d_ctas", "n_tiles", "n_items", "n_groups", "n_mrows", "n_prows",
                   "p_rows", "d_rows", "p_batch", "d_batch", "decode_chunk", "ws_lo", "ws_hi",
-                  "p_tma", "d_tma", "p_mask")
+                  "p_tma", "d_tma", "p_mask", "rope")
 
 
 def plan_summary(h: PodHandle) -> dict:
@@ -367,6 +370,15 @@ def pod_plan_set_logits_transform(h: PodHandle, soft_cap: float = 0.0, alibi_slo
     h.alibi = alibi_slopes
 
 
+def pod_plan_set_rope(h: PodHandle, rope_scale: float = 1.0, rope_theta: float = 1e4):
+    """ROPE_LLAMA on both halves (rope_scale 0 turns it off). Plans the handle
+    again and releases its workspace: bind again."""
+    _check(load_library().pod_plan_set_rope(ctypes.c_void_p(h.ptr), float(rope_scale),
+                                            float(rope_theta)))
+    h.workspace_bytes = pod_workspace_size(h)
+    h.workspace_ptr = None
+
+
 _LAYOUTS = {"NHD": 0, "HND": 1, 0: 0, 1: 1}
 
 
@@ -393,7 +405,11 @@ def plan_inputs(inp, workspace=None, num_sms=0, stream=None) -> PodHandle:
     inputs' scales, a packed custom mask on the prefill half
     pod_plan_set_prefill_mask (moved to the GPU when there is one)."""
     mask = getattr(inp.p, "packed_mask", None)
-    h = _plan_inputs(inp, None if mask is not None else workspace, num_sms, stream)
+    rope = getattr(inp, "rope", None)
+    replans = mask is not None or rope is not None
+    h = _plan_inputs(inp, None if replans else workspace, num_sms, stream)
+    if rope is not None:
+        pod_plan_set_rope(h, *rope)
     import torch
     if inp.d.rows and getattr(inp.d.kv, "dtype", None) == torch.float8_e4m3fn:
         pod_plan_set_decode_fp8(h, inp.k_scale, inp.v_scale)
@@ -410,8 +426,8 @@ def plan_inputs(inp, workspace=None, num_sms=0, stream=None) -> PodHandle:
         if torch.cuda.is_available():
             t = t.cuda()
         pod_plan_set_prefill_mask(h, t)
-        if workspace is not None:
-            pod_bind_workspace(h, workspace, stream)
+    if replans and workspace is not None:
+        pod_bind_workspace(h, workspace, stream)
     return h
 
 

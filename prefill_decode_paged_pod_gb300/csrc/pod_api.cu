@@ -19,6 +19,7 @@
 #include "../../include/pod.h"
 #include "pod_launch.h"
 #include "pod_planner.hpp"
+#include "pod_rope.h"
 
 struct pod_plan_s {
   PodPlanHost plan;
@@ -33,6 +34,8 @@ struct pod_plan_s {
   // custom prefill mask: caller-owned device bytes read by every run
   const void* p_mask = nullptr;
   int64_t p_mask_bytes = 0;
+  // RoPE: the workspace whose cos/sin table is filled (nullptr: none yet)
+  const void* rope_table_ws = nullptr;
   void* workspace = nullptr;      // bound device workspace (nullptr = host-only plan)
   size_t workspace_bytes = 0;
   // TMA descriptors of the last run, re-encoded only when a tensor pointer changes
@@ -78,6 +81,7 @@ pod_status upload(pod_plan_s* h, void* ws, size_t bytes, void* stream) {
   if (e != cudaSuccess) return cuda_err(e, "cudaStreamSynchronize(plan metadata)");
   h->workspace = ws;
   h->workspace_bytes = bytes;
+  h->rope_table_ws = nullptr;
   return POD_OK;
 }
 
@@ -212,6 +216,38 @@ pod_status encode_kv_decode_fp8(CUtensorMap* m, const void* ptr, int num_pages, 
   return POD_OK;
 }
 
+// Plan arguments that rebuild `O` from the handle's own copies of the page
+// tables (the optional switches can then be changed one at a time).
+PodPlanArgs args_of(const PodPlanHost& O) {
+  PodPlanArgs a;
+  a.p_q_indptr = O.p.q_indptr.data(); a.p_kv_indptr = O.p.kv_indptr.data();
+  a.p_kv_indices = O.p.kv_indices.data(); a.p_last_page_len = O.p.last_page_len.data();
+  a.p_batch = O.p.batch; a.p_num_pages = O.p.num_pages;
+  a.d_q_indptr = O.dd.q_indptr.data(); a.d_kv_indptr = O.dd.kv_indptr.data();
+  a.d_kv_indices = O.dd.kv_indices.data(); a.d_last_page_len = O.dd.last_page_len.data();
+  a.d_batch = O.dd.batch; a.d_num_pages = O.dd.num_pages;
+  a.H = O.H; a.Hk = O.Hk; a.d = O.d; a.ps = O.ps; a.causal = O.causal;
+  a.window_left = O.window_left; a.sm_scale = O.sm_scale; a.dtype = O.dtype;
+  a.has_sinks = O.has_sinks; a.num_sms = O.num_sms; a.p_custom_mask = O.p_custom_mask;
+  a.rope = O.rope; a.rope_scale = O.rope_scale; a.rope_theta = O.rope_theta;
+  return a;
+}
+
+// Replaces the handle's plan by one made from `a`; the layout may change, so
+// any bound workspace is released (the caller binds again).
+pod_status replan(pod_plan_s* h, const PodPlanArgs& a) {
+  PodPlanHost fresh;
+  std::string err;
+  const int rc = pod_build_plan(a, fresh, &err);
+  if (rc != 0) return set_err((pod_status)rc, err);
+  h->plan = std::move(fresh);
+  h->workspace = nullptr;
+  h->workspace_bytes = 0;
+  h->rope_table_ws = nullptr;
+  for (int i = 0; i < 4; ++i) h->tm_ptr[i] = nullptr;
+  return POD_OK;
+}
+
 }  // namespace
 
 // Lets other translation units of the library report a message through
@@ -249,6 +285,7 @@ pod_status pod_plan(const int32_t* p_q_indptr, const int32_t* p_kv_indptr,
   a.causal = causal; a.window_left = window_left; a.sm_scale = sm_scale;
   a.dtype = (int)dtype; a.has_sinks = has_sinks; a.num_sms = num_sms;
   a.p_custom_mask = 0;
+  a.rope = 0; a.rope_scale = 1.0; a.rope_theta = 1e4;
 
   pod_plan_s* h = new (std::nothrow) pod_plan_s();
   if (!h) return set_err(POD_ERR_INVALID_ARG, "out of host memory");
@@ -319,6 +356,57 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
       return set_err(POD_ERR_INVALID_ARG, "the custom prefill mask is not device memory");
   }
 
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // RoPE: rotated copies of the queries and of every page-table entry's page
+  // (NHD) are written into the workspace; the kernels read those instead
+  int p_layout = h->p_layout, d_layout = h->d_layout;
+  int p_pages = P.p.num_pages, d_pages = P.dd.num_pages;
+  if (P.rope) {
+    cudaStream_t st = (cudaStream_t)stream;
+    const float2* table = reinterpret_cast<const float2*>(ws + P.off_rope_table);
+    if (h->rope_table_ws != workspace) {
+      PodRopeFreq f;
+      for (int j = 0; j < P.d / 2; ++j)
+        f.freq[j] = std::pow(P.rope_theta, -2.0 * j / P.d) / P.rope_scale;
+      cudaError_t e = pod_rope_table(reinterpret_cast<float2*>(ws + P.off_rope_table), P.rope_rows,
+                                     P.d / 2, f, st);
+      if (e != cudaSuccess) return cuda_err(e, "RoPE table launch");
+      h->rope_table_ws = workspace;
+    }
+    const void* srcs[4] = {q_p, kv_p, q_d, kv_d};
+    for (const void* p : srcs)
+      if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0)
+        return set_err(POD_ERR_INVALID_ARG, "q and kv tensors must be 16-byte aligned");
+    auto I32 = [&](size_t off) { return reinterpret_cast<const int32_t*>(ws + off); };
+    for (int half = 0; half < 2; ++half) {
+      const PodHalfHost& hh = half ? P.dd : P.p;
+      if (hh.rows == 0) continue;
+      PodRopeQ q;
+      q.q_src = half ? q_d : q_p;
+      q.q_dst = ws + (half ? P.off_d_qcopy : P.off_p_qcopy);
+      q.qpos = I32(half ? P.off_d_rope_qpos : P.off_p_rope_qpos);
+      q.table = table;
+      q.rows = hh.rows; q.H = P.H; q.d = P.d;
+      cudaError_t e = pod_rope_q(q, P.dtype, st);
+      if (e != cudaSuccess) return cuda_err(e, "RoPE query launch");
+      PodRopeKV k;
+      k.kv_src = half ? kv_d : kv_p;
+      k.kv_dst = ws + (half ? P.off_d_kvcopy : P.off_p_kvcopy);
+      k.src_pages = I32(half ? P.off_d_rope_src : P.off_p_rope_src);
+      k.ent = I32(half ? P.off_d_rope_ent : P.off_p_rope_ent);
+      k.table = table;
+      k.entries = (int)hh.kv_indices.size(); k.ps = P.ps; k.Hk = P.Hk; k.d = P.d;
+      k.hnd = half ? h->d_layout : h->p_layout;
+      e = pod_rope_kv(k, P.dtype, st);
+      if (e != cudaSuccess) return cuda_err(e, "RoPE key launch");
+    }
+    q_p = ws + P.off_p_qcopy; kv_p = ws + P.off_p_kvcopy;
+    q_d = ws + P.off_d_qcopy; kv_d = ws + P.off_d_kvcopy;
+    p_layout = d_layout = 0;
+    p_pages = (int)P.p.kv_indices.size();
+    d_pages = (int)P.dd.kv_indices.size();
+  }
+
   // TMA descriptors for the tensors of this call (cached while pointers repeat)
   const void* ptrs[4] = {q_p, kv_p, q_d, kv_d};
   for (int i = 0; i < 4; ++i) {
@@ -327,20 +415,19 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
     if (hh.rows == 0) continue;
     if (i % 2 == 1 && !(pre ? P.p_tma : P.d_tma)) continue;
     if (h->tm_ptr[i] == ptrs[i]) continue;
+    const int npages = pre ? p_pages : d_pages;
     pod_status st = (i % 2 == 0)
         ? encode_q(&h->tm[i], ptrs[i], hh.rows, P.H, P.d, P.G, pre ? P.tq : P.tu, P.dtype)
-        : pre ? encode_kv(&h->tm[i], ptrs[i], hh.num_pages, P.ps, P.Hk, P.d, P.p_tma, P.dtype,
-                          h->p_layout)
+        : pre ? encode_kv(&h->tm[i], ptrs[i], npages, P.ps, P.Hk, P.d, P.p_tma, P.dtype, p_layout)
               : h->d_fp8
-                    ? encode_kv_decode_fp8(&h->tm[i], ptrs[i], hh.num_pages, P.ps, P.Hk, P.d, P.d_tma,
-                                           h->d_layout)
-                    : encode_kv_decode(&h->tm[i], ptrs[i], hh.num_pages, P.ps, P.Hk, P.d, P.d_tma,
-                                       P.dtype, h->d_layout);
+                    ? encode_kv_decode_fp8(&h->tm[i], ptrs[i], npages, P.ps, P.Hk, P.d, P.d_tma,
+                                           d_layout)
+                    : encode_kv_decode(&h->tm[i], ptrs[i], npages, P.ps, P.Hk, P.d, P.d_tma,
+                                       P.dtype, d_layout);
     if (st != POD_OK) return st;
     h->tm_ptr[i] = ptrs[i];
   }
 
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
   PodParams K;
   memset(&K, 0, sizeof(K));
   if (P.p.rows) {
@@ -353,8 +440,8 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
   }
   K.p_tma = P.p_tma;
   K.d_tma = P.d_tma;
-  K.p_num_pages = P.p.num_pages;
-  K.d_num_pages = P.dd.num_pages;
+  K.p_num_pages = p_pages;
+  K.d_num_pages = d_pages;
   K.tq = P.tq;
   K.tu = P.tu;
   K.H = P.H; K.Hk = P.Hk; K.G = P.G; K.d = P.d; K.ps = P.ps;
@@ -362,8 +449,8 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
   for (int s = 0; s < 31; ++s)
     if ((1 << s) == P.ps) K.ps_shift = s;
   K.causal = P.causal; K.window_left = P.window_left; K.has_sinks = P.has_sinks;
-  K.p_hnd = h->p_layout;
-  K.d_hnd = h->d_layout;
+  K.p_hnd = p_layout;
+  K.d_hnd = d_layout;
   K.lt = h->soft_cap > 0.f ? POD_LT_SOFTCAP : (h->alibi ? POD_LT_ALIBI : POD_LT_NONE);
   K.lt_c = h->soft_cap / P.sm_scale;
   K.lt_inv_scale = 1.f / P.sm_scale;
@@ -415,6 +502,7 @@ pod_status pod_plan_set_decode_fp8(pod_handle h, float k_scale, float v_scale) {
     return set_err(POD_ERR_INVALID_ARG, "k_scale and v_scale must be finite and positive");
   if (h->soft_cap > 0.f || h->alibi)
     return set_err(POD_ERR_UNSUPPORTED, "an FP8 decode cache with a soft cap or ALiBi");
+  if (h->plan.rope) return set_err(POD_ERR_UNSUPPORTED, "an FP8 decode cache with RoPE");
   h->d_fp8 = 1;
   h->k_scale = k_scale;
   h->v_scale = v_scale;
@@ -435,6 +523,25 @@ pod_status pod_plan_set_logits_transform(pod_handle h, float logits_soft_cap,
   h->soft_cap = logits_soft_cap;
   h->alibi = alibi_slopes;
   return POD_OK;
+}
+
+pod_status pod_plan_set_rope(pod_handle h, float rope_scale, float rope_theta) {
+  g_err.clear();
+  if (!h) return set_err(POD_ERR_INVALID_ARG, "handle is NULL");
+  const int want = rope_scale != 0.f ? 1 : 0;
+  if (want && (!(rope_scale > 0.f) || !(rope_theta > 0.f) || !std::isfinite(rope_scale) ||
+               !std::isfinite(rope_theta)))
+    return set_err(POD_ERR_INVALID_ARG, "rope_scale and rope_theta must be finite and positive");
+  if (want && h->d_fp8)
+    return set_err(POD_ERR_UNSUPPORTED, "RoPE with an FP8 decode cache");
+  const PodPlanHost& O = h->plan;
+  if (want == O.rope && (!want || (O.rope_scale == rope_scale && O.rope_theta == rope_theta)))
+    return POD_OK;
+  PodPlanArgs a = args_of(O);
+  a.rope = want;
+  a.rope_scale = want ? rope_scale : 1.0;
+  a.rope_theta = want ? rope_theta : 1e4;
+  return replan(h, a);
 }
 
 pod_status pod_plan_set_kv_layout(pod_handle h, int32_t p_layout, int32_t d_layout) {
@@ -463,27 +570,11 @@ pod_status pod_plan_set_prefill_mask(pod_handle h, const void* packed_mask, int6
                                               std::to_string((bits + 7) / 8));
   }
   if (want != O.p_custom_mask) {
-    // plan again from the handle's own copies of the page tables: the prefill
-    // tiles now span every key the window allows
-    PodPlanArgs a;
-    a.p_q_indptr = O.p.q_indptr.data(); a.p_kv_indptr = O.p.kv_indptr.data();
-    a.p_kv_indices = O.p.kv_indices.data(); a.p_last_page_len = O.p.last_page_len.data();
-    a.p_batch = O.p.batch; a.p_num_pages = O.p.num_pages;
-    a.d_q_indptr = O.dd.q_indptr.data(); a.d_kv_indptr = O.dd.kv_indptr.data();
-    a.d_kv_indices = O.dd.kv_indices.data(); a.d_last_page_len = O.dd.last_page_len.data();
-    a.d_batch = O.dd.batch; a.d_num_pages = O.dd.num_pages;
-    a.H = O.H; a.Hk = O.Hk; a.d = O.d; a.ps = O.ps; a.causal = O.causal;
-    a.window_left = O.window_left; a.sm_scale = O.sm_scale; a.dtype = O.dtype;
-    a.has_sinks = O.has_sinks; a.num_sms = O.num_sms; a.p_custom_mask = want;
-    PodPlanHost fresh;
-    std::string err;
-    const int rc = pod_build_plan(a, fresh, &err);
-    if (rc != 0) return set_err((pod_status)rc, err);
-    h->plan = std::move(fresh);
-    // the layout may have changed: the caller binds a workspace again
-    h->workspace = nullptr;
-    h->workspace_bytes = 0;
-    for (int i = 0; i < 4; ++i) h->tm_ptr[i] = nullptr;
+    // plan again: the prefill tiles now span every key the window allows
+    PodPlanArgs a = args_of(O);
+    a.p_custom_mask = want;
+    const pod_status st = replan(h, a);
+    if (st != POD_OK) return st;
   }
   h->p_mask = packed_mask;
   h->p_mask_bytes = want ? mask_bytes : 0;
@@ -531,6 +622,10 @@ pod_status pod_plan_table(pod_handle h, int32_t which, int32_t* out, int64_t cap
     case 9: v = &P.dqueue; break;
     case 10: v = &P.dqrec; break;
     case 11: v = &P.p_mask_off; break;
+    case 12: v = &P.p_rope_ent; break;
+    case 13: v = &P.d_rope_ent; break;
+    case 14: v = &P.p_rope_qpos; break;
+    case 15: v = &P.d_rope_qpos; break;
     default: return set_err(POD_ERR_INVALID_ARG, "unknown plan table");
   }
   if (count) *count = (int64_t)v->size();

@@ -54,7 +54,7 @@ enum PodSummary {
   S_H = 0, S_HK, S_D, S_PS, S_CAUSAL, S_WINDOW, S_DTYPE, S_SINKS, S_NUM_SMS, S_GRID,
   S_NP_CTAS, S_ND_CTAS, S_NTILES, S_NITEMS, S_NGROUPS, S_NMROWS, S_NPROWS,
   S_P_ROWS, S_D_ROWS, S_P_BATCH, S_D_BATCH, S_DECODE_CHUNK, S_WS_LO, S_WS_HI,
-  S_P_TMA, S_D_TMA, S_P_MASK, S_COUNT
+  S_P_TMA, S_D_TMA, S_P_MASK, S_ROPE, S_COUNT
 };
 
 // Everything a kernel needs, passed by value at launch (as a __grid_constant__

@@ -437,6 +437,12 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   P.H = a.H; P.Hk = a.Hk; P.G = G; P.d = a.d; P.ps = a.ps;
   P.causal = a.causal ? 1 : 0; P.window_left = a.window_left;
   P.p_custom_mask = a.p_custom_mask ? 1 : 0;
+  P.rope = a.rope ? 1 : 0;
+  P.rope_scale = a.rope_scale;
+  P.rope_theta = a.rope_theta;
+  if (P.rope && (!(a.rope_scale > 0.0) || !(a.rope_theta > 0.0) || !std::isfinite(a.rope_scale) ||
+                 !std::isfinite(a.rope_theta)))
+    return fail(err, kInvalid, "rope_scale and rope_theta must be finite and positive");
   P.dtype = a.dtype; P.has_sinks = a.has_sinks ? 1 : 0; P.num_sms = a.num_sms;
   P.sm_scale = a.sm_scale > 0.f ? a.sm_scale : (float)(1.0 / std::sqrt((double)a.d));
   P.scale_log2 = (float)((double)P.sm_scale * 1.4426950408889634);
@@ -455,10 +461,16 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   // ---- decode units ---------------------------------------------------------
   const int Tu = std::max(1, POD_DECODE_ROWS / G);
   P.tu = Tu;
-  P.p_tma = tma_box_keys(P.p, a.ps);
+  // under RoPE the kernels read compact copies through identity page tables
+  auto identity_half = [](const PodHalfHost& h) {
+    PodHalfHost c = h;
+    for (size_t i = 0; i < c.kv_indices.size(); ++i) c.kv_indices[i] = (int32_t)i;
+    return c;
+  };
+  P.p_tma = tma_box_keys(P.rope ? identity_half(P.p) : P.p, a.ps);
   // decode boxes hold both 64-element halves of head_dim; they are laid out
   // for page_size >= 8 (a page per box) and 1 (runs of pages) only
-  P.d_tma = (a.ps == 1 || a.ps >= 8) ? tma_box_keys(P.dd, a.ps) : 0;
+  P.d_tma = (a.ps == 1 || a.ps >= 8) ? tma_box_keys(P.rope ? identity_half(P.dd) : P.dd, a.ps) : 0;
   std::vector<DecodeUnit> units;
   double d_bytes = 0.0;
   for (int r = 0; r < P.dd.batch; ++r) {
@@ -771,6 +783,32 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
     P.p_mask_bits = bit;
   }
 
+  // ---- RoPE pre-pass tables: per page-table entry the position of slot 0 and
+  // the slots below kv_len; per query row its bottom-right position
+  P.p_rope_ent.clear(); P.d_rope_ent.clear(); P.p_rope_qpos.clear(); P.d_rope_qpos.clear();
+  P.rope_rows = 0;
+  if (P.rope) {
+    int64_t rows = 1;
+    auto tables = [&](const PodHalfHost& h, std::vector<int32_t>& ent, std::vector<int32_t>& qpos) {
+      for (int r = 0; r < h.batch; ++r) {
+        const int np = h.kv_indptr[r + 1] - h.kv_indptr[r];
+        for (int i = 0; i < np; ++i) {
+          ent.push_back(i * P.ps);
+          ent.push_back(std::max(0, std::min(P.ps, h.kv_len[r] - i * P.ps)));
+        }
+        rows = std::max<int64_t>(rows, (int64_t)np * P.ps);
+        for (int i = 0; i < h.q_len[r]; ++i) {
+          const int64_t pos = (int64_t)h.kv_len[r] - h.q_len[r] + i;
+          qpos.push_back((int32_t)pos);
+          rows = std::max<int64_t>(rows, (pos < 0 ? -pos : pos) + 1);
+        }
+      }
+    };
+    tables(P.p, P.p_rope_ent, P.p_rope_qpos);
+    tables(P.dd, P.d_rope_ent, P.d_rope_qpos);
+    P.rope_rows = (int)rows;
+  }
+
   // ---- workspace layout -----------------------------------------------------------
   size_t off = 0;
   auto place = [&](size_t n_int32) {
@@ -797,10 +835,33 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   P.off_dqueue = place(P.dqueue.size());
   P.off_dqrec = place(P.dqrec.size());
   P.off_p_mask_off = place(P.p_mask_off.size());
+  if (P.rope) {
+    P.off_p_rope_src = place(P.p.kv_indices.size());
+    P.off_d_rope_src = place(P.dd.kv_indices.size());
+    P.off_p_rope_ent = place(P.p_rope_ent.size());
+    P.off_d_rope_ent = place(P.d_rope_ent.size());
+    P.off_p_rope_qpos = place(P.p_rope_qpos.size());
+    P.off_d_rope_qpos = place(P.d_rope_qpos.size());
+  }
   P.int_bytes = align_up(off, 256);
   P.off_part_o = P.int_bytes;
   P.off_part_lse = align_up(P.off_part_o + (size_t)n_prows * a.d * 4, 256);
-  P.total_bytes = align_up(P.off_part_lse + (size_t)std::max(n_prows, 1) * 4, 256);
+  size_t end = align_up(P.off_part_lse + (size_t)std::max(n_prows, 1) * 4, 256);
+  if (P.rope) {
+    // cos/sin table [rows][d/2] (float2), then the rotated copies (16-bit)
+    const size_t page_bytes = (size_t)2 * P.ps * P.Hk * a.d * 2;
+    P.off_rope_table = end;
+    end = align_up(end + (size_t)P.rope_rows * (a.d / 2) * 8, 256);
+    P.off_p_kvcopy = end;
+    end = align_up(end + P.p.kv_indices.size() * page_bytes, 256);
+    P.off_d_kvcopy = end;
+    end = align_up(end + P.dd.kv_indices.size() * page_bytes, 256);
+    P.off_p_qcopy = end;
+    end = align_up(end + (size_t)P.p.rows * P.H * a.d * 2, 256);
+    P.off_d_qcopy = end;
+    end = align_up(end + (size_t)P.dd.rows * P.H * a.d * 2, 256);
+  }
+  P.total_bytes = end;
 
   P.int_image.assign(P.int_bytes, 0);
   auto put = [&](size_t o, const std::vector<int32_t>& v) {
@@ -808,11 +869,17 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   };
   put(P.off_p_q_indptr, P.p.q_indptr);
   put(P.off_p_kv_indptr, P.p.kv_indptr);
-  put(P.off_p_kv_indices, P.p.kv_indices);
+  std::vector<int32_t> ident;
+  auto identity = [&](size_t n) -> const std::vector<int32_t>& {
+    ident.resize(n);
+    for (size_t i = 0; i < n; ++i) ident[i] = (int32_t)i;
+    return ident;
+  };
+  put(P.off_p_kv_indices, P.rope ? identity(P.p.kv_indices.size()) : P.p.kv_indices);
   put(P.off_p_kv_len, P.p.kv_len);
   put(P.off_d_q_indptr, P.dd.q_indptr);
   put(P.off_d_kv_indptr, P.dd.kv_indptr);
-  put(P.off_d_kv_indices, P.dd.kv_indices);
+  put(P.off_d_kv_indices, P.rope ? identity(P.dd.kv_indices.size()) : P.dd.kv_indices);
   put(P.off_d_kv_len, P.dd.kv_len);
   put(P.off_ptiles, P.ptiles);
   put(P.off_ditems, P.ditems);
@@ -824,6 +891,14 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   put(P.off_dqueue, P.dqueue);
   put(P.off_dqrec, P.dqrec);
   put(P.off_p_mask_off, P.p_mask_off);
+  if (P.rope) {
+    put(P.off_p_rope_src, P.p.kv_indices);
+    put(P.off_d_rope_src, P.dd.kv_indices);
+    put(P.off_p_rope_ent, P.p_rope_ent);
+    put(P.off_d_rope_ent, P.d_rope_ent);
+    put(P.off_p_rope_qpos, P.p_rope_qpos);
+    put(P.off_d_rope_qpos, P.d_rope_qpos);
+  }
 
   P.summary.assign(S_COUNT, 0);
   int32_t* s = P.summary.data();
@@ -839,5 +914,6 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   s[S_P_TMA] = P.p_tma;
   s[S_D_TMA] = P.d_tma;
   s[S_P_MASK] = P.p_custom_mask;
+  s[S_ROPE] = P.rope;
   return 0;
 }

@@ -23,6 +23,17 @@ struct PodPlanHost {
   int p_custom_mask = 0;
   int64_t p_mask_bits = 0;
   std::vector<int32_t> p_mask_off;
+  // rotary position encoding (ROPE_LLAMA) of both halves: a pre-pass writes
+  // rotated copies of each half's queries and of every page-table entry's
+  // page (compact, in page-table order, NHD) into the workspace, and the
+  // kernels read those through identity page tables. Per page-table entry:
+  // the position of its slot 0 and its valid slots; per query row: its
+  // position (negative when a non-causal row lies before the keys).
+  int rope = 0;
+  double rope_scale = 1.0, rope_theta = 1e4;
+  int rope_rows = 0;            // positions covered by the cos/sin table
+  std::vector<int32_t> p_rope_ent, d_rope_ent;   // [entries][2]: pos0, valid slots
+  std::vector<int32_t> p_rope_qpos, d_rope_qpos; // [rows]
   float sm_scale = 0.f, scale_log2 = 0.f;
   PodHalfHost p, dd;
   // schedule
@@ -36,7 +47,10 @@ struct PodPlanHost {
          off_p_kv_len = 0, off_d_q_indptr = 0, off_d_kv_indptr = 0, off_d_kv_indices = 0,
          off_d_kv_len = 0, off_ptiles = 0, off_ditems = 0, off_cta_ptr = 0, off_cta_list = 0,
          off_mgroups = 0, off_mrow_ptr = 0, off_pqueue = 0, off_dqueue = 0, off_dqrec = 0,
-         off_p_mask_off = 0, int_bytes = 0, off_part_o = 0, off_part_lse = 0, total_bytes = 0;
+         off_p_mask_off = 0, off_p_rope_src = 0, off_d_rope_src = 0, off_p_rope_ent = 0,
+         off_d_rope_ent = 0, off_p_rope_qpos = 0, off_d_rope_qpos = 0, int_bytes = 0,
+         off_part_o = 0, off_part_lse = 0, off_rope_table = 0, off_p_kvcopy = 0,
+         off_d_kvcopy = 0, off_p_qcopy = 0, off_d_qcopy = 0, total_bytes = 0;
   std::vector<uint8_t> int_image;   // bytes [0, int_bytes) of the workspace
   std::vector<int32_t> summary;
 };
@@ -50,6 +64,8 @@ struct PodPlanArgs {
   float sm_scale;
   int dtype, has_sinks, num_sms;
   int p_custom_mask;   // 1: a custom mask replaces the causal rule on the prefill half
+  int rope;            // 1: ROPE_LLAMA with rope_scale, rope_theta
+  double rope_scale, rope_theta;
 };
 
 // Returns 0 on success, else a pod_status code with *err set.

@@ -48,6 +48,12 @@ int main(void)
     CHECK(pod_plan_set_logits_transform(h, 30.0f, NULL));
     CHECK(pod_plan_set_logits_transform(h, 0.0f, NULL));
     CHECK(pod_plan_set_prefill_mask(h, NULL, 0));
+    CHECK(pod_plan_set_rope(h, 1.0f, 10000.0f));
+    if (pod_workspace_size(h) <= need) {
+        printf("RoPE did not grow the workspace\n");
+        return 1;
+    }
+    CHECK(pod_plan_set_rope(h, 0.0f, 0.0f));
     if (pod_plan_set_kv_layout(h, 2, 0) != POD_ERR_INVALID_ARG || strlen(pod_last_error()) == 0) {
         printf("layout 2 was not refused\n");
         return 1;

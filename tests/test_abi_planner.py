@@ -488,3 +488,57 @@ def test_binding_refuses_host_mask_and_slopes_before_launch(lib):
     pod.pod_plan_set_logits_transform(h2, 0.0, alibi_slopes(8))
     with pytest.raises(pod.PodError, match="ALiBi"):
         pod.pod_run(h2, q, inp.p.kv, inp.d.q, inp.d.kv, torch.empty(256, dtype=torch.uint8))
+
+
+# ------------------------------------------------------------- RoPE pre-pass plan
+def test_rope_plan_tables(lib):
+    """With RoPE the plan keeps its tiles and items, and its tables give each
+    page-table entry the position of its slot 0 and its slots below kv_len,
+    and each query row its bottom-right position (negative for a non-causal
+    row before the keys); the workspace grows by the rotated copies."""
+    inp = make_custom("rp", torch.bfloat16, 8, 2, 128, 16, False, -1, [5, 70], [40, 33],
+                      [1, 4], [300, 17], seed=5)
+    h = plan_host(inp, num_sms=8)
+    base = pod.pod_workspace_size(h)
+    tiles0 = pod.pod_plan_table(h, 1).copy()
+    pod.pod_plan_set_rope(h, 2.0, 500.0)
+    s = pod.plan_summary(h)
+    assert s["rope"] == 1 and np.array_equal(pod.pod_plan_table(h, 1), tiles0)
+    ps = inp.page_size
+    for half, hh, te, tq in (("p", inp.p, 12, 14), ("d", inp.d, 13, 15)):
+        ent = pod.pod_plan_table(h, te).reshape(-1, 2)
+        want, qpos = [], []
+        for r in range(hh.batch):
+            kvl = int(hh.kv_lens[r])
+            for i in range(int(hh.kv_indptr[r + 1] - hh.kv_indptr[r])):
+                want.append((i * ps, max(0, min(ps, kvl - i * ps))))
+            ql = int(hh.q_indptr[r + 1] - hh.q_indptr[r])
+            qpos += [kvl - ql + i for i in range(ql)]
+        assert [tuple(x) for x in ent.tolist()] == want, half
+        assert pod.pod_plan_table(h, tq).tolist() == qpos, half
+    # rotated copies: every page-table entry's page and both halves' queries
+    page = 2 * ps * 2 * 128 * 2
+    grow = (len(inp.p.kv_indices) + len(inp.d.kv_indices)) * page + \
+        (inp.p.rows + inp.d.rows) * 8 * 128 * 2
+    assert pod.pod_workspace_size(h) >= base + grow
+    assert min(pod.pod_plan_table(h, 14)) < 0          # request 1: 70 queries, 33 keys
+    pod.pod_plan_set_rope(h, 0.0, 0.0)
+    assert pod.plan_summary(h)["rope"] == 0 and pod.pod_workspace_size(h) == base
+
+
+def test_rope_host_checks(lib):
+    from pod_workloads import with_fp8_decode_cache
+    inp = make_custom("rp", torch.bfloat16, 16, 2, 128, 16, True, -1, [5], [9], [1], [40], seed=1)
+    h = plan_host(inp, num_sms=4)
+    for sc, th in ((-1.0, 1e4), (1.0, 0.0), (float("nan"), 1e4), (1.0, float("inf"))):
+        with pytest.raises(pod.PodError) as e:
+            pod.pod_plan_set_rope(h, sc, th)
+        assert e.value.code == 1
+    h8 = plan_host(with_fp8_decode_cache(inp), num_sms=4)
+    with pytest.raises(pod.PodError) as e:
+        pod.pod_plan_set_rope(h8, 1.0, 1e4)
+    assert e.value.code == 2
+    pod.pod_plan_set_rope(h, 1.0, 1e4)
+    with pytest.raises(pod.PodError) as e:
+        pod.pod_plan_set_decode_fp8(h, 1.0, 1.0)
+    assert e.value.code == 2

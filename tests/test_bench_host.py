@@ -85,7 +85,7 @@ def test_variant_switches_reach_the_inputs():
     import argparse
     from pod_workloads import make_config
     args = argparse.Namespace(kv_fp8=False, kv_layout="HND", soft_cap=0.0, alibi=True,
-                              prefill_mask=0.3)
+                              prefill_mask=0.3, rope=True)
     base = make_config("c1")
     inp = bench.with_kv_option(make_config("c1"), args)
     assert inp.p.kv_layout == inp.d.kv_layout == "HND"
@@ -97,3 +97,4 @@ def test_variant_switches_reach_the_inputs():
     desc = bench.variant_desc(args)
     assert desc["kv_layout"] == "HND" and "alibi" in desc
     assert desc["prefill_custom_mask_density"] == 0.3
+    assert inp.rope == (1.0, 1e4) and "ROPE_LLAMA" in desc["pos_encoding"]

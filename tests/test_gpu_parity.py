@@ -447,3 +447,39 @@ def test_logits_transform(case):
         assert pod.plan_summary(h)["n_groups"] > 0, "expected decode splits"
     compare_half(inp, "p", op, lp, tag=name + " ")
     compare_half(inp, "d", od, ld, tag=name + " ")
+
+
+# ------------------------------------------------------------- ROPE_LLAMA
+ROPE_CASES = [
+    # name, dtype, H, Hk, d, ps, causal, window, sinks, p_q, p_kv, d_q, d_kv, rope, extra
+    ("r16", torch.bfloat16, 16, 2, 128, 16, True, -1, True, [100, 37], [300, 37], [1, 4],
+     [500, 900], (1.0, 1e4), {}),
+    ("r64nc", torch.float16, 8, 2, 64, 4, False, -1, False, [70], [50], [2, 1], [33, 90],
+     (2.0, 500.0), {}),
+    ("rhnd", torch.bfloat16, 16, 2, 128, 16, True, 256, False, [64], [64], [1, 2], [700, 300],
+     (1.0, 1e4), {"hnd": True, "soft_cap": 30.0}),
+    ("rlong", torch.bfloat16, 32, 8, 128, 16, True, -1, False, [], [], [1, 4], [20000, 17000],
+     (1.0, 1e6), {"num_sms": 16}),
+    ("r1", torch.float16, 4, 2, 64, 1, True, -1, False, [80], [200], [2], [129],
+     (4.0, 1e4), {"pages": "contig"}),
+]
+
+
+@pytest.mark.parametrize("case", ROPE_CASES, ids=[c[0] for c in ROPE_CASES])
+def test_rope(case):
+    """ROPE_LLAMA on both halves through the rotated-copy pre-pass: TMA and
+    gather page sizes, a non-causal prefill with more queries than keys
+    (negative positions), an HND source cache with a soft cap, positions
+    past 16 Ki with decode splits, and contiguous page_size 1."""
+    from pod_workloads import with_kv_layout
+    name, dt, H, Hk, d, ps, causal, window, sinks, pq, pkv, dq, dkv, rope, extra = case
+    inp = make_custom(name, dt, H, Hk, d, ps, causal, window, pq, pkv, dq, dkv, seed=51,
+                      sinks=sinks, pages=extra.get("pages", "perm"))
+    if extra.get("hnd"):
+        inp = with_kv_layout(inp, "HND")
+    inp.soft_cap = extra.get("soft_cap", 0.0)
+    inp.rope = rope
+    (op, lp, od, ld), h, ws = run_pod(inp, num_sms=extra.get("num_sms", 0))
+    assert pod.plan_summary(h)["rope"] == 1
+    compare_half(inp, "p", op, lp, tag=name + " ")
+    compare_half(inp, "d", od, ld, tag=name + " ")
