@@ -128,7 +128,9 @@ pod_status pod_bind_workspace(pod_handle h, void* workspace, size_t workspace_by
  * Launches the persistent POD kernel (prefill tiles on tcgen05 tensor cores
  * and split-KV decode on the same grid), then, when the plan split any KV
  * range, the partial-output/LSE merge kernel chained with programmatic
- * dependent launch. No host synchronisation; capturable in a CUDA graph.
+ * dependent launch. With RoPE (pod_plan_set_rope) the rotated-copy pre-pass
+ * kernels run first on the same stream. No host synchronisation; capturable
+ * in a CUDA graph.
  * q_p/kv_p may be NULL when the prefill half is empty (same for the decode
  * half). lse_p / lse_d may be NULL (LSE not written). sinks must be non-NULL
  * exactly when the plan has has_sinks. `workspace` must be the buffer the
