@@ -542,3 +542,26 @@ def test_rope_host_checks(lib):
     with pytest.raises(pod.PodError) as e:
         pod.pod_plan_set_decode_fp8(h, 1.0, 1.0)
     assert e.value.code == 2
+
+
+def test_replanning_switches_keep_each_other(lib):
+    """The custom mask and RoPE each plan the handle again; switching one
+    keeps the other, and switching both off gives the original plan back."""
+    from pod_workloads import with_prefill_custom_mask
+    inp = with_prefill_custom_mask(
+        make_custom("sw", torch.bfloat16, 16, 2, 128, 16, True, 100, [70, 20], [300, 20],
+                    [1, 3], [500, 60], seed=8))
+    h = plan_host(inp, num_sms=8)                  # plan_inputs sets the mask
+    orig = make_custom("sw", torch.bfloat16, 16, 2, 128, 16, True, 100, [70, 20], [300, 20],
+                       [1, 3], [500, 60], seed=8)
+    h0 = plan_host(orig, num_sms=8)
+    pod.pod_plan_set_rope(h, 1.0, 1e4)
+    s = pod.plan_summary(h)
+    assert s["p_mask"] == 1 and s["rope"] == 1
+    pod.pod_plan_set_prefill_mask(h, None)
+    s = pod.plan_summary(h)
+    assert s["p_mask"] == 0 and s["rope"] == 1
+    pod.pod_plan_set_rope(h, 0.0, 0.0)
+    assert pod.pod_workspace_size(h) == pod.pod_workspace_size(h0)
+    for w in range(12):
+        assert np.array_equal(pod.pod_plan_table(h, w), pod.pod_plan_table(h0, w)), w
