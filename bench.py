@@ -503,7 +503,12 @@ def run_ours(args, ws, rank, local):
     kernel_ms = float(np.mean(per))
     step_ms = total_ms / args.steps if flush is None else kernel_ms
     step_ms = max_over_ranks(step_ms, ws, device)
+    # the fused kernel, the merge kernel when the plan splits, and under RoPE
+    # the copy pre-pass (queries and pages of each non-empty half; the angle
+    # table runs once per bound workspace, before the timed steps)
     launches = 1 + (1 if summ["n_mrows"] > 0 else 0)
+    if summ.get("rope"):
+        launches += 2 * ((1 if inp.p.rows else 0) + (1 if inp.d.rows else 0))
 
     # --- single-half runs of the same kernel: prefill TFLOP/s and decode GB/s
     halves = {}
