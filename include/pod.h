@@ -175,8 +175,8 @@ pod_status pod_plan_set_decode_fp8(pod_handle h, float k_scale, float v_scale);
  * Sinks stay plain logits; the LSE is that of the transformed logits.
  * Takes effect from the next pod_run; the plan and workspace are kept.
  * Errors: POD_ERR_INVALID_ARG (NULL handle, negative or non-finite cap),
- * POD_ERR_UNSUPPORTED (both at once, or with an FP8 decode cache; pod_run
- * also refuses slopes that are not device memory).
+ * POD_ERR_UNSUPPORTED (both at once, ALiBi under RoPE, or either with an
+ * FP8 decode cache; pod_run also refuses slopes that are not device memory).
  */
 pod_status pod_plan_set_logits_transform(pod_handle h, float logits_soft_cap,
                                          const float* alibi_slopes);
@@ -189,14 +189,20 @@ pod_status pod_plan_set_logits_transform(pod_handle h, float logits_soft_cap,
  * bottom-right position p = kv_len - q_len + i, key t at t; element j pairs
  * with j + head_dim/2 and turns by (pos / rope_scale) * rope_theta^(-2j/d).
  * Values are not rotated. rope_scale = 0 turns it off.
- * Each pod_run first writes rotated copies of both halves' queries and of
- * every page-table entry's page into the workspace (so the workspace grows
- * by about the size of the pages the page tables name) and runs the kernels
- * on them; the caller's tensors are only read.
+ * No rotated operand is rounded to 16 bits: each is kept as a 16-bit high
+ * part and a 16-bit low part, and every logit is formed as
+ * q_hi.k_hi + q_hi.k_lo + q_lo.k_hi. Each pod_run first writes the rotated
+ * queries of both halves, and copies of the prefill half's pages (rotated K
+ * as high and low parts, V), into the workspace; the workspace grows by
+ * about 1.5x the prefill pages plus twice the queries. Decode keys are
+ * rotated inside the fused kernel, read once from the caller's cache. The
+ * caller's tensors are only read. Under RoPE the fused kernel runs one CTA
+ * per SM (the low parts need the shared memory of a second CTA).
  * Switching it on, off or to other values plans the handle again: any bound
  * workspace is released, bind again (the size changes).
  * Errors: POD_ERR_INVALID_ARG (NULL handle, non-finite or non-positive
- * values), POD_ERR_UNSUPPORTED (with an FP8 decode cache).
+ * values), POD_ERR_UNSUPPORTED (with an FP8 decode cache, or with ALiBi
+ * slopes set: one position encoding at a time).
  */
 pod_status pod_plan_set_rope(pod_handle h, float rope_scale, float rope_theta);
 
@@ -265,8 +271,9 @@ pod_status pod_read_device_status(pod_handle h, void* workspace, void* stream,
  * custom-mask bit of each prefill request and the total, as int64 values
  * stored as little-endian int32 pairs (empty without a custom mask); under
  * RoPE, 12 / 13 = per page-table entry of the prefill / decode half the
- * position of its slot 0 and its slots below kv_len (2 ints), 14 / 15 = the
- * position of each prefill / decode query row (empty without RoPE).
+ * position of its slot 0 and its slots below kv_len (2 ints; the decode half
+ * has no page copies, so 13 is empty), 14 / 15 = the position of each
+ * prefill / decode query row (empty without RoPE).
  * Copies min(count, capacity) int32 values into `out` (may be NULL to query
  * *count). Each table's record format is documented beside the planner
  * (csrc/pod_plan.h in the library sources).

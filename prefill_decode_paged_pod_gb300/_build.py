@@ -16,7 +16,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libpod_gb300.so")
-SOURCES = ["pod_kernels.cu", "pod_api.cu", "pod_planner.cpp", "pod_noalloc.cu", "pod_rope.cu"]
+SOURCES = ["pod_k1_plain.cu", "pod_k1_lt.cu", "pod_k1_rope.cu", "pod_launch.cu", "pod_api.cu",
+           "pod_planner.cpp", "pod_noalloc.cu", "pod_rope.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -2,7 +2,7 @@
 //
 // Host-side only: argument checks, the planner call, the one metadata upload
 // and the kernel launches. Every step of the attention itself runs in the
-// kernels of pod_kernels.cu.
+// kernels (pod_kernels.cuh, launched through pod_launch.cu).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -38,9 +38,10 @@ struct pod_plan_s {
   const void* rope_table_ws = nullptr;
   void* workspace = nullptr;      // bound device workspace (nullptr = host-only plan)
   size_t workspace_bytes = 0;
-  // TMA descriptors of the last run, re-encoded only when a tensor pointer changes
-  const void* tm_ptr[4] = {nullptr, nullptr, nullptr, nullptr};
-  CUtensorMap tm[4];
+  // TMA descriptors of the last run, re-encoded only when a tensor pointer
+  // changes: q_p, kv_p, q_d, kv_d, then (RoPE) the low parts of q_p and q_d
+  const void* tm_ptr[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  CUtensorMap tm[6];
 };
 
 namespace {
@@ -120,21 +121,23 @@ pod_status encode_q(CUtensorMap* m, const void* ptr, int rows, int H, int d, int
   return POD_OK;
 }
 
-// Paged cache viewed as [pages][2][ps][Hk][d] (dims listed the same way for
-// an HND cache, [pages][2][Hk][ps][d] in memory, with its strides); a box holds `kbx` keys:
-// 64 elements x 1 head x kbx slots x 1 x 1 page when ps >= 8 (kbx <= ps), or
-// 64 x 1 x ps slots x 1 x (kbx / ps) pages when ps < 8.
+// Paged cache viewed as [pages][nkv][ps][Hk][d] (dims listed the same way for
+// an HND cache, [pages][nkv][Hk][ps][d] in memory, with its strides); nkv = 2
+// (K, V), or 3 for the RoPE prefill copies (K_hi, V, K_lo). A box holds `kbx`
+// keys: 64 elements x 1 head x kbx slots x 1 x 1 page when ps >= 8
+// (kbx <= ps), or 64 x 1 x ps slots x 1 x (kbx / ps) pages when ps < 8.
 pod_status encode_kv(CUtensorMap* m, const void* ptr, int num_pages, int ps, int Hk, int d,
-                     int kbx, int dtype, int hnd) {
+                     int kbx, int dtype, int hnd, int nkv) {
   auto fn = encode_fn();
   if (!fn) return set_err(POD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   if ((reinterpret_cast<uintptr_t>(ptr) & 15u) != 0)
     return set_err(POD_ERR_INVALID_ARG, "kv caches must be 16-byte aligned");
-  cuuint64_t dims[5] = {(cuuint64_t)d, (cuuint64_t)Hk, (cuuint64_t)ps, 2, (cuuint64_t)num_pages};
+  cuuint64_t dims[5] = {(cuuint64_t)d, (cuuint64_t)Hk, (cuuint64_t)ps, (cuuint64_t)nkv,
+                        (cuuint64_t)num_pages};
   cuuint64_t row = (cuuint64_t)d * 2;
   // the same logical dims for both layouts; HND swaps the head and slot strides
   cuuint64_t strides[4] = {hnd ? row * ps : row, hnd ? row : row * Hk, row * Hk * ps,
-                           row * Hk * ps * 2};
+                           row * Hk * ps * nkv};
   cuuint32_t box[5] = {64, 1, (cuuint32_t)(ps >= 8 ? kbx : ps), 1,
                        (cuuint32_t)(ps >= 8 ? 1 : kbx / ps)};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
@@ -244,7 +247,7 @@ pod_status replan(pod_plan_s* h, const PodPlanArgs& a) {
   h->workspace = nullptr;
   h->workspace_bytes = 0;
   h->rope_table_ws = nullptr;
-  for (int i = 0; i < 4; ++i) h->tm_ptr[i] = nullptr;
+  for (int i = 0; i < 6; ++i) h->tm_ptr[i] = nullptr;
   return POD_OK;
 }
 
@@ -357,13 +360,17 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
   }
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  // RoPE: rotated copies of the queries and of every page-table entry's page
-  // (NHD) are written into the workspace; the kernels read those instead
+  // RoPE: the rotated queries of both halves (high and low parts) and copies
+  // of the prefill half's pages (K_hi, V, K_lo) are written into the
+  // workspace; the kernels read those, and rotate the decode keys themselves
   int p_layout = h->p_layout, d_layout = h->d_layout;
   int p_pages = P.p.num_pages, d_pages = P.dd.num_pages;
+  const void* q_p_lo = nullptr;
+  const void* q_d_lo = nullptr;
+  const float2* rope_tab = nullptr;
   if (P.rope) {
     cudaStream_t st = (cudaStream_t)stream;
-    const float2* table = reinterpret_cast<const float2*>(ws + P.off_rope_table);
+    rope_tab = reinterpret_cast<const float2*>(ws + P.off_rope_table);
     if (h->rope_table_ws != workspace) {
       PodRopeFreq f;
       for (int j = 0; j < P.d / 2; ++j)
@@ -383,47 +390,54 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
       if (hh.rows == 0) continue;
       PodRopeQ q;
       q.q_src = half ? q_d : q_p;
-      q.q_dst = ws + (half ? P.off_d_qcopy : P.off_p_qcopy);
+      q.q_hi = ws + (half ? P.off_d_qcopy : P.off_p_qcopy);
+      q.q_lo = ws + (half ? P.off_d_qcopy_lo : P.off_p_qcopy_lo);
       q.qpos = I32(half ? P.off_d_rope_qpos : P.off_p_rope_qpos);
-      q.table = table;
+      q.table = rope_tab;
       q.rows = hh.rows; q.H = P.H; q.d = P.d;
       cudaError_t e = pod_rope_q(q, P.dtype, st);
       if (e != cudaSuccess) return cuda_err(e, "RoPE query launch");
+    }
+    if (P.p.rows > 0) {
       PodRopeKV k;
-      k.kv_src = half ? kv_d : kv_p;
-      k.kv_dst = ws + (half ? P.off_d_kvcopy : P.off_p_kvcopy);
-      k.src_pages = I32(half ? P.off_d_rope_src : P.off_p_rope_src);
-      k.ent = I32(half ? P.off_d_rope_ent : P.off_p_rope_ent);
-      k.table = table;
-      k.entries = (int)hh.kv_indices.size(); k.ps = P.ps; k.Hk = P.Hk; k.d = P.d;
-      k.hnd = half ? h->d_layout : h->p_layout;
-      e = pod_rope_kv(k, P.dtype, st);
-      if (e != cudaSuccess) return cuda_err(e, "RoPE key launch");
+      k.kv_src = kv_p;
+      k.kv_dst = ws + P.off_p_kvcopy;
+      k.src_pages = I32(P.off_p_rope_src);
+      k.ent = I32(P.off_p_rope_ent);
+      k.table = rope_tab;
+      k.entries = (int)P.p.kv_indices.size(); k.ps = P.ps; k.Hk = P.Hk; k.d = P.d;
+      k.hnd = h->p_layout;
+      cudaError_t e = pod_rope_kv(k, P.dtype, st);
+      if (e != cudaSuccess) return cuda_err(e, "RoPE prefill key launch");
     }
     q_p = ws + P.off_p_qcopy; kv_p = ws + P.off_p_kvcopy;
-    q_d = ws + P.off_d_qcopy; kv_d = ws + P.off_d_kvcopy;
-    p_layout = d_layout = 0;
+    q_p_lo = ws + P.off_p_qcopy_lo;
+    q_d = ws + P.off_d_qcopy;
+    q_d_lo = ws + P.off_d_qcopy_lo;
+    p_layout = 0;
     p_pages = (int)P.p.kv_indices.size();
-    d_pages = (int)P.dd.kv_indices.size();
   }
 
   // TMA descriptors for the tensors of this call (cached while pointers repeat)
-  const void* ptrs[4] = {q_p, kv_p, q_d, kv_d};
-  for (int i = 0; i < 4; ++i) {
-    const bool pre = i < 2;
+  const void* ptrs[6] = {q_p, kv_p, q_d, kv_d, q_p_lo, q_d_lo};
+  for (int i = 0; i < 6; ++i) {
+    const bool pre = i < 2 || i == 4;
     const PodHalfHost& hh = pre ? P.p : P.dd;
     if (hh.rows == 0) continue;
-    if (i % 2 == 1 && !(pre ? P.p_tma : P.d_tma)) continue;
+    if (i >= 4 && !P.rope) continue;
+    if ((i == 1 || i == 3) && !(pre ? P.p_tma : P.d_tma)) continue;
     if (h->tm_ptr[i] == ptrs[i]) continue;
     const int npages = pre ? p_pages : d_pages;
-    pod_status st = (i % 2 == 0)
-        ? encode_q(&h->tm[i], ptrs[i], hh.rows, P.H, P.d, P.G, pre ? P.tq : P.tu, P.dtype)
-        : pre ? encode_kv(&h->tm[i], ptrs[i], npages, P.ps, P.Hk, P.d, P.p_tma, P.dtype, p_layout)
-              : h->d_fp8
-                    ? encode_kv_decode_fp8(&h->tm[i], ptrs[i], npages, P.ps, P.Hk, P.d, P.d_tma,
-                                           d_layout)
-                    : encode_kv_decode(&h->tm[i], ptrs[i], npages, P.ps, P.Hk, P.d, P.d_tma,
-                                       P.dtype, d_layout);
+    pod_status st;
+    if (i == 0 || i == 2 || i >= 4)
+      st = encode_q(&h->tm[i], ptrs[i], hh.rows, P.H, P.d, P.G, pre ? P.tq : P.tu, P.dtype);
+    else if (pre)
+      st = encode_kv(&h->tm[i], ptrs[i], npages, P.ps, P.Hk, P.d, P.p_tma, P.dtype, p_layout,
+                     P.rope ? 3 : 2);
+    else if (h->d_fp8)
+      st = encode_kv_decode_fp8(&h->tm[i], ptrs[i], npages, P.ps, P.Hk, P.d, P.d_tma, d_layout);
+    else
+      st = encode_kv_decode(&h->tm[i], ptrs[i], npages, P.ps, P.Hk, P.d, P.d_tma, P.dtype, d_layout);
     if (st != POD_OK) return st;
     h->tm_ptr[i] = ptrs[i];
   }
@@ -437,6 +451,14 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
   if (P.dd.rows) {
     K.tm_q_d = h->tm[2];
     if (P.d_tma) K.tm_kv_d = h->tm[3];
+  }
+  if (P.rope) {
+    if (P.p.rows) K.tm_qlo_p = h->tm[4];
+    if (P.dd.rows) K.tm_qlo_d = h->tm[5];
+    K.rope = 1;
+    K.rope_rows = P.rope_rows;
+    K.rope_tab = rope_tab;
+    K.q_d_lo = q_d_lo;
   }
   K.p_tma = P.p_tma;
   K.d_tma = P.d_tma;
@@ -518,6 +540,8 @@ pod_status pod_plan_set_logits_transform(pod_handle h, float logits_soft_cap,
     return set_err(POD_ERR_INVALID_ARG, "logits_soft_cap must be finite and >= 0");
   if (logits_soft_cap > 0.f && alibi_slopes)
     return set_err(POD_ERR_UNSUPPORTED, "a soft cap and ALiBi together");
+  if (alibi_slopes && h->plan.rope)
+    return set_err(POD_ERR_UNSUPPORTED, "ALiBi with RoPE (one position encoding at a time)");
   if ((logits_soft_cap > 0.f || alibi_slopes) && h->d_fp8)
     return set_err(POD_ERR_UNSUPPORTED, "a soft cap or ALiBi with an FP8 decode cache");
   h->soft_cap = logits_soft_cap;
@@ -534,6 +558,8 @@ pod_status pod_plan_set_rope(pod_handle h, float rope_scale, float rope_theta) {
     return set_err(POD_ERR_INVALID_ARG, "rope_scale and rope_theta must be finite and positive");
   if (want && h->d_fp8)
     return set_err(POD_ERR_UNSUPPORTED, "RoPE with an FP8 decode cache");
+  if (want && h->alibi)
+    return set_err(POD_ERR_UNSUPPORTED, "RoPE with ALiBi (one position encoding at a time)");
   const PodPlanHost& O = h->plan;
   if (want == O.rope && (!want || (O.rope_scale == rope_scale && O.rope_theta == rope_theta)))
     return POD_OK;

@@ -266,11 +266,23 @@ POD_DEV float soft_cap(float x, float c, float inv_c) {
 
 template <typename T>
 struct Pack;
+// two(): two floats rounded to a packed pair (first in the low half).
+// unpack(): the inverse widening. split(): a, b as high parts (rounded) and
+// low parts (the rounded remainders), so a ~ hi + lo to about twice the
+// type's mantissa.
 template <>
 struct Pack<__nv_bfloat16> {
   static POD_DEV uint32_t two(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+  }
+  static POD_DEV float2 unpack(uint32_t v) {
+    return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&v));
+  }
+  static POD_DEV void split(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = two(a, b);
+    const float2 h = unpack(hi);
+    lo = two(a - h.x, b - h.y);
   }
   static constexpr bool kBF16 = true;
 };
@@ -279,6 +291,12 @@ struct Pack<__half> {
   static POD_DEV uint32_t two(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+  }
+  static POD_DEV float2 unpack(uint32_t v) { return __half22float2(*reinterpret_cast<__half2*>(&v)); }
+  static POD_DEV void split(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = two(a, b);
+    const float2 h = unpack(hi);
+    lo = two(a - h.x, b - h.y);
   }
   static constexpr bool kBF16 = false;
 };

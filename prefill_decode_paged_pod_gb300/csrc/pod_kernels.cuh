@@ -1,4 +1,8 @@
-// pod_kernels.cu — the fused POD launch for sm_103a and the split merge.
+// pod_kernels.cuh — the fused POD kernel for sm_103a (K1), as templates.
+//
+// Each variant family is instantiated in its own translation unit
+// (pod_k1_plain.cu, pod_k1_lt.cu, pod_k1_rope.cu) so that they compile in
+// parallel; pod_launch.cu holds the split merge (K2) and the dispatch.
 //
 // K1 `pod_kernel`: one persistent grid; CTA c < n_prefill_ctas runs prefill
 // tiles, the other CTAs run decode items (POD walkthrough, "POD 是什么": one
@@ -24,12 +28,22 @@
 //    warps combine through shared memory and write the final output, or an
 //    fp32 partial (o, lse) when the plan split the KV range.
 //
-// K2 `pod_merge_kernel`: merges the split partials of each row with base-2
-// LSE weights, adds the sink, writes out and LSE (flashinfer.cudnn page,
-// "LSE 契约": base-2 LSE feeds a cascade merge). Launched with programmatic
-// dependent launch; it waits on griddepcontrol.wait (POD walkthrough, "PDL").
+// ROPE_LLAMA (template flag RP, FlashInfer guide, "快速上手": pos_encoding_mode
+// with rope_scale and rope_theta): queries arrive rotated, as a 16-bit high
+// part and a 16-bit low part (q = q_hi + q_lo to about 16 bits of mantissa),
+// from a pre-pass. The prefill keys arrive the same way (copies of the
+// prefill pages, K_hi / V / K_lo per page). The decode keys are rotated in
+// registers from the caller's cache, right after ldmatrix, in fp32, then
+// split into high and low parts. Both halves form each logit from three
+// products q_hi.k_hi + q_hi.k_lo + q_lo.k_hi, so no rotated operand is
+// rounded to 16 bits. The RoPE kernel runs one CTA per SM: the low parts
+// need the shared memory of a second CTA.
+#pragma once
 #include <cuda_runtime.h>
 #include <math.h>
+
+#include <atomic>
+#include <mutex>
 
 #include "pod_device.cuh"
 #include "pod_launch.h"
@@ -42,16 +56,19 @@ namespace {
 constexpr int kThreads = 256;
 
 // ------------------------------------------------------------------ layouts
-template <int D>
+template <int D, bool RP>
 struct PLayout {                                   // prefill shared memory
   static constexpr int NKB = D / 64;               // 64-element K blocks of head_dim
   static constexpr int QBLK = POD_TILE_ROWS * 128; // 128 rows x 128 B
   static constexpr int KVBLK = POD_KBLOCK * 128;   // 64 rows x 128 B
   static constexpr int KSTAGE = NKB * KVBLK;       // one 64-key K or V block
+  static constexpr int NQ = RP ? 2 : 1;            // Q tile (RoPE: high, then low part)
+  static constexpr int KSTEP = NQ * KSTAGE;        // K stage (RoPE: high, then low part)
   static constexpr int NK = 3, NV = 2;             // K and V stage rings
   static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + NKB * QBLK;
-  static constexpr int V_OFF = K_OFF + NK * KSTAGE;
+  static constexpr int QLO_OFF = Q_OFF + NKB * QBLK;
+  static constexpr int K_OFF = Q_OFF + NQ * NKB * QBLK;
+  static constexpr int V_OFF = K_OFF + NK * KSTEP;
   static constexpr int BAR_OFF = V_OFF + NV * KSTAGE;
   // BAR_OFF + 0: mbarriers, +224: TMEM address, +228: abort flag,
   // +256: tile-id ring [8], +288: published count, +320: per-warp read counts [8]
@@ -61,16 +78,19 @@ struct PLayout {                                   // prefill shared memory
   static constexpr int TM_S = 0, TM_O = 128;
 };
 
-template <int D>
+template <int D, bool RP>
 struct DLayout {                                   // decode shared memory
   static constexpr int NKB = D / 64;
   static constexpr int QDH = POD_DECODE_ROWS * 128; // one 64-column half of Q: 32 rows x 128 B
   static constexpr int KDH = POD_DECODE_STAGE * 128;// one half of a 64-key K or V block
   static constexpr int KBYTES = NKB * KDH;
   static constexpr int STAGE_BYTES = 2 * KBYTES;    // K then V
-  static constexpr int NSTAGE = 3;
+  // RoPE runs one CTA per SM: a deeper ring keeps the bytes in flight per SM
+  static constexpr int NSTAGE = RP ? 6 : 3;
+  static constexpr int NQ = RP ? 2 : 1;             // Q (RoPE: high, then low part)
   static constexpr int Q_OFF = 0;
-  static constexpr int STAGE_OFF = NKB * QDH;
+  static constexpr int QLO_OFF = NKB * QDH;
+  static constexpr int STAGE_OFF = NQ * NKB * QDH;
   static constexpr int BAR_OFF = STAGE_OFF + NSTAGE * STAGE_BYTES;
   static constexpr int TOTAL = BAR_OFF + 128;
   // FP8 (E4M3) cache, head_dim 128 only: the ring holds one-byte codes,
@@ -83,11 +103,13 @@ struct DLayout {                                   // decode shared memory
   static constexpr int SCR_ML = STAGE_OFF + 8 * 16 * D * 4;
   static_assert(SCR_ML + 8 * 16 * 2 * 4 <= BAR_OFF, "combine scratch must fit in the stages");
   static_assert(STAGE_OFF % 1024 == 0, "stages must be 1024-byte aligned");
+  static_assert(NSTAGE * 8 <= 64, "stage barriers overlap the abort flag");
 };
 
-template <int D>
+template <int D, bool RP>
 constexpr int smem_bytes() {
-  return PLayout<D>::TOTAL > DLayout<D>::TOTAL ? PLayout<D>::TOTAL : DLayout<D>::TOTAL;
+  return PLayout<D, RP>::TOTAL > DLayout<D, RP>::TOTAL ? PLayout<D, RP>::TOTAL
+                                                       : DLayout<D, RP>::TOTAL;
 }
 
 POD_DEV void raise_status(int32_t* status, int code) { atomicOr(status, code); }
@@ -118,9 +140,9 @@ enum {
 // tiles from the global queue and publishes them in order on a small ring in
 // shared memory; every other warp that walks tiles reads the same sequence.
 // Returns false when a wait ran out (the status word then says so).
-template <typename T, int D, int LT>
+template <typename T, int D, int LT, bool RP>
 __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
-  using L = PLayout<D>;
+  using L = PLayout<D, RP>;
   constexpr int NK = L::NK, NV = L::NV;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_u32(smem);
@@ -203,7 +225,7 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
     fence_proxy_async();  // generic accesses of an earlier decode phase come first
     int kfill = 0, vfill = 0, qfill = 0;
     bool ok = true;
-    const uint32_t q_bytes = (uint32_t)(L::NKB * 128 * G * P.tq);
+    const uint32_t q_bytes = (uint32_t)(L::NQ * L::NKB * 128 * G * P.tq);
     if (P.p_tma) {
       // warp 5 fetches Q and K, warp 6 fetches V, each running ahead on its own
       // ring. Lane i looks up the page of box group i and issues its boxes, so
@@ -226,9 +248,13 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
             if (!warp_wait(BAR(B_QEMPTY), (qfill & 1) ^ 1, abort_flag)) { ok = false; break; }
             if (lane == 0) {
               mbar_arrive_expect_tx(BAR(B_QFULL), q_bytes);
-              for (int dh = 0; dh < L::NKB; ++dh)
+              for (int dh = 0; dh < L::NKB; ++dh) {
                 tma_load_3d(sbase + L::Q_OFF + dh * L::QBLK, &P.tm_q_p, dh * 64, g * G,
                             P.p_q_indptr[req] + tok0, BAR(B_QFULL));
+                if (RP)
+                  tma_load_3d(sbase + L::QLO_OFF + dh * L::QBLK, &P.tm_qlo_p, dh * 64, g * G,
+                              P.p_q_indptr[req] + tok0, BAR(B_QFULL));
+              }
             }
             ++qfill;
           }
@@ -240,9 +266,9 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
             const int s = fill % NS;
             const int empty = (is_v ? B_VEMPTY : B_KEMPTY) + s, full = (is_v ? B_VFULL : B_KFULL) + s;
             if (!warp_wait(BAR(empty), ((fill / NS) & 1) ^ 1, abort_flag)) { ok = false; break; }
-            if (lane == 0) mbar_arrive_expect_tx(BAR(full), (uint32_t)L::KSTAGE);
+            if (lane == 0) mbar_arrive_expect_tx(BAR(full), (uint32_t)(is_v ? L::KSTAGE : L::KSTEP));
             __syncwarp();
-            const uint32_t dst0 = sbase + (is_v ? L::V_OFF : L::K_OFF) + s * L::KSTAGE;
+            const uint32_t dst0 = is_v ? sbase + L::V_OFF + s * L::KSTAGE : sbase + L::K_OFF + s * L::KSTEP;
             const int kb = b0 + j * POD_KBLOCK;
             for (int gi = lane; gi < ngroups; gi += 32) {
               const int o = gi * P.p_tma;
@@ -250,9 +276,14 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
               const int pidx = t >> P.ps_shift;
               const int page = pidx < npages ? __ldg(P.p_kv_indices + page_base + pidx) : P.p_num_pages;
               const int tin = P.ps >= 8 ? (t & (P.ps - 1)) : 0;
-              for (int dh = 0; dh < L::NKB; ++dh)
+              for (int dh = 0; dh < L::NKB; ++dh) {
                 tma_load_5d(dst0 + dh * L::KVBLK + o * 128, tkv, dh * 64, g, tin, is_v ? 1 : 0, page,
                             BAR(full));
+                // RoPE copies hold K_hi, V, K_lo per page: the low part is row 2
+                if (RP && !is_v)
+                  tma_load_5d(dst0 + L::KSTAGE + dh * L::KVBLK + o * 128, tkv, dh * 64, g, tin, 2,
+                              page, BAR(full));
+              }
             }
             if (is_v) ++vfill; else ++kfill;
           }
@@ -263,6 +294,7 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
       const int lt = tid - 160;  // 0..95
       const T* __restrict__ kvg = reinterpret_cast<const T*>(P.kv_p);
       const size_t vstride = (size_t)P.ps * P.Hk * D;   // K row -> V row of the same page
+      constexpr int NKV = RP ? 3 : 2;                    // rows per page (RoPE: K_hi, V, K_lo)
       constexpr int KCH = POD_KBLOCK * (D / 8);
       constexpr int PER = (KCH + 95) / 96;
       for (int seq = 0; ok; ++seq) {
@@ -276,9 +308,13 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
           if (!mbar_wait(BAR(B_QEMPTY), (qfill & 1) ^ 1, abort_flag)) ok = false;
           if (ok) {
             mbar_arrive_expect_tx(BAR(B_QFULL), q_bytes);
-            for (int dh = 0; dh < L::NKB; ++dh)
+            for (int dh = 0; dh < L::NKB; ++dh) {
               tma_load_3d(sbase + L::Q_OFF + dh * L::QBLK, &P.tm_q_p, dh * 64, g * G,
                           P.p_q_indptr[req] + tok0, BAR(B_QFULL));
+              if (RP)
+                tma_load_3d(sbase + L::QLO_OFF + dh * L::QBLK, &P.tm_qlo_p, dh * 64, g * G,
+                            P.p_q_indptr[req] + tok0, BAR(B_QFULL));
+            }
           }
         }
         ++qfill;
@@ -308,10 +344,13 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
               const int tt = valid ? t : kb;
               const int slot = P.ps_shift >= 0 ? (tt & (P.ps - 1)) : (tt % P.ps);
               const T* src = kvg + (P.p_hnd
-                  ? (((size_t)pages[i] * 2 * P.Hk + g) * P.ps + slot) * D + c * 8
-                  : (((size_t)pages[i] * 2 * P.ps + slot) * P.Hk + g) * D + c * 8);
+                  ? (((size_t)pages[i] * NKV * P.Hk + g) * P.ps + slot) * D + c * 8
+                  : (((size_t)pages[i] * NKV * P.ps + slot) * P.Hk + g) * D + c * 8);
               cp_async16(dst_base + (c >> 3) * L::KVBLK + sw128_off(key, c & 7),
                          is_v ? src + vstride : src, valid ? 16u : 0u);
+              if (RP && !is_v)
+                cp_async16(dst_base + L::KSTAGE + (c >> 3) * L::KVBLK + sw128_off(key, c & 7),
+                           src + 2 * vstride, valid ? 16u : 0u);
             }
           }
         };
@@ -319,7 +358,7 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
           if (st < nb) {
             const int s = kfill % NK;
             if (!mbar_wait(BAR(B_KEMPTY + s), ((kfill / NK) & 1) ^ 1, abort_flag)) { ok = false; break; }
-            load_block(st, false, sbase + L::K_OFF + s * L::KSTAGE);
+            load_block(st, false, sbase + L::K_OFF + s * L::KSTEP);
             cp_async_mbar_arrive(BAR(B_KFULL + s));
             ++kfill;
           }
@@ -370,12 +409,21 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
             if (!P.p_tma) fence_proxy_async();
             const int b = (sc0 + j) & 1;
             const uint32_t qa = sbase + L::Q_OFF;
-            const uint32_t ka = sbase + L::K_OFF + s * L::KSTAGE;
+            const uint32_t ka = sbase + L::K_OFF + s * L::KSTEP;
 #pragma unroll
             for (int k = 0; k < D / 16; ++k) {
-              const uint64_t ad = sdesc_sw128(qa + (k >> 2) * L::QBLK + (k & 3) * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(ka + (k >> 2) * L::KVBLK + (k & 3) * 32, 16, 1024);
+              const uint32_t qo = (k >> 2) * L::QBLK + (k & 3) * 32;
+              const uint32_t ko = (k >> 2) * L::KVBLK + (k & 3) * 32;
+              const uint64_t ad = sdesc_sw128(qa + qo, 16, 1024);
+              const uint64_t bd = sdesc_sw128(ka + ko, 16, 1024);
               mma_f16_ss(tmem + L::TM_S + b * POD_KBLOCK, ad, bd, id_qk, k > 0 ? 1u : 0u);
+              if (RP) {
+                // q.k = q_hi.k_hi + q_hi.k_lo + q_lo.k_hi (q_lo.k_lo is below fp32 rounding)
+                const uint64_t adl = sdesc_sw128(qa + (L::QLO_OFF - L::Q_OFF) + qo, 16, 1024);
+                const uint64_t bdl = sdesc_sw128(ka + L::KSTAGE + ko, 16, 1024);
+                mma_f16_ss(tmem + L::TM_S + b * POD_KBLOCK, ad, bdl, id_qk, 1u);
+                mma_f16_ss(tmem + L::TM_S + b * POD_KBLOCK, adl, bd, id_qk, 1u);
+              }
             }
             mma_commit(BAR(B_SFULL + b));
             mma_commit(BAR(B_KEMPTY + s));
@@ -470,7 +518,8 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
         const uint32_t s_addr = tmem + lane_base + L::TM_S + b * POD_KBLOCK;
         float s[POD_KBLOCK];
         tmem_ld64(s_addr, s);
-        if constexpr (LT == POD_LT_SOFTCAP) {
+        // (the RoPE kernel takes the soft cap as a run-time switch)
+        if (LT == POD_LT_SOFTCAP || (RP && P.lt == POD_LT_SOFTCAP)) {
           // cap * tanh(x / cap) of the scaled logit, kept in raw q.k units
           const float c = P.lt_c, ic = 1.f / P.lt_c;
 #pragma unroll
@@ -496,16 +545,18 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
           for (int i = 0; i < POD_KBLOCK; ++i)
             if (!((bits >> i) & 1ull)) s[i] = NEG_INF;
         }
-        // row max with three-input max: four independent chains
+        // row max with three-input max: four independent chains over s[4..59]
+        // (seven steps of eight), then s[60..63] one per chain
+        static_assert(POD_KBLOCK == 64, "the max chains cover 64 columns");
         float c0 = s[0], c1 = s[1], c2 = s[2], c3 = s[3];
 #pragma unroll
-        for (int i = 4; i < POD_KBLOCK; i += 8) {
+        for (int i = 4; i + 8 <= POD_KBLOCK; i += 8) {
           c0 = max3(c0, s[i], s[i + 1]);
           c1 = max3(c1, s[i + 2], s[i + 3]);
           c2 = max3(c2, s[i + 4], s[i + 5]);
           c3 = max3(c3, s[i + 6], s[i + 7]);
         }
-        const float bmax = max3(fmaxf(c0, c1), c2, c3);
+        const float bmax = max3(max3(c0, c1, s[60]), max3(c2, c3, s[61]), fmaxf(s[62], s[63]));
         const float scale = P.scale_log2;
         const float m_new = fmaxf(m_ref, bmax * scale);
         const bool rescale = m_new > m_ref + 8.0f;   // also true for the first finite max
@@ -619,9 +670,9 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
 // ============================================================ decode role
 // Runs decode items from the shared queue until it is empty. Returns false
 // when a wait ran out (the status word then says so).
-template <typename T, int D, bool F8, int LT>
+template <typename T, int D, bool F8, int LT, bool RP>
 __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
-  using L = DLayout<D>;
+  using L = DLayout<D, RP>;
   constexpr bool BF16 = Pack<T>::kBF16;
   constexpr int NKB = L::NKB;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -644,7 +695,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
     tma_prefetch_desc(&P.tm_kv_d);
     tma_prefetch_desc(&P.tm_q_d);
   }
-  const uint32_t q_bytes = (uint32_t)(NKB * 128 * G * P.tu);
+  const uint32_t q_bytes = (uint32_t)(L::NQ * NKB * 128 * G * P.tu);
   // K/V stage layout: [key / kbx][d half][key % kbx][64 elements] in 128-byte
   // swizzled rows, kbx = keys per TMA box (64 on the cp.async path, where it
   // is [d half][key][64]). Row offset of key k in its d half 0:
@@ -702,9 +753,13 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
             mbar_arrive_expect_tx(full, (F8 ? (uint32_t)L::F8_STAGE : 2u * L::KBYTES) +
                                             (st == 0 ? q_bytes : 0u));
             if (st == 0)
-              for (int dh = 0; dh < NKB; ++dh)
+              for (int dh = 0; dh < NKB; ++dh) {
                 tma_load_3d(sbase + L::Q_OFF + dh * L::QDH, &P.tm_q_d, dh * 64, g * G, q_base + tok0,
                             full);
+                if (RP)
+                  tma_load_3d(sbase + L::QLO_OFF + dh * L::QDH, &P.tm_qlo_d, dh * 64, g * G,
+                              q_base + tok0, full);
+              }
           }
           __syncwarp();
           if (F8 && lane < POD_DECODE_STAGE / P.d_tma) {
@@ -743,9 +798,12 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
             const bool valid = r < R;
             const int tok = tok0 + (valid ? r / G : 0);
             const int head = g * G + (valid ? r % G : 0);
-            const T* src = qg + ((size_t)(q_base + tok) * H + head) * D + c * 8;
-            cp_async16(sbase + L::Q_OFF + (c >> 3) * L::QDH + sw128_off(r, c & 7), src,
+            const size_t qoff = ((size_t)(q_base + tok) * H + head) * D + c * 8;
+            cp_async16(sbase + L::Q_OFF + (c >> 3) * L::QDH + sw128_off(r, c & 7), qg + qoff,
                        valid ? 16u : 0u);
+            if (RP)
+              cp_async16(sbase + L::QLO_OFF + (c >> 3) * L::QDH + sw128_off(r, c & 7),
+                         reinterpret_cast<const T*>(P.q_d_lo) + qoff, valid ? 16u : 0u);
           }
         }
         if constexpr (F8) {
@@ -883,6 +941,58 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
                              e4m3x2_to<T>((uint16_t)(k1 >> 16)));
             }
           }
+        } else if constexpr (RP) {
+          // Keys rotated in registers: chunk kk (d 16kk..) pairs with chunk
+          // kk + D/32 (d + D/2). A thread holds, for its keys ka (b[0], b[1])
+          // and ka + 8 (b[2], b[3]), elements j = 16kk + 2(lane%4) + {0, 1}
+          // (b[0], b[2]) and j + 8 (b[1], b[3]) of both chunks; each pair turns
+          // by the angle of (key, j) from the cos/sin table (fp32 values of fp64
+          // sincos), then splits into 16-bit high and low parts.
+          constexpr int NC = D / 32;
+          const int ta = min(kbase + (lane >> 2), P.rope_rows - 1);
+          const int tb = min(kbase + 8 + (lane >> 2), P.rope_rows - 1);
+          const float4* tra = reinterpret_cast<const float4*>(P.rope_tab + (size_t)ta * (D / 2));
+          const float4* trb = reinterpret_cast<const float4*>(P.rope_tab + (size_t)tb * (D / 2));
+#pragma unroll
+          for (int kk = 0; kk < NC; ++kk) {
+            uint32_t bx[4], by[4];
+            {
+              const int key = ks * 16 + (lane & 7) + ((mi >> 1) << 3);
+              const int c0 = kk * 2 + (mi & 1), c1 = (kk + NC) * 2 + (mi & 1);
+              ldsm_x4(sk + key_row(key) + (c0 >> 3) * half_stride + (((c0 & 7) ^ (lane & 7)) << 4),
+                      bx[0], bx[1], bx[2], bx[3]);
+              ldsm_x4(sk + key_row(key) + (c1 >> 3) * half_stride + (((c1 & 7) ^ (lane & 7)) << 4),
+                      by[0], by[1], by[2], by[3]);
+            }
+            const float4 cs[4] = {__ldg(tra + 8 * kk + (lane & 3)), __ldg(tra + 8 * kk + 4 + (lane & 3)),
+                                  __ldg(trb + 8 * kk + (lane & 3)), __ldg(trb + 8 * kk + 4 + (lane & 3))};
+            uint32_t xh[4], xl[4], yh[4], yl[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 x = Pack<T>::unpack(bx[i]), y = Pack<T>::unpack(by[i]);
+              const float x0 = fmaf(x.x, cs[i].x, -y.x * cs[i].y), y0 = fmaf(y.x, cs[i].x, x.x * cs[i].y);
+              const float x1 = fmaf(x.y, cs[i].z, -y.y * cs[i].w), y1 = fmaf(y.y, cs[i].z, x.y * cs[i].w);
+              Pack<T>::split(x0, x1, xh[i], xl[i]);
+              Pack<T>::split(y0, y1, yh[i], yl[i]);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int c = (kk + h * NC) * 2 + (mi >> 1);
+              const int rr = mt * 16 + (lane & 7) + ((mi & 1) << 3);
+              uint32_t ah[4], al[4];
+              ldsm_x4(sq + (c >> 3) * L::QDH + sw128_off(rr, c & 7), ah[0], ah[1], ah[2], ah[3]);
+              ldsm_x4(sq + (L::QLO_OFF - L::Q_OFF) + (c >> 3) * L::QDH + sw128_off(rr, c & 7), al[0],
+                      al[1], al[2], al[3]);
+              const uint32_t* bh = h ? yh : xh;
+              const uint32_t* bl = h ? yl : xl;
+              mma16816<BF16>(s0, ah, bh[0], bh[1]);
+              mma16816<BF16>(s0, ah, bl[0], bl[1]);
+              mma16816<BF16>(s0, al, bh[0], bh[1]);
+              mma16816<BF16>(s1, ah, bh[2], bh[3]);
+              mma16816<BF16>(s1, ah, bl[2], bl[3]);
+              mma16816<BF16>(s1, al, bh[2], bh[3]);
+            }
+          }
         } else {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -916,7 +1026,8 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             float x = *v[e];
-            if constexpr (LT == POD_LT_SOFTCAP) x = soft_cap(x, P.lt_c, 1.f / P.lt_c);
+            if (LT == POD_LT_SOFTCAP || (RP && P.lt == POD_LT_SOFTCAP))
+              x = soft_cap(x, P.lt_c, 1.f / P.lt_c);
             if constexpr (LT == POD_LT_ALIBI) x = fmaf(a_slope[h2], (float)(key[e] - a_pd[h2]), x);
             if (key[e] < row_lo[h2] || key[e] >= row_hi[h2]) x = NEG_INF;
             *v[e] = x;
@@ -1107,8 +1218,10 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
 // ============================================================ kernels
 // F8: the decode half reads an FP8 (E4M3) cache (head_dim 128 only).
 // LT: logits transform of both halves (POD_LT_NONE, _SOFTCAP, _ALIBI).
-template <typename T, int D, bool F8, int LT>
-__global__ void __launch_bounds__(kThreads, POD_CTAS_PER_SM) pod_kernel(const __grid_constant__ PodParams P) {
+// RP: ROPE_LLAMA (one CTA per SM; a soft cap is then a run-time switch).
+template <typename T, int D, bool F8, int LT, bool RP>
+__global__ void __launch_bounds__(kThreads, RP ? 1 : POD_CTAS_PER_SM)
+    pod_kernel(const __grid_constant__ PodParams P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   // the merge kernel may start its prologue now; it waits for this grid's completion
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1119,15 +1232,15 @@ __global__ void __launch_bounds__(kThreads, POD_CTAS_PER_SM) pod_kernel(const __
   } else {
     // Every CTA holds 256 TMEM columns for its life (two CTAs fill an SM's
     // 512); giving up the allocation permit at once lets the second CTA in.
-    const uint32_t tslot = smem_u32(smem) + PLayout<D>::BAR_OFF + 224;
+    const uint32_t tslot = smem_u32(smem) + PLayout<D, RP>::BAR_OFF + 224;
     if (warp == 4) {
-      tmem_alloc(tslot, PLayout<D>::TMEM_COLS);
+      tmem_alloc(tslot, PLayout<D, RP>::TMEM_COLS);
       tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + PLayout<D>::BAR_OFF + 224);
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + PLayout<D, RP>::BAR_OFF + 224);
     // Both queues are drained by every CTA: its own role's queue first (the
     // plan sizes the split), then the other one, so whichever half finishes
     // early helps with the rest.
@@ -1139,12 +1252,13 @@ __global__ void __launch_bounds__(kThreads, POD_CTAS_PER_SM) pod_kernel(const __
       // shared memory changes hands between the generic and the async proxy
       fence_proxy_async();
       __syncthreads();
-      ok = do_prefill ? prefill_role<T, D, LT>(P, smem, tmem) : decode_role<T, D, F8, LT>(P, smem);
+      ok = do_prefill ? prefill_role<T, D, LT, RP>(P, smem, tmem)
+                      : decode_role<T, D, F8, LT, RP>(P, smem);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 4) tmem_dealloc(tmem, PLayout<D>::TMEM_COLS);
+    if (warp == 4) tmem_dealloc(tmem, PLayout<D, RP>::TMEM_COLS);
   }
   // the last CTA to finish rewinds the queue counters for the next launch
   if (tid == 0) {
@@ -1157,114 +1271,31 @@ __global__ void __launch_bounds__(kThreads, POD_CTAS_PER_SM) pod_kernel(const __
   }
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(256) pod_merge_kernel(const __grid_constant__ PodParams P) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (gw >= P.n_mrows) return;
-  // merge group containing merge row gw
-  int lo = 0, hi = P.n_groups - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (P.mrow_ptr[mid] <= gw) lo = mid; else hi = mid - 1;
-  }
-  const int32_t* gr = P.mgroups + POD_REC * lo;
-  const int half = gr[0], req = gr[1], g = gr[2], tok0 = gr[3], prow0 = gr[5], nsplit = gr[6],
-            R = gr[7];
-  const int r = gw - P.mrow_ptr[lo];
-  const int tok = tok0 + r / P.G, head = g * P.G + r % P.G;
-  float M = -INFINITY;
-  for (int j = 0; j < nsplit; ++j) M = fmaxf(M, P.part_lse[prow0 + j * R + r]);
-  const float Ms = (M == -INFINITY) ? 0.f : M;
-  constexpr int PER = D / 32;
-  float acc[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-  float wsum = 0.f;
-  for (int j = 0; j < nsplit; ++j) {
-    const int pr = prow0 + j * R + r;
-    const float wgt = ex2(P.part_lse[pr] - Ms);
-    wsum += wgt;
-    const float* src = P.part_o + (size_t)pr * D + lane * PER;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] += wgt * src[i];
-  }
-  float denom = wsum;
-  if (P.has_sinks) denom += ex2(P.sinks[head] * 1.4426950408889634f - Ms);
-  const float inv = denom > 0.f ? 1.f / denom : 0.f;
-  const int q_base = half ? P.d_q_indptr[req] : P.p_q_indptr[req];
-  const size_t orow = (size_t)(q_base + tok) * P.H + head;
-  T* out = reinterpret_cast<T*>(half ? P.out_d : P.out_p) + orow * D + lane * PER;
-#pragma unroll
-  for (int i = 0; i < PER; i += 2) {
-    const uint32_t v = Pack<T>::two(acc[i] * inv, acc[i + 1] * inv);
-    *reinterpret_cast<uint32_t*>(out + i) = v;
-  }
-  float* lse = half ? P.lse_d : P.lse_p;
-  if (lane == 0 && lse) lse[orow] = wsum > 0.f ? M + log2f(wsum) : -INFINITY;
-}
-
-template <typename T, int D, bool F8, int LT>
+// Launches K1 for one variant. The dynamic shared-memory attributes belong to
+// each device's context: they are set once per device (and thread-safely).
+template <typename T, int D, bool F8, int LT, bool RP>
 cudaError_t launch_pod(const PodParams& P, cudaStream_t stream) {
-  constexpr int SMEM = smem_bytes<D>();
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(pod_kernel<T, D, F8, LT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  constexpr int SMEM = smem_bytes<D, RP>();
+  static std::atomic<unsigned long long> done{0ull};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit == 0ull || !(done.load(std::memory_order_acquire) & bit)) {
+    std::lock_guard<std::mutex> lock(mu);
+    e = cudaFuncSetAttribute(pod_kernel<T, D, F8, LT, RP>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     // two CTAs per SM need the largest shared-memory carveout
-    e = cudaFuncSetAttribute(pod_kernel<T, D, F8, LT>,
+    e = cudaFuncSetAttribute(pod_kernel<T, D, F8, LT, RP>,
                              cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    done.fetch_or(bit, std::memory_order_acq_rel);
   }
-  pod_kernel<T, D, F8, LT><<<P.grid, kThreads, SMEM, stream>>>(P);
+  pod_kernel<T, D, F8, LT, RP><<<P.grid, kThreads, SMEM, stream>>>(P);
   return cudaGetLastError();
 }
 
-template <typename T, int D>
-cudaError_t launch_impl(const PodParams& P, cudaStream_t stream) {
-  if (P.grid > 0) {
-    cudaError_t e;
-    // the host refuses a logits transform with an FP8 decode cache
-    if (P.lt == POD_LT_SOFTCAP)
-      e = launch_pod<T, D, false, POD_LT_SOFTCAP>(P, stream);
-    else if (P.lt == POD_LT_ALIBI)
-      e = launch_pod<T, D, false, POD_LT_ALIBI>(P, stream);
-    else if constexpr (D == 128)
-      e = P.d_fp8 ? launch_pod<T, D, true, POD_LT_NONE>(P, stream)
-                  : launch_pod<T, D, false, POD_LT_NONE>(P, stream);
-    else
-      e = launch_pod<T, D, false, POD_LT_NONE>(P, stream);
-    if (e != cudaSuccess) return e;
-  }
-  if (P.n_mrows > 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((P.n_mrows + 7) / 8));
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, pod_merge_kernel<T, D>, P);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
-}
-
 }  // namespace
-
-cudaError_t pod_launch(const PodParams& P, int dtype, cudaStream_t stream) {
-  if (P.d == 128) {
-    return dtype == 1 ? launch_impl<__nv_bfloat16, 128>(P, stream)
-                      : launch_impl<__half, 128>(P, stream);
-  }
-  return dtype == 1 ? launch_impl<__nv_bfloat16, 64>(P, stream) : launch_impl<__half, 64>(P, stream);
-}
-
-int pod_kernel_smem_bytes(int d) { return d == 128 ? smem_bytes<128>() : smem_bytes<64>(); }

@@ -37,6 +37,7 @@
 #pragma once
 #include <cuda.h>
 #include <stdint.h>
+#include <vector_types.h>
 
 #define POD_REC 8
 #define POD_DQREC 16
@@ -64,6 +65,8 @@ struct PodParams {
   // as [pages, 2, ps, Hk, d] (box 64 x 1 x rows x 1 x pages); valid when the
   // half's *_tma flag is set (Q maps whenever the half is non-empty).
   CUtensorMap tm_q_p, tm_kv_p, tm_q_d, tm_kv_d;
+  // RoPE: the low parts of the rotated queries, [rows, H, d] like tm_q_*
+  CUtensorMap tm_qlo_p, tm_qlo_d;
   int p_tma, d_tma;          // keys per TMA K/V box of the half; 0 = cp.async gather
   int p_num_pages, d_num_pages;
   int tq, tu;                // tokens per prefill tile / per decode unit
@@ -95,6 +98,12 @@ struct PodParams {
   int32_t* status;           // device status word
   const void *q_p, *kv_p, *q_d, *kv_d;
   const float* sinks;
+  // RoPE (ROPE_LLAMA): rope = 1; q_* point at the rotated high parts and
+  // q_d_lo at the decode low parts; kv_p at the prefill copies (K_hi, V, K_lo
+  // per page); rope_tab = (cos, sin) [rope_rows][d/2] of position x frequency
+  int rope, rope_rows;
+  const void* q_d_lo;
+  const float2* rope_tab;
   // custom prefill mask (NULL = none): packed bits, little bit order, of each
   // request's [q_len, kv_len] matrix; p_mask_off[r] = request r's first bit
   const uint8_t* p_mask;

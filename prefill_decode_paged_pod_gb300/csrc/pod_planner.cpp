@@ -81,8 +81,9 @@ CostModel cost_model(int d) {
 }
 
 // Co-residency class of CTA c (0 alone, 1 other role, 2 same role) when CTAs
-// [0, n_p) run prefill and [n_p, n_p + n_d) decode.
-int neighbour_class(int c, int n_p, int n_d, int S) {
+// [0, n_p) run prefill and [n_p, n_p + n_d) decode, `cps` CTAs per SM.
+int neighbour_class(int c, int n_p, int n_d, int S, int cps) {
+  if (cps < 2) return 0;
   const int other = c < S ? c + S : c - S;
   if (other >= n_p + n_d) return 0;
   const bool me_p = c < n_p, other_p = other < n_p;
@@ -455,13 +456,18 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   if (rc) return rc;
   if (P.dd.rows > 0 && G > POD_DECODE_ROWS)
     return fail(err, kUnsupported, "more than 32 qo heads per kv head on the decode half");
+  // The RoPE kernel holds the low parts of the rotated operands and runs one
+  // CTA per SM; the plain kernels run two.
+  const int cps = P.rope ? 1 : POD_CTAS_PER_SM;
+  P.ctas_per_sm = cps;
 
   const CostModel cm = cost_model(a.d);
 
   // ---- decode units ---------------------------------------------------------
   const int Tu = std::max(1, POD_DECODE_ROWS / G);
   P.tu = Tu;
-  // under RoPE the kernels read compact copies through identity page tables
+  // under RoPE the prefill half reads compact copies through an identity
+  // page table; the decode half reads the caller's cache
   auto identity_half = [](const PodHalfHost& h) {
     PodHalfHost c = h;
     for (size_t i = 0; i < c.kv_indices.size(); ++i) c.kv_indices[i] = (int32_t)i;
@@ -470,7 +476,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   P.p_tma = tma_box_keys(P.rope ? identity_half(P.p) : P.p, a.ps);
   // decode boxes hold both 64-element halves of head_dim; they are laid out
   // for page_size >= 8 (a page per box) and 1 (runs of pages) only
-  P.d_tma = (a.ps == 1 || a.ps >= 8) ? tma_box_keys(P.rope ? identity_half(P.dd) : P.dd, a.ps) : 0;
+  P.d_tma = (a.ps == 1 || a.ps >= 8) ? tma_box_keys(P.dd, a.ps) : 0;
   std::vector<DecodeUnit> units;
   double d_bytes = 0.0;
   for (int r = 0; r < P.dd.batch; ++r) {
@@ -496,7 +502,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   // stream (c4) the tiles already finish early; a split there only adds the
   // merge.
   const int Tq = std::max(1, POD_TILE_ROWS / G);
-  const int grid_cap = a.num_sms * POD_CTAS_PER_SM;
+  const int grid_cap = a.num_sms * cps;
   struct TileUnit { int r, g, t0, nt, lo, hi; };
   std::vector<TileUnit> tunits;
   for (int r = 0; r < P.p.batch; ++r) {
@@ -558,13 +564,14 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
 
   // ---- CTA split between the halves ----------------------------------------
   const int S = a.num_sms;
-  const int grid_max = S * POD_CTAS_PER_SM;
+  const int grid_max = S * cps;
   // per-CTA rates for a split: prefill in blocks per ns, decode in bytes per ns
   auto rates = [&](int n_p, int n_d, std::vector<double>& rp, std::vector<double>& rd) {
     rp.resize(n_p);
     rd.resize(n_d);
-    for (int c = 0; c < n_p; ++c) rp[c] = 1.0 / cm.p_block_ns[neighbour_class(c, n_p, n_d, S)];
-    for (int c = 0; c < n_d; ++c) rd[c] = cm.d_bytes_per_ns[neighbour_class(n_p + c, n_p, n_d, S)];
+    for (int c = 0; c < n_p; ++c) rp[c] = 1.0 / cm.p_block_ns[neighbour_class(c, n_p, n_d, S, cps)];
+    for (int c = 0; c < n_d; ++c)
+      rd[c] = cm.d_bytes_per_ns[neighbour_class(n_p + c, n_p, n_d, S, cps)];
   };
   int n_p = 0;
   int chunk = 0;
@@ -614,7 +621,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
       w.p_ns.resize(n);
       w.d_rate.resize(n);
       for (int c = 0; c < n; ++c) {
-        const int cls = neighbour_class(c, np, n - np, S);
+        const int cls = neighbour_class(c, np, n - np, S, cps);
         w.p_ns[c] = cm.p_block_ns[cls];
         w.d_rate[c] = cm.d_bytes_per_ns[cls];
         w.c[c] = c;   // all loads zero: index order is a valid heap
@@ -783,18 +790,21 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
     P.p_mask_bits = bit;
   }
 
-  // ---- RoPE pre-pass tables: per page-table entry the position of slot 0 and
-  // the slots below kv_len; per query row its bottom-right position
+  // ---- RoPE pre-pass tables: per prefill page-table entry the position of
+  // slot 0 and the slots below kv_len; per query row of either half its
+  // bottom-right position. The cos/sin table covers every key position of
+  // both halves (decode keys are rotated in the kernel) and every |query
+  // position|.
   P.p_rope_ent.clear(); P.d_rope_ent.clear(); P.p_rope_qpos.clear(); P.d_rope_qpos.clear();
   P.rope_rows = 0;
   if (P.rope) {
     int64_t rows = 1;
-    auto tables = [&](const PodHalfHost& h, std::vector<int32_t>& ent, std::vector<int32_t>& qpos) {
+    auto tables = [&](const PodHalfHost& h, std::vector<int32_t>* ent, std::vector<int32_t>& qpos) {
       for (int r = 0; r < h.batch; ++r) {
         const int np = h.kv_indptr[r + 1] - h.kv_indptr[r];
-        for (int i = 0; i < np; ++i) {
-          ent.push_back(i * P.ps);
-          ent.push_back(std::max(0, std::min(P.ps, h.kv_len[r] - i * P.ps)));
+        for (int i = 0; i < np && ent; ++i) {
+          ent->push_back(i * P.ps);
+          ent->push_back(std::max(0, std::min(P.ps, h.kv_len[r] - i * P.ps)));
         }
         rows = std::max<int64_t>(rows, (int64_t)np * P.ps);
         for (int i = 0; i < h.q_len[r]; ++i) {
@@ -804,8 +814,8 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
         }
       }
     };
-    tables(P.p, P.p_rope_ent, P.p_rope_qpos);
-    tables(P.dd, P.d_rope_ent, P.d_rope_qpos);
+    tables(P.p, &P.p_rope_ent, P.p_rope_qpos);
+    tables(P.dd, nullptr, P.d_rope_qpos);
     P.rope_rows = (int)rows;
   }
 
@@ -837,9 +847,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   P.off_p_mask_off = place(P.p_mask_off.size());
   if (P.rope) {
     P.off_p_rope_src = place(P.p.kv_indices.size());
-    P.off_d_rope_src = place(P.dd.kv_indices.size());
     P.off_p_rope_ent = place(P.p_rope_ent.size());
-    P.off_d_rope_ent = place(P.d_rope_ent.size());
     P.off_p_rope_qpos = place(P.p_rope_qpos.size());
     P.off_d_rope_qpos = place(P.d_rope_qpos.size());
   }
@@ -848,18 +856,23 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   P.off_part_lse = align_up(P.off_part_o + (size_t)n_prows * a.d * 4, 256);
   size_t end = align_up(P.off_part_lse + (size_t)std::max(n_prows, 1) * 4, 256);
   if (P.rope) {
-    // cos/sin table [rows][d/2] (float2), then the rotated copies (16-bit)
-    const size_t page_bytes = (size_t)2 * P.ps * P.Hk * a.d * 2;
+    // cos/sin table [rows][d/2] (float2), then the prefill page copies
+    // (rows K_hi, V, K_lo: 16-bit) and the high and low parts of the rotated
+    // queries of both halves
+    const size_t page_bytes = (size_t)3 * P.ps * P.Hk * a.d * 2;
     P.off_rope_table = end;
     end = align_up(end + (size_t)P.rope_rows * (a.d / 2) * 8, 256);
     P.off_p_kvcopy = end;
     end = align_up(end + P.p.kv_indices.size() * page_bytes, 256);
-    P.off_d_kvcopy = end;
-    end = align_up(end + P.dd.kv_indices.size() * page_bytes, 256);
+    const size_t pq = (size_t)P.p.rows * P.H * a.d * 2, dq = (size_t)P.dd.rows * P.H * a.d * 2;
     P.off_p_qcopy = end;
-    end = align_up(end + (size_t)P.p.rows * P.H * a.d * 2, 256);
+    end = align_up(end + pq, 256);
+    P.off_p_qcopy_lo = end;
+    end = align_up(end + pq, 256);
     P.off_d_qcopy = end;
-    end = align_up(end + (size_t)P.dd.rows * P.H * a.d * 2, 256);
+    end = align_up(end + dq, 256);
+    P.off_d_qcopy_lo = end;
+    end = align_up(end + dq, 256);
   }
   P.total_bytes = end;
 
@@ -879,7 +892,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   put(P.off_p_kv_len, P.p.kv_len);
   put(P.off_d_q_indptr, P.dd.q_indptr);
   put(P.off_d_kv_indptr, P.dd.kv_indptr);
-  put(P.off_d_kv_indices, P.rope ? identity(P.dd.kv_indices.size()) : P.dd.kv_indices);
+  put(P.off_d_kv_indices, P.dd.kv_indices);
   put(P.off_d_kv_len, P.dd.kv_len);
   put(P.off_ptiles, P.ptiles);
   put(P.off_ditems, P.ditems);
@@ -893,9 +906,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   put(P.off_p_mask_off, P.p_mask_off);
   if (P.rope) {
     put(P.off_p_rope_src, P.p.kv_indices);
-    put(P.off_d_rope_src, P.dd.kv_indices);
     put(P.off_p_rope_ent, P.p_rope_ent);
-    put(P.off_d_rope_ent, P.d_rope_ent);
     put(P.off_p_rope_qpos, P.p_rope_qpos);
     put(P.off_d_rope_qpos, P.d_rope_qpos);
   }

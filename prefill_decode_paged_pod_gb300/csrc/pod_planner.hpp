@@ -24,11 +24,13 @@ struct PodPlanHost {
   int64_t p_mask_bits = 0;
   std::vector<int32_t> p_mask_off;
   // rotary position encoding (ROPE_LLAMA) of both halves: a pre-pass writes
-  // rotated copies of each half's queries and of every page-table entry's
-  // page (compact, in page-table order, NHD) into the workspace, and the
-  // kernels read those through identity page tables. Per page-table entry:
-  // the position of its slot 0 and its valid slots; per query row: its
-  // position (negative when a non-causal row lies before the keys).
+  // the rotated queries of both halves (high and low 16-bit parts) and
+  // copies of every prefill page-table entry's page (compact, in page-table
+  // order, NHD, rows K_hi, V, K_lo) into the workspace; the prefill half
+  // reads those through an identity page table, the decode half rotates its
+  // keys in the kernel. Per prefill page-table entry: the position of its
+  // slot 0 and its valid slots; per query row: its position (negative when a
+  // non-causal row lies before the keys). d_rope_ent stays empty.
   int rope = 0;
   double rope_scale = 1.0, rope_theta = 1e4;
   int rope_rows = 0;            // positions covered by the cos/sin table
@@ -38,6 +40,7 @@ struct PodPlanHost {
   PodHalfHost p, dd;
   // schedule
   int grid = 0, n_p_ctas = 0, n_d_ctas = 0, decode_chunk = 0;
+  int ctas_per_sm = POD_CTAS_PER_SM;   // 1 under RoPE
   int p_tma = 0, d_tma = 0;   // keys per TMA K/V box of the half (0 = cp.async gather)
   int tq = 0, tu = 0;         // tokens per prefill tile / decode unit
   std::vector<int32_t> ptiles, ditems, cta_ptr, cta_list, mgroups, mrow_ptr, pqueue, dqueue, dqrec;
@@ -47,10 +50,10 @@ struct PodPlanHost {
          off_p_kv_len = 0, off_d_q_indptr = 0, off_d_kv_indptr = 0, off_d_kv_indices = 0,
          off_d_kv_len = 0, off_ptiles = 0, off_ditems = 0, off_cta_ptr = 0, off_cta_list = 0,
          off_mgroups = 0, off_mrow_ptr = 0, off_pqueue = 0, off_dqueue = 0, off_dqrec = 0,
-         off_p_mask_off = 0, off_p_rope_src = 0, off_d_rope_src = 0, off_p_rope_ent = 0,
-         off_d_rope_ent = 0, off_p_rope_qpos = 0, off_d_rope_qpos = 0, int_bytes = 0,
-         off_part_o = 0, off_part_lse = 0, off_rope_table = 0, off_p_kvcopy = 0,
-         off_d_kvcopy = 0, off_p_qcopy = 0, off_d_qcopy = 0, total_bytes = 0;
+         off_p_mask_off = 0, off_p_rope_src = 0, off_p_rope_ent = 0, off_p_rope_qpos = 0,
+         off_d_rope_qpos = 0, int_bytes = 0, off_part_o = 0, off_part_lse = 0,
+         off_rope_table = 0, off_p_kvcopy = 0, off_p_qcopy = 0, off_p_qcopy_lo = 0,
+         off_d_qcopy = 0, off_d_qcopy_lo = 0, total_bytes = 0;
   std::vector<uint8_t> int_image;   // bytes [0, int_bytes) of the workspace
   std::vector<int32_t> summary;
 };

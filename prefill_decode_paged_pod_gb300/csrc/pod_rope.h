@@ -8,8 +8,9 @@ struct PodRopeFreq {
   double freq[128];
 };
 
-// One half's cache: rotated K and copied V of every page-table entry, written
-// compact (entry i -> page i of kv_dst, NHD [entries, 2, ps, Hk, d]).
+// The prefill half's cache: for every page-table entry, rotated K as a 16-bit
+// high part and low part, and V copied, written compact (entry i -> page i
+// of kv_dst, NHD [entries, 3, ps, Hk, d] with rows K_hi, V, K_lo).
 struct PodRopeKV {
   const void* kv_src;          // the caller's cache, NHD or HND (hnd = 1)
   void* kv_dst;
@@ -19,10 +20,11 @@ struct PodRopeKV {
   int entries, ps, Hk, d, hnd;
 };
 
-// One half's queries: rotated copies of [rows, H, d].
+// One half's queries: rotated copies of [rows, H, d] as high and low parts.
 struct PodRopeQ {
   const void* q_src;
-  void* q_dst;
+  void* q_hi;
+  void* q_lo;
   const int32_t* qpos;         // [rows] position of each query row
   const float2* table;
   int rows, H, d;

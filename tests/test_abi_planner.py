@@ -492,18 +492,24 @@ def test_binding_refuses_host_mask_and_slopes_before_launch(lib):
 
 # ------------------------------------------------------------- RoPE pre-pass plan
 def test_rope_plan_tables(lib):
-    """With RoPE the plan keeps its tiles and items, and its tables give each
-    page-table entry the position of its slot 0 and its slots below kv_len,
-    and each query row its bottom-right position (negative for a non-causal
-    row before the keys); the workspace grows by the rotated copies."""
+    """With RoPE the plan keeps its tiles and items and runs one CTA per SM;
+    its tables give each prefill page-table entry the position of its slot 0
+    and its slots below kv_len (the decode half has no page copies: its keys
+    are rotated in the kernel), and each query row of either half its
+    bottom-right position (negative for a non-causal row before the keys);
+    the workspace grows by the prefill page copies (K_hi, V, K_lo) and the
+    high and low parts of both halves' rotated queries."""
     inp = make_custom("rp", torch.bfloat16, 8, 2, 128, 16, False, -1, [5, 70], [40, 33],
                       [1, 4], [300, 17], seed=5)
     h = plan_host(inp, num_sms=8)
     base = pod.pod_workspace_size(h)
     tiles0 = pod.pod_plan_table(h, 1).copy()
+    items0 = pod.pod_plan_table(h, 2).copy()
     pod.pod_plan_set_rope(h, 2.0, 500.0)
     s = pod.plan_summary(h)
     assert s["rope"] == 1 and np.array_equal(pod.pod_plan_table(h, 1), tiles0)
+    assert np.array_equal(pod.pod_plan_table(h, 2), items0)
+    assert s["grid"] <= 8, "one CTA per SM under RoPE"
     ps = inp.page_size
     for half, hh, te, tq in (("p", inp.p, 12, 14), ("d", inp.d, 13, 15)):
         ent = pod.pod_plan_table(h, te).reshape(-1, 2)
@@ -514,13 +520,15 @@ def test_rope_plan_tables(lib):
                 want.append((i * ps, max(0, min(ps, kvl - i * ps))))
             ql = int(hh.q_indptr[r + 1] - hh.q_indptr[r])
             qpos += [kvl - ql + i for i in range(ql)]
+        if half == "d":
+            want = []
         assert [tuple(x) for x in ent.tolist()] == want, half
         assert pod.pod_plan_table(h, tq).tolist() == qpos, half
-    # rotated copies: every page-table entry's page and both halves' queries
-    page = 2 * ps * 2 * 128 * 2
-    grow = (len(inp.p.kv_indices) + len(inp.d.kv_indices)) * page + \
-        (inp.p.rows + inp.d.rows) * 8 * 128 * 2
+    # prefill page copies (3 rows a page) and both halves' queries (hi + lo)
+    page = 3 * ps * 2 * 128 * 2
+    grow = len(inp.p.kv_indices) * page + (inp.p.rows + inp.d.rows) * 8 * 128 * 2 * 2
     assert pod.pod_workspace_size(h) >= base + grow
+    # the decode page table is the caller's (no identity over copies)
     assert min(pod.pod_plan_table(h, 14)) < 0          # request 1: 70 queries, 33 keys
     pod.pod_plan_set_rope(h, 0.0, 0.0)
     assert pod.plan_summary(h)["rope"] == 0 and pod.pod_workspace_size(h) == base
@@ -541,6 +549,11 @@ def test_rope_host_checks(lib):
     pod.pod_plan_set_rope(h, 1.0, 1e4)
     with pytest.raises(pod.PodError) as e:
         pod.pod_plan_set_decode_fp8(h, 1.0, 1.0)
+    assert e.value.code == 2
+    # RoPE and ALiBi are two position encodings: one at a time
+    from pod_workloads import alibi_slopes
+    with pytest.raises(pod.PodError) as e:
+        pod.pod_plan_set_logits_transform(h, 0.0, alibi_slopes(16))
     assert e.value.code == 2
 
 
