@@ -301,7 +301,9 @@ def with_kv_option(inp, args):
     --soft-cap C: logits soft cap C on both halves;
     --alibi: geometric ALiBi slopes on both halves;
     --prefill-mask P: a random custom prefill mask, each bit set with probability P;
-    --rope: ROPE_LLAMA (rope_scale 1, rope_theta 1e4) on both halves."""
+    --rope: ROPE_LLAMA (rope_scale 1, rope_theta 1e4) on both halves;
+    --decode-requests N: only the first N decode requests (compact page pool),
+    the smaller case the ncu captures use."""
     from pod_workloads import (alibi_slopes, with_fp8_decode_cache, with_kv_layout,
                                with_prefill_custom_mask)
     if getattr(args, "kv_layout", "NHD") == "HND":
@@ -316,6 +318,9 @@ def with_kv_option(inp, args):
         inp = with_prefill_custom_mask(inp, seed=7, density=float(args.prefill_mask))
     if getattr(args, "rope", False):
         inp.rope = (1.0, 1e4)
+    if getattr(args, "decode_requests", None) is not None:
+        from pod_workloads import with_decode_subset
+        inp = with_decode_subset(inp, args.decode_requests)
     return inp
 
 
@@ -331,7 +336,10 @@ def variant_desc(args) -> dict:
     if getattr(args, "prefill_mask", None) is not None:
         v["prefill_custom_mask_density"] = float(args.prefill_mask)
     if getattr(args, "rope", False):
-        v["pos_encoding"] = "ROPE_LLAMA (scale 1, theta 1e4), rotated-copy pre-pass"
+        v["pos_encoding"] = ("ROPE_LLAMA (scale 1, theta 1e4): hi/lo rotated queries and prefill "
+                             "pages from a pre-pass, decode keys rotated in the kernel")
+    if getattr(args, "decode_requests", None) is not None:
+        v["decode_requests"] = int(args.decode_requests)
     return v
 
 
@@ -450,6 +458,15 @@ def run_ours(args, ws, rank, local):
                sinks=inp.sinks.to(device) if inp.sinks is not None else None)
     h = pod.plan_inputs(inp)
     summ = pod.plan_summary(h)
+    # host planning time of this batch (once per serving step), through the
+    # binding, on the calling thread
+    plan_ts = []
+    for _ in range(5):
+        t0 = time.perf_counter()
+        hp = pod.plan_inputs(inp)
+        plan_ts.append(time.perf_counter() - t0)
+        pod.pod_destroy(hp)
+    plan_us = float(np.median(plan_ts)) * 1e6
     wsb = torch.empty(pod.pod_workspace_size(h), dtype=torch.uint8, device=device)
     pod.pod_bind_workspace(h, wsb)
     H, d = inp.num_qo_heads, inp.head_dim
@@ -503,11 +520,11 @@ def run_ours(args, ws, rank, local):
     step_ms = total_ms / args.steps if flush is None else kernel_ms
     step_ms = max_over_ranks(step_ms, ws, device)
     # the fused kernel, the merge kernel when the plan splits, and under RoPE
-    # the copy pre-pass (queries and pages of each non-empty half; the angle
-    # table runs once per bound workspace, before the timed steps)
+    # the pre-pass (queries of each non-empty half, pages of the prefill half;
+    # the angle table runs once per bound workspace, before the timed steps)
     launches = 1 + (1 if summ["n_mrows"] > 0 else 0)
     if summ.get("rope"):
-        launches += 2 * ((1 if inp.p.rows else 0) + (1 if inp.d.rows else 0))
+        launches += (2 if inp.p.rows else 0) + (1 if inp.d.rows else 0)
 
     # --- single-half runs of the same kernel: prefill TFLOP/s and decode GB/s
     halves = {}
@@ -647,6 +664,7 @@ def run_ours(args, ws, rank, local):
         "plan": {k: summ[k] for k in ("grid", "n_p_ctas", "n_d_ctas", "n_tiles", "n_items",
                                        "n_groups", "decode_chunk")},
         "launch_us_median": float(np.median(per)) * 1e3,
+        "plan_us": plan_us,
     }
     line.update(extra)
     if rank == 0:
@@ -727,6 +745,8 @@ def main(argv=None):
     ap.add_argument("--prefill-mask", type=float, default=None, metavar="DENSITY",
                     help="random custom prefill mask with this fraction of allowed keys")
     ap.add_argument("--rope", action="store_true", help="ROPE_LLAMA on both halves")
+    ap.add_argument("--decode-requests", type=int, default=None, metavar="N",
+                    help="only the first N decode requests (a smaller case for profiler captures)")
     ap.add_argument("--profile", choices=["fused", "prefill", "decode"], default=None,
                     help="only launch this variant (for ncu captures); prints a summary line")
     args = ap.parse_args(argv)

@@ -32,7 +32,7 @@ import torch
 
 __all__ = ["HalfInputs", "PODInputs", "make_half", "make_config", "make_custom",
            "CONFIG_NAMES", "page_table_from_lens", "pack_mask", "with_prefill_custom_mask",
-           "with_kv_layout", "alibi_slopes"]
+           "with_kv_layout", "alibi_slopes", "with_decode_subset"]
 
 CONFIG_NAMES = ("c1", "c2", "c3", "c4", "c5")
 
@@ -280,3 +280,28 @@ def alibi_slopes(num_heads: int) -> torch.Tensor:
     count: 2^(-8 (h + 1) / H), h = 0..H-1 (fp32)."""
     h = torch.arange(1, num_heads + 1, dtype=torch.float64)
     return torch.pow(2.0, -8.0 * h / num_heads).to(torch.float32)
+
+
+def with_decode_subset(inp: PODInputs, n: int) -> PODInputs:
+    """The same inputs with only the first ``n`` decode requests. Their pages
+    are copied into a compact pool (the pages keep their relative order, so a
+    permuted pool stays permuted), so the device holds only what they use; a
+    smaller case of the same decode distribution for profiler captures.
+    Returns a new PODInputs; the prefill half is untouched."""
+    import copy
+    n = max(0, min(int(n), inp.d.batch))
+    out = copy.copy(inp)
+    d = copy.copy(inp.d)
+    used = np.asarray(inp.d.kv_indices[: int(inp.d.kv_indptr[n])], dtype=np.int64)
+    keep = np.unique(used)
+    d.q_indptr = np.ascontiguousarray(inp.d.q_indptr[: n + 1])
+    d.kv_indptr = np.ascontiguousarray(inp.d.kv_indptr[: n + 1])
+    d.last_page_len = np.ascontiguousarray(inp.d.last_page_len[:n])
+    d.kv_indices = np.searchsorted(keep, used).astype(np.int32)
+    d.num_pages = max(int(len(keep)), 1)
+    d.kv = inp.d.kv[torch.from_numpy(keep)] if len(keep) else inp.d.kv[:1].clone()
+    d.q = inp.d.q[: int(inp.d.q_indptr[n])].clone()
+    d.q_lens = np.ascontiguousarray(inp.d.q_lens[:n])
+    d.kv_lens = np.ascontiguousarray(inp.d.kv_lens[:n])
+    out.d = d
+    return out

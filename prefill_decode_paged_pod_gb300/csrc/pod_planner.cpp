@@ -17,34 +17,79 @@
 //     that both halves are predicted to finish together, and assign the work
 //     with longest-processing-time-first list scheduling;
 //  5. lay out the workspace: metadata (uploaded once) then split partials.
-// Everything is a deterministic function of the inputs and num_sms.
+// Everything is a deterministic function of the inputs and num_sms. The
+// schedule simulations run on integer times (1/256 ns), so they give the same
+// result on every host; planning runs on the calling thread.
 #include "pod_planner.hpp"
 
 #include <algorithm>
 #include <cstdlib>
 #include <limits>
-#include <thread>
 #include <cmath>
 #include <cstring>
 #include <functional>
-#include <queue>
 #include <utility>
 
 namespace {
 
 constexpr int kInvalid = 1, kUnsupported = 2;
 
-// Host threads the planner may use for its what-if simulations: the
-// POD_PLAN_THREADS environment variable (1..64), else the hardware's count
-// capped at 8. The plan does not depend on it.
-int plan_threads() {
-  static const int n = [] {
-    const char* e = getenv("POD_PLAN_THREADS");
-    if (e) return std::max(1, std::min(64, atoi(e)));
-    return std::max(1, std::min(8, (int)std::thread::hardware_concurrency()));
-  }();
-  return n;
-}
+// ---- schedule arithmetic -----------------------------------------------------
+// Simulated times are integers in 1/256 ns. A heap key packs a CTA's finish
+// time and its index, (time << kCtaBits) | cta, so that comparing keys orders
+// CTAs by finish time, then by index (the tie rule of every simulation here).
+constexpr double kTicksPerNs = 256.0;
+constexpr int kCtaBits = 20;                     // grids of up to 2^20 CTAs
+constexpr uint64_t kCtaMask = (1ull << kCtaBits) - 1;
+constexpr int64_t kNever = std::numeric_limits<int64_t>::max() >> (kCtaBits + 1);
+
+int64_t ticks(double ns) { return (int64_t)std::llround(ns * kTicksPerNs); }
+double ns_of(int64_t t) { return (double)t / kTicksPerNs; }
+uint64_t key_of(int64_t t, int cta) { return ((uint64_t)t << kCtaBits) | (uint64_t)cta; }
+int64_t time_of(uint64_t k) { return (int64_t)(k >> kCtaBits); }
+int cta_of(uint64_t k) { return (int)(k & kCtaMask); }
+
+// 4-ary min-heap of keys; the root is replaced in place (a CTA that takes a
+// job finishes later and sinks).
+struct KeyHeap {
+  std::vector<uint64_t> k;
+  // CTAs `ctas` (ascending) all free at time 0: ascending keys are a heap
+  void reset(const std::vector<int>& ctas) {
+    k.resize(ctas.size());
+    for (size_t i = 0; i < ctas.size(); ++i) k[i] = key_of(0, ctas[i]);
+  }
+  void reset_range(int n) {
+    k.resize((size_t)n);
+    for (int i = 0; i < n; ++i) k[(size_t)i] = key_of(0, i);
+  }
+  uint64_t top() const { return k[0]; }
+  void replace_top(uint64_t key) {
+    uint64_t* a = k.data();
+    const size_t n = k.size();
+    size_t i = 0;
+    for (;;) {
+      const size_t c = 4 * i + 1;
+      size_t m;
+      uint64_t mk;
+      if (c + 3 < n) {   // four children: pick the least without branches
+        const size_t i01 = a[c + 1] < a[c] ? c + 1 : c;
+        const size_t i23 = a[c + 3] < a[c + 2] ? c + 3 : c + 2;
+        m = a[i23] < a[i01] ? i23 : i01;
+        mk = a[m];
+      } else {
+        if (c >= n) break;
+        m = c;
+        mk = a[c];
+        for (size_t j = c + 1; j < n; ++j)
+          if (a[j] < mk) { mk = a[j]; m = j; }
+      }
+      if (mk >= key) break;
+      a[i] = mk;
+      i = m;
+    }
+    a[i] = key;
+  }
+};
 
 
 // ---- cost model; constants measured on GB300 ------------------------------
@@ -176,105 +221,79 @@ int64_t nblocks(int lo, int hi) {
   return (hi - b0 + POD_KBLOCK - 1) / POD_KBLOCK;
 }
 
-// Longest-processing-time-first list scheduling on CTAs of different speeds:
-// jobs in decreasing size go to the CTA that would finish them first. `work`
-// is in work units, `rate[c]` units per ns, `overhead` ns per job. Returns the
-// makespan (ns) and, if `assign` is given, the CTA of each job. CTAs of equal
-// rate form one class (a min-heap on load, ties to the lowest index), so a job
-// costs one probe per class. Ties between jobs: larger first, then lower index.
-double lpt(const std::vector<double>& work, double overhead, const std::vector<double>& rate,
-           std::vector<int>* order, std::vector<int>* assign) {
-  const int n_cta = (int)rate.size();
-  if (n_cta <= 0 || work.empty()) return 0.0;
-  std::vector<int> idx(work.size());
-  for (size_t i = 0; i < idx.size(); ++i) idx[i] = (int)i;
-  std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return work[a] > work[b]; });
-  typedef std::pair<double, int> Slot;
-  typedef std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> Heap;
-  std::vector<double> rates;
-  std::vector<Heap> heaps;
-  for (int c = 0; c < n_cta; ++c) {
-    size_t k = 0;
-    while (k < rates.size() && rates[k] != rate[c]) ++k;
-    if (k == rates.size()) {
-      rates.push_back(rate[c]);
-      heaps.emplace_back();
-    }
-    heaps[k].push(Slot(0.0, c));
-  }
-  if (assign) assign->assign(work.size(), -1);
-  double makespan = 0.0;
-  for (int j : idx) {
-    int best = -1;
-    double best_t = 0.0;
-    for (size_t k = 0; k < heaps.size(); ++k) {
-      const Slot& s = heaps[k].top();
-      const double t = s.first + overhead + work[j] / rates[k];
-      if (best < 0 || t < best_t || (t == best_t && s.second < heaps[best].top().second)) {
-        best = (int)k;
-        best_t = t;
+// The makespan of longest-processing-time-first list scheduling on CTAs of
+// different speeds: jobs, given in decreasing size, go to the CTA that would
+// finish them first. `work` is in work units, `rate[c]` units per ns,
+// `overhead` ns per job. CTAs of equal rate form one class (a heap on finish
+// time, ties to the lowest index), so a job costs one probe per class.
+// Returns the makespan (ns); stops as soon as it reaches `bound` and returns
+// that time.
+struct RateClasses {
+  std::vector<double> rate;
+  std::vector<KeyHeap> heap;
+  void build(const std::vector<double>& r) {
+    rate.clear();
+    heap.clear();
+    std::vector<std::vector<int>> members;
+    for (int c = 0; c < (int)r.size(); ++c) {
+      size_t k = 0;
+      while (k < rate.size() && rate[k] != r[c]) ++k;
+      if (k == rate.size()) {
+        rate.push_back(r[c]);
+        members.emplace_back();
       }
+      members[k].push_back(c);
     }
-    Slot s = heaps[best].top();
-    heaps[best].pop();
-    s.first = best_t;
-    makespan = std::max(makespan, s.first);
-    if (assign) (*assign)[j] = s.second;
-    heaps[best].push(s);
+    heap.resize(rate.size());
+    for (size_t k = 0; k < rate.size(); ++k) heap[k].reset(members[k]);
   }
-  if (order) *order = idx;
-  return makespan;
-}
+};
 
-// The makespan lpt() returns for jobs already in decreasing order, without
-// the schedule: each rate class is an array heap of (finish time, CTA index)
-// whose root is pushed down in place. Returns early, with the makespan so
-// far, once it reaches `bound`.
 double lpt_makespan(const std::vector<double>& sorted_work, double overhead,
                     const std::vector<double>& rate, double bound) {
-  const int n_cta = (int)rate.size();
-  if (n_cta <= 0 || sorted_work.empty()) return 0.0;
-  struct Cls { double rate; std::vector<double> t; std::vector<int> c; };
-  std::vector<Cls> cls;
-  for (int c = 0; c < n_cta; ++c) {
-    size_t k = 0;
-    while (k < cls.size() && cls[k].rate != rate[c]) ++k;
-    if (k == cls.size()) cls.push_back(Cls{rate[c], {}, {}});
-    cls[k].t.push_back(0.0);   // CTAs join in index order: a valid heap
-    cls[k].c.push_back(c);
-  }
-  double makespan = 0.0;
+  if (rate.empty() || sorted_work.empty()) return 0.0;
+  RateClasses cl;
+  cl.build(rate);
+  const int64_t tb = std::isinf(bound) ? kNever : ticks(bound);
+  int64_t makespan = 0;
   for (double w : sorted_work) {
     int best = -1;
-    double best_t = 0.0;
-    for (size_t k = 0; k < cls.size(); ++k) {
-      const double t = cls[k].t[0] + overhead + w / cls[k].rate;
-      if (best < 0 || t < best_t || (t == best_t && cls[k].c[0] < cls[best].c[0])) {
-        best = (int)k;
-        best_t = t;
-      }
+    uint64_t bk = 0;
+    for (size_t k = 0; k < cl.rate.size(); ++k) {
+      const uint64_t top = cl.heap[k].top();
+      const uint64_t cand = key_of(time_of(top) + ticks(overhead + w / cl.rate[k]), cta_of(top));
+      if (best < 0 || cand < bk) { best = (int)k; bk = cand; }
     }
-    makespan = std::max(makespan, best_t);
-    if (makespan >= bound) return makespan;
-    Cls& h = cls[best];
-    const int n = (int)h.t.size(), cid = h.c[0];
-    int i = 0;
-    for (;;) {
-      const int l = 2 * i + 1, r = l + 1;
-      int m = -1;
-      double mt = best_t;
-      int mc = cid;
-      if (l < n && (h.t[l] < mt || (h.t[l] == mt && h.c[l] < mc))) { m = l; mt = h.t[l]; mc = h.c[l]; }
-      if (r < n && (h.t[r] < mt || (h.t[r] == mt && h.c[r] < mc))) { m = r; mt = h.t[r]; mc = h.c[r]; }
-      if (m < 0) break;
-      h.t[i] = mt;
-      h.c[i] = mc;
-      i = m;
-    }
-    h.t[i] = best_t;
-    h.c[i] = cid;
+    makespan = std::max(makespan, time_of(bk));
+    if (makespan >= tb) return ns_of(makespan);
+    cl.heap[best].replace_top(bk);
   }
-  return makespan;
+  return ns_of(makespan);
+}
+
+// What-if simulations run on a scaled copy of a schedule: every `s`
+// consecutive jobs of a list sorted by decreasing cost become one job of
+// their mean cost (the total work is kept), and every `s`-th CTA stands for
+// its group. A makespan then takes about 1/s of the heap operations; it
+// stays comparable across the candidates a search weighs. s is the largest
+// power of two up to 8 that divides the CTA count and leaves at least 1024
+// jobs.
+int sim_scale(size_t jobs, int ctas) {
+  int s = 1;
+  while (s < 8 && ctas % (2 * s) == 0 && jobs / (size_t)(2 * s) >= 1024) s *= 2;
+  return s;
+}
+std::vector<double> scaled_jobs(const std::vector<double>& sorted, int s) {
+  if (s <= 1) return sorted;
+  std::vector<double> out;
+  out.reserve(sorted.size() / s + 1);
+  for (size_t i = 0; i < sorted.size(); i += (size_t)s) {
+    const size_t e = std::min(sorted.size(), i + (size_t)s);
+    double sum = 0.0;
+    for (size_t j = i; j < e; ++j) sum += sorted[j];
+    out.push_back(sum / (double)s);
+  }
+  return out;
 }
 
 struct DecodeUnit {
@@ -324,6 +343,34 @@ double decode_time(const std::vector<DecodeUnit>& units, const std::vector<doubl
   // item counts by key count, for items of <= 16 rows ([0]) and more ([1])
   int max_keys = 0;
   for (const DecodeUnit& u : units) max_keys = std::max(max_keys, u.hi - u.lo);
+  // Capacity bound: over a makespan T, CTA c does at most rate[c] * (T -
+  // overhead * its items) work, so T >= (work + items * overhead * r_min) /
+  // sum(rate). Splitting keeps the total work (an item's work is linear in
+  // its keys) and only adds items, so the bound with one item per unit, plus
+  // the merge launch a split plan pays, holds before any item is built.
+  double r_min = std::numeric_limits<double>::infinity(), r_sum = 0.0;
+  for (double r : rate) {
+    r_min = std::min(r_min, r);
+    r_sum += r;
+  }
+  // A unit longer than the chunk splits into ceil(len / chunk) parts (inner
+  // boundaries are at least chunk - 64 >= 192 keys apart for the chunks
+  // searched, so none coincide): the item count and the partial rows' bytes
+  // are known before any item is built.
+  if (chunk > 0 && !std::isinf(bound) && r_sum > 0.0) {
+    double w = 0.0, items = 0.0, sbytes = 0.0;
+    for (const DecodeUnit& u : units) {
+      const int len = u.hi - u.lo;
+      w += item_work(len, d, u.ntok * G);
+      const int n = len > chunk ? (len + chunk - 1) / chunk : 1;
+      items += n;
+      if (n > 1) sbytes += (double)n * u.ntok * G * (d + 1) * 4.0 * 2.0;
+    }
+    const double ex = sbytes > 0 ? 8000.0 + sbytes / cm.hbm_bytes_per_ns : 0.0;
+    const double lb = std::max(total_bytes / cm.hbm_bytes_per_ns + ex,
+                               (w + items * cm.d_item_ns * r_min) / r_sum + ex);
+    if (lb >= bound) return lb;
+  }
   std::vector<int> cnt[2] = {std::vector<int>(max_keys + 1, 0), std::vector<int>(max_keys + 1, 0)};
   std::vector<std::pair<int, int>> parts;
   double split_bytes = 0.0;
@@ -339,6 +386,15 @@ double decode_time(const std::vector<DecodeUnit>& units, const std::vector<doubl
   const double extra = split_bytes > 0 ? 8000.0 + split_bytes / cm.hbm_bytes_per_ns : 0.0;
   const double floor_t = total_bytes / cm.hbm_bytes_per_ns + extra;
   if (floor_t >= bound) return floor_t;
+  // the capacity bound again, with the items this chunk makes
+  if (r_sum > 0.0) {
+    double w = 0.0;
+    for (int f = 0; f < 2; ++f)
+      for (int k = 0; k <= max_keys; ++k)
+        if (cnt[f][k]) w += cnt[f][k] * item_work(k, d, f ? 32 : 16);
+    const double lb = (w + (double)n_items * cm.d_item_ns * r_min) / r_sum + extra;
+    if (lb >= bound) return lb;
+  }
   // only the makespan is needed and equal jobs are interchangeable: the work
   // values in decreasing order (the order lpt's index sort gives), merged
   // from the two count tables
@@ -359,7 +415,11 @@ double decode_time(const std::vector<DecodeUnit>& units, const std::vector<doubl
       cnt[1][k1] = 0;
     }
   }
-  double t = lpt_makespan(work, cm.d_item_ns, rate, bound - extra);
+  const int sc = sim_scale(work.size(), (int)rate.size());
+  std::vector<double> srate;
+  for (size_t c = 0; c < rate.size(); c += (size_t)sc) srate.push_back(rate[c]);
+  // a scaled job stands for `sc` jobs: its per-job overhead is theirs, shared
+  double t = lpt_makespan(scaled_jobs(work, sc), cm.d_item_ns, srate, bound - extra);
   t = std::max(t, total_bytes / cm.hbm_bytes_per_ns);
   return t + extra;
 }
@@ -367,29 +427,20 @@ double decode_time(const std::vector<DecodeUnit>& units, const std::vector<doubl
 DecodeChoice best_decode(const std::vector<DecodeUnit>& units, const std::vector<double>& rate,
                          int G, int d, const CostModel& cm, double total_bytes) {
   DecodeChoice best;
-  best.time = -1.0;
-  // 0 = no split; then 16 Ki .. 256 keys, each estimated on its own thread
+  // 0 = no split; then 16 Ki .. 256 keys. A candidate at or above the longest
+  // key range splits nothing and is the unsplit plan again: skipped.
   const int cands[] = {0, 16384, 8192, 4096, 2048, 1024, 512, 256};
-  constexpr int NC = (int)(sizeof(cands) / sizeof(cands[0]));
-  double times[NC];
-  // the unsplit estimate first: a candidate is taken only below
-  // best * (1 - 1e-9) <= times[0] * (1 - 1e-9), which bounds the others
-  times[0] = decode_time(units, rate, cands[0], G, d, cm, total_bytes);
-  const double bound = times[0] * (1.0 - 1e-9);
-  // threads pay off only for larger batches
-  const int nt = units.size() < 512 ? 1 : std::min(plan_threads(), NC - 1);
-  auto work = [&](int k) {
-    for (int j = 1 + k; j < NC; j += nt)
-      times[j] = decode_time(units, rate, cands[j], G, d, cm, total_bytes, bound);
-  };
-  std::vector<std::thread> pool;
-  for (int k = 1; k < nt; ++k) pool.emplace_back(work, k);
-  work(0);
-  for (auto& th : pool) th.join();
-  for (int j = 0; j < NC; ++j) {
-    if (best.time < 0 || times[j] < best.time * (1.0 - 1e-9)) {
-      best.time = times[j];
-      best.chunk = cands[j];
+  int max_keys = 0;
+  for (const DecodeUnit& u : units) max_keys = std::max(max_keys, u.hi - u.lo);
+  best.time = decode_time(units, rate, 0, G, d, cm, total_bytes);
+  best.chunk = 0;
+  for (int c : cands) {
+    if (c == 0 || c >= max_keys) continue;
+    // taken only below best * (1 - 1e-9): no simulation needs to run past that
+    const double t = decode_time(units, rate, c, G, d, cm, total_bytes, best.time * (1.0 - 1e-9));
+    if (t < best.time * (1.0 - 1e-9)) {
+      best.time = t;
+      best.chunk = c;
     }
   }
   return best;
@@ -606,92 +657,85 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
       for (auto& pr : parts) item_b.push_back(item_work(pr.second - pr.first, a.d, u.ntok * G));
     }
     std::sort(item_b.begin(), item_b.end(), std::greater<double>());
-    // makespan when CTAs [0, np) start on tiles and the rest on items; a CTA
-    // takes the next job of its queue when free, the other queue's once its
-    // own is empty. CTAs are served in (finish time, index) order from a
-    // binary heap. The simulation stops as soon as a CTA's finish time reaches
-    // `bound` (the candidate can no longer win) and returns that time.
+    // Makespan when CTAs [0, np) start on tiles and the rest on items: a CTA
+    // takes the next job of its own queue when free, the other queue's once
+    // its own is empty; CTAs are served in (finish time, index) order. Job
+    // costs are precomputed for each co-residency class. The simulation stops
+    // as soon as a CTA's finish time reaches `bound` (the candidate can no
+    // longer win) and returns that time.
     const double floor_t = std::max(p_flops / cm.p_flops_per_ns, d_bytes / cm.hbm_bytes_per_ns);
-    struct Scratch { std::vector<double> t, p_ns, d_rate; std::vector<int> c; };
-    auto queue_makespan = [&](int np, double bound, Scratch& w) {
+    // the simulations run scaled by sc (sc CTAs, sc jobs per simulated one)
+    const int sc = sim_scale(tile_ns.size() + item_b.size(), S);
+    const std::vector<double> tile_s = scaled_jobs(tile_ns, sc), item_s = scaled_jobs(item_b, sc);
+    const int S_s = S / sc, grid_s = grid_max / sc;
+    std::vector<int64_t> tile_t[3], item_t[3];
+    for (int k = 0; k < 3; ++k) {
+      tile_t[k].resize(tile_s.size());
+      item_t[k].resize(item_s.size());
+      for (size_t t = 0; t < tile_s.size(); ++t)
+        tile_t[k][t] = ticks(cm.p_tile_ns + tile_s[t] * cm.p_block_ns[k]);
+      for (size_t t = 0; t < item_s.size(); ++t)
+        item_t[k][t] = ticks(cm.d_item_ns + item_s[t] / cm.d_bytes_per_ns[k]);
+    }
+    KeyHeap heap;
+    std::vector<int> cls(grid_s);
+    auto queue_makespan = [&](int np, double bound) -> double {
       if (floor_t >= bound) return floor_t;
-      const int n = grid_max;
-      w.t.assign(n, 0.0);
-      w.c.resize(n);
-      w.p_ns.resize(n);
-      w.d_rate.resize(n);
-      for (int c = 0; c < n; ++c) {
-        const int cls = neighbour_class(c, np, n - np, S, cps);
-        w.p_ns[c] = cm.p_block_ns[cls];
-        w.d_rate[c] = cm.d_bytes_per_ns[cls];
-        w.c[c] = c;   // all loads zero: index order is a valid heap
-      }
-      double* ht = w.t.data();
-      int* hc = w.c.data();
+      const int64_t tb = std::isinf(bound) ? kNever : ticks(bound);
+      for (int c = 0; c < grid_s; ++c) cls[c] = neighbour_class(c, np, grid_s - np, S_s, cps);
+      heap.reset_range(grid_s);
+      const size_t nt = tile_s.size(), ni = item_s.size();
       size_t it = 0, id = 0;
-      double makespan = 0.0;
-      while (it < tile_ns.size() || id < item_b.size()) {
-        const int c = hc[0];
-        const bool want_p = c < np ? it < tile_ns.size() : id >= item_b.size();
-        const double cost = want_p ? cm.p_tile_ns + tile_ns[it++] * w.p_ns[c]
-                                   : cm.d_item_ns + item_b[id++] / w.d_rate[c];
-        const double tnew = ht[0] + cost;
-        makespan = std::max(makespan, tnew);
-        if (makespan >= bound) return makespan;
-        // the root grew: sift it down
-        int i = 0;
-        for (;;) {
-          const int l = 2 * i + 1, r = l + 1;
-          int m = -1;
-          double mt = tnew;
-          int mc = c;
-          if (l < n && (ht[l] < mt || (ht[l] == mt && hc[l] < mc))) { m = l; mt = ht[l]; mc = hc[l]; }
-          if (r < n && (ht[r] < mt || (ht[r] == mt && hc[r] < mc))) { m = r; mt = ht[r]; mc = hc[r]; }
-          if (m < 0) break;
-          ht[i] = mt;
-          hc[i] = mc;
-          i = m;
-        }
-        ht[i] = tnew;
-        hc[i] = c;
+      int64_t makespan = 0;
+      while (it < nt || id < ni) {
+        const uint64_t top = heap.top();
+        const int c = cta_of(top);
+        const bool want_p = c < np ? it < nt : id >= ni;
+        const int64_t tn = time_of(top) + (want_p ? tile_t[cls[c]][it++] : item_t[cls[c]][id++]);
+        makespan = std::max(makespan, tn);
+        if (makespan >= tb) return ns_of(makespan);
+        heap.replace_top(key_of(tn, c));
       }
-      return std::max(makespan, floor_t);
+      return std::max(ns_of(makespan), floor_t);
     };
-    // candidates are evaluated on a few host threads; each result does not
-    // depend on the others, and the choice below walks them in order
-    auto eval_all = [&](const std::vector<int>& nps, double bound, std::vector<double>& out) {
-      out.assign(nps.size(), 0.0);
-      const size_t jobs = tile_ns.size() + item_b.size();
-      const int nt = jobs < 2048 ? 1 : std::max(1, std::min<int>(plan_threads(), (int)nps.size()));
-      std::vector<Scratch> ws(nt);
-      auto work = [&](int k) {
-        for (size_t j = k; j < nps.size(); j += nt) out[j] = queue_makespan(nps[j], bound, ws[k]);
-      };
-      std::vector<std::thread> pool;
-      for (int k = 1; k < nt; ++k) pool.emplace_back(work, k);
-      work(0);
-      for (auto& th : pool) th.join();
-    };
-    Scratch w0;
-    const double share_t = queue_makespan(n_p, std::numeric_limits<double>::infinity(), w0);
-    int best_np = n_p;
-    double best_t = share_t;
     const int hi_np = std::min(grid_max - 1, n_tiles);
-    const int step = std::max(1, hi_np / 32);
-    // a candidate is taken only below best_t * (1 - 1e-9) <= share_t * (1 - 1e-9):
-    // no simulation needs to run past that
-    std::vector<int> nps;
-    std::vector<double> ts;
-    for (int np = 1; np <= hi_np; np += step) nps.push_back(np);
-    eval_all(nps, share_t * (1.0 - 1e-9), ts);
-    for (size_t j = 0; j < nps.size(); ++j)
-      if (ts[j] < best_t * (1.0 - 1e-9)) { best_t = ts[j]; best_np = nps[j]; }
-    nps.clear();
-    for (int np = std::max(1, best_np - step); np <= std::min(hi_np, best_np + step); ++np)
-      nps.push_back(np);
-    eval_all(nps, best_t * (1.0 - 1e-9), ts);
-    for (size_t j = 0; j < nps.size(); ++j)
-      if (ts[j] < best_t * (1.0 - 1e-9)) { best_t = ts[j]; best_np = nps[j]; }
+    const int hi_s = std::max(1, std::min(grid_s - 1, (hi_np + sc - 1) / sc));
+    const int np0_s = std::max(1, std::min(hi_s, (n_p + sc / 2) / sc));
+    const double share_t = queue_makespan(np0_s, std::numeric_limits<double>::infinity());
+    int best_np = np0_s;
+    double best_t = share_t;
+    // Golden-section search of the split over [1, hi_s] (the makespan is
+    // close to unimodal in it: too few prefill-first CTAs start long tiles
+    // late, too many starve the decode stream), then the last few points.
+    // Every simulation runs against the best time so far, which it can only
+    // beat by more than 1e-9 to be taken.
+    std::vector<double> seen(hi_s + 2, -1.0);
+    auto eval = [&](int np) -> double {
+      if (seen[np] < 0.0) {
+        seen[np] = np == np0_s ? share_t : queue_makespan(np, best_t * (1.0 - 1e-9));
+        if (seen[np] < best_t * (1.0 - 1e-9)) { best_t = seen[np]; best_np = np; }
+      }
+      return seen[np];
+    };
+    {
+      const double phi = 0.6180339887498949;
+      int lo = 1, hi = hi_s;
+      int x1 = hi - (int)std::lround(phi * (hi - lo)), x2 = lo + (int)std::lround(phi * (hi - lo));
+      while (hi - lo > 3) {
+        if (x1 >= x2) x2 = x1 + 1;
+        if (eval(x1) <= eval(x2)) {
+          hi = x2;
+          x2 = x1;
+          x1 = hi - (int)std::lround(phi * (hi - lo));
+        } else {
+          lo = x1;
+          x1 = x2;
+          x2 = lo + (int)std::lround(phi * (hi - lo));
+        }
+      }
+      for (int np = lo; np <= hi; ++np) eval(np);
+    }
+    best_np = best_np == np0_s ? n_p : std::min(hi_np, best_np * sc);
     // the model is coarse: leave the balanced split unless the queues are
     // predicted to finish at least 1 % earlier another way
     if (best_t < 0.99 * share_t) n_p = best_np;
@@ -738,28 +782,34 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   P.n_prows = n_prows;
   P.n_mrows = P.mrow_ptr.back();
 
-  // ---- per-CTA work lists -----------------------------------------------------
+  // ---- work queues and per-CTA lists ------------------------------------------
+  // The kernel's queues hold every tile / item in decreasing cost (ties by
+  // index). The per-CTA lists deal each queue round-robin over the CTAs that
+  // start on it: what each CTA would take if all ran at one speed. The kernel
+  // serves the queues; the lists are kept for inspection.
   P.cta_ptr.assign(P.grid + 1, 0);
   P.cta_list.clear();
   {
-    std::vector<int> order, assign;
+    auto order_of = [](const std::vector<double>& cost) {
+      std::vector<int> idx(cost.size());
+      for (size_t i = 0; i < idx.size(); ++i) idx[i] = (int)i;
+      std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return cost[a] > cost[b]; });
+      return idx;
+    };
     std::vector<std::vector<int>> lists(P.grid);
-    std::vector<double> rp, rd;
-    rates(n_p, n_d, rp, rd);
-    // the kernel's work queues: every tile / item, largest first
     P.pqueue.clear();
     P.dqueue.clear();
     if (n_p > 0) {
-      lpt(tile_cost, cm.p_tile_ns, rp, &order, &assign);
-      for (int j : order) lists[assign[j]].push_back(j);
-      P.pqueue.assign(order.begin(), order.end());
+      P.pqueue = order_of(tile_cost);
+      for (size_t k = 0; k < P.pqueue.size(); ++k) lists[k % (size_t)n_p].push_back(P.pqueue[k]);
     }
     if (n_d > 0) {
-      lpt(item_cost, cm.d_item_ns, rd, &order, &assign);
-      for (int j : order) lists[n_p + assign[j]].push_back(j);
-      P.dqueue.assign(order.begin(), order.end());
+      P.dqueue = order_of(item_cost);
+      for (size_t k = 0; k < P.dqueue.size(); ++k)
+        lists[n_p + k % (size_t)n_d].push_back(P.dqueue[k]);
     }
     P.dqrec.clear();
+    P.dqrec.reserve(P.dqueue.size() * POD_DQREC);
     for (int j : P.dqueue) {
       const int32_t* rec = &P.ditems[(size_t)j * POD_REC];
       const int r = rec[0];
@@ -769,6 +819,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
                                                P.dd.kv_indptr[r + 1] - P.dd.kv_indptr[r], 0, 0, 0};
       P.dqrec.insert(P.dqrec.end(), ext, ext + POD_DQREC - POD_REC);
     }
+    P.cta_list.reserve(P.pqueue.size() + P.dqueue.size());
     for (int c = 0; c < P.grid; ++c) {
       P.cta_ptr[c] = (int32_t)P.cta_list.size();
       P.cta_list.insert(P.cta_list.end(), lists[c].begin(), lists[c].end());

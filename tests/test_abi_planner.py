@@ -445,9 +445,9 @@ def test_plain_c_client(lib, tmp_path):
     assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
 
 
-def test_plan_independent_of_planner_threads(lib):
-    """The planner's what-if simulations run on POD_PLAN_THREADS host threads;
-    the plan is the same bit for bit with 1 and with 8 of them."""
+def test_plan_is_deterministic_across_processes(lib):
+    """The schedule search runs on integer times on the calling thread: two
+    processes plan c3-c5 bit for bit alike."""
     import subprocess
     import sys
     code = (
@@ -463,13 +463,26 @@ def test_plan_independent_of_planner_threads(lib):
         "        h.update(pod.pod_plan_table(p, w).tobytes())\n"
         "print(h.hexdigest())\n")
     digests = set()
-    for t in ("1", "8"):
-        env = dict(os.environ, POD_PLAN_THREADS=t)
-        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
-                           timeout=600)
+    for _ in range(2):
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
         assert r.returncode == 0, r.stderr
         digests.add(r.stdout.strip())
     assert len(digests) == 1
+
+
+def test_plan_latency(lib):
+    """Planning is on the serving path (once per batch): the c5 plan (4408
+    tiles, 4096 decode items) takes a few ms on one host thread. The bound
+    here is loose (shared CI hosts); bench.py reports the measured time."""
+    import time
+    inp = make_config("c5", with_data=False)
+    ts = []
+    for _ in range(5):
+        t0 = time.perf_counter()
+        h = pod.plan_inputs(inp, num_sms=152)
+        ts.append(time.perf_counter() - t0)
+        pod.pod_destroy(h)
+    assert min(ts) < 0.02, ts
 
 
 def test_binding_refuses_host_mask_and_slopes_before_launch(lib):
