@@ -144,6 +144,7 @@ template <typename T, int D, int LT, bool RP>
 __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
   using L = PLayout<D, RP>;
   constexpr int NK = L::NK, NV = L::NV;
+  static_assert(NK == 3 && NV == 2, "the barrier slots below are laid out for 3 K and 2 V stages");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + L::BAR_OFF;
@@ -224,6 +225,10 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
     // ------------------------------------------------------------ loaders
     fence_proxy_async();  // generic accesses of an earlier decode phase come first
     int kfill = 0, vfill = 0, qfill = 0;
+    // L2 priorities: a Q tile is read once; the prefill K/V blocks are re-read
+    // by every tile of their request and head, next to a decode stream that
+    // would otherwise evict them
+    const uint64_t pol_q = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
     bool ok = true;
     const uint32_t q_bytes = (uint32_t)(L::NQ * L::NKB * 128 * G * P.tq);
     if (P.p_tma) {
@@ -249,11 +254,11 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
             if (lane == 0) {
               mbar_arrive_expect_tx(BAR(B_QFULL), q_bytes);
               for (int dh = 0; dh < L::NKB; ++dh) {
-                tma_load_3d(sbase + L::Q_OFF + dh * L::QBLK, &P.tm_q_p, dh * 64, g * G,
-                            P.p_q_indptr[req] + tok0, BAR(B_QFULL));
+                tma_load_3d_hint(sbase + L::Q_OFF + dh * L::QBLK, &P.tm_q_p, dh * 64, g * G,
+                                 P.p_q_indptr[req] + tok0, BAR(B_QFULL), pol_q);
                 if (RP)
-                  tma_load_3d(sbase + L::QLO_OFF + dh * L::QBLK, &P.tm_qlo_p, dh * 64, g * G,
-                              P.p_q_indptr[req] + tok0, BAR(B_QFULL));
+                  tma_load_3d_hint(sbase + L::QLO_OFF + dh * L::QBLK, &P.tm_qlo_p, dh * 64, g * G,
+                                   P.p_q_indptr[req] + tok0, BAR(B_QFULL), pol_q);
               }
             }
             ++qfill;
@@ -277,12 +282,12 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
               const int page = pidx < npages ? __ldg(P.p_kv_indices + page_base + pidx) : P.p_num_pages;
               const int tin = P.ps >= 8 ? (t & (P.ps - 1)) : 0;
               for (int dh = 0; dh < L::NKB; ++dh) {
-                tma_load_5d(dst0 + dh * L::KVBLK + o * 128, tkv, dh * 64, g, tin, is_v ? 1 : 0, page,
-                            BAR(full));
+                tma_load_5d_hint(dst0 + dh * L::KVBLK + o * 128, tkv, dh * 64, g, tin, is_v ? 1 : 0,
+                                 page, BAR(full), pol_kv);
                 // RoPE copies hold K_hi, V, K_lo per page: the low part is row 2
                 if (RP && !is_v)
-                  tma_load_5d(dst0 + L::KSTAGE + dh * L::KVBLK + o * 128, tkv, dh * 64, g, tin, 2,
-                              page, BAR(full));
+                  tma_load_5d_hint(dst0 + L::KSTAGE + dh * L::KVBLK + o * 128, tkv, dh * 64, g, tin, 2,
+                                   page, BAR(full), pol_kv);
               }
             }
             if (is_v) ++vfill; else ++kfill;
@@ -309,11 +314,11 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
           if (ok) {
             mbar_arrive_expect_tx(BAR(B_QFULL), q_bytes);
             for (int dh = 0; dh < L::NKB; ++dh) {
-              tma_load_3d(sbase + L::Q_OFF + dh * L::QBLK, &P.tm_q_p, dh * 64, g * G,
-                          P.p_q_indptr[req] + tok0, BAR(B_QFULL));
+              tma_load_3d_hint(sbase + L::Q_OFF + dh * L::QBLK, &P.tm_q_p, dh * 64, g * G,
+                               P.p_q_indptr[req] + tok0, BAR(B_QFULL), pol_q);
               if (RP)
-                tma_load_3d(sbase + L::QLO_OFF + dh * L::QBLK, &P.tm_qlo_p, dh * 64, g * G,
-                            P.p_q_indptr[req] + tok0, BAR(B_QFULL));
+                tma_load_3d_hint(sbase + L::QLO_OFF + dh * L::QBLK, &P.tm_qlo_p, dh * 64, g * G,
+                                 P.p_q_indptr[req] + tok0, BAR(B_QFULL), pol_q);
             }
           }
         }
@@ -346,11 +351,11 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
               const T* src = kvg + (P.p_hnd
                   ? (((size_t)pages[i] * NKV * P.Hk + g) * P.ps + slot) * D + c * 8
                   : (((size_t)pages[i] * NKV * P.ps + slot) * P.Hk + g) * D + c * 8);
-              cp_async16(dst_base + (c >> 3) * L::KVBLK + sw128_off(key, c & 7),
-                         is_v ? src + vstride : src, valid ? 16u : 0u);
+              cp_async16_hint(dst_base + (c >> 3) * L::KVBLK + sw128_off(key, c & 7),
+                              is_v ? src + vstride : src, valid ? 16u : 0u, pol_kv);
               if (RP && !is_v)
-                cp_async16(dst_base + L::KSTAGE + (c >> 3) * L::KVBLK + sw128_off(key, c & 7),
-                           src + 2 * vstride, valid ? 16u : 0u);
+                cp_async16_hint(dst_base + L::KSTAGE + (c >> 3) * L::KVBLK + sw128_off(key, c & 7),
+                                src + 2 * vstride, valid ? 16u : 0u, pol_kv);
             }
           }
         };

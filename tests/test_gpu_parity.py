@@ -1,8 +1,8 @@
 """GPU parity: the POD library (through its C-ABI binding) against the fp64
 oracle on the same seeded inputs, element by element.
 
-Covers the five benchmark workloads (c1, c2 fully; c3-c5 at full size on a
-deterministic sample of rows), a randomized sweep shaped like the FlashInfer
+Covers the five benchmark workloads (every row of c1-c5 at full size, and of
+the c5 decode half with an FP8 cache), a randomized sweep shaped like the FlashInfer
 POD test grid (page size 1/16, GQA groups, decode batches 1/17/127, prefill
 lengths that are not tile multiples), edge cases, determinism and the tcgen05
 building blocks in isolation.
@@ -62,14 +62,15 @@ def test_config_full(name):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["c3", "c4", "c5"])
-def test_config_full_size_sampled(name):
+def test_config_full_size(name):
+    """Every output row and LSE of both halves of c3-c5 at full size, in the
+    launch configuration the benchmark times, against the fp64 oracle element
+    by element (the oracle takes about half a minute for c5 on 16 host
+    cores)."""
     inp = make_config(name)
     (op, lp, od, ld), h, ws = run_pod(inp)
-    H = inp.num_qo_heads
-    st, sh = sample_rows(inp.p, H, 48, seed=1)
-    compare_half(inp, "p", op, lp, st, sh, tag=name)
-    st, sh = sample_rows(inp.d, H, 96, seed=2)
-    compare_half(inp, "d", od, ld, st, sh, tag=name)
+    compare_half(inp, "p", op, lp, tag=name)
+    compare_half(inp, "d", od, ld, tag=name)
     assert np.isfinite(op).all() and np.isfinite(od).all()
     assert np.isfinite(lp).all() and np.isfinite(ld).all()
 
@@ -305,12 +306,12 @@ def test_fp8_unused_page_slots_do_not_leak():
 
 
 @pytest.mark.slow
-def test_fp8_decode_c5_full_size_sampled():
+def test_fp8_decode_c5_full_size():
+    """The FP8 (E4M3) decode cache on c5 at full size: every decode row."""
     from pod_workloads import with_fp8_decode_cache
     inp = with_fp8_decode_cache(make_config("c5"), k_scale=0.05, v_scale=0.05)
     (op, lp, od, ld), h, ws = run_pod(inp)
-    st, sh = sample_rows(inp.d, inp.num_qo_heads, 96, seed=4)
-    compare_half(inp, "d", od, ld, st, sh, tag="fp8 c5 ")
+    compare_half(inp, "d", od, ld, tag="fp8 c5 ")
     assert np.isfinite(od).all() and np.isfinite(ld).all()
 
 
