@@ -15,8 +15,9 @@
  * side ("Decode 侧参数与'plan 覆盖'行为"); run takes tensors only. Optional
  * policies are set on the handle between pod_plan and pod_run:
  * pod_plan_set_decode_fp8, pod_plan_set_kv_layout,
- * pod_plan_set_logits_transform, pod_plan_set_rope and
- * pod_plan_set_prefill_mask.
+ * pod_plan_set_logits_transform, pod_plan_set_rope,
+ * pod_plan_set_prefill_mask and pod_plan_set_graph_capacity (then
+ * pod_replan plans each new step into the same workspace).
  *
  * Conventions shared by every entry point
  *  - Errors are returned as pod_status codes; nothing aborts or throws.
@@ -111,13 +112,16 @@ pod_status pod_plan(const int32_t* p_q_indptr, const int32_t* p_kv_indptr,
                     void* workspace, size_t workspace_bytes, void* stream,
                     pod_handle* out_handle, size_t* required_workspace_bytes);
 
-/* Bytes of device workspace the plan needs (0 for a NULL handle). */
+/* Bytes of device workspace the plan needs (0 for a NULL handle). Library
+ * mechanics (the pages size the workspace by hand); no passage. */
 size_t pod_workspace_size(pod_handle h);
 
 /*
  * pod_bind_workspace — copy a host-only plan's metadata into `workspace`
- * (device, >= pod_workspace_size bytes) on `stream`. After it, pod_run may be
- * called with this workspace. Errors: POD_ERR_WORKSPACE, POD_ERR_CUDA.
+ * (device, >= pod_workspace_size bytes) on `stream`, and wait for the copy
+ * (it reads host memory the handle owns). After it, pod_run may be called
+ * with this workspace. Library mechanics (plan on the host first, learn the
+ * size, then bind); no passage. Errors: POD_ERR_WORKSPACE, POD_ERR_CUDA.
  */
 pod_status pod_bind_workspace(pod_handle h, void* workspace, size_t workspace_bytes, void* stream);
 
@@ -245,10 +249,61 @@ pod_status pod_plan_set_kv_layout(pod_handle h, int32_t p_layout, int32_t d_layo
  */
 pod_status pod_plan_set_prefill_mask(pod_handle h, const void* packed_mask, int64_t mask_bytes);
 
-/* Release the handle (host memory only). NULL is accepted. */
+/*
+ * pod_plan_set_graph_capacity — plans for CUDA-graph replay (POD walkthrough,
+ * "CUDAGraph 模式的运行时约束": a fixed batch, page-table buffers reserved at
+ * their maximum size, and plan run outside capture).
+ *
+ * max_p_batch / max_p_rows / max_p_pages: the most prefill requests, query
+ * rows and page-table entries any later plan of this handle will have; the
+ * same for the decode half. All zero turns the mode off. From then on:
+ *  - the workspace layout depends on these capacities only
+ *    (pod_workspace_size reports it; bind again, the handle's workspace is
+ *    released);
+ *  - every launch runs the full grid (two CTAs per SM), the merge kernel is
+ *    always launched, and the kernels read the plan's counts from the
+ *    workspace, so a pod_run captured once serves every later plan;
+ *  - the q and out tensors passed to pod_run hold max_*_rows rows (rows past
+ *    the plan's own are neither read for keys nor written), and a half with a
+ *    non-zero capacity needs its tensors on every run;
+ *  - page sizes below 8 use the cp.async gather (the load path may not
+ *    depend on the page tables), and prefill key ranges are not split.
+ * Library mechanics beyond the passage (its capacity rules are the pages';
+ * the fixed layout is this library's way to meet them).
+ * Errors: POD_ERR_INVALID_ARG (NULL handle, a negative capacity, or the
+ * current plan exceeding one), POD_ERR_UNSUPPORTED (with RoPE or a custom
+ * prefill mask).
+ */
+pod_status pod_plan_set_graph_capacity(pod_handle h, int32_t max_p_batch, int32_t max_p_rows,
+                                       int32_t max_p_pages, int32_t max_d_batch,
+                                       int32_t max_d_rows, int32_t max_d_pages);
+
+/*
+ * pod_replan — plan new page tables into a capacity handle's bound workspace
+ * (POD walkthrough, "CUDAGraph 模式的运行时约束": each step plans again,
+ * outside capture, within the reserved sizes; "plan/run 生命周期").
+ * The arrays are host int32 as for pod_plan (the page pools, heads,
+ * head_dim, page size and every policy stay the plan's). The new metadata
+ * overwrites the workspace with one host-to-device copy on `stream`, which
+ * the call waits for; a pod_run captured earlier on this handle and
+ * workspace then computes the new plan when replayed (the caller updates the
+ * tensors it captured, e.g. the cache pages and queries, in place).
+ * Errors: POD_ERR_INVALID_ARG (no capacity mode, a table that fails pod_plan's
+ * checks or exceeds a capacity), POD_ERR_WORKSPACE (no bound workspace),
+ * POD_ERR_CUDA.
+ */
+pod_status pod_replan(pod_handle h, const int32_t* p_q_indptr, const int32_t* p_kv_indptr,
+                      const int32_t* p_kv_indices, const int32_t* p_last_page_len,
+                      int32_t p_batch, const int32_t* d_q_indptr, const int32_t* d_kv_indptr,
+                      const int32_t* d_kv_indices, const int32_t* d_last_page_len,
+                      int32_t d_batch, void* stream);
+
+/* Release the handle (host memory only). NULL is accepted. Library
+ * mechanics; no passage. */
 pod_status pod_destroy(pod_handle h);
 
-/* Thread-local message of the last error ("" if none). Valid until the next call. */
+/* Thread-local message of the last error ("" if none). Valid until the next
+ * call. Library mechanics; no passage. */
 const char* pod_last_error(void);
 
 /*
@@ -256,7 +311,8 @@ const char* pod_last_error(void);
  * status word in `workspace`. *device_status receives 0 when every kernel
  * finished its work; otherwise a bit mask (1 = a bounded wait of the prefill
  * pipeline ran out, 2 = shared-memory alignment check failed). Returns
- * POD_ERR_DEVICE_STATUS when the word was non-zero.
+ * POD_ERR_DEVICE_STATUS when the word was non-zero. Library mechanics (the
+ * bounded waits report here instead of hanging); no passage.
  */
 pod_status pod_read_device_status(pod_handle h, void* workspace, void* stream,
                                   int32_t* device_status);
@@ -276,7 +332,8 @@ pod_status pod_read_device_status(pod_handle h, void* workspace, void* stream,
  * prefill / decode query row (empty without RoPE).
  * Copies min(count, capacity) int32 values into `out` (may be NULL to query
  * *count). Each table's record format is documented beside the planner
- * (csrc/pod_plan.h in the library sources).
+ * (csrc/pod_plan.h in the library sources). Library mechanics (plan
+ * introspection for tests and tools); no passage.
  */
 pod_status pod_plan_table(pod_handle h, int32_t which, int32_t* out, int64_t capacity,
                           int64_t* count);
@@ -296,7 +353,9 @@ pod_status pod_plan_table(pod_handle h, int32_t which, int32_t* out, int64_t cap
  * passes the input and output tensors, with the same meaning as for pod_run.
  *
  * Each call uploads the plan's metadata into that array (clearing the status
- * word) and then runs the same kernels as pod_run. Every call on a device
+ * word) with a host-to-device copy, waits for the stream to finish that copy
+ * (so every call blocks the host until the work queued before it on the
+ * stream is done), and then runs the same kernels as pod_run. Every call on a device
  * shares the one array, which keeps the last call's contents: calls that
  * overlap on the GPU (other streams, other threads) race and must be
  * serialised by the caller. The handle becomes bound to the array (a later
@@ -313,7 +372,8 @@ pod_status pod_run_static_scratch(pod_handle h, const void* q_p, const void* kv_
                                   void* out_p, float* lse_p, void* out_d, float* lse_d,
                                   void* stream);
 
-/* Size in bytes of the static scratch array used by pod_run_static_scratch. */
+/* Size in bytes of the static scratch array used by pod_run_static_scratch.
+ * Library mechanics; no passage. */
 size_t pod_static_scratch_capacity(void);
 
 #ifdef __cplusplus

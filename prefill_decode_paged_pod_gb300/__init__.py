@@ -31,7 +31,7 @@ __all__ = [
     "pod_plan_table", "PodHandle", "LIB_PATH", "DEFAULT_WORKSPACE_BYTES",
     "pod_run_static_scratch", "pod_static_scratch_capacity", "pod_plan_set_decode_fp8",
     "pod_plan_set_prefill_mask", "pod_plan_set_kv_layout", "pod_plan_set_logits_transform",
-    "pod_plan_set_rope",
+    "pod_plan_set_rope", "pod_plan_set_graph_capacity", "pod_replan",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -94,6 +94,10 @@ def load_library(path: Optional[str] = None):
     lib.pod_plan_set_kv_layout.argtypes = [V, I32, I32]
     lib.pod_plan_set_prefill_mask.restype = ctypes.c_int
     lib.pod_plan_set_prefill_mask.argtypes = [V, V, ctypes.c_int64]
+    lib.pod_plan_set_graph_capacity.restype = ctypes.c_int
+    lib.pod_plan_set_graph_capacity.argtypes = [V] + [I32] * 6
+    lib.pod_replan.restype = ctypes.c_int
+    lib.pod_replan.argtypes = [V, V, V, V, V, I32, V, V, V, V, I32, V]
     if path is None:
         _lib = lib
     return lib
@@ -439,3 +443,27 @@ def _plan_inputs(inp, workspace, num_sms, stream) -> PodHandle:
                     p_num_pages=inp.p.num_pages, d_num_pages=inp.d.num_pages,
                     has_sinks=inp.sinks is not None, num_sms=num_sms, workspace=workspace,
                     stream=stream)
+
+
+def pod_plan_set_graph_capacity(h: PodHandle, max_p_batch: int, max_p_rows: int, max_p_pages: int,
+                                max_d_batch: int, max_d_rows: int, max_d_pages: int):
+    """Capacity mode for CUDA-graph replay: the workspace layout and launch
+    shapes depend on these maxima only; rebind the workspace afterwards. The
+    q/out tensors given to pod_run then hold max_*_rows rows."""
+    _check(load_library().pod_plan_set_graph_capacity(
+        ctypes.c_void_p(h.ptr), int(max_p_batch), int(max_p_rows), int(max_p_pages),
+        int(max_d_batch), int(max_d_rows), int(max_d_pages)))
+    h.workspace_bytes = pod_workspace_size(h)
+    h.p_rows, h.d_rows = int(max_p_rows), int(max_d_rows)
+
+
+def pod_replan(h: PodHandle, p_q_indptr, p_kv_indptr, p_kv_indices, p_last_page_len,
+               d_q_indptr, d_kv_indptr, d_kv_indices, d_last_page_len, stream=None):
+    """Plan new page tables into a capacity handle's bound workspace (outside
+    any capture); a pod_run captured earlier then replays the new plan."""
+    arrs = [_i32(x) for x in (p_q_indptr, p_kv_indptr, p_kv_indices, p_last_page_len,
+                              d_q_indptr, d_kv_indptr, d_kv_indices, d_last_page_len)]
+    p_batch = 0 if arrs[0] is None else len(arrs[0]) - 1
+    d_batch = 0 if arrs[4] is None else len(arrs[4]) - 1
+    _check(load_library().pod_replan(ctypes.c_void_p(h.ptr), *[_ptr(a) for a in arrs[:4]], p_batch,
+                                     *[_ptr(a) for a in arrs[4:]], d_batch, _stream(stream)))

@@ -233,6 +233,9 @@ PodPlanArgs args_of(const PodPlanHost& O) {
   a.window_left = O.window_left; a.sm_scale = O.sm_scale; a.dtype = O.dtype;
   a.has_sinks = O.has_sinks; a.num_sms = O.num_sms; a.p_custom_mask = O.p_custom_mask;
   a.rope = O.rope; a.rope_scale = O.rope_scale; a.rope_theta = O.rope_theta;
+  a.graph = O.graph;
+  a.cap_p_batch = O.cap_p_batch; a.cap_p_rows = O.cap_p_rows; a.cap_p_pages = O.cap_p_pages;
+  a.cap_d_batch = O.cap_d_batch; a.cap_d_rows = O.cap_d_rows; a.cap_d_pages = O.cap_d_pages;
   return a;
 }
 
@@ -289,6 +292,8 @@ pod_status pod_plan(const int32_t* p_q_indptr, const int32_t* p_kv_indptr,
   a.dtype = (int)dtype; a.has_sinks = has_sinks; a.num_sms = num_sms;
   a.p_custom_mask = 0;
   a.rope = 0; a.rope_scale = 1.0; a.rope_theta = 1e4;
+  a.graph = 0;
+  a.cap_p_batch = a.cap_p_rows = a.cap_p_pages = a.cap_d_batch = a.cap_d_rows = a.cap_d_pages = 0;
 
   pod_plan_s* h = new (std::nothrow) pod_plan_s();
   if (!h) return set_err(POD_ERR_INVALID_ARG, "out of host memory");
@@ -336,9 +341,13 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
   if (!h->workspace) return set_err(POD_ERR_WORKSPACE, "the plan has no bound workspace");
   if (workspace != h->workspace)
     return set_err(POD_ERR_WORKSPACE, "workspace differs from the one the plan was bound to");
-  if (P.p.rows > 0 && (!q_p || !kv_p || !out_p))
+  // capacity mode: a captured launch replays later plans, so every half with
+  // a capacity needs its tensors (sized for the capacity) on every run
+  const int p_rows_t = P.graph ? P.cap_p_rows : P.p.rows;
+  const int d_rows_t = P.graph ? P.cap_d_rows : P.dd.rows;
+  if (p_rows_t > 0 && (!q_p || !kv_p || !out_p))
     return set_err(POD_ERR_INVALID_ARG, "prefill half is non-empty but q_p/kv_p/out_p is NULL");
-  if (P.dd.rows > 0 && (!q_d || !kv_d || !out_d))
+  if (d_rows_t > 0 && (!q_d || !kv_d || !out_d))
     return set_err(POD_ERR_INVALID_ARG, "decode half is non-empty but q_d/kv_d/out_d is NULL");
   if (P.has_sinks && !sinks) return set_err(POD_ERR_INVALID_ARG, "plan has sinks but sinks is NULL");
   if (!P.has_sinks && sinks)
@@ -422,15 +431,15 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
   const void* ptrs[6] = {q_p, kv_p, q_d, kv_d, q_p_lo, q_d_lo};
   for (int i = 0; i < 6; ++i) {
     const bool pre = i < 2 || i == 4;
-    const PodHalfHost& hh = pre ? P.p : P.dd;
-    if (hh.rows == 0) continue;
+    const int rows = pre ? p_rows_t : d_rows_t;   // the q tensor's rows
+    if (rows == 0) continue;
     if (i >= 4 && !P.rope) continue;
     if ((i == 1 || i == 3) && !(pre ? P.p_tma : P.d_tma)) continue;
     if (h->tm_ptr[i] == ptrs[i]) continue;
     const int npages = pre ? p_pages : d_pages;
     pod_status st;
     if (i == 0 || i == 2 || i >= 4)
-      st = encode_q(&h->tm[i], ptrs[i], hh.rows, P.H, P.d, P.G, pre ? P.tq : P.tu, P.dtype);
+      st = encode_q(&h->tm[i], ptrs[i], rows, P.H, P.d, P.G, pre ? P.tq : P.tu, P.dtype);
     else if (pre)
       st = encode_kv(&h->tm[i], ptrs[i], npages, P.ps, P.Hk, P.d, P.p_tma, P.dtype, p_layout,
                      P.rope ? 3 : 2);
@@ -444,11 +453,11 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
 
   PodParams K;
   memset(&K, 0, sizeof(K));
-  if (P.p.rows) {
+  if (p_rows_t) {
     K.tm_q_p = h->tm[0];
     if (P.p_tma) K.tm_kv_p = h->tm[1];
   }
-  if (P.dd.rows) {
+  if (d_rows_t) {
     K.tm_q_d = h->tm[2];
     if (P.d_tma) K.tm_kv_d = h->tm[3];
   }
@@ -482,7 +491,9 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
   K.d_scale_log2 = P.scale_log2 * h->k_scale;
   K.v_scale = h->v_scale;
   K.n_p_ctas = P.n_p_ctas; K.grid = P.grid;
-  K.n_groups = (int)(P.mgroups.size() / POD_REC); K.n_mrows = P.n_mrows;
+  // the merge grid covers the capacity's merge rows in capacity mode (the
+  // kernel reads the plan's own count from the workspace)
+  K.n_groups = (int)(P.mgroups.size() / POD_REC); K.n_mrows = P.cap_mrows;
   K.p_batch = P.p.batch; K.d_batch = P.dd.batch;
   auto I = [&](size_t off) { return reinterpret_cast<const int32_t*>(ws + off); };
   K.p_q_indptr = I(P.off_p_q_indptr); K.p_kv_indptr = I(P.off_p_kv_indptr);
@@ -605,6 +616,54 @@ pod_status pod_plan_set_prefill_mask(pod_handle h, const void* packed_mask, int6
   h->p_mask = packed_mask;
   h->p_mask_bytes = want ? mask_bytes : 0;
   return POD_OK;
+}
+
+pod_status pod_plan_set_graph_capacity(pod_handle h, int32_t max_p_batch, int32_t max_p_rows,
+                                       int32_t max_p_pages, int32_t max_d_batch,
+                                       int32_t max_d_rows, int32_t max_d_pages) {
+  g_err.clear();
+  if (!h) return set_err(POD_ERR_INVALID_ARG, "handle is NULL");
+  PodPlanArgs a = args_of(h->plan);
+  const int32_t caps[6] = {max_p_batch, max_p_rows, max_p_pages, max_d_batch, max_d_rows,
+                           max_d_pages};
+  const bool off = caps[0] == 0 && caps[1] == 0 && caps[2] == 0 && caps[3] == 0 && caps[4] == 0 &&
+                   caps[5] == 0;
+  a.graph = off ? 0 : 1;
+  a.cap_p_batch = max_p_batch; a.cap_p_rows = max_p_rows; a.cap_p_pages = max_p_pages;
+  a.cap_d_batch = max_d_batch; a.cap_d_rows = max_d_rows; a.cap_d_pages = max_d_pages;
+  return replan(h, a);
+}
+
+pod_status pod_replan(pod_handle h, const int32_t* p_q_indptr, const int32_t* p_kv_indptr,
+                      const int32_t* p_kv_indices, const int32_t* p_last_page_len, int32_t p_batch,
+                      const int32_t* d_q_indptr, const int32_t* d_kv_indptr,
+                      const int32_t* d_kv_indices, const int32_t* d_last_page_len,
+                      int32_t d_batch, void* stream) {
+  g_err.clear();
+  if (!h) return set_err(POD_ERR_INVALID_ARG, "handle is NULL");
+  const PodPlanHost& O = h->plan;
+  if (!O.graph)
+    return set_err(POD_ERR_INVALID_ARG,
+                   "pod_replan needs a plan with a CUDA-graph capacity (pod_plan_set_graph_capacity)");
+  if (!h->workspace) return set_err(POD_ERR_WORKSPACE, "the plan has no bound workspace");
+  PodPlanArgs a = args_of(O);
+  a.p_q_indptr = p_q_indptr; a.p_kv_indptr = p_kv_indptr; a.p_kv_indices = p_kv_indices;
+  a.p_last_page_len = p_last_page_len; a.p_batch = p_batch;
+  a.d_q_indptr = d_q_indptr; a.d_kv_indptr = d_kv_indptr; a.d_kv_indices = d_kv_indices;
+  a.d_last_page_len = d_last_page_len; a.d_batch = d_batch;
+  PodPlanHost fresh;
+  std::string err;
+  const int rc = pod_build_plan(a, fresh, &err);
+  if (rc != 0) return set_err((pod_status)rc, err);
+  // the layout depends on the capacities alone; a difference is a library bug
+  if (fresh.total_bytes != O.total_bytes || fresh.int_bytes != O.int_bytes ||
+      fresh.off_dqrec != O.off_dqrec || fresh.off_part_lse != O.off_part_lse ||
+      fresh.grid != O.grid || fresh.p_tma != O.p_tma || fresh.d_tma != O.d_tma)
+    return set_err(POD_ERR_INVALID_ARG, "the new plan's layout differs from the bound one");
+  void* ws = h->workspace;
+  const size_t bytes = h->workspace_bytes;
+  h->plan = std::move(fresh);
+  return upload(h, ws, bytes, stream);
 }
 
 const char* pod_last_error(void) { return g_err.c_str(); }

@@ -141,7 +141,7 @@ enum {
 // shared memory; every other warp that walks tiles reads the same sequence.
 // Returns false when a wait ran out (the status word then says so).
 template <typename T, int D, int LT, bool RP>
-__device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
+__device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem, int n_tiles) {
   using L = PLayout<D, RP>;
   constexpr int NK = L::NK, NV = L::NV;
   static_assert(NK == 3 && NV == 2, "the barrier slots below are laid out for 3 K and 2 V stages");
@@ -162,7 +162,7 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
     int id = -1;
     if (lane == 0) {
       const int idx = atomicAdd(P.status + 8, 1);
-      id = idx < P.n_tiles ? __ldg(P.pqueue + idx) : -1;
+      id = idx < n_tiles ? __ldg(P.pqueue + idx) : -1;
       const uint64_t t0 = globaltimer();
       for (int r = 0; r < 8 && id != -2; ++r)
         while (tq_used[r] < seq - 7)
@@ -676,7 +676,7 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
 // Runs decode items from the shared queue until it is empty. Returns false
 // when a wait ran out (the status word then says so).
 template <typename T, int D, bool F8, int LT, bool RP>
-__device__ bool decode_role(const PodParams& P, uint8_t* smem) {
+__device__ bool decode_role(const PodParams& P, uint8_t* smem, int n_items) {
   using L = DLayout<D, RP>;
   constexpr bool BF16 = Pack<T>::kBF16;
   constexpr int NKB = L::NKB;
@@ -718,7 +718,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
     // the item needs, so the claim costs one dependent load
     if (tid == 0) {
       const int idx = atomicAdd(P.status + 9, 1);
-      *item_slot = idx < P.n_items ? idx : -1;
+      *item_slot = idx < n_items ? idx : -1;
     }
     __syncthreads();
     const int pos = *item_slot;
@@ -1249,16 +1249,18 @@ __global__ void __launch_bounds__(kThreads, RP ? 1 : POD_CTAS_PER_SM)
     // Both queues are drained by every CTA: its own role's queue first (the
     // plan sizes the split), then the other one, so whichever half finishes
     // early helps with the rest.
-    const bool p_first = (int)blockIdx.x < P.n_p_ctas;
+    // the plan's counts, from the workspace (written with the plan)
+    const int n_tiles = P.status[POD_ST_NTILES], n_items = P.status[POD_ST_NITEMS];
+    const bool p_first = (int)blockIdx.x < P.status[POD_ST_NPCTAS];
     bool ok = true;
     for (int phase = 0; phase < 2 && ok; ++phase) {
       const bool do_prefill = (phase == 0) == p_first;
-      if (do_prefill ? P.n_tiles == 0 : P.n_items == 0) continue;
+      if (do_prefill ? n_tiles == 0 : n_items == 0) continue;
       // shared memory changes hands between the generic and the async proxy
       fence_proxy_async();
       __syncthreads();
-      ok = do_prefill ? prefill_role<T, D, LT, RP>(P, smem, tmem)
-                      : decode_role<T, D, F8, LT, RP>(P, smem);
+      ok = do_prefill ? prefill_role<T, D, LT, RP>(P, smem, tmem, n_tiles)
+                      : decode_role<T, D, F8, LT, RP>(P, smem, n_items);
     }
     tc_fence_before();
     __syncthreads();

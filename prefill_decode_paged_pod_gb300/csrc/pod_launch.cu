@@ -24,9 +24,10 @@ __global__ void __launch_bounds__(256) pod_merge_kernel(const __grid_constant__ 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (gw >= P.n_mrows) return;
+  // the plan's counts, from the workspace (the grid may be sized for a capacity)
+  if (gw >= P.status[POD_ST_NMROWS]) return;
   // merge group containing merge row gw
-  int lo = 0, hi = P.n_groups - 1;
+  int lo = 0, hi = P.status[POD_ST_NGROUPS] - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (P.mrow_ptr[mid] <= gw) lo = mid; else hi = mid - 1;

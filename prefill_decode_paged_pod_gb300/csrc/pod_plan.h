@@ -39,6 +39,18 @@
 #include <stdint.h>
 #include <vector_types.h>
 
+// Status block: int32 words at the start of the workspace. [0] device status
+// word; [8], [9], [10] the tile and item queue heads and the count of
+// finished CTAs (the last CTA rewinds them); [16..20] the plan's counts
+// below. The kernels read the counts here rather than from their launch
+// parameters, so a launch captured in a CUDA graph serves every later plan
+// written into the same capacity-sized workspace.
+#define POD_ST_NTILES 16   // prefill tiles in the queue
+#define POD_ST_NITEMS 17   // decode items in the queue
+#define POD_ST_NPCTAS 18   // CTAs that start on the prefill queue
+#define POD_ST_NGROUPS 19  // merge groups
+#define POD_ST_NMROWS 20   // merge rows
+
 #define POD_REC 8
 #define POD_DQREC 16
 #define POD_TILE_ROWS 128      // prefill tile rows (tcgen05 M)

@@ -424,8 +424,25 @@ double decode_time(const std::vector<DecodeUnit>& units, const std::vector<doubl
   return t + extra;
 }
 
+// Items and partial rows a chunk makes (a unit longer than the chunk splits
+// into ceil(len / chunk) parts, each writing R = ntok * G partial rows).
+void chunk_counts(const std::vector<DecodeUnit>& units, int chunk, int G, int64_t* items,
+                  int64_t* prows) {
+  *items = 0;
+  *prows = 0;
+  for (const DecodeUnit& u : units) {
+    const int len = u.hi - u.lo;
+    const int64_t n = (chunk > 0 && len > chunk) ? (len + chunk - 1) / chunk : 1;
+    *items += n;
+    if (n > 1) *prows += n * u.ntok * G;
+  }
+}
+
+// The decode chunk with the least estimated time; with limits (>= 0), only
+// chunks whose items and partial rows fit them (no split always does).
 DecodeChoice best_decode(const std::vector<DecodeUnit>& units, const std::vector<double>& rate,
-                         int G, int d, const CostModel& cm, double total_bytes) {
+                         int G, int d, const CostModel& cm, double total_bytes,
+                         int64_t max_items = -1, int64_t max_prows = -1) {
   DecodeChoice best;
   // 0 = no split; then 16 Ki .. 256 keys. A candidate at or above the longest
   // key range splits nothing and is the unsplit plan again: skipped.
@@ -436,6 +453,11 @@ DecodeChoice best_decode(const std::vector<DecodeUnit>& units, const std::vector
   best.chunk = 0;
   for (int c : cands) {
     if (c == 0 || c >= max_keys) continue;
+    if (max_items >= 0) {
+      int64_t it, pr;
+      chunk_counts(units, c, G, &it, &pr);
+      if (it > max_items || pr > max_prows) continue;
+    }
     // taken only below best * (1 - 1e-9): no simulation needs to run past that
     const double t = decode_time(units, rate, c, G, d, cm, total_bytes, best.time * (1.0 - 1e-9));
     if (t < best.time * (1.0 - 1e-9)) {
@@ -512,6 +534,35 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   const int cps = P.rope ? 1 : POD_CTAS_PER_SM;
   P.ctas_per_sm = cps;
 
+  // CUDA-graph capacity mode (POD walkthrough, "CUDAGraph 模式的运行时约束":
+  // a fixed batch and page-table buffers reserved at their maximum size,
+  // with plan run outside capture): every table is laid out for the
+  // capacities, the grid is the full grid, and this plan must fit them.
+  P.graph = a.graph ? 1 : 0;
+  if (P.graph) {
+    if (P.rope || P.p_custom_mask)
+      return fail(err, kUnsupported, "CUDA-graph capacity with RoPE or a custom prefill mask");
+    const int caps[6] = {a.cap_p_batch, a.cap_p_rows, a.cap_p_pages,
+                         a.cap_d_batch, a.cap_d_rows, a.cap_d_pages};
+    for (int c : caps)
+      if (c < 0) return fail(err, kInvalid, "capacities must be >= 0");
+    const PodHalfHost* hh[2] = {&P.p, &P.dd};
+    const char* nm[2] = {"prefill", "decode"};
+    for (int k = 0; k < 2; ++k) {
+      const int64_t pages = hh[k]->kv_indptr.back();
+      if (hh[k]->batch > caps[3 * k] || hh[k]->rows > caps[3 * k + 1] || pages > caps[3 * k + 2])
+        return fail(err, kInvalid, std::string(nm[k]) + " half exceeds its capacity: " +
+                                       std::to_string(hh[k]->batch) + " requests, " +
+                                       std::to_string(hh[k]->rows) + " rows, " +
+                                       std::to_string(pages) + " pages against " +
+                                       std::to_string(caps[3 * k]) + ", " +
+                                       std::to_string(caps[3 * k + 1]) + ", " +
+                                       std::to_string(caps[3 * k + 2]));
+    }
+    P.cap_p_batch = a.cap_p_batch; P.cap_p_rows = a.cap_p_rows; P.cap_p_pages = a.cap_p_pages;
+    P.cap_d_batch = a.cap_d_batch; P.cap_d_rows = a.cap_d_rows; P.cap_d_pages = a.cap_d_pages;
+  }
+
   const CostModel cm = cost_model(a.d);
 
   // ---- decode units ---------------------------------------------------------
@@ -528,6 +579,12 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   // decode boxes hold both 64-element halves of head_dim; they are laid out
   // for page_size >= 8 (a page per box) and 1 (runs of pages) only
   P.d_tma = (a.ps == 1 || a.ps >= 8) ? tma_box_keys(P.dd, a.ps) : 0;
+  // in capacity mode the load path may not depend on the page tables: page
+  // boxes for page_size >= 8, the cp.async gather below
+  if (P.graph) {
+    P.p_tma = a.ps >= 8 ? P.p_tma : 0;
+    P.d_tma = a.ps >= 8 ? P.d_tma : 0;
+  }
   std::vector<DecodeUnit> units;
   double d_bytes = 0.0;
   for (int r = 0; r < P.dd.batch; ++r) {
@@ -566,7 +623,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
     }
   }
   int p_split = 1;
-  if (P.p.rows <= 1536 && !tunits.empty() && 2 * (int)tunits.size() <= grid_cap) {
+  if (!P.graph && P.p.rows <= 1536 && !tunits.empty() && 2 * (int)tunits.size() <= grid_cap) {
     double longest = 0.0, total = 0.0;
     for (const TileUnit& u : tunits) {
       const double t = cm.p_tile_ns + (double)nblocks(u.lo, u.hi) * cm.p_block_ns[2];
@@ -616,6 +673,16 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   // ---- CTA split between the halves ----------------------------------------
   const int S = a.num_sms;
   const int grid_max = S * cps;
+  // capacity mode: table sizes from the capacities alone. A request of q
+  // rows makes ceil(q / t) token blocks of each kv head; splits may add up to
+  // one item per CTA, and the partial rows of split items are bounded.
+  int64_t cap_tiles = 0, cap_units = 0, cap_items = 0, cap_prows = 0;
+  if (P.graph) {
+    cap_tiles = ((int64_t)(P.cap_p_rows + Tq - 1) / Tq + P.cap_p_batch) * P.Hk;
+    cap_units = ((int64_t)(P.cap_d_rows + Tu - 1) / Tu + P.cap_d_batch) * P.Hk;
+    cap_items = cap_units + grid_max;
+    cap_prows = (int64_t)2 * grid_max * POD_DECODE_ROWS;
+  }
   // per-CTA rates for a split: prefill in blocks per ns, decode in bytes per ns
   auto rates = [&](int n_p, int n_d, std::vector<double>& rp, std::vector<double>& rd) {
     rp.resize(n_p);
@@ -639,7 +706,8 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
     n_p = std::min(std::max(n_p, n_tiles > 0 ? 1 : 0), std::min(grid_max - 1, n_tiles));
     std::vector<double> rp, rd;
     rates(n_p, grid_max - n_p, rp, rd);
-    chunk = best_decode(units, rd, G, a.d, cm, d_bytes).chunk;
+    chunk = best_decode(units, rd, G, a.d, cm, d_bytes, P.graph ? cap_items : -1,
+                        P.graph ? cap_prows : -1).chunk;
   }
   int n_d_max = grid_max - n_p;
   // The kernel serves both queues to every CTA, so the split only sets where
@@ -775,6 +843,9 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   // CTAs than jobs
   int n_d = std::min(n_d_max, std::max(n_items, n_tiles + n_items - n_p));
   if (n_items == 0) n_d = 0;
+  // capacity mode: the launch shape may not depend on the plan, so the grid
+  // is always full (CTAs that find both queues empty leave at once)
+  if (P.graph) n_d = grid_max - n_p;
   P.n_p_ctas = n_p;
   P.n_d_ctas = n_d;
   P.grid = n_p + n_d;
@@ -877,24 +948,33 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
     off = align_up(off + std::max<size_t>(n_int32, 1) * 4, 16);
     return o;
   };
+  // capacity mode: every table at its capacity (this plan fits: checked
+  // above for the page tables, by construction for the rest)
+  auto sz = [&](size_t actual, int64_t capacity) -> size_t {
+    return P.graph ? (size_t)std::max<int64_t>(capacity, (int64_t)actual) : actual;
+  };
+  if (P.graph && ((int64_t)n_tiles > cap_tiles || (int64_t)n_items > cap_items ||
+                  (int64_t)n_prows > cap_prows || (int64_t)P.n_mrows > cap_prows))
+    return fail(err, kInvalid, "plan exceeds the capacity layout");
+  P.cap_mrows = P.graph ? (int)cap_prows : P.n_mrows;
   P.off_status = place(64);
-  P.off_p_q_indptr = place(P.p.q_indptr.size());
-  P.off_p_kv_indptr = place(P.p.kv_indptr.size());
-  P.off_p_kv_indices = place(P.p.kv_indices.size());
-  P.off_p_kv_len = place(P.p.kv_len.size());
-  P.off_d_q_indptr = place(P.dd.q_indptr.size());
-  P.off_d_kv_indptr = place(P.dd.kv_indptr.size());
-  P.off_d_kv_indices = place(P.dd.kv_indices.size());
-  P.off_d_kv_len = place(P.dd.kv_len.size());
-  P.off_ptiles = place(P.ptiles.size());
-  P.off_ditems = place(P.ditems.size());
-  P.off_cta_ptr = place(P.cta_ptr.size());
-  P.off_cta_list = place(P.cta_list.size());
-  P.off_mgroups = place(P.mgroups.size());
-  P.off_mrow_ptr = place(P.mrow_ptr.size());
-  P.off_pqueue = place(P.pqueue.size());
-  P.off_dqueue = place(P.dqueue.size());
-  P.off_dqrec = place(P.dqrec.size());
+  P.off_p_q_indptr = place(sz(P.p.q_indptr.size(), (int64_t)P.cap_p_batch + 1));
+  P.off_p_kv_indptr = place(sz(P.p.kv_indptr.size(), (int64_t)P.cap_p_batch + 1));
+  P.off_p_kv_indices = place(sz(P.p.kv_indices.size(), P.cap_p_pages));
+  P.off_p_kv_len = place(sz(P.p.kv_len.size(), P.cap_p_batch));
+  P.off_d_q_indptr = place(sz(P.dd.q_indptr.size(), (int64_t)P.cap_d_batch + 1));
+  P.off_d_kv_indptr = place(sz(P.dd.kv_indptr.size(), (int64_t)P.cap_d_batch + 1));
+  P.off_d_kv_indices = place(sz(P.dd.kv_indices.size(), P.cap_d_pages));
+  P.off_d_kv_len = place(sz(P.dd.kv_len.size(), P.cap_d_batch));
+  P.off_ptiles = place(sz(P.ptiles.size(), cap_tiles * POD_REC));
+  P.off_ditems = place(sz(P.ditems.size(), cap_items * POD_REC));
+  P.off_cta_ptr = place(sz(P.cta_ptr.size(), (int64_t)grid_max + 1));
+  P.off_cta_list = place(sz(P.cta_list.size(), cap_tiles + cap_items));
+  P.off_mgroups = place(sz(P.mgroups.size(), cap_units * POD_REC));
+  P.off_mrow_ptr = place(sz(P.mrow_ptr.size(), cap_units + 1));
+  P.off_pqueue = place(sz(P.pqueue.size(), cap_tiles));
+  P.off_dqueue = place(sz(P.dqueue.size(), cap_items));
+  P.off_dqrec = place(sz(P.dqrec.size(), cap_items * POD_DQREC));
   P.off_p_mask_off = place(P.p_mask_off.size());
   if (P.rope) {
     P.off_p_rope_src = place(P.p.kv_indices.size());
@@ -904,8 +984,9 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   }
   P.int_bytes = align_up(off, 256);
   P.off_part_o = P.int_bytes;
-  P.off_part_lse = align_up(P.off_part_o + (size_t)n_prows * a.d * 4, 256);
-  size_t end = align_up(P.off_part_lse + (size_t)std::max(n_prows, 1) * 4, 256);
+  const size_t prows_sz = sz((size_t)n_prows, cap_prows);
+  P.off_part_lse = align_up(P.off_part_o + prows_sz * a.d * 4, 256);
+  size_t end = align_up(P.off_part_lse + std::max<size_t>(prows_sz, 1) * 4, 256);
   if (P.rope) {
     // cos/sin table [rows][d/2] (float2), then the prefill page copies
     // (rows K_hi, V, K_lo: 16-bit) and the high and low parts of the rotated
@@ -931,6 +1012,14 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   auto put = [&](size_t o, const std::vector<int32_t>& v) {
     if (!v.empty()) std::memcpy(P.int_image.data() + o, v.data(), v.size() * 4);
   };
+  {
+    int32_t* st = reinterpret_cast<int32_t*>(P.int_image.data() + P.off_status);
+    st[POD_ST_NTILES] = n_tiles;
+    st[POD_ST_NITEMS] = n_items;
+    st[POD_ST_NPCTAS] = P.n_p_ctas;
+    st[POD_ST_NGROUPS] = (int32_t)(P.mgroups.size() / POD_REC);
+    st[POD_ST_NMROWS] = P.n_mrows;
+  }
   put(P.off_p_q_indptr, P.p.q_indptr);
   put(P.off_p_kv_indptr, P.p.kv_indptr);
   std::vector<int32_t> ident;

@@ -41,6 +41,13 @@ struct PodPlanHost {
   // schedule
   int grid = 0, n_p_ctas = 0, n_d_ctas = 0, decode_chunk = 0;
   int ctas_per_sm = POD_CTAS_PER_SM;   // 1 under RoPE
+  // CUDA-graph capacity mode: the workspace layout and the launch shapes
+  // depend only on these capacities (see PodPlanArgs), so a launch captured
+  // once serves every later plan of tables within them
+  int graph = 0;
+  int cap_p_batch = 0, cap_p_rows = 0, cap_p_pages = 0, cap_d_batch = 0, cap_d_rows = 0,
+      cap_d_pages = 0;
+  int cap_mrows = 0;          // merge rows the merge kernel's grid covers
   int p_tma = 0, d_tma = 0;   // keys per TMA K/V box of the half (0 = cp.async gather)
   int tq = 0, tu = 0;         // tokens per prefill tile / decode unit
   std::vector<int32_t> ptiles, ditems, cta_ptr, cta_list, mgroups, mrow_ptr, pqueue, dqueue, dqrec;
@@ -69,6 +76,10 @@ struct PodPlanArgs {
   int p_custom_mask;   // 1: a custom mask replaces the causal rule on the prefill half
   int rope;            // 1: ROPE_LLAMA with rope_scale, rope_theta
   double rope_scale, rope_theta;
+  // 1: CUDA-graph capacity mode with these maxima per half (requests, query
+  // rows, page-table entries); 0: the layout fits this plan exactly
+  int graph;
+  int cap_p_batch, cap_p_rows, cap_p_pages, cap_d_batch, cap_d_rows, cap_d_pages;
 };
 
 // Returns 0 on success, else a pod_status code with *err set.

@@ -591,3 +591,53 @@ def test_replanning_switches_keep_each_other(lib):
     assert pod.pod_workspace_size(h) == pod.pod_workspace_size(h0)
     for w in range(12):
         assert np.array_equal(pod.pod_plan_table(h, w), pod.pod_plan_table(h0, w)), w
+
+
+# ------------------------------------------------------------- CUDA-graph capacity mode
+def _caps_case(seed, d_kv, p_q, p_kv):
+    return make_custom("gc", torch.bfloat16, 16, 2, 128, 16, True, -1, [p_q], [p_kv],
+                       [1] * len(d_kv), d_kv, seed=seed)
+
+
+def test_graph_capacity_layout_is_fixed(lib):
+    """Under a CUDA-graph capacity the workspace layout and the launch shape
+    depend on the capacities only: two plans of different lengths within the
+    same capacities have the same workspace size and the full grid, and their
+    counts sit in the status block the kernels read."""
+    caps = (2, 256, 64, 8, 8, 800)
+    sizes, grids = set(), set()
+    for seed, d_kv, pq, pkv in ((1, [300, 500, 77, 1000], 64, 64),
+                                (2, [301, 501, 78, 1001, 17, 3000], 128, 192)):
+        inp = _caps_case(seed, d_kv, pq, pkv)
+        h = plan_host(inp, num_sms=8)
+        pod.pod_plan_set_graph_capacity(h, *caps)
+        s = pod.plan_summary(h)
+        sizes.add(pod.pod_workspace_size(h))
+        grids.add(s["grid"])
+        assert s["grid"] == 16                      # 2 CTAs x 8 SMs, whatever the work
+        check_against_reference(inp, h)
+        pod.pod_destroy(h)
+    assert len(sizes) == 1 and grids == {16}
+
+
+def test_graph_capacity_and_replan_errors(lib):
+    inp = _caps_case(1, [300, 500], 64, 64)
+    h = plan_host(inp, num_sms=8)
+    with pytest.raises(pod.PodError) as e:             # no capacity mode
+        pod.pod_replan(h, inp.p.q_indptr, inp.p.kv_indptr, inp.p.kv_indices, inp.p.last_page_len,
+                       inp.d.q_indptr, inp.d.kv_indptr, inp.d.kv_indices, inp.d.last_page_len)
+    assert e.value.code == 1
+    with pytest.raises(pod.PodError) as e:             # the current plan exceeds a capacity
+        pod.pod_plan_set_graph_capacity(h, 1, 256, 64, 1, 8, 800)
+    assert e.value.code == 1
+    pod.pod_plan_set_graph_capacity(h, 2, 256, 64, 8, 8, 800)
+    with pytest.raises(pod.PodError) as e:             # no bound workspace yet
+        pod.pod_replan(h, inp.p.q_indptr, inp.p.kv_indptr, inp.p.kv_indices, inp.p.last_page_len,
+                       inp.d.q_indptr, inp.d.kv_indptr, inp.d.kv_indices, inp.d.last_page_len)
+    assert e.value.code == 3
+    with pytest.raises(pod.PodError) as e:             # one capacity mode at a time with RoPE
+        pod.pod_plan_set_rope(h, 1.0, 1e4)
+    assert e.value.code == 2
+    pod.pod_plan_set_graph_capacity(h, 0, 0, 0, 0, 0, 0)   # off again
+    assert pod.plan_summary(h)["grid"] <= 16
+    pod.pod_destroy(h)

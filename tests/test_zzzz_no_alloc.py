@@ -6,8 +6,11 @@ cudaMalloc's implicit synchronisation) get the kernels' scratch from a fixed
 array inside the library instead of a workspace of their own. These tests go
 through the C ABI (ctypes binding) and check that this entry point returns
 what pod_run returns with a caller-allocated workspace, on two calls in a row
-that use different plans, and that a plan too large for the array is refused.
-This file is collected last on purpose.
+that use different plans (one under RoPE, whose angle table and rotated
+copies also live in the array and must be rebuilt when another plan used it
+in between), and that a plan too large for the array is refused. The file
+name sorts after every other test file on purpose: a run that stops at the
+first failure has run all the others before this one.
 """
 import numpy as np
 import pytest
@@ -53,8 +56,12 @@ def test_static_scratch_matches_pod_run_two_calls():
         make_custom("split", torch.bfloat16, 16, 2, 128, 16, True, -1, [40], [300],
                     [1, 2, 1], [5000, 7000, 3000], seed=11, sinks=True),
         make_config("c1"),
+        make_custom("rope", torch.bfloat16, 16, 2, 128, 16, True, -1, [70], [100], [1, 4],
+                    [300, 129], seed=13),
+        make_config("c1"),
     ]
-    sms = [4, 0]
+    cases[2].rope = (1.0, 1e4)
+    sms = [4, 0, 0, 0]
     for inp, ns in zip(cases, sms):
         dev = to_dev(inp)
         # existing entry point, caller-allocated workspace
