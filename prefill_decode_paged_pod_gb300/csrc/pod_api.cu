@@ -491,9 +491,11 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
   K.d_scale_log2 = P.scale_log2 * h->k_scale;
   K.v_scale = h->v_scale;
   K.n_p_ctas = P.n_p_ctas; K.grid = P.grid;
-  // the merge grid covers the capacity's merge rows in capacity mode (the
-  // kernel reads the plan's own count from the workspace)
-  K.n_groups = (int)(P.mgroups.size() / POD_REC); K.n_mrows = P.cap_mrows;
+  K.n_groups = (int)(P.mgroups.size() / POD_REC); K.n_mrows = P.n_mrows;
+  // CUDA-graph capacity mode: counts from the workspace, merge grid for the
+  // capacity's merge rows
+  K.counts_in_ws = P.graph;
+  K.mrows_grid = P.cap_mrows;
   K.p_batch = P.p.batch; K.d_batch = P.dd.batch;
   auto I = [&](size_t off) { return reinterpret_cast<const int32_t*>(ws + off); };
   K.p_q_indptr = I(P.off_p_q_indptr); K.p_kv_indptr = I(P.off_p_kv_indptr);
@@ -504,7 +506,9 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p, const void* 
   K.cta_ptr = I(P.off_cta_ptr); K.cta_list = I(P.off_cta_list);
   K.mgroups = I(P.off_mgroups); K.mrow_ptr = I(P.off_mrow_ptr);
   K.pqueue = I(P.off_pqueue); K.dqueue = I(P.off_dqueue); K.dqrec = I(P.off_dqrec);
-  K.n_tiles = (int)P.pqueue.size(); K.n_items = (int)P.dqueue.size();
+  // capacity mode: the queues' capacities (sentinels follow the plan's records)
+  K.n_tiles = P.graph ? P.cap_tiles : (int)P.pqueue.size();
+  K.n_items = P.graph ? P.cap_items : (int)P.dqueue.size();
   K.part_o = reinterpret_cast<float*>(ws + P.off_part_o);
   K.part_lse = reinterpret_cast<float*>(ws + P.off_part_lse);
   K.status = reinterpret_cast<int32_t*>(ws + P.off_status);

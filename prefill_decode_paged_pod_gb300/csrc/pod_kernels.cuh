@@ -141,7 +141,7 @@ enum {
 // shared memory; every other warp that walks tiles reads the same sequence.
 // Returns false when a wait ran out (the status word then says so).
 template <typename T, int D, int LT, bool RP>
-__device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem, int n_tiles) {
+__device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
   using L = PLayout<D, RP>;
   constexpr int NK = L::NK, NV = L::NV;
   static_assert(NK == 3 && NV == 2, "the barrier slots below are laid out for 3 K and 2 V stages");
@@ -161,8 +161,10 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem, i
   auto fetch_tile = [&](int seq) -> int {
     int id = -1;
     if (lane == 0) {
+      // (in CUDA-graph capacity mode n_tiles is the capacity and the queue
+      // holds -1 past the plan's own tiles: the queue is empty there too)
       const int idx = atomicAdd(P.status + 8, 1);
-      id = idx < n_tiles ? __ldg(P.pqueue + idx) : -1;
+      id = idx < P.n_tiles ? __ldg(P.pqueue + idx) : -1;
       const uint64_t t0 = globaltimer();
       for (int r = 0; r < 8 && id != -2; ++r)
         while (tq_used[r] < seq - 7)
@@ -227,8 +229,10 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem, i
     int kfill = 0, vfill = 0, qfill = 0;
     // L2 priorities: a Q tile is read once; the prefill K/V blocks are re-read
     // by every tile of their request and head, next to a decode stream that
-    // would otherwise evict them
-    const uint64_t pol_q = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
+    // would otherwise evict them. (Each policy is made where it is used, one
+    // instruction, rather than held in registers across the loops.)
+#define pol_q l2_policy_evict_first()
+#define pol_kv l2_policy_evict_last()
     bool ok = true;
     const uint32_t q_bytes = (uint32_t)(L::NQ * L::NKB * 128 * G * P.tq);
     if (P.p_tma) {
@@ -382,6 +386,8 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem, i
       *abort_flag = 1;
       raise_status(P.status, POD_STATUS_TIMEOUT);
     }
+#undef pol_q
+#undef pol_kv
   } else if (warp == 4) {
     // ------------------------------------------------------------ MMA issuer
     // Order per tile: QK_0, [QK_1, PV_0], [QK_2, PV_1], ..., PV_{nb-1}. QK_{j+2}
@@ -676,7 +682,7 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem, i
 // Runs decode items from the shared queue until it is empty. Returns false
 // when a wait ran out (the status word then says so).
 template <typename T, int D, bool F8, int LT, bool RP>
-__device__ bool decode_role(const PodParams& P, uint8_t* smem, int n_items) {
+__device__ bool decode_role(const PodParams& P, uint8_t* smem) {
   using L = DLayout<D, RP>;
   constexpr bool BF16 = Pack<T>::kBF16;
   constexpr int NKB = L::NKB;
@@ -718,12 +724,15 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem, int n_items) {
     // the item needs, so the claim costs one dependent load
     if (tid == 0) {
       const int idx = atomicAdd(P.status + 9, 1);
-      *item_slot = idx < n_items ? idx : -1;
+      *item_slot = idx < P.n_items ? idx : -1;
     }
     __syncthreads();
     const int pos = *item_slot;
     if (pos < 0 || !ok) break;
     const int32_t* rec = P.dqrec + POD_DQREC * pos;
+    // CUDA-graph capacity mode: n_items is the capacity and the records past
+    // the plan's own items have request -1 (the queue is empty there)
+    if (rec[0] < 0) break;
     const int g = rec[1], tok0 = rec[2], ntok = rec[3], k0 = rec[4], k1 = rec[5];
     const int R = ntok * G;
     const int Mt = (R + 15) >> 4;
@@ -1249,18 +1258,16 @@ __global__ void __launch_bounds__(kThreads, RP ? 1 : POD_CTAS_PER_SM)
     // Both queues are drained by every CTA: its own role's queue first (the
     // plan sizes the split), then the other one, so whichever half finishes
     // early helps with the rest.
-    // the plan's counts, from the workspace (written with the plan)
-    const int n_tiles = P.status[POD_ST_NTILES], n_items = P.status[POD_ST_NITEMS];
-    const bool p_first = (int)blockIdx.x < P.status[POD_ST_NPCTAS];
+    const bool p_first = (int)blockIdx.x < P.n_p_ctas;
     bool ok = true;
     for (int phase = 0; phase < 2 && ok; ++phase) {
       const bool do_prefill = (phase == 0) == p_first;
-      if (do_prefill ? n_tiles == 0 : n_items == 0) continue;
+      if (do_prefill ? P.n_tiles == 0 : P.n_items == 0) continue;
       // shared memory changes hands between the generic and the async proxy
       fence_proxy_async();
       __syncthreads();
-      ok = do_prefill ? prefill_role<T, D, LT, RP>(P, smem, tmem, n_tiles)
-                      : decode_role<T, D, F8, LT, RP>(P, smem, n_items);
+      ok = do_prefill ? prefill_role<T, D, LT, RP>(P, smem, tmem)
+                      : decode_role<T, D, F8, LT, RP>(P, smem);
     }
     tc_fence_before();
     __syncthreads();

@@ -24,10 +24,12 @@ __global__ void __launch_bounds__(256) pod_merge_kernel(const __grid_constant__ 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  // the plan's counts, from the workspace (the grid may be sized for a capacity)
-  if (gw >= P.status[POD_ST_NMROWS]) return;
+  // in CUDA-graph capacity mode the grid covers the capacity and the plan's
+  // counts come from the workspace
+  const int n_mrows = P.counts_in_ws ? P.status[POD_ST_NMROWS] : P.n_mrows;
+  if (gw >= n_mrows) return;
   // merge group containing merge row gw
-  int lo = 0, hi = P.status[POD_ST_NGROUPS] - 1;
+  int lo = 0, hi = (P.counts_in_ws ? P.status[POD_ST_NGROUPS] : P.n_groups) - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (P.mrow_ptr[mid] <= gw) lo = mid; else hi = mid - 1;
@@ -71,7 +73,8 @@ __global__ void __launch_bounds__(256) pod_merge_kernel(const __grid_constant__ 
 template <typename T, int D>
 cudaError_t launch_merge(const PodParams& P, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((P.n_mrows + 7) / 8));
+  const int rows = P.counts_in_ws ? P.mrows_grid : P.n_mrows;
+  cfg.gridDim = dim3((unsigned)((rows + 7) / 8));
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -94,7 +97,7 @@ cudaError_t pod_launch(const PodParams& P, int dtype, cudaStream_t stream) {
                                             : pod_k1_plain(P, dtype, stream);
     if (e != cudaSuccess) return e;
   }
-  if (P.n_mrows > 0) {
+  if ((P.counts_in_ws ? P.mrows_grid : P.n_mrows) > 0) {
     cudaError_t e;
     if (P.d == 128)
       e = dtype == 1 ? launch_merge<__nv_bfloat16, 128>(P, stream) : launch_merge<__half, 128>(P, stream);

@@ -42,9 +42,9 @@
 // Status block: int32 words at the start of the workspace. [0] device status
 // word; [8], [9], [10] the tile and item queue heads and the count of
 // finished CTAs (the last CTA rewinds them); [16..20] the plan's counts
-// below. The kernels read the counts here rather than from their launch
-// parameters, so a launch captured in a CUDA graph serves every later plan
-// written into the same capacity-sized workspace.
+// below. In CUDA-graph capacity mode the merge kernel reads its counts here
+// rather than from its launch parameters, so a launch captured once serves
+// every later plan written into the same capacity-sized workspace.
 #define POD_ST_NTILES 16   // prefill tiles in the queue
 #define POD_ST_NITEMS 17   // decode items in the queue
 #define POD_ST_NPCTAS 18   // CTAs that start on the prefill queue
@@ -105,6 +105,13 @@ struct PodParams {
   const int32_t *ptiles, *ditems, *cta_ptr, *cta_list, *mgroups, *mrow_ptr;
   const int32_t *pqueue, *dqueue, *dqrec;
   int n_tiles, n_items;
+  // CUDA-graph capacity mode (1): n_tiles / n_items are the capacities (the
+  // queues hold sentinels past the plan's own records), the merge kernel
+  // takes its counts from the workspace status block and its grid covers
+  // mrows_grid rows. A load of the counts per claim in the fused kernel
+  // measured 1.6 % slower, so K1 takes them from these parameters.
+  int counts_in_ws;
+  int mrows_grid;
   float* part_o;             // [n_prows, d]
   float* part_lse;           // [n_prows]
   int32_t* status;           // device status word

@@ -957,6 +957,8 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
                   (int64_t)n_prows > cap_prows || (int64_t)P.n_mrows > cap_prows))
     return fail(err, kInvalid, "plan exceeds the capacity layout");
   P.cap_mrows = P.graph ? (int)cap_prows : P.n_mrows;
+  P.cap_tiles = P.graph ? (int)cap_tiles : n_tiles;
+  P.cap_items = P.graph ? (int)cap_items : n_items;
   P.off_status = place(64);
   P.off_p_q_indptr = place(sz(P.p.q_indptr.size(), (int64_t)P.cap_p_batch + 1));
   P.off_p_kv_indptr = place(sz(P.p.kv_indptr.size(), (int64_t)P.cap_p_batch + 1));
@@ -1043,6 +1045,15 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   put(P.off_pqueue, P.pqueue);
   put(P.off_dqueue, P.dqueue);
   put(P.off_dqrec, P.dqrec);
+  // capacity mode: the kernels serve the queues up to their capacities, so
+  // every position past the plan's own records is a sentinel (tile -1, a
+  // decode record of request -1)
+  if (P.graph) {
+    int32_t* pq = reinterpret_cast<int32_t*>(P.int_image.data() + P.off_pqueue);
+    for (int i = n_tiles; i < P.cap_tiles; ++i) pq[i] = -1;
+    int32_t* dq = reinterpret_cast<int32_t*>(P.int_image.data() + P.off_dqrec);
+    for (int i = n_items; i < P.cap_items; ++i) dq[(size_t)i * POD_DQREC] = -1;
+  }
   put(P.off_p_mask_off, P.p_mask_off);
   if (P.rope) {
     put(P.off_p_rope_src, P.p.kv_indices);

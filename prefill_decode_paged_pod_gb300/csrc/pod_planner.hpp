@@ -48,6 +48,7 @@ struct PodPlanHost {
   int cap_p_batch = 0, cap_p_rows = 0, cap_p_pages = 0, cap_d_batch = 0, cap_d_rows = 0,
       cap_d_pages = 0;
   int cap_mrows = 0;          // merge rows the merge kernel's grid covers
+  int cap_tiles = 0, cap_items = 0;   // queue capacities (sentinels past the plan's)
   int p_tma = 0, d_tma = 0;   // keys per TMA K/V box of the half (0 = cp.async gather)
   int tq = 0, tu = 0;         // tokens per prefill tile / decode unit
   std::vector<int32_t> ptiles, ditems, cta_ptr, cta_list, mgroups, mrow_ptr, pqueue, dqueue, dqrec;
