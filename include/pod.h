@@ -96,8 +96,11 @@ typedef enum { POD_F16 = 0, POD_BF16 = 1 } pod_dtype;
  * is not monotone from 0, last_page_len is outside [1, page_size] for a
  * request with queries, an index is outside the pool, kv_len < q_len under
  * causal, or kv_len == 0 for a request with queries. POD_ERR_UNSUPPORTED for
- * head_dim other than 64/128, more than 128 qo heads per KV head, or more
- * than 32 qo heads per KV head on the decode half. POD_ERR_WORKSPACE when the
+ * head_dim other than 64/128/256, more than 128 qo heads per KV head, or
+ * more than 32 qo heads per KV head on the decode half. At head_dim 256 the
+ * fused kernel runs one CTA per SM (its O takes 256 TMEM columns and its
+ * prefill stages most of the shared memory); RoPE, FP8 decode caches, the
+ * soft cap and ALiBi are not built there (refused by their setters). POD_ERR_WORKSPACE when the
  * workspace is too small. On error *out_handle is NULL.
  */
 pod_status pod_plan(const int32_t* p_q_indptr, const int32_t* p_kv_indptr,
@@ -179,8 +182,9 @@ pod_status pod_plan_set_decode_fp8(pod_handle h, float k_scale, float v_scale);
  * Sinks stay plain logits; the LSE is that of the transformed logits.
  * Takes effect from the next pod_run; the plan and workspace are kept.
  * Errors: POD_ERR_INVALID_ARG (NULL handle, negative or non-finite cap),
- * POD_ERR_UNSUPPORTED (both at once, ALiBi under RoPE, or either with an
- * FP8 decode cache; pod_run also refuses slopes that are not device memory).
+ * POD_ERR_UNSUPPORTED (both at once, ALiBi under RoPE, either with an FP8
+ * decode cache or at head_dim 256; pod_run also refuses slopes that are not
+ * device memory).
  */
 pod_status pod_plan_set_logits_transform(pod_handle h, float logits_soft_cap,
                                          const float* alibi_slopes);
@@ -205,8 +209,8 @@ pod_status pod_plan_set_logits_transform(pod_handle h, float logits_soft_cap,
  * Switching it on, off or to other values plans the handle again: any bound
  * workspace is released, bind again (the size changes).
  * Errors: POD_ERR_INVALID_ARG (NULL handle, non-finite or non-positive
- * values), POD_ERR_UNSUPPORTED (with an FP8 decode cache, or with ALiBi
- * slopes set: one position encoding at a time).
+ * values), POD_ERR_UNSUPPORTED (with an FP8 decode cache, at head_dim 256,
+ * or with ALiBi slopes set: one position encoding at a time).
  */
 pod_status pod_plan_set_rope(pod_handle h, float rope_scale, float rope_theta);
 

@@ -559,6 +559,8 @@ pod_status pod_plan_set_logits_transform(pod_handle h, float logits_soft_cap,
     return set_err(POD_ERR_UNSUPPORTED, "ALiBi with RoPE (one position encoding at a time)");
   if ((logits_soft_cap > 0.f || alibi_slopes) && h->d_fp8)
     return set_err(POD_ERR_UNSUPPORTED, "a soft cap or ALiBi with an FP8 decode cache");
+  if ((logits_soft_cap > 0.f || alibi_slopes) && h->plan.d == 256)
+    return set_err(POD_ERR_UNSUPPORTED, "a soft cap or ALiBi with head_dim 256");
   h->soft_cap = logits_soft_cap;
   h->alibi = alibi_slopes;
   return POD_OK;

@@ -74,9 +74,18 @@ struct PLayout {                                   // prefill shared memory
   // +256: tile-id ring [8], +288: published count, +320: per-warp read counts [8]
   static constexpr int TQ_OFF = BAR_OFF + 256;
   static constexpr int TOTAL = BAR_OFF + 384;
-  static constexpr int TMEM_COLS = 256;            // S/P[2] (2 x 64) + O (<= 128)
+  // TMEM: S/P[2] (2 x 64 columns) then O (D columns); 256 columns let two
+  // CTAs share an SM's 512, head_dim 256 takes them all (one CTA per SM)
   static constexpr int TM_S = 0, TM_O = 128;
+  static constexpr int TMEM_COLS = TM_O + D <= 256 ? 256 : 512;
 };
+
+// CTAs per SM of an instantiation: RoPE (low parts of the rotated operands)
+// and head_dim 256 (shared memory and TMEM) run one, the others two.
+template <int D, bool RP>
+constexpr int ctas_per_sm() {
+  return (RP || D > 128) ? 1 : POD_CTAS_PER_SM;
+}
 
 template <int D, bool RP>
 struct DLayout {                                   // decode shared memory
@@ -1234,7 +1243,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
 // LT: logits transform of both halves (POD_LT_NONE, _SOFTCAP, _ALIBI).
 // RP: ROPE_LLAMA (one CTA per SM; a soft cap is then a run-time switch).
 template <typename T, int D, bool F8, int LT, bool RP>
-__global__ void __launch_bounds__(kThreads, RP ? 1 : POD_CTAS_PER_SM)
+__global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, RP>()))
     pod_kernel(const __grid_constant__ PodParams P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   // the merge kernel may start its prologue now; it waits for this grid's completion

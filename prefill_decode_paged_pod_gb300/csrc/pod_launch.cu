@@ -99,7 +99,9 @@ cudaError_t pod_launch(const PodParams& P, int dtype, cudaStream_t stream) {
   }
   if ((P.counts_in_ws ? P.mrows_grid : P.n_mrows) > 0) {
     cudaError_t e;
-    if (P.d == 128)
+    if (P.d == 256)
+      e = dtype == 1 ? launch_merge<__nv_bfloat16, 256>(P, stream) : launch_merge<__half, 256>(P, stream);
+    else if (P.d == 128)
       e = dtype == 1 ? launch_merge<__nv_bfloat16, 128>(P, stream) : launch_merge<__half, 128>(P, stream);
     else
       e = dtype == 1 ? launch_merge<__nv_bfloat16, 64>(P, stream) : launch_merge<__half, 64>(P, stream);

@@ -501,7 +501,10 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   if (a.H % a.Hk != 0)
     return fail(err, kInvalid, "num_qo_heads must be a multiple of num_kv_heads");
   if (a.ps <= 0) return fail(err, kInvalid, "page_size must be positive");
-  if (a.d != 64 && a.d != 128) return fail(err, kUnsupported, "head_dim must be 64 or 128");
+  if (a.d != 64 && a.d != 128 && a.d != 256)
+    return fail(err, kUnsupported, "head_dim must be 64, 128 or 256");
+  if (a.d == 256 && a.rope)
+    return fail(err, kUnsupported, "RoPE with head_dim 256");
   if (a.dtype != 0 && a.dtype != 1) return fail(err, kUnsupported, "dtype must be fp16 or bf16");
   if (a.window_left < -1) return fail(err, kInvalid, "window_left must be -1 or >= 0");
   if (a.num_sms <= 0) return fail(err, kInvalid, "num_sms must be positive");
@@ -529,9 +532,10 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
   if (rc) return rc;
   if (P.dd.rows > 0 && G > POD_DECODE_ROWS)
     return fail(err, kUnsupported, "more than 32 qo heads per kv head on the decode half");
-  // The RoPE kernel holds the low parts of the rotated operands and runs one
-  // CTA per SM; the plain kernels run two.
-  const int cps = P.rope ? 1 : POD_CTAS_PER_SM;
+  // The RoPE kernel holds the low parts of the rotated operands and the
+  // head_dim 256 kernel a 256-column O (TMEM) and 224 KB of stages: they run
+  // one CTA per SM; the others two.
+  const int cps = (P.rope || a.d > 128) ? 1 : POD_CTAS_PER_SM;
   P.ctas_per_sm = cps;
 
   // CUDA-graph capacity mode (POD walkthrough, "CUDAGraph 模式的运行时约束":

@@ -641,3 +641,22 @@ def test_graph_capacity_and_replan_errors(lib):
     pod.pod_plan_set_graph_capacity(h, 0, 0, 0, 0, 0, 0)   # off again
     assert pod.plan_summary(h)["grid"] <= 16
     pod.pod_destroy(h)
+
+
+def test_head_dim_256_plans_one_cta_per_sm(lib):
+    """head_dim 256 (a 256-column O in TMEM, 224 KB of prefill stages) plans
+    one CTA per SM; the logits transforms and RoPE are refused there."""
+    from pod_workloads import alibi_slopes
+    inp = make_custom("d256", torch.bfloat16, 16, 2, 256, 16, True, -1, [300, 33], [300, 40],
+                      [1, 4], [900, 77], seed=3, sinks=True)
+    h = plan_host(inp, num_sms=16)
+    s = check_against_reference(inp, h)
+    assert s["grid"] <= 16
+    for call in (lambda: pod.pod_plan_set_logits_transform(h, 30.0, None),
+                 lambda: pod.pod_plan_set_logits_transform(h, 0.0, alibi_slopes(16)),
+                 lambda: pod.pod_plan_set_rope(h, 1.0, 1e4),
+                 lambda: pod.pod_plan_set_decode_fp8(h, 1.0, 1.0)):
+        with pytest.raises(pod.PodError) as e:
+            call()
+        assert e.value.code == 2
+    pod.pod_destroy(h)

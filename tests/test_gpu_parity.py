@@ -373,3 +373,33 @@ def test_custom_prefill_mask(case):
     first = inp.p.q_indptr[:-1][np.diff(inp.p.q_indptr) > 2]
     assert np.all(op[first] == 0.0) and np.all(np.isneginf(lp[first]))
 
+
+
+# ------------------------------------------------------------- head_dim 256
+D256_CASES = [
+    # name, dtype, H, Hk, ps, causal, window, sinks, p_q, p_kv, d_q, d_kv, pages, num_sms
+    ("b16", torch.bfloat16, 16, 2, 16, True, -1, True, [300, 33], [300, 40], [1, 4, 1],
+     [900, 77, 2000], "perm", 0),
+    ("f8g", torch.float16, 64, 8, 16, True, 500, False, [129], [700], [1, 1, 3], [1500, 64, 300],
+     "perm", 0),
+    ("mha1", torch.bfloat16, 4, 4, 1, False, -1, True, [70], [90], [2, 1], [400, 17], "contig", 0),
+    ("gather", torch.float16, 8, 2, 3, True, -1, False, [50], [80], [1, 2], [250, 33], "perm", 0),
+    ("split", torch.bfloat16, 16, 2, 16, True, -1, True, [40], [300], [1, 4], [6000, 9000],
+     "perm", 8),
+]
+
+
+@pytest.mark.parametrize("case", D256_CASES, ids=[c[0] for c in D256_CASES])
+def test_head_dim_256(case):
+    """head_dim 256 on both halves (one CTA per SM, O over 256 TMEM columns,
+    PV at N = 256): GQA groups 2, 8 and MHA, page boxes, runs of single-token
+    pages and the cp.async gather (page size 3), windows, sinks, and decode
+    splits merged by the second kernel."""
+    name, dt, H, Hk, ps, causal, window, sinks, pq, pkv, dq, dkv, pages, nsm = case
+    inp = make_custom(name, dt, H, Hk, 256, ps, causal, window, pq, pkv, dq, dkv, seed=61,
+                      sinks=sinks, pages=pages, extra_pages=3)
+    (op, lp, od, ld), h, ws = run_pod(inp, num_sms=nsm)
+    if name == "split":
+        assert pod.plan_summary(h)["n_groups"] > 0, "expected decode splits"
+    compare_half(inp, "p", op, lp, tag=name + " ")
+    compare_half(inp, "d", od, ld, tag=name + " ")

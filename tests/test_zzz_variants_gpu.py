@@ -37,6 +37,10 @@ HND_CASES = [
      ("HND", "HND"), True),
     ("f8h4", torch.bfloat16, 16, 2, 128, 4, True, -1, False, [], [], [1, 4], [200, 51],
      ("NHD", "HND"), True),
+    ("h256", torch.bfloat16, 16, 2, 256, 16, True, -1, True, [100, 37], [300, 37], [1, 4],
+     [500, 900], ("HND", "HND"), False),
+    ("h256g", torch.float16, 8, 4, 256, 3, True, 60, False, [40], [90], [1, 2], [77, 130],
+     ("HND", "HND"), False),
 ]
 
 
