@@ -299,7 +299,10 @@ def with_decode_subset(inp: PODInputs, n: int) -> PODInputs:
     d.last_page_len = np.ascontiguousarray(inp.d.last_page_len[:n])
     d.kv_indices = np.searchsorted(keep, used).astype(np.int32)
     d.num_pages = max(int(len(keep)), 1)
-    d.kv = inp.d.kv[torch.from_numpy(keep)] if len(keep) else inp.d.kv[:1].clone()
+    # gathered as bytes: CPU indexing has no float8 kernels
+    raw = inp.d.kv.view(torch.uint8)
+    raw = raw[torch.from_numpy(keep)] if len(keep) else raw[:1].clone()
+    d.kv = raw.view(inp.d.kv.dtype)
     d.q = inp.d.q[: int(inp.d.q_indptr[n])].clone()
     d.q_lens = np.ascontiguousarray(inp.d.q_lens[:n])
     d.kv_lens = np.ascontiguousarray(inp.d.kv_lens[:n])

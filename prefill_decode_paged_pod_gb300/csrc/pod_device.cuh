@@ -400,4 +400,45 @@ POD_DEV void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
   }
 }
 
+// D += A.B on e4m3 codes, fp32 accumulate: A 16x32 (row), B 32x8 (col);
+// a register holds four consecutive k of one row (A) or column (B), the
+// lowest byte first.
+POD_DEV void mma16832_e4m3(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// two floats to two E4M3 codes (round to nearest even, saturating to +-448);
+// lo lands in the low byte
+POD_DEV uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+// a packed fp16 pair to two E4M3 codes, the low half to the low byte
+POD_DEV uint32_t f16x2_to_e4m3x2(uint32_t h2) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(d) : "r"(h2));
+  return d;
+}
+POD_DEV uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Four non-negative floats below 448 as two E4M3 words whose sum is the
+// values to about 8 significant bits: hi = the values rounded to E4M3, lo =
+// the remainders (taken in fp16) rounded to E4M3. Byte i holds value i.
+POD_DEV void e4m3_hi_lo4(float x0, float x1, float x2, float x3, uint32_t& hi, uint32_t& lo) {
+  const uint32_t h01 = f32x2_to_e4m3x2(x0, x1), h23 = f32x2_to_e4m3x2(x2, x3);
+  const uint32_t r01 = hsub2_u32(Pack<__half>::two(x0, x1), e4m3x2_to<__half>((uint16_t)h01));
+  const uint32_t r23 = hsub2_u32(Pack<__half>::two(x2, x3), e4m3x2_to<__half>((uint16_t)h23));
+  hi = h01 | (h23 << 16);
+  lo = f16x2_to_e4m3x2(r01) | (f16x2_to_e4m3x2(r23) << 16);
+}
+
 }  // namespace pod

@@ -101,12 +101,21 @@ struct DLayout {                                   // decode shared memory
   static constexpr int QLO_OFF = NKB * QDH;
   static constexpr int STAGE_OFF = NQ * NKB * QDH;
   static constexpr int BAR_OFF = STAGE_OFF + NSTAGE * STAGE_BYTES;
-  static constexpr int TOTAL = BAR_OFF + 128;
-  // FP8 (E4M3) cache, head_dim 128 only: the ring holds one-byte codes,
-  // [key][128 B] per K or V (16 KB a stage), widened in registers as the
-  // mma fragments are built
-  static constexpr int F8_HALF = POD_DECODE_STAGE * 128;   // K or V of a stage
+  // FP8 (E4M3) cache, head_dim 128 only: stages of 128 keys, [key][128 B]
+  // codes per K or V (32 KB a stage, as a 16-bit stage), fed to e4m3 MMAs as
+  // they are. Each item's Q is rewritten as up to three e4m3 parts of 32 rows
+  // x 128 B: parts 0 and 1 over the 16-bit Q, part 2 after the barriers, then
+  // one fp32 row scale per row.
+  static constexpr bool F8OK = D == 128 && !RP;
+  static constexpr int F8_KEYS = 2 * POD_DECODE_STAGE;
+  static constexpr int F8_HALF = F8_KEYS * 128;            // K or V of a stage
   static constexpr int F8_STAGE = 2 * F8_HALF;
+  static constexpr int Q8_PART = POD_DECODE_ROWS * 128;
+  static constexpr int Q8X_OFF = BAR_OFF + 128;
+  static constexpr int QSC_OFF = Q8X_OFF + Q8_PART;
+  static constexpr int TOTAL = F8OK ? QSC_OFF + POD_DECODE_ROWS * 16 : BAR_OFF + 128;
+  static_assert(!F8OK || (F8_STAGE <= STAGE_BYTES && 2 * Q8_PART <= NKB * QDH),
+                "FP8 stages and Q parts must fit the 16-bit ones");
   // combine scratch (reuses the stages): 8 warps x 16 rows x D floats, then m/l
   static constexpr int SCR_O = STAGE_OFF;
   static constexpr int SCR_ML = STAGE_OFF + 8 * 16 * D * 4;
@@ -690,11 +699,153 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
 // ============================================================ decode role
 // Runs decode items from the shared queue until it is empty. Returns false
 // when a wait ran out (the status word then says so).
+// One FP8 decode stage of one warp: 16 rows (m-tile mt) x KSL = 32 keys
+// (slice ks of a 128-key stage), both products on e4m3 tensor cores.
+// K and V stay the cache's codes. Q enters as NP e4m3 parts of the row scaled
+// by 2^e (qp0 + p * qpart for parts 0-1, qp2 for part 2) and every logit sums
+// the parts' products, fp32 accumulate; sc0/sc1 fold 2^-e into the softmax
+// scale of rows g and g + 8. P is carried as 256 P (largest 256 <= 448) and
+// split into an E4M3 high part and an E4M3 remainder, both multiplied into O.
+// Key order inside an MMA: the accumulator gives a thread keys 8n + 2t +
+// {0, 1} (n-tile n); its A words use slots 4t..4t+3 for keys {2t, 2t+1, 8+2t,
+// 9+2t} and slots 16+4t.. for {16+2t, 17+2t, 24+2t, 25+2t}, and the V words
+// are byte-permuted from ldmatrix.trans tiles into the same order.
+template <bool BF16, int D, int KSL>
+__device__ __forceinline__ void decode_stage_f8(uint32_t sk, int vhalf, uint32_t qp0, int qpart,
+                                                uint32_t qp2, int mt, int ks, int lane, int kbase,
+                                                int kv_len, uint32_t rowinfo,
+                                                float (&m)[2], float (&l)[2], float (&o)[D / 8][4]) {
+  int row_lo[2], row_hi[2];
+  float sc[2];
+#pragma unroll
+  for (int h2 = 0; h2 < 2; ++h2) {
+    const uint32_t a = rowinfo + (uint32_t)(mt * 16 + (lane >> 2) + 8 * h2) * 16u;
+    asm volatile("ld.shared.v2.s32 {%0, %1}, [%2];" : "=r"(row_lo[h2]), "=r"(row_hi[h2]) : "r"(a));
+    asm volatile("ld.shared.f32 %0, [%1 + 8];" : "=f"(sc[h2]) : "r"(a));
+  }
+  static_assert(KSL == 32 && D == 128, "FP8 stages are 32 keys per warp at head_dim 128");
+  constexpr int NP = BF16 ? 2 : 3;
+  const float NEG_INF = -INFINITY;
+  float s[4][4];
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+  // ---- S = Q K^T: per 32-d step, two ldmatrix.x4 give the B words of the 4
+  // n-tiles (keys 16 np + 8 (lane/16) + lane%8, 16-byte chunk 2j + (lane/8)%2)
+#pragma unroll
+  for (int j = 0; j < D / 32; ++j) {
+    uint32_t kf[2][4];
+#pragma unroll
+    for (int np = 0; np < 2; ++np) {
+      const int key = ks * KSL + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+      const int ch = 2 * j + ((lane >> 3) & 1);
+      ldsm_x4(sk + key * 128 + ((ch ^ (key & 7)) << 4), kf[np][0], kf[np][1], kf[np][2], kf[np][3]);
+    }
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      const int rr = mt * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+      const int ch = 2 * j + (lane >> 4);
+      const uint32_t qb = p < 2 ? qp0 + p * qpart : qp2;
+      uint32_t a[4];
+      ldsm_x4(qb + rr * 128 + ((ch ^ (rr & 7)) << 4), a[0], a[1], a[2], a[3]);
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+        mma16832_e4m3(s[nt], a, kf[nt >> 1][2 * (nt & 1)], kf[nt >> 1][2 * (nt & 1) + 1]);
+    }
+  }
+  // ---- mask (only where some key of the slice is outside a row's range),
+  // online softmax in base 2
+  const int kq = kbase + 2 * (lane & 3);
+  const bool inner = __all_sync(0xffffffffu, kbase >= row_lo[0] && kbase >= row_lo[1] &&
+                                                 kbase + KSL <= row_hi[0] && kbase + KSL <= row_hi[1]);
+  float alpha[2];
+#pragma unroll
+  for (int h2 = 0; h2 < 2; ++h2) {
+    float mm = NEG_INF;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float x = s[nt][2 * h2 + e];
+        if (!inner) {
+          const int key = kq + 8 * nt + e;
+          if (key < row_lo[h2] || key >= row_hi[h2]) x = NEG_INF;
+          s[nt][2 * h2 + e] = x;
+        }
+        mm = fmaxf(mm, x);
+      }
+    mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, 1));
+    mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, 2));
+    const float m_new = fmaxf(m[h2], mm * sc[h2]);
+    const float m_sub = (m_new == NEG_INF) ? 0.f : m_new;
+    alpha[h2] = ex2(m[h2] - m_sub);
+    m[h2] = m_new;
+    const float off = 8.f - m_sub;  // 256 P
+    float sum = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float pv = ex2(fmaf(s[nt][2 * h2 + e], sc[h2], off));
+        s[nt][2 * h2 + e] = pv;
+        sum += pv;
+      }
+    l[h2] = l[h2] * alpha[h2] + sum;
+  }
+  // a running max that did not move leaves alpha = 1 on every row of the warp
+  if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      o[i][0] *= alpha[0];
+      o[i][1] *= alpha[0];
+      o[i][2] *= alpha[1];
+      o[i][3] *= alpha[1];
+    }
+  }
+  // ---- A words of 256 P: rows g (words 0, 2) and g + 8 (1, 3)
+  uint32_t ph[4], pl[4];
+  e4m3_hi_lo4(s[0][0], s[0][1], s[1][0], s[1][1], ph[0], pl[0]);
+  e4m3_hi_lo4(s[0][2], s[0][3], s[1][2], s[1][3], ph[1], pl[1]);
+  e4m3_hi_lo4(s[2][0], s[2][1], s[3][0], s[3][1], ph[2], pl[2]);
+  e4m3_hi_lo4(s[2][2], s[2][3], s[3][2], s[3][3], ph[3], pl[3]);
+  // ---- O += P V over the 8 16-byte d chunks. ldmatrix.trans of keys 8i..8i+7
+  // (i = lane/8) gives a thread bytes (key 8i+2t, 8i+2t+1) x (d 2g, 2g+1);
+  // the even-d and odd-d bytes make two n8 tiles: o[2c] holds d 16c + 4t +
+  // {0, 2}, o[2c+1] d 16c + 4t + {1, 3}. Keys at or past kv_len may be unused
+  // slots of the last page: their V bytes are zeroed so that P = 0 never
+  // meets a NaN code.
+  auto pv = [&](uint32_t vm0, uint32_t vm1) {
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+      const int key = ks * KSL + lane;
+      uint32_t r0, r1, r2, r3;
+      ldsm_x4_t(sk + vhalf + key * 128 + ((c ^ (key & 7)) << 4), r0, r1, r2, r3);
+      const uint32_t be0 = __byte_perm(r0, r1, 0x6420) & vm0, be1 = __byte_perm(r2, r3, 0x6420) & vm1;
+      const uint32_t bo0 = __byte_perm(r0, r1, 0x7531) & vm0, bo1 = __byte_perm(r2, r3, 0x7531) & vm1;
+      mma16832_e4m3(o[2 * c], ph, be0, be1);
+      mma16832_e4m3(o[2 * c], pl, be0, be1);
+      mma16832_e4m3(o[2 * c + 1], ph, bo0, bo1);
+      mma16832_e4m3(o[2 * c + 1], pl, bo0, bo1);
+    }
+  };
+  if (kbase + KSL > kv_len) {
+    auto bm = [&](int k) -> uint32_t { return k < kv_len ? 0xffu : 0u; };
+    pv(bm(kq) | (bm(kq + 1) << 8) | (bm(kq + 8) << 16) | (bm(kq + 9) << 24),
+       bm(kq + 16) | (bm(kq + 17) << 8) | (bm(kq + 24) << 16) | (bm(kq + 25) << 24));
+  } else {
+    pv(0xffffffffu, 0xffffffffu);
+  }
+}
+
 template <typename T, int D, bool F8, int LT, bool RP>
 __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
   using L = DLayout<D, RP>;
   constexpr bool BF16 = Pack<T>::kBF16;
   constexpr int NKB = L::NKB;
+  static_assert(!F8 || (L::F8OK && LT == POD_LT_NONE),
+                "FP8 decode caches are built for head_dim 128 without a logits transform");
+  // keys per stage and per warp (each m-tile's 4 warps split a stage's keys)
+  constexpr int KST = F8 ? L::F8_KEYS : POD_DECODE_STAGE;
+  constexpr int KSL = KST / 4;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int mt = warp >> 2, ks = warp & 3;
   const uint32_t sbase = smem_u32(smem);
@@ -750,14 +901,18 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
     const int q_len = rec[10];
     const int page_base = rec[11];
     const int npages = rec[12];
-    const int kb0 = (k0 / POD_DECODE_STAGE) * POD_DECODE_STAGE;
-    const int nst = (k1 - kb0 + POD_DECODE_STAGE - 1) / POD_DECODE_STAGE;
+    const int kb0 = (k0 / KST) * KST;
+    const int nst = (k1 - kb0 + KST - 1) / KST;
 
-    // TMA path: page of box `lane` of stage st (lane < 64 / d_tma <= 8); an id
-    // past the request's last page is the out-of-range page TMA fills with zeros
+    // TMA path: page of box `lane` of stage st (lane < KST / d_tma <= 16). A
+    // box past the request's last page (with an FP8 cache also one wholly
+    // outside [k0, k1): its 128-key stages overhang 64-key chunk bounds) takes
+    // the out-of-range page id, which TMA fills with zeros without reading HBM.
     auto page_for = [&](int st) -> int {
-      const int pidx = (kb0 + st * POD_DECODE_STAGE + lane * P.d_tma) >> P.ps_shift;
-      return pidx < npages ? __ldg(P.d_kv_indices + page_base + pidx) : P.d_num_pages;
+      const int t = kb0 + st * KST + lane * P.d_tma;
+      const int pidx = t >> P.ps_shift;
+      return (pidx < npages && (!F8 || (t < k1 && t + P.d_tma > k0)))
+                 ? __ldg(P.d_kv_indices + page_base + pidx) : P.d_num_pages;
     };
     // fill stage st of this item (Q travels with stage 0) into ring slot
     // (fills + st) % 3; TMA path: `page` = page_for(st) of this lane, or -1
@@ -768,7 +923,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
       const uint32_t full = bar0 + 8 * buf;
       const uint32_t sk = sbase + L::STAGE_OFF + buf * L::STAGE_BYTES;
       const uint32_t sv = sk + L::KBYTES;
-      const int kb = kb0 + st * POD_DECODE_STAGE;
+      const int kb = kb0 + st * KST;
       if (P.d_tma) {
         // warp 0: lane 0 registers the bytes, lane i fetches box group i
         if (warp == 0) {
@@ -785,7 +940,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
               }
           }
           __syncwarp();
-          if (F8 && lane < POD_DECODE_STAGE / P.d_tma) {
+          if (F8 && lane < KST / P.d_tma) {
             // one-byte codes: a key's head row is one 128-byte row
             if (page < 0) page = page_for(st);
             const int o = lane * P.d_tma;
@@ -834,26 +989,20 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
           const uint8_t* __restrict__ kv8 = reinterpret_cast<const uint8_t*>(P.kv_d);
           const uint32_t k8 = sbase + L::STAGE_OFF + buf * L::F8_STAGE;
           const size_t vstride8 = (size_t)P.ps * P.Hk * D;
-          constexpr int PER8 = POD_DECODE_STAGE * 8 / kThreads;
-          int pages8[PER8];
-#pragma unroll
-          for (int i = 0; i < PER8; ++i) {
-            const int t = kb + ((tid + kThreads * i) >> 3);
-            const int tt = (t >= k0 && t < k1) ? t : k0;
-            pages8[i] = __ldg(P.d_kv_indices + page_base +
-                              (P.ps_shift >= 0 ? (tt >> P.ps_shift) : (tt / P.ps)));
-          }
-#pragma unroll
+          constexpr int PER8 = KST * 8 / kThreads;
+#pragma unroll 1
           for (int i = 0; i < PER8; ++i) {
             const int idx = tid + kThreads * i;
             const int key = idx >> 3, c = idx & 7;
             const int t = kb + key;
             const bool valid = t >= k0 && t < k1;
             const int tt = valid ? t : k0;
+            const int pg = __ldg(P.d_kv_indices + page_base +
+                                 (P.ps_shift >= 0 ? (tt >> P.ps_shift) : (tt / P.ps)));
             const int slot = P.ps_shift >= 0 ? (tt & (P.ps - 1)) : (tt % P.ps);
             const uint8_t* src = kv8 + (P.d_hnd
-                ? (((size_t)pages8[i] * 2 * P.Hk + g) * P.ps + slot) * D + c * 16
-                : (((size_t)pages8[i] * 2 * P.ps + slot) * P.Hk + g) * D + c * 16);
+                ? (((size_t)pg * 2 * P.Hk + g) * P.ps + slot) * D + c * 16
+                : (((size_t)pg * 2 * P.ps + slot) * P.Hk + g) * D + c * 16);
             const uint32_t off = (uint32_t)key * 128u + (uint32_t)((c ^ (key & 7)) << 4);
             cp_async16(k8 + off, src, valid ? 16u : 0u);
             cp_async16(k8 + L::F8_HALF + off, src + vstride8, valid ? 16u : 0u);
@@ -912,12 +1061,95 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
         a_pd[h2] = pd;
       }
     }
+    if (F8 && nst > 0) {
+      // wait for stage 0 here (the stage loop's own wait then passes at once),
+      // before the accumulators are live
+      const bool got = __all_sync(
+          0xffffffffu,
+          mbar_wait(bar0 + 8 * (fills % L::NSTAGE), (fills / L::NSTAGE) & 1, abort_flag));
+      // Q landed with stage 0: rewrite it as NP e4m3 parts. Row r is first
+      // scaled by 2^e (e puts its largest |q| in [128, 256)); part p holds
+      // the E4M3 rounding of what parts 0..p-1 left, so the parts sum to
+      // the scaled row: exactly for bf16 (8 bits in two parts of 4) and to
+      // 12 bits for fp16 (three parts), down to 2^-9 of the scaled units.
+      constexpr int NP = BF16 ? 2 : 3;
+      const int row = tid >> 3, seg = tid & 7;   // 16 elements: d 16 seg ..
+      float x[16];
+      float mxq = 0.f;
+      {
+        const int dh = seg >> 2, c0 = 2 * (seg & 3);
+        const uint32_t ra = sbase + L::Q_OFF + dh * L::QDH + row * 128;
+        uint32_t w[8];
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(ra + ((c0 ^ (row & 7)) << 4)));
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                     : "r"(ra + (((c0 + 1) ^ (row & 7)) << 4)));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float2 v = Pack<T>::unpack(w[i]);
+          x[2 * i] = v.x;
+          x[2 * i + 1] = v.y;
+          mxq = fmaxf(mxq, fmaxf(fabsf(v.x), fabsf(v.y)));
+        }
+      }
+      mxq = fmaxf(mxq, __shfl_xor_sync(0xffffffffu, mxq, 1));
+      mxq = fmaxf(mxq, __shfl_xor_sync(0xffffffffu, mxq, 2));
+      mxq = fmaxf(mxq, __shfl_xor_sync(0xffffffffu, mxq, 4));
+      const int eb = (int)((__float_as_uint(mxq) >> 23) & 0xffu);  // biased exponent
+      const int e = mxq > 0.f ? min(max(134 - eb, -120), 120) : 0;  // 7 - floor(log2)
+      const float up = __uint_as_float((uint32_t)(127 + e) << 23);
+      uint32_t part[NP][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float v[4] = {x[4 * i] * up, x[4 * i + 1] * up, x[4 * i + 2] * up, x[4 * i + 3] * up};
+#pragma unroll
+        for (int pp = 0; pp < NP; ++pp) {
+          const uint32_t h01 = f32x2_to_e4m3x2(v[0], v[1]), h23 = f32x2_to_e4m3x2(v[2], v[3]);
+          part[pp][i] = h01 | (h23 << 16);
+          if (pp + 1 < NP) {
+            const uint32_t f01 = e4m3x2_to<__half>((uint16_t)h01);
+            const uint32_t f23 = e4m3x2_to<__half>((uint16_t)h23);
+            const float2 g01 = __half22float2(*reinterpret_cast<const __half2*>(&f01));
+            const float2 g23 = __half22float2(*reinterpret_cast<const __half2*>(&f23));
+            v[0] -= g01.x;
+            v[1] -= g01.y;
+            v[2] -= g23.x;
+            v[3] -= g23.y;
+          }
+        }
+      }
+      __syncthreads();  // every 16-bit Q element is read before parts 0-1 overwrite them
+      if (got) {
+#pragma unroll
+        for (int pp = 0; pp < NP; ++pp) {
+          const uint32_t dst = sbase + (pp < 2 ? L::Q_OFF + pp * L::Q8_PART : L::Q8X_OFF) +
+                               row * 128 + ((seg ^ (row & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(part[pp][0]),
+                       "r"(part[pp][1]), "r"(part[pp][2]), "r"(part[pp][3]) : "memory");
+        }
+        if (seg == 0) {
+          // row info for the stages: key range [lo, hi) and the softmax scale with 2^-e
+          const int tok = tok0 + (row < R ? row / G : 0);
+          const int pd = kv_len - q_len + tok;
+          int4 ri;
+          ri.x = max(P.window_left >= 0 ? max(pd - P.window_left, 0) : 0, k0);
+          ri.y = min(P.causal ? min(pd + 1, kv_len) : kv_len, k1);
+          ri.z = (int)__float_as_uint(P.d_scale_log2 * __uint_as_float((uint32_t)(127 - e) << 23));
+          ri.w = 0;
+          asm volatile("st.shared.v4.s32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + L::QSC_OFF + row * 16),
+                       "r"(ri.x), "r"(ri.y), "r"(ri.z), "r"(ri.w) : "memory");
+        }
+      }
+      __syncthreads();
+    }
     float m[2] = {NEG_INF, NEG_INF}, l[2] = {0.f, 0.f};
     float o[D / 8][4];
 #pragma unroll
     for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     const bool active = mt < Mt;
     const int mi = lane >> 3;
+
 
     for (int st = 0; st < nst; ++st) {
       const int f = fills + st;
@@ -926,45 +1158,22 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
       // that the load latency hides behind the compute
       const int next_page =
           (P.d_tma && warp == 0 && st + L::NSTAGE < nst) ? page_for(st + L::NSTAGE) : -1;
-      const bool got = mbar_wait(bar0 + 8 * buf, (f / L::NSTAGE) & 1, abort_flag);
-      // 16-bit cache: K of the stage (V follows at +KBYTES); FP8: its codes
-      const uint32_t sk = F8 ? sbase + L::STAGE_OFF + buf * L::F8_STAGE
-                                  : sbase + L::STAGE_OFF + buf * L::STAGE_BYTES;
-      const int kbase = kb0 + st * POD_DECODE_STAGE + ks * 16;
-      if (got && active && kbase < k1 && kbase + 16 > k0) {
+      // FP8: made warp-uniform, so that every lane reaches the warp votes of its stage
+      const bool got_l = mbar_wait(bar0 + 8 * buf, (f / L::NSTAGE) & 1, abort_flag);
+      const bool got = F8 ? __all_sync(0xffffffffu, got_l) : got_l;
+      const int kbase = kb0 + st * KST + ks * KSL;
+      if (got && active && kbase < k1 && kbase + KSL > k0) {
+       if constexpr (F8) {
+        decode_stage_f8<BF16, D, KSL>(sbase + L::STAGE_OFF + buf * L::F8_STAGE, L::F8_HALF,
+                                      sbase + L::Q_OFF, L::Q8_PART, sbase + L::Q8X_OFF, mt, ks,
+                                      lane, kbase, kv_len, sbase + L::QSC_OFF, m, l, o);
+       } else {
+        // 16-bit cache: K of the stage, V at +KBYTES
+        const uint32_t sk = sbase + L::STAGE_OFF + buf * L::STAGE_BYTES;
         const uint32_t sq = sbase + L::Q_OFF;
-        const uint32_t sv = sk + (F8 ? (uint32_t)L::F8_HALF : (uint32_t)L::KBYTES);
+        const uint32_t sv = sk + (uint32_t)L::KBYTES;
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-        // FP8 rows are [key][128 one-byte codes]; ldmatrix reads them as 8x8
-        // tiles of byte pairs. Lane addresses: matrix i = lane/8 holds keys
-        // 8(i&1) + lane%8 of the warp's slice and 16-byte chunk 2j + i/2.
-        const int f8key = ks * 16 + (lane & 7) + ((mi & 1) << 3);
-        if constexpr (F8) {
-          // A thread's K bytes are d 4t..4t+3 of a 16-d chunk (t = lane%4); the
-          // k16 step sums over d, so Q is read with the same order: a0/a1 =
-          // d 4t, 4t+1 and a2/a3 = d 4t+2, 4t+3 (rows g and g+8, g = lane/4).
-          const int rq = mt * 16 + (lane >> 2);
-#pragma unroll
-          for (int j = 0; j < D / 32; ++j) {
-            uint32_t r[4];
-            ldsm_x4(sk + f8key * 128 + ((((2 * j + (mi >> 1)) ^ (f8key & 7))) << 4), r[0], r[1],
-                    r[2], r[3]);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int d0 = 32 * j + 16 * h + 4 * (lane & 3);
-              const int e = d0 & 63, ch = e >> 3;
-              const uint32_t qa = sq + (d0 >> 6) * L::QDH + ((e & 7) << 1);
-              const uint2 q0 = ld_shared_v2(qa + rq * 128 + ((ch ^ (rq & 7)) << 4));
-              const uint2 q1 = ld_shared_v2(qa + (rq + 8) * 128 + ((ch ^ ((rq + 8) & 7)) << 4));
-              uint32_t a[4] = {q0.x, q1.x, q0.y, q1.y};
-              const uint32_t k0 = r[2 * h], k1 = r[2 * h + 1];   // keys 0-7 / 8-15 of the slice
-              mma16816<BF16>(s0, a, e4m3x2_to<T>((uint16_t)(k0 & 0xffffu)),
-                             e4m3x2_to<T>((uint16_t)(k0 >> 16)));
-              mma16816<BF16>(s1, a, e4m3x2_to<T>((uint16_t)(k1 & 0xffffu)),
-                             e4m3x2_to<T>((uint16_t)(k1 >> 16)));
-            }
-          }
-        } else if constexpr (RP) {
+        if constexpr (RP) {
           // Keys rotated in registers: chunk kk (d 16kk..) pairs with chunk
           // kk + D/32 (d + D/2). A thread holds, for its keys ka (b[0], b[1])
           // and ka + 8 (b[2], b[3]), elements j = 16kk + 2(lane%4) + {0, 1}
@@ -1079,20 +1288,12 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
             o[i][2 * h2 + 1] *= alpha;
           }
         }
-        // P <= 1: with an FP8 cache the PV product runs in fp16 (V widens to
-        // fp16 in one conversion), otherwise in the plan's 16-bit type
+        // P <= 1 rounded to the plan's 16-bit type for the PV product
         uint32_t pa[4];
-        if constexpr (F8) {
-          pa[0] = Pack<__half>::two(s0[0], s0[1]);
-          pa[1] = Pack<__half>::two(s0[2], s0[3]);
-          pa[2] = Pack<__half>::two(s1[0], s1[1]);
-          pa[3] = Pack<__half>::two(s1[2], s1[3]);
-        } else {
-          pa[0] = Pack<T>::two(s0[0], s0[1]);
-          pa[1] = Pack<T>::two(s0[2], s0[3]);
-          pa[2] = Pack<T>::two(s1[0], s1[1]);
-          pa[3] = Pack<T>::two(s1[2], s1[3]);
-        }
+        pa[0] = Pack<T>::two(s0[0], s0[1]);
+        pa[1] = Pack<T>::two(s0[2], s0[3]);
+        pa[2] = Pack<T>::two(s1[0], s1[1]);
+        pa[3] = Pack<T>::two(s1[2], s1[3]);
         // V rows at or past kv_len may be unused slots of the last page: zero
         // them in the fragments so that P = 0 never meets a non-finite value
         uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
@@ -1100,40 +1301,17 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
           vm0 = (kq < kv_len ? 0x0000ffffu : 0u) | (kq + 1 < kv_len ? 0xffff0000u : 0u);
           vm1 = (kq + 8 < kv_len ? 0x0000ffffu : 0u) | (kq + 9 < kv_len ? 0xffff0000u : 0u);
         }
-        if constexpr (F8) {
-          // transposed byte-pair tiles: a register holds V[2t][2g], V[2t][2g+1],
-          // V[2t+1][2g], V[2t+1][2g+1] (keys 2t, 2t+1; d pair g); the even-d
-          // and odd-d bytes make two n8 tiles: o[2q] holds d 16q + 4t + {0, 2},
-          // o[2q+1] d 16q + 4t + {1, 3} (columns 2t, 2t+1 of each tile)
 #pragma unroll
-          for (int j = 0; j < D / 32; ++j) {
-            uint32_t r[4];
-            ldsm_x4_t(sv + f8key * 128 + ((((2 * j + (mi >> 1)) ^ (f8key & 7))) << 4), r[0], r[1],
-                      r[2], r[3]);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint32_t lo = r[2 * h], hi = r[2 * h + 1];   // keys 2t.. / 2t+8..
-              const uint32_t be0 = e4m3x2_to<__half>((uint16_t)((lo & 0xffu) | ((lo >> 8) & 0xff00u)));
-              const uint32_t bo0 = e4m3x2_to<__half>((uint16_t)(((lo >> 8) & 0xffu) | ((lo >> 16) & 0xff00u)));
-              const uint32_t be1 = e4m3x2_to<__half>((uint16_t)((hi & 0xffu) | ((hi >> 8) & 0xff00u)));
-              const uint32_t bo1 = e4m3x2_to<__half>((uint16_t)(((hi >> 8) & 0xffu) | ((hi >> 16) & 0xff00u)));
-              const int q = 2 * j + h;
-              mma16816<false>(o[2 * q], pa, be0 & vm0, be1 & vm1);
-              mma16816<false>(o[2 * q + 1], pa, bo0 & vm0, bo1 & vm1);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < D / 16; ++j) {
-            uint32_t b[4];
-            const int key = ks * 16 + (lane & 7) + ((mi & 1) << 3);
-            const int c = 2 * j + (mi >> 1);
-            ldsm_x4_t(sv + key_row(key) + (c >> 3) * half_stride + (((c & 7) ^ (lane & 7)) << 4), b[0],
-                      b[1], b[2], b[3]);
-            mma16816<BF16>(o[2 * j], pa, b[0] & vm0, b[1] & vm1);
-            mma16816<BF16>(o[2 * j + 1], pa, b[2] & vm0, b[3] & vm1);
-          }
+        for (int j = 0; j < D / 16; ++j) {
+          uint32_t b[4];
+          const int key = ks * 16 + (lane & 7) + ((mi & 1) << 3);
+          const int c = 2 * j + (mi >> 1);
+          ldsm_x4_t(sv + key_row(key) + (c >> 3) * half_stride + (((c & 7) ^ (lane & 7)) << 4), b[0],
+                    b[1], b[2], b[3]);
+          mma16816<BF16>(o[2 * j], pa, b[0] & vm0, b[1] & vm1);
+          mma16816<BF16>(o[2 * j + 1], pa, b[2] & vm0, b[3] & vm1);
         }
+       }
       }
       if (!__syncthreads_and(got)) { ok = false; break; }
       if (st + L::NSTAGE < nst) issue(st + L::NSTAGE, next_page);
@@ -1205,10 +1383,13 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
       }
       const int tok = ctok0 + rr / G;
       const int head = cg * G + rr % G;
+      // FP8: the slices carried 256 P (sums and outputs)
+      constexpr float kPU = F8 ? 1.f / 256.f : 1.f;
+      wsum *= kPU;
       if (prow < 0) {
         float denom = wsum;
         if (P.has_sinks) denom += ex2(P.sinks[head] * 1.4426950408889634f - Ms);
-        const float inv = denom > 0.f ? P.v_scale / denom : 0.f;
+        const float inv = denom > 0.f ? P.v_scale * kPU / denom : 0.f;
         const size_t orow = (size_t)(cq_base + tok) * H + head;
         uint2 v;
         v.x = Pack<T>::two(acc.x * inv, acc.y * inv);
@@ -1216,7 +1397,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
         *reinterpret_cast<uint2*>(outg + orow * D + c4) = v;
         if (c4 == 0 && P.lse_d) P.lse_d[orow] = wsum > 0.f ? M + log2f(wsum) : NEG_INF;
       } else {
-        const float inv = wsum > 0.f ? P.v_scale / wsum : 0.f;
+        const float inv = wsum > 0.f ? P.v_scale * kPU / wsum : 0.f;
         *reinterpret_cast<float4*>(P.part_o + (size_t)(prow + rr) * D + c4) =
             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         if (c4 == 0) P.part_lse[prow + rr] = wsum > 0.f ? M + log2f(wsum) : NEG_INF;
