@@ -113,7 +113,8 @@ struct DLayout {                                   // decode shared memory
   static constexpr int Q8_PART = POD_DECODE_ROWS * 128;
   static constexpr int Q8X_OFF = BAR_OFF + 128;
   static constexpr int QSC_OFF = Q8X_OFF + Q8_PART;
-  static constexpr int TOTAL = F8OK ? QSC_OFF + POD_DECODE_ROWS * 16 : BAR_OFF + 128;
+  static constexpr int TOTAL = BAR_OFF + 128;                  // 16-bit cache
+  static constexpr int TOTAL_F8 = QSC_OFF + POD_DECODE_ROWS * 16;  // FP8 cache
   static_assert(!F8OK || (F8_STAGE <= STAGE_BYTES && 2 * Q8_PART <= NKB * QDH),
                 "FP8 stages and Q parts must fit the 16-bit ones");
   // combine scratch (reuses the stages): 8 warps x 16 rows x D floats, then m/l
@@ -124,10 +125,12 @@ struct DLayout {                                   // decode shared memory
   static_assert(NSTAGE * 8 <= 64, "stage barriers overlap the abort flag");
 };
 
-template <int D, bool RP>
+// Dynamic shared memory of an instantiation: the FP8 regions are requested
+// only by the FP8 kernels (a larger request leaves less of the SM's L1).
+template <int D, bool RP, bool F8 = false>
 constexpr int smem_bytes() {
-  return PLayout<D, RP>::TOTAL > DLayout<D, RP>::TOTAL ? PLayout<D, RP>::TOTAL
-                                                       : DLayout<D, RP>::TOTAL;
+  constexpr int DT = F8 ? DLayout<D, RP>::TOTAL_F8 : DLayout<D, RP>::TOTAL;
+  return PLayout<D, RP>::TOTAL > DT ? PLayout<D, RP>::TOTAL : DT;
 }
 
 POD_DEV void raise_status(int32_t* status, int code) { atomicOr(status, code); }
@@ -697,14 +700,17 @@ __device__ bool prefill_role(const PodParams& P, uint8_t* smem, uint32_t tmem) {
 }
 
 // ============================================================ decode role
-// Runs decode items from the shared queue until it is empty. Returns false
-// when a wait ran out (the status word then says so).
+// decode_role (16-bit caches) and decode_role_f8 (FP8 caches) run decode
+// items from the shared queue until it is empty. They return false when a
+// wait ran out (the status word then says so).
+//
 // One FP8 decode stage of one warp: 16 rows (m-tile mt) x KSL = 32 keys
 // (slice ks of a 128-key stage), both products on e4m3 tensor cores.
 // K and V stay the cache's codes. Q enters as NP e4m3 parts of the row scaled
 // by 2^e (qp0 + p * qpart for parts 0-1, qp2 for part 2) and every logit sums
-// the parts' products, fp32 accumulate; sc0/sc1 fold 2^-e into the softmax
-// scale of rows g and g + 8. P is carried as 256 P (largest 256 <= 448) and
+// the parts' products, fp32 accumulate. The row info at `rowinfo` (16 bytes
+// a row: key range [lo, hi), then the softmax scale with 2^-e folded in)
+// masks and scales rows g and g + 8. P is carried as 256 P (largest 256 <= 448) and
 // split into an E4M3 high part and an E4M3 remainder, both multiplied into O.
 // Key order inside an MMA: the accumulator gives a thread keys 8n + 2t +
 // {0, 1} (n-tile n); its A words use slots 4t..4t+3 for keys {2t, 2t+1, 8+2t,
@@ -836,15 +842,18 @@ __device__ __forceinline__ void decode_stage_f8(uint32_t sk, int vhalf, uint32_t
   }
 }
 
+// The decode role over an FP8 (E4M3) cache: the 16-bit role's item queue,
+// stage ring and combine, with 128-key stages of one-byte codes, the item's
+// Q rewritten as e4m3 parts and decode_stage_f8 for the products.
 template <typename T, int D, bool F8, int LT, bool RP>
-__device__ bool decode_role(const PodParams& P, uint8_t* smem) {
+__device__ bool decode_role_f8(const PodParams& P, uint8_t* smem) {
   using L = DLayout<D, RP>;
   constexpr bool BF16 = Pack<T>::kBF16;
   constexpr int NKB = L::NKB;
-  static_assert(!F8 || (L::F8OK && LT == POD_LT_NONE),
+  static_assert(F8 && L::F8OK && LT == POD_LT_NONE,
                 "FP8 decode caches are built for head_dim 128 without a logits transform");
   // keys per stage and per warp (each m-tile's 4 warps split a stage's keys)
-  constexpr int KST = F8 ? L::F8_KEYS : POD_DECODE_STAGE;
+  constexpr int KST = L::F8_KEYS;
   constexpr int KSL = KST / 4;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int mt = warp >> 2, ks = warp & 3;
@@ -867,15 +876,6 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
     tma_prefetch_desc(&P.tm_q_d);
   }
   const uint32_t q_bytes = (uint32_t)(L::NQ * NKB * 128 * G * P.tu);
-  // K/V stage layout: [key / kbx][d half][key % kbx][64 elements] in 128-byte
-  // swizzled rows, kbx = keys per TMA box (64 on the cp.async path, where it
-  // is [d half][key][64]). Row offset of key k in its d half 0:
-  const int kshift = (P.d_tma && !F8) ? 31 - __clz(P.d_tma) : 6;
-  const uint32_t half_stride = 128u << kshift;  // bytes between the d halves of a box
-  auto key_row = [&](int k) -> uint32_t {
-    return (uint32_t)((k >> kshift) << kshift) * (NKB * 128u) +
-           (uint32_t)(k & ((1 << kshift) - 1)) * 128u;
-  };
   int fills = 0;
   bool ok = true;
 
@@ -905,13 +905,13 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
     const int nst = (k1 - kb0 + KST - 1) / KST;
 
     // TMA path: page of box `lane` of stage st (lane < KST / d_tma <= 16). A
-    // box past the request's last page (with an FP8 cache also one wholly
-    // outside [k0, k1): its 128-key stages overhang 64-key chunk bounds) takes
-    // the out-of-range page id, which TMA fills with zeros without reading HBM.
+    // box past the request's last page, or wholly outside [k0, k1) (the
+    // 128-key stages overhang the 64-key chunk bounds), takes the
+    // out-of-range page id, which TMA fills with zeros without reading HBM.
     auto page_for = [&](int st) -> int {
       const int t = kb0 + st * KST + lane * P.d_tma;
       const int pidx = t >> P.ps_shift;
-      return (pidx < npages && (!F8 || (t < k1 && t + P.d_tma > k0)))
+      return (pidx < npages && t < k1 && t + P.d_tma > k0)
                  ? __ldg(P.d_kv_indices + page_base + pidx) : P.d_num_pages;
     };
     // fill stage st of this item (Q travels with stage 0) into ring slot
@@ -921,26 +921,19 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
       const int f = fills + st;
       const int buf = f % L::NSTAGE;
       const uint32_t full = bar0 + 8 * buf;
-      const uint32_t sk = sbase + L::STAGE_OFF + buf * L::STAGE_BYTES;
-      const uint32_t sv = sk + L::KBYTES;
       const int kb = kb0 + st * KST;
       if (P.d_tma) {
         // warp 0: lane 0 registers the bytes, lane i fetches box group i
         if (warp == 0) {
           if (lane == 0) {
-            mbar_arrive_expect_tx(full, (F8 ? (uint32_t)L::F8_STAGE : 2u * L::KBYTES) +
-                                            (st == 0 ? q_bytes : 0u));
+            mbar_arrive_expect_tx(full, (uint32_t)L::F8_STAGE + (st == 0 ? q_bytes : 0u));
             if (st == 0)
-              for (int dh = 0; dh < NKB; ++dh) {
+              for (int dh = 0; dh < NKB; ++dh)
                 tma_load_3d(sbase + L::Q_OFF + dh * L::QDH, &P.tm_q_d, dh * 64, g * G, q_base + tok0,
                             full);
-                if (RP)
-                  tma_load_3d(sbase + L::QLO_OFF + dh * L::QDH, &P.tm_qlo_d, dh * 64, g * G,
-                              q_base + tok0, full);
-              }
           }
           __syncwarp();
-          if (F8 && lane < KST / P.d_tma) {
+          if (lane < KST / P.d_tma) {
             // one-byte codes: a key's head row is one 128-byte row
             if (page < 0) page = page_for(st);
             const int o = lane * P.d_tma;
@@ -953,23 +946,10 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
               tma_load_4d(k8, &P.tm_kv_d, 0, page, g, 0, full);
               tma_load_4d(k8 + L::F8_HALF, &P.tm_kv_d, 0, page, g, 1, full);
             }
-          } else if (lane < POD_DECODE_STAGE / P.d_tma) {
-            if (page < 0) page = page_for(st);
-            const int o = lane * P.d_tma;
-            const uint32_t dst = (uint32_t)o * (NKB * 128u);
-            if (P.ps >= 8) {  // coordinates (x, slot, half, head, 2 * page + kv)
-              const int tin = (kb + o) & (P.ps - 1);
-              tma_load_5d(sk + dst, &P.tm_kv_d, 0, tin, 0, g, 2 * page, full);
-              tma_load_5d(sv + dst, &P.tm_kv_d, 0, tin, 0, g, 2 * page + 1, full);
-            } else {          // page_size 1: (x, page, half, head, kv)
-              tma_load_5d(sk + dst, &P.tm_kv_d, 0, page, 0, g, 0, full);
-              tma_load_5d(sv + dst, &P.tm_kv_d, 0, page, 0, g, 1, full);
-            }
           }
         }
       } else {
         const T* __restrict__ qg = reinterpret_cast<const T*>(P.q_d);
-        const T* __restrict__ kvg = reinterpret_cast<const T*>(P.kv_d);
         if (st == 0) {
           for (int idx = tid; idx < POD_DECODE_ROWS * (D / 8); idx += kThreads) {
             const int r = idx / (D / 8), c = idx % (D / 8);
@@ -979,64 +959,29 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
             const size_t qoff = ((size_t)(q_base + tok) * H + head) * D + c * 8;
             cp_async16(sbase + L::Q_OFF + (c >> 3) * L::QDH + sw128_off(r, c & 7), qg + qoff,
                        valid ? 16u : 0u);
-            if (RP)
-              cp_async16(sbase + L::QLO_OFF + (c >> 3) * L::QDH + sw128_off(r, c & 7),
-                         reinterpret_cast<const T*>(P.q_d_lo) + qoff, valid ? 16u : 0u);
           }
         }
-        if constexpr (F8) {
-          // one-byte codes, [key][128 B] per K or V: 8 chunks of 16 B a key
-          const uint8_t* __restrict__ kv8 = reinterpret_cast<const uint8_t*>(P.kv_d);
-          const uint32_t k8 = sbase + L::STAGE_OFF + buf * L::F8_STAGE;
-          const size_t vstride8 = (size_t)P.ps * P.Hk * D;
-          constexpr int PER8 = KST * 8 / kThreads;
+        // one-byte codes, [key][128 B] per K or V: 8 chunks of 16 B a key
+        const uint8_t* __restrict__ kv8 = reinterpret_cast<const uint8_t*>(P.kv_d);
+        const uint32_t k8 = sbase + L::STAGE_OFF + buf * L::F8_STAGE;
+        const size_t vstride8 = (size_t)P.ps * P.Hk * D;
+        constexpr int PER8 = KST * 8 / kThreads;
 #pragma unroll 1
-          for (int i = 0; i < PER8; ++i) {
-            const int idx = tid + kThreads * i;
-            const int key = idx >> 3, c = idx & 7;
-            const int t = kb + key;
-            const bool valid = t >= k0 && t < k1;
-            const int tt = valid ? t : k0;
-            const int pg = __ldg(P.d_kv_indices + page_base +
-                                 (P.ps_shift >= 0 ? (tt >> P.ps_shift) : (tt / P.ps)));
-            const int slot = P.ps_shift >= 0 ? (tt & (P.ps - 1)) : (tt % P.ps);
-            const uint8_t* src = kv8 + (P.d_hnd
-                ? (((size_t)pg * 2 * P.Hk + g) * P.ps + slot) * D + c * 16
-                : (((size_t)pg * 2 * P.ps + slot) * P.Hk + g) * D + c * 16);
-            const uint32_t off = (uint32_t)key * 128u + (uint32_t)((c ^ (key & 7)) << 4);
-            cp_async16(k8 + off, src, valid ? 16u : 0u);
-            cp_async16(k8 + L::F8_HALF + off, src + vstride8, valid ? 16u : 0u);
-          }
-          cp_async_mbar_arrive(full);
-          return;
-        }
-        constexpr int CH = POD_DECODE_STAGE * (D / 8);
-        constexpr int PER = CH / kThreads;
-        static_assert(CH % kThreads == 0, "stage chunks must divide evenly");
-        int pages[PER];
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-          const int key = (tid + kThreads * i) / (D / 8);
-          const int t = kb + key;
-          const int tt = (t >= k0 && t < k1) ? t : k0;
-          const int pg_i = P.ps_shift >= 0 ? (tt >> P.ps_shift) : (tt / P.ps);
-          pages[i] = __ldg(P.d_kv_indices + page_base + pg_i);
-        }
-        const size_t vstride = (size_t)P.ps * P.Hk * D;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
+        for (int i = 0; i < PER8; ++i) {
           const int idx = tid + kThreads * i;
-          const int key = idx / (D / 8), c = idx % (D / 8);
+          const int key = idx >> 3, c = idx & 7;
           const int t = kb + key;
           const bool valid = t >= k0 && t < k1;
           const int tt = valid ? t : k0;
+          const int pg = __ldg(P.d_kv_indices + page_base +
+                               (P.ps_shift >= 0 ? (tt >> P.ps_shift) : (tt / P.ps)));
           const int slot = P.ps_shift >= 0 ? (tt & (P.ps - 1)) : (tt % P.ps);
-          const T* src = kvg + (P.d_hnd
-              ? (((size_t)pages[i] * 2 * P.Hk + g) * P.ps + slot) * D + c * 8
-              : (((size_t)pages[i] * 2 * P.ps + slot) * P.Hk + g) * D + c * 8);
-          const uint32_t off = (c >> 3) * L::KDH + sw128_off(key, c & 7);
-          cp_async16(sk + off, src, valid ? 16u : 0u);
-          cp_async16(sv + off, src + vstride, valid ? 16u : 0u);
+          const uint8_t* src = kv8 + (P.d_hnd
+              ? (((size_t)pg * 2 * P.Hk + g) * P.ps + slot) * D + c * 16
+              : (((size_t)pg * 2 * P.ps + slot) * P.Hk + g) * D + c * 16);
+          const uint32_t off = (uint32_t)key * 128u + (uint32_t)((c ^ (key & 7)) << 4);
+          cp_async16(k8 + off, src, valid ? 16u : 0u);
+          cp_async16(k8 + L::F8_HALF + off, src + vstride8, valid ? 16u : 0u);
         }
         cp_async_mbar_arrive(full);
       }
@@ -1044,24 +989,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
     const int npre = nst < L::NSTAGE ? nst : L::NSTAGE;
     for (int st = 0; st < npre; ++st) issue(st, -1);
 
-    // rows of this thread inside its m-tile: r0 = 16 mt + lane/4, r1 = r0 + 8
-    int row_lo[2], row_hi[2];
-    // ALiBi only: the rows' slopes (raw q.k units) and diagonal positions
-    float a_slope[2] = {0.f, 0.f};
-    int a_pd[2] = {0, 0};
-#pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      const int rr = mt * 16 + (lane >> 2) + 8 * h2;
-      const int tok = tok0 + (rr < R ? rr / G : 0);
-      const int pd = kv_len - q_len + tok;
-      row_hi[h2] = min(P.causal ? min(pd + 1, kv_len) : kv_len, k1);
-      row_lo[h2] = max(P.window_left >= 0 ? max(pd - P.window_left, 0) : 0, k0);
-      if constexpr (LT == POD_LT_ALIBI) {
-        a_slope[h2] = __ldg(P.alibi + g * G + (rr < R ? rr % G : 0)) * P.lt_inv_scale;
-        a_pd[h2] = pd;
-      }
-    }
-    if (F8 && nst > 0) {
+    if (nst > 0) {
       // wait for stage 0 here (the stage loop's own wait then passes at once),
       // before the accumulators are live
       const bool got = __all_sync(
@@ -1148,8 +1076,6 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
 #pragma unroll
     for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     const bool active = mt < Mt;
-    const int mi = lane >> 3;
-
 
     for (int st = 0; st < nst; ++st) {
       const int f = fills + st;
@@ -1158,18 +1084,309 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
       // that the load latency hides behind the compute
       const int next_page =
           (P.d_tma && warp == 0 && st + L::NSTAGE < nst) ? page_for(st + L::NSTAGE) : -1;
-      // FP8: made warp-uniform, so that every lane reaches the warp votes of its stage
-      const bool got_l = mbar_wait(bar0 + 8 * buf, (f / L::NSTAGE) & 1, abort_flag);
-      const bool got = F8 ? __all_sync(0xffffffffu, got_l) : got_l;
+      // warp-uniform, so that every lane reaches the warp votes of its stage
+      const bool got =
+          __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * buf, (f / L::NSTAGE) & 1, abort_flag));
       const int kbase = kb0 + st * KST + ks * KSL;
-      if (got && active && kbase < k1 && kbase + KSL > k0) {
-       if constexpr (F8) {
+      if (got && active && kbase < k1 && kbase + KSL > k0)
         decode_stage_f8<BF16, D, KSL>(sbase + L::STAGE_OFF + buf * L::F8_STAGE, L::F8_HALF,
                                       sbase + L::Q_OFF, L::Q8_PART, sbase + L::Q8X_OFF, mt, ks,
                                       lane, kbase, kv_len, sbase + L::QSC_OFF, m, l, o);
-       } else {
-        // 16-bit cache: K of the stage, V at +KBYTES
-        const uint32_t sk = sbase + L::STAGE_OFF + buf * L::STAGE_BYTES;
+      if (!__syncthreads_and(got)) { ok = false; break; }
+      if (st + L::NSTAGE < nst) issue(st + L::NSTAGE, next_page);
+    }
+    fills += nst;
+    if (!ok) break;
+
+    // ---- combine the 4 key slices of each m-tile through shared memory
+    // (the output placement is read from the record again rather than kept
+    // live in registers across the stage loop)
+    const int32_t* crec = P.dqrec + POD_DQREC * pos;
+    const int cg = __ldg(crec + 1), ctok0 = __ldg(crec + 2), prow = __ldg(crec + 6);
+    const int cq_base = __ldg(crec + 9);
+    float* scr_o = reinterpret_cast<float*>(smem + L::SCR_O);
+    float* scr_ml = reinterpret_cast<float*>(smem + L::SCR_ML);
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      l[h2] += __shfl_xor_sync(0xffffffffu, l[h2], 1);
+      l[h2] += __shfl_xor_sync(0xffffffffu, l[h2], 2);
+    }
+    if (active) {
+      float* wo = scr_o + warp * 16 * D;
+      const int rl = lane >> 2;
+      // d 16q + 4t .. +3 from the even / odd tiles of chunk q
+#pragma unroll
+      for (int q = 0; q < D / 16; ++q) {
+        const int col = 16 * q + 4 * (lane & 3);
+        *reinterpret_cast<float4*>(wo + rl * D + col) =
+            make_float4(o[2 * q][0], o[2 * q + 1][0], o[2 * q][1], o[2 * q + 1][1]);
+        *reinterpret_cast<float4*>(wo + (rl + 8) * D + col) =
+            make_float4(o[2 * q][2], o[2 * q + 1][2], o[2 * q][3], o[2 * q + 1][3]);
+      }
+      if ((lane & 3) == 0) {
+        const int rl = lane >> 2;
+        scr_ml[(warp * 16 + rl) * 2 + 0] = m[0];
+        scr_ml[(warp * 16 + rl) * 2 + 1] = l[0];
+        scr_ml[(warp * 16 + rl + 8) * 2 + 0] = m[1];
+        scr_ml[(warp * 16 + rl + 8) * 2 + 1] = l[1];
+      }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < R * (D / 4); idx += kThreads) {
+      const int rr = idx / (D / 4), c4 = (idx % (D / 4)) * 4;
+      const int mtr = rr >> 4, rl = rr & 15;
+      float M = NEG_INF;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) M = fmaxf(M, scr_ml[((mtr * 4 + k) * 16 + rl) * 2]);
+      const float Ms = (M == NEG_INF) ? 0.f : M;
+      float wsum = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int wk = mtr * 4 + k;
+        const float wgt = ex2(scr_ml[(wk * 16 + rl) * 2] - Ms);
+        wsum += wgt * scr_ml[(wk * 16 + rl) * 2 + 1];
+        const float4 v = *reinterpret_cast<const float4*>(scr_o + (wk * 16 + rl) * D + c4);
+        acc.x += wgt * v.x;
+        acc.y += wgt * v.y;
+        acc.z += wgt * v.z;
+        acc.w += wgt * v.w;
+      }
+      const int tok = ctok0 + rr / G;
+      const int head = cg * G + rr % G;
+      // the slices carried 256 P (sums and outputs)
+      constexpr float kPU = 1.f / 256.f;
+      wsum *= kPU;
+      if (prow < 0) {
+        float denom = wsum;
+        if (P.has_sinks) denom += ex2(P.sinks[head] * 1.4426950408889634f - Ms);
+        const float inv = denom > 0.f ? P.v_scale * kPU / denom : 0.f;
+        const size_t orow = (size_t)(cq_base + tok) * H + head;
+        uint2 v;
+        v.x = Pack<T>::two(acc.x * inv, acc.y * inv);
+        v.y = Pack<T>::two(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(outg + orow * D + c4) = v;
+        if (c4 == 0 && P.lse_d) P.lse_d[orow] = wsum > 0.f ? M + log2f(wsum) : NEG_INF;
+      } else {
+        const float inv = wsum > 0.f ? P.v_scale * kPU / wsum : 0.f;
+        *reinterpret_cast<float4*>(P.part_o + (size_t)(prow + rr) * D + c4) =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        if (c4 == 0) P.part_lse[prow + rr] = wsum > 0.f ? M + log2f(wsum) : NEG_INF;
+      }
+    }
+    // the combine's generic accesses to the stage area come before the next
+    // item's TMA writes into it (stage reads within an item are ordered by the
+    // per-stage barrier)
+    fence_proxy_async();
+    __syncthreads();
+  }
+  if (!ok) {
+    *abort_flag = 1;
+    if (tid == 0) raise_status(P.status, POD_STATUS_TIMEOUT);
+  }
+  cp_async_wait_all();
+  if (ok && tid == 0)  // every filled stage was waited on: no transfer is pending
+    for (int s = 0; s < L::NSTAGE; ++s) mbar_inval(bar0 + 8 * s);
+  return ok;
+}
+
+template <typename T, int D, bool F8, int LT, bool RP>
+__device__ bool decode_role(const PodParams& P, uint8_t* smem) {
+  static_assert(!F8, "FP8 decode caches run decode_role_f8");  // 16-bit caches
+  using L = DLayout<D, RP>;
+  constexpr bool BF16 = Pack<T>::kBF16;
+  constexpr int NKB = L::NKB;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int mt = warp >> 2, ks = warp & 3;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L::BAR_OFF;   // full[NSTAGE]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR_OFF + 64);
+  const int G = P.G, H = P.H;
+  T* __restrict__ outg = reinterpret_cast<T*>(P.out_d);
+  const float NEG_INF = -INFINITY;
+  volatile int* item_slot = reinterpret_cast<volatile int*>(smem + L::BAR_OFF + 96);
+
+  if (tid == 0) {
+    for (int s = 0; s < L::NSTAGE; ++s) mbar_init(bar0 + 8 * s, P.d_tma ? 1u : (uint32_t)kThreads);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (P.d_tma && tid == 0) {
+    tma_prefetch_desc(&P.tm_kv_d);
+    tma_prefetch_desc(&P.tm_q_d);
+  }
+  const uint32_t q_bytes = (uint32_t)(L::NQ * NKB * 128 * G * P.tu);
+  // K/V stage layout: [key / kbx][d half][key % kbx][64 elements] in 128-byte
+  // swizzled rows, kbx = keys per TMA box (64 on the cp.async path, where it
+  // is [d half][key][64]). Row offset of key k in its d half 0:
+  const int kshift = P.d_tma ? 31 - __clz(P.d_tma) : 6;
+  const uint32_t half_stride = 128u << kshift;  // bytes between the d halves of a box
+  auto key_row = [&](int k) -> uint32_t {
+    return (uint32_t)((k >> kshift) << kshift) * (NKB * 128u) +
+           (uint32_t)(k & ((1 << kshift) - 1)) * 128u;
+  };
+  int fills = 0;
+  bool ok = true;
+
+  for (;;) {
+    // thread 0 takes the next queue position; its record carries everything
+    // the item needs, so the claim costs one dependent load
+    if (tid == 0) {
+      const int idx = atomicAdd(P.status + 9, 1);
+      *item_slot = idx < P.n_items ? idx : -1;
+    }
+    __syncthreads();
+    const int pos = *item_slot;
+    if (pos < 0 || !ok) break;
+    const int32_t* rec = P.dqrec + POD_DQREC * pos;
+    // CUDA-graph capacity mode: n_items is the capacity and the records past
+    // the plan's own items have request -1 (the queue is empty there)
+    if (rec[0] < 0) break;
+    const int g = rec[1], tok0 = rec[2], ntok = rec[3], k0 = rec[4], k1 = rec[5];
+    const int R = ntok * G;
+    const int Mt = (R + 15) >> 4;
+    const int kv_len = rec[8];
+    const int q_base = rec[9];
+    const int q_len = rec[10];
+    const int page_base = rec[11];
+    const int npages = rec[12];
+    const int kb0 = (k0 / POD_DECODE_STAGE) * POD_DECODE_STAGE;
+    const int nst = (k1 - kb0 + POD_DECODE_STAGE - 1) / POD_DECODE_STAGE;
+
+    // TMA path: page of box `lane` of stage st (lane < 64 / d_tma <= 8); an id
+    // past the request's last page is the out-of-range page TMA fills with zeros
+    auto page_for = [&](int st) -> int {
+      const int pidx = (kb0 + st * POD_DECODE_STAGE + lane * P.d_tma) >> P.ps_shift;
+      return pidx < npages ? __ldg(P.d_kv_indices + page_base + pidx) : P.d_num_pages;
+    };
+    // fill stage st of this item (Q travels with stage 0) into ring slot
+    // (fills + st) % 3; TMA path: `page` = page_for(st) of this lane, or -1
+    // to look it up here
+    auto issue = [&](int st, int page) {
+      const int f = fills + st;
+      const int buf = f % L::NSTAGE;
+      const uint32_t full = bar0 + 8 * buf;
+      const uint32_t sk = sbase + L::STAGE_OFF + buf * L::STAGE_BYTES;
+      const uint32_t sv = sk + L::KBYTES;
+      const int kb = kb0 + st * POD_DECODE_STAGE;
+      if (P.d_tma) {
+        // warp 0: lane 0 registers the bytes, lane i fetches box group i
+        if (warp == 0) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(full, 2u * L::KBYTES +
+                                            (st == 0 ? q_bytes : 0u));
+            if (st == 0)
+              for (int dh = 0; dh < NKB; ++dh) {
+                tma_load_3d(sbase + L::Q_OFF + dh * L::QDH, &P.tm_q_d, dh * 64, g * G, q_base + tok0,
+                            full);
+                if (RP)
+                  tma_load_3d(sbase + L::QLO_OFF + dh * L::QDH, &P.tm_qlo_d, dh * 64, g * G,
+                              q_base + tok0, full);
+              }
+          }
+          __syncwarp();
+          if (lane < POD_DECODE_STAGE / P.d_tma) {
+            if (page < 0) page = page_for(st);
+            const int o = lane * P.d_tma;
+            const uint32_t dst = (uint32_t)o * (NKB * 128u);
+            if (P.ps >= 8) {  // coordinates (x, slot, half, head, 2 * page + kv)
+              const int tin = (kb + o) & (P.ps - 1);
+              tma_load_5d(sk + dst, &P.tm_kv_d, 0, tin, 0, g, 2 * page, full);
+              tma_load_5d(sv + dst, &P.tm_kv_d, 0, tin, 0, g, 2 * page + 1, full);
+            } else {          // page_size 1: (x, page, half, head, kv)
+              tma_load_5d(sk + dst, &P.tm_kv_d, 0, page, 0, g, 0, full);
+              tma_load_5d(sv + dst, &P.tm_kv_d, 0, page, 0, g, 1, full);
+            }
+          }
+        }
+      } else {
+        const T* __restrict__ qg = reinterpret_cast<const T*>(P.q_d);
+        const T* __restrict__ kvg = reinterpret_cast<const T*>(P.kv_d);
+        if (st == 0) {
+          for (int idx = tid; idx < POD_DECODE_ROWS * (D / 8); idx += kThreads) {
+            const int r = idx / (D / 8), c = idx % (D / 8);
+            const bool valid = r < R;
+            const int tok = tok0 + (valid ? r / G : 0);
+            const int head = g * G + (valid ? r % G : 0);
+            const size_t qoff = ((size_t)(q_base + tok) * H + head) * D + c * 8;
+            cp_async16(sbase + L::Q_OFF + (c >> 3) * L::QDH + sw128_off(r, c & 7), qg + qoff,
+                       valid ? 16u : 0u);
+            if (RP)
+              cp_async16(sbase + L::QLO_OFF + (c >> 3) * L::QDH + sw128_off(r, c & 7),
+                         reinterpret_cast<const T*>(P.q_d_lo) + qoff, valid ? 16u : 0u);
+          }
+        }
+        constexpr int CH = POD_DECODE_STAGE * (D / 8);
+        constexpr int PER = CH / kThreads;
+        static_assert(CH % kThreads == 0, "stage chunks must divide evenly");
+        int pages[PER];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          const int key = (tid + kThreads * i) / (D / 8);
+          const int t = kb + key;
+          const int tt = (t >= k0 && t < k1) ? t : k0;
+          const int pg_i = P.ps_shift >= 0 ? (tt >> P.ps_shift) : (tt / P.ps);
+          pages[i] = __ldg(P.d_kv_indices + page_base + pg_i);
+        }
+        const size_t vstride = (size_t)P.ps * P.Hk * D;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          const int idx = tid + kThreads * i;
+          const int key = idx / (D / 8), c = idx % (D / 8);
+          const int t = kb + key;
+          const bool valid = t >= k0 && t < k1;
+          const int tt = valid ? t : k0;
+          const int slot = P.ps_shift >= 0 ? (tt & (P.ps - 1)) : (tt % P.ps);
+          const T* src = kvg + (P.d_hnd
+              ? (((size_t)pages[i] * 2 * P.Hk + g) * P.ps + slot) * D + c * 8
+              : (((size_t)pages[i] * 2 * P.ps + slot) * P.Hk + g) * D + c * 8);
+          const uint32_t off = (c >> 3) * L::KDH + sw128_off(key, c & 7);
+          cp_async16(sk + off, src, valid ? 16u : 0u);
+          cp_async16(sv + off, src + vstride, valid ? 16u : 0u);
+        }
+        cp_async_mbar_arrive(full);
+      }
+    };
+    const int npre = nst < L::NSTAGE ? nst : L::NSTAGE;
+    for (int st = 0; st < npre; ++st) issue(st, -1);
+
+    // rows of this thread inside its m-tile: r0 = 16 mt + lane/4, r1 = r0 + 8
+    int row_lo[2], row_hi[2];
+    // ALiBi only: the rows' slopes (raw q.k units) and diagonal positions
+    float a_slope[2] = {0.f, 0.f};
+    int a_pd[2] = {0, 0};
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int rr = mt * 16 + (lane >> 2) + 8 * h2;
+      const int tok = tok0 + (rr < R ? rr / G : 0);
+      const int pd = kv_len - q_len + tok;
+      row_hi[h2] = min(P.causal ? min(pd + 1, kv_len) : kv_len, k1);
+      row_lo[h2] = max(P.window_left >= 0 ? max(pd - P.window_left, 0) : 0, k0);
+      if constexpr (LT == POD_LT_ALIBI) {
+        a_slope[h2] = __ldg(P.alibi + g * G + (rr < R ? rr % G : 0)) * P.lt_inv_scale;
+        a_pd[h2] = pd;
+      }
+    }
+    float m[2] = {NEG_INF, NEG_INF}, l[2] = {0.f, 0.f};
+    float o[D / 8][4];
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    const bool active = mt < Mt;
+    const int mi = lane >> 3;
+
+    for (int st = 0; st < nst; ++st) {
+      const int f = fills + st;
+      const int buf = f % L::NSTAGE;
+      // look up the pages of the stage this one's slot is refilled with now, so
+      // that the load latency hides behind the compute
+      const int next_page =
+          (P.d_tma && warp == 0 && st + L::NSTAGE < nst) ? page_for(st + L::NSTAGE) : -1;
+      const bool got = mbar_wait(bar0 + 8 * buf, (f / L::NSTAGE) & 1, abort_flag);
+      // K of the stage (V follows at +KBYTES)
+      const uint32_t sk = sbase + L::STAGE_OFF + buf * L::STAGE_BYTES;
+      const int kbase = kb0 + st * POD_DECODE_STAGE + ks * 16;
+      if (got && active && kbase < k1 && kbase + 16 > k0) {
         const uint32_t sq = sbase + L::Q_OFF;
         const uint32_t sv = sk + (uint32_t)L::KBYTES;
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1246,7 +1463,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
         }
         // mask, online softmax in base 2 (rows h2 = 0: c0,c1; h2 = 1: c2,c3)
         const int kq = kbase + 2 * (lane & 3);
-        const float scale = P.d_scale_log2;  // sm_scale * log2(e), times k_scale for FP8
+        const float scale = P.d_scale_log2;  // sm_scale * log2(e)
         float mx[2];
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
@@ -1311,7 +1528,6 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
           mma16816<BF16>(o[2 * j], pa, b[0] & vm0, b[1] & vm1);
           mma16816<BF16>(o[2 * j + 1], pa, b[2] & vm0, b[3] & vm1);
         }
-       }
       }
       if (!__syncthreads_and(got)) { ok = false; break; }
       if (st + L::NSTAGE < nst) issue(st + L::NSTAGE, next_page);
@@ -1335,22 +1551,11 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
     if (active) {
       float* wo = scr_o + warp * 16 * D;
       const int rl = lane >> 2;
-      if constexpr (F8) {  // d 16q + 4t .. +3 from the even / odd tiles of chunk q
 #pragma unroll
-        for (int q = 0; q < D / 16; ++q) {
-          const int col = 16 * q + 4 * (lane & 3);
-          *reinterpret_cast<float4*>(wo + rl * D + col) =
-              make_float4(o[2 * q][0], o[2 * q + 1][0], o[2 * q][1], o[2 * q + 1][1]);
-          *reinterpret_cast<float4*>(wo + (rl + 8) * D + col) =
-              make_float4(o[2 * q][2], o[2 * q + 1][2], o[2 * q][3], o[2 * q + 1][3]);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-          const int col = 8 * i + 2 * (lane & 3);
-          *reinterpret_cast<float2*>(wo + rl * D + col) = make_float2(o[i][0], o[i][1]);
-          *reinterpret_cast<float2*>(wo + (rl + 8) * D + col) = make_float2(o[i][2], o[i][3]);
-        }
+      for (int i = 0; i < D / 8; ++i) {
+        const int col = 8 * i + 2 * (lane & 3);
+        *reinterpret_cast<float2*>(wo + rl * D + col) = make_float2(o[i][0], o[i][1]);
+        *reinterpret_cast<float2*>(wo + (rl + 8) * D + col) = make_float2(o[i][2], o[i][3]);
       }
       if ((lane & 3) == 0) {
         const int rl = lane >> 2;
@@ -1383,13 +1588,10 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
       }
       const int tok = ctok0 + rr / G;
       const int head = cg * G + rr % G;
-      // FP8: the slices carried 256 P (sums and outputs)
-      constexpr float kPU = F8 ? 1.f / 256.f : 1.f;
-      wsum *= kPU;
       if (prow < 0) {
         float denom = wsum;
         if (P.has_sinks) denom += ex2(P.sinks[head] * 1.4426950408889634f - Ms);
-        const float inv = denom > 0.f ? P.v_scale * kPU / denom : 0.f;
+        const float inv = denom > 0.f ? P.v_scale / denom : 0.f;
         const size_t orow = (size_t)(cq_base + tok) * H + head;
         uint2 v;
         v.x = Pack<T>::two(acc.x * inv, acc.y * inv);
@@ -1397,7 +1599,7 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
         *reinterpret_cast<uint2*>(outg + orow * D + c4) = v;
         if (c4 == 0 && P.lse_d) P.lse_d[orow] = wsum > 0.f ? M + log2f(wsum) : NEG_INF;
       } else {
-        const float inv = wsum > 0.f ? P.v_scale * kPU / wsum : 0.f;
+        const float inv = wsum > 0.f ? P.v_scale / wsum : 0.f;
         *reinterpret_cast<float4*>(P.part_o + (size_t)(prow + rr) * D + c4) =
             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         if (c4 == 0) P.part_lse[prow + rr] = wsum > 0.f ? M + log2f(wsum) : NEG_INF;
@@ -1417,6 +1619,12 @@ __device__ bool decode_role(const PodParams& P, uint8_t* smem) {
   if (ok && tid == 0)  // every filled stage was waited on: no transfer is pending
     for (int s = 0; s < L::NSTAGE; ++s) mbar_inval(bar0 + 8 * s);
   return ok;
+}
+
+template <typename T, int D, bool F8, int LT, bool RP>
+__device__ __forceinline__ bool decode_dispatch(const PodParams& P, uint8_t* smem) {
+  if constexpr (F8) return decode_role_f8<T, D, F8, LT, RP>(P, smem);
+  else return decode_role<T, D, F8, LT, RP>(P, smem);
 }
 
 // ============================================================ kernels
@@ -1457,7 +1665,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, RP>()))
       fence_proxy_async();
       __syncthreads();
       ok = do_prefill ? prefill_role<T, D, LT, RP>(P, smem, tmem)
-                      : decode_role<T, D, F8, LT, RP>(P, smem);
+                      : decode_dispatch<T, D, F8, LT, RP>(P, smem);
     }
     tc_fence_before();
     __syncthreads();
@@ -1479,7 +1687,7 @@ __global__ void __launch_bounds__(kThreads, (ctas_per_sm<D, RP>()))
 // each device's context: they are set once per device (and thread-safely).
 template <typename T, int D, bool F8, int LT, bool RP>
 cudaError_t launch_pod(const PodParams& P, cudaStream_t stream) {
-  constexpr int SMEM = smem_bytes<D, RP>();
+  constexpr int SMEM = smem_bytes<D, RP, F8>();
   static std::atomic<unsigned long long> done{0ull};
   static std::mutex mu;
   int dev = 0;
