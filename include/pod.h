@@ -365,8 +365,7 @@ pod_status pod_plan_table(pod_handle h, int32_t which, int32_t* out, int64_t cap
  * serialised by the caller. The handle becomes bound to the array (a later
  * pod_run on it must pass that array's address or re-bind with
  * pod_bind_workspace). The first call on a device looks up the array's device
- * address with that device current; make that first call before any stream
- * capture. No device memory is allocated or freed.
+ * address with that device current. No device memory is allocated or freed.
  *
  * Errors: POD_ERR_WORKSPACE (with a message) when pod_workspace_size(h)
  * exceeds the array; otherwise those of pod_bind_workspace and pod_run.

@@ -125,6 +125,19 @@ CostModel cost_model(int d) {
   return c;
 }
 
+// Co-residency rates when most decode bytes are in items of more than 16
+// rows (both mma m-tiles, all 8 decode warps busy): a timeline of the fused
+// c5 launch on GB300 (per-record %globaltimer stamps) measured 17.1 GB/s for
+// a decode CTA next to a prefill CTA against 19.3 GB/s next to a decode CTA,
+// and prefill CTAs 1 % slower next to a decode CTA than next to another
+// prefill CTA. Items of at most 16 rows leave half the decode warps idle and
+// keep the rates above (measured best for c2-c4).
+void wide_decode_neighbours(CostModel& c, int d) {
+  const double f = 0.4 + 0.6 * d / 128.0;
+  c.p_block_ns[1] = 1160.0 * f;
+  c.d_bytes_per_ns[1] = c.d_bytes_per_ns[2] * (17.1 / 19.3);
+}
+
 // Co-residency class of CTA c (0 alone, 1 other role, 2 same role) when CTAs
 // [0, n_p) run prefill and [n_p, n_p + n_d) decode, `cps` CTAs per SM.
 int neighbour_class(int c, int n_p, int n_d, int S, int cps) {
@@ -567,7 +580,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
     P.cap_d_batch = a.cap_d_batch; P.cap_d_rows = a.cap_d_rows; P.cap_d_pages = a.cap_d_pages;
   }
 
-  const CostModel cm = cost_model(a.d);
+  CostModel cm = cost_model(a.d);
 
   // ---- decode units ---------------------------------------------------------
   const int Tu = std::max(1, POD_DECODE_ROWS / G);
@@ -590,7 +603,7 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
     P.d_tma = a.ps >= 8 ? P.d_tma : 0;
   }
   std::vector<DecodeUnit> units;
-  double d_bytes = 0.0;
+  double d_bytes = 0.0, d_bytes_wide = 0.0;
   for (int r = 0; r < P.dd.batch; ++r) {
     int ql = P.dd.q_len[r], kl = P.dd.kv_len[r];
     for (int t0 = 0; t0 < ql; t0 += Tu) {
@@ -600,9 +613,11 @@ int pod_build_plan(const PodPlanArgs& a, PodPlanHost& P, std::string* err) {
       for (int g = 0; g < P.Hk; ++g) {
         units.push_back({r, g, t0, nt, lo, hi});
         d_bytes += 4.0 * a.d * (double)(hi - lo);
+        if (nt * G > 16) d_bytes_wide += 4.0 * a.d * (double)(hi - lo);
       }
     }
   }
+  if (d_bytes_wide > 0.5 * d_bytes) wide_decode_neighbours(cm, a.d);
 
   // ---- prefill tiles --------------------------------------------------------
   // A tile's key range is split into chunks (merged like decode splits) when

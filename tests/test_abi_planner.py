@@ -313,15 +313,19 @@ def test_large_prefill_is_not_split(lib):
         assert not np.any(groups[:, 0] == 0) if len(groups) else True
 
 
-def test_split_keeps_balanced_start_when_no_tile_dominates(lib):
-    """c5: no prefill tile is long next to the decode stream, so the split
-    stays near the CTA-time balance (a third to a half of the grid starts on
-    prefill) and every CTA has work (grid = 2 x SMs)."""
-    inp = make_config("c5", with_data=False)
-    h = plan_host(inp)
-    s = pod.plan_summary(h)
-    assert s["grid"] == 2 * s["num_sms"], s
-    assert 0.25 * s["grid"] <= s["n_p_ctas"] <= 0.5 * s["grid"], s
+def test_split_follows_decode_item_width(lib):
+    """The split depends on how decode CTAs share an SM with prefill CTAs.
+    c5's decode items have 32 rows (both m-tiles, all 8 decode warps busy),
+    and a decode CTA next to a prefill CTA is measured 11 % slower: the plan
+    starts nearly every CTA on decode and lets them cross to the prefill
+    queue afterwards. c3's items have 8 rows (half the decode warps idle):
+    the split stays near the CTA-time balance (a quarter to a half of the
+    grid starts on prefill). Every CTA has work in both (grid = 2 x SMs)."""
+    for name, lo, hi in (("c5", 1, 0.1), ("c3", 0.25, 0.5)):
+        h = plan_host(make_config(name, with_data=False))
+        s = pod.plan_summary(h)
+        assert s["grid"] == 2 * s["num_sms"], s
+        assert lo * (s["grid"] if lo < 1 else 1) <= s["n_p_ctas"] <= hi * s["grid"], (name, s)
 
 
 # ------------------------------------------------------------- custom prefill mask
