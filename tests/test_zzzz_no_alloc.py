@@ -5,10 +5,11 @@ process under a fixed device-memory budget, a serving loop that cannot take
 cudaMalloc's implicit synchronisation) get the kernels' scratch from a fixed
 array inside the library instead of a workspace of their own. These tests go
 through the C ABI (ctypes binding) and check that this entry point returns
-what pod_run returns with a caller-allocated workspace, on two calls in a row
+what pod_run returns with a caller-allocated workspace, on calls in a row
 that use different plans (one under RoPE, whose angle table and rotated
 copies also live in the array and must be rebuilt when another plan used it
-in between), and that a plan too large for the array is refused. The file
+in between, and one with a custom prefill mask, whose bits live there too),
+and that a plan too large for the array is refused. The file
 name sorts after every other test file on purpose: a run that stops at the
 first failure has run all the others before this one.
 """
@@ -17,7 +18,7 @@ import pytest
 import torch
 
 import prefill_decode_paged_pod_gb300 as pod
-from pod_workloads import make_config, make_custom
+from pod_workloads import make_config, make_custom, with_prefill_custom_mask
 from podtest_util import LSE_ATOL, OUT_ATOL, OUT_RTOL, to_dev
 
 
@@ -59,9 +60,13 @@ def test_static_scratch_matches_pod_run_two_calls():
         make_custom("rope", torch.bfloat16, 16, 2, 128, 16, True, -1, [70], [100], [1, 4],
                     [300, 129], seed=13),
         make_config("c1"),
+        with_prefill_custom_mask(
+            make_custom("mask", torch.float16, 8, 2, 64, 16, False, -1, [90, 40], [200, 40],
+                        [1, 1], [100, 33], seed=15), seed=16, density=0.5),
+        make_config("c1"),
     ]
     cases[2].rope = (1.0, 1e4)
-    sms = [4, 0, 0, 0]
+    sms = [4, 0, 0, 0, 0, 0]
     for inp, ns in zip(cases, sms):
         dev = to_dev(inp)
         # existing entry point, caller-allocated workspace
@@ -79,7 +84,10 @@ def test_static_scratch_matches_pod_run_two_calls():
             if r.numel() == 0:
                 continue
             if name.startswith("lse"):
-                assert float((r - g).abs().max()) <= LSE_ATOL, name
+                # rows a custom mask leaves without keys have lse = -inf on both
+                assert torch.equal(torch.isinf(r), torch.isinf(g)), name
+                fin = torch.isfinite(r)
+                assert float((r[fin] - g[fin]).abs().max()) <= LSE_ATOL, name
             else:
                 assert _close(r, g), name
         pod.pod_destroy(h)
