@@ -162,7 +162,13 @@ pod_status pod_run(pod_handle h, const void* q_p, const void* kv_p,
  * kernel folds k_scale into its softmax scale and multiplies the decode
  * outputs (split partials included) by v_scale; the decode LSE is that of the
  * scaled logits. q_d and out_d keep the plan's 16-bit dtype; the prefill half
- * is unchanged. May be called again to change the scales. Errors:
+ * is unchanged. Both products run on e4m3 tensor cores with the codes as
+ * they are: each query row enters as e4m3 parts of the row scaled by a power
+ * of two, which hold a bf16 row exactly and an fp16 row to 12 significant
+ * bits, and the softmax weights as two e4m3 parts (about 8 significant bits
+ * for weights above 2^-10 of the row's largest, as the bf16 weights of the
+ * 16-bit path, and within about 2^-18 of the largest below). May be called
+ * again to change the scales. Errors:
  * POD_ERR_UNSUPPORTED unless head_dim is 128, or with a logits transform set
  * (pod_plan_set_logits_transform) or RoPE (pod_plan_set_rope);
  * POD_ERR_INVALID_ARG for a NULL handle or scales that are not finite and
